@@ -1,0 +1,15 @@
+"""GB300-native (sm_103a) KV-cache codec for multi-agent KV sharing.
+
+SharedKVPool ("PolyKV": int8 keys with a per-tensor scale; values rotated by
+a Walsh-Hadamard transform and coded at 3 bits with the Lloyd-Max N(0,1)
+codebook; fan-out decode into N agent caches) and CacheCard ("QKVShare":
+per-token {2,4,8,16}-bit asymmetric group quantization with metadata), as a
+C-ABI CUDA library (include/kvpool.h) with this thin ctypes binding.
+"""
+from .binding import (  # noqa: F401
+    KVP_ERR_ALIGN, KVP_ERR_ARG, KVP_ERR_BITS, KVP_ERR_CUDA, KVP_ERR_HEADER, KVP_ERR_NONFINITE,
+    KVP_ERR_RANGE, KVP_ERR_SIZE, KVP_ERR_UNSUPPORTED_D, KVP_MAX_LAYERS, KVP_OK, CardHeader, KVPError,
+    Shape, cachecard_bytes, cachecard_pack, cachecard_read_header, cachecard_status, cachecard_unpack,
+    check, declared_functions, kvp_launch_count, kvp_strerror, kvpool_decode_into, kvpool_encode,
+    kvpool_pool_bytes, kvpool_status, kvpool_workspace_bytes, load,
+)

@@ -1,0 +1,425 @@
+// cachecard.cu -- QKVShare CacheCard ("QKVShare: Quantized KV-Cache Handoff
+// for Multi-Agent On-Device LLMs", Methodology 1-3): per-token bitwidth from
+// {2,4,8,16}; asymmetric min/max quantization in groups of 32 coordinates
+// with fp16 scale and zero point; the receiver rebuilds bf16 past_key_values.
+//
+// cachecard_pack: card_scan (one block: bitwidths -> record offsets, header)
+// then card_pack (one warp per (layer, token, K|V) record half).
+// cachecard_unpack: card_unpack, the inverse, one warp per record half.
+#include "kvp_internal.cuh"
+
+namespace kvp {
+
+constexpr int CARD_THREADS = 256;
+constexpr int CARD_WARPS = CARD_THREADS / 32;
+constexpr int SCAN_THREADS = 1024;
+constexpr float RNE_MAGIC_C = 12582912.0f;  // 1.5 * 2^23
+
+struct CardArgs {
+    const uint4 *src[2][KVP_MAX_LAYERS];  // pack: K, V inputs.  unpack: unused
+    uint4 *dst[2][KVP_MAX_LAYERS];        // unpack: K, V outputs
+    uint8_t *card;
+    const uint8_t *bits_dev;
+    uint64_t card_bytes;
+    uint64_t model_id;
+    int64_t pos_offset;
+    uint64_t off_offsets, off_layers, layer_stride;
+    int L, H, T, d;
+};
+
+// ---------------------------------------------------------------------------
+// Offsets and header ("QKVShare" Methodology 2: bitwidths + metadata).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(SCAN_THREADS) card_scan(const __grid_constant__ CardArgs a) {
+    __shared__ unsigned long long wsum[SCAN_THREADS / 32];
+    __shared__ uint32_t wbad[SCAN_THREADS / 32];
+    const int T = a.T;
+    const int per = (T + SCAN_THREADS - 1) / SCAN_THREADS;
+    const int t0 = min(T, int(threadIdx.x) * per), t1 = min(T, t0 + per);
+    unsigned long long sum = 0;
+    uint32_t bad = 0;
+    for (int t = t0; t < t1; ++t) {
+        const int b = a.bits_dev[t];
+        if (valid_bits(b)) sum += card_record_bytes(b, a.H, a.d);
+        else bad = 1;
+    }
+    // block-wide exclusive scan of the per-thread sums
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    unsigned long long incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    bad = __reduce_or_sync(0xffffffffu, bad);
+    if (lane == 31) wsum[warp] = incl;
+    if (lane == 0) wbad[warp] = bad;
+    __syncthreads();
+    unsigned long long wpre = 0, total = 0;
+    uint32_t anybad = 0;
+    for (int w = 0; w < SCAN_THREADS / 32; ++w) {
+        if (w < warp) wpre += wsum[w];
+        total += wsum[w];
+        anybad |= wbad[w];
+    }
+    unsigned long long run = wpre + incl - sum;
+    uint8_t *bits = a.card + CARD_HEADER_BYTES;
+    uint32_t *offs = reinterpret_cast<uint32_t *>(a.card + a.off_offsets);
+    for (int t = t0; t < t1; ++t) {
+        const int b = a.bits_dev[t];
+        bits[t] = uint8_t(b);
+        offs[t] = uint32_t(run);
+        if (valid_bits(b)) run += card_record_bytes(b, a.H, a.d);
+    }
+    // zero the gaps after bits[] and after off[]
+    for (uint64_t i = CARD_HEADER_BYTES + uint64_t(T) + threadIdx.x; i < a.off_offsets; i += SCAN_THREADS) a.card[i] = 0;
+    for (uint64_t i = a.off_offsets + 4ull * uint64_t(T) + threadIdx.x; i < a.off_layers; i += SCAN_THREADS)
+        a.card[i] = 0;
+    if (threadIdx.x == 0) {
+        const uint64_t stride = align256(total);
+        const uint64_t bytes = a.off_layers + uint64_t(a.L) * stride;
+        uint32_t err = 0;
+        if (anybad) err |= FLAG_BITS;
+        if (total >= (1ull << 32) || bytes > a.card_bytes) err |= FLAG_SIZE;
+        kvp_card_header h;
+        h.magic = CARD_MAGIC;
+        h.version = CARD_VERSION;
+        h.seq_len = T;
+        h.n_layers = a.L;
+        h.n_kv_heads = a.H;
+        h.head_dim = a.d;
+        h.group_size = CARD_GROUP;
+        h.dtype = 1;
+        h.model_id = a.model_id;
+        h.pos_offset = a.pos_offset;
+        h.off_bits = CARD_HEADER_BYTES;
+        h.off_offsets = a.off_offsets;
+        h.off_layers = a.off_layers;
+        h.layer_stride = stride;
+        h.total_bytes = bytes;
+        h.error = err;
+        for (int i = 0; i < 9; ++i) h.reserved[i] = 0;
+        *reinterpret_cast<kvp_card_header *>(a.card) = h;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// fp16 group scale, correctly rounded: s_h = RNE_fp16((mx - mn) / qmax).
+// mx - mn is carried exactly as hi + lo (two-sum); the fp16 estimate from
+// fp32 arithmetic is then checked against its two neighbouring fp16
+// midpoints m, where the sign of (hi + lo) - m*qmax is exact (m*qmax has at
+// most 20 significant bits; hi - m*qmax is exact when the two are within a
+// factor 2, and dominates lo otherwise).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int cmp_mid(float hi, float lo, float m, float qmax) {
+    const float r = (hi - m * qmax) + lo;
+    return r > 0.0f ? 1 : (r < 0.0f ? -1 : 0);
+}
+
+__device__ uint16_t group_scale_f16(float mx, float mn, float qmax) {
+    const float hi = mx - mn;
+    const float bb = hi - mx;
+    const float lo = (mx - (hi - bb)) + (-mn - bb);
+    uint16_t h = __half_as_ushort(__float2half_rn(hi / qmax));
+    if (h == 0x7C00u) return cmp_mid(hi, lo, 65520.0f, qmax) < 0 ? uint16_t(0x7BFFu) : h;
+    const float vh = __half2float(__ushort_as_half(h));
+    const float vn = h == 0x7BFFu ? 65536.0f : __half2float(__ushort_as_half(uint16_t(h + 1)));
+    int c = cmp_mid(hi, lo, 0.5f * (vh + vn), qmax);
+    if (c > 0 || (c == 0 && (h & 1u))) return uint16_t(h + 1);
+    if (h == 0) return h;
+    const float vp = __half2float(__ushort_as_half(uint16_t(h - 1)));
+    c = cmp_mid(hi, lo, 0.5f * (vp + vh), qmax);
+    if (c < 0 || (c == 0 && (h & 1u))) return uint16_t(h - 1);
+    return h;
+}
+
+// ---------------------------------------------------------------------------
+// Pack: one warp per (layer, token, K|V).  Lane chunk c covers coordinates
+// 8c..8c+7 of the token's [H][d] row set (head c / (d/8)); 4 consecutive
+// lanes form one group of 32.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(CARD_THREADS) card_pack(const __grid_constant__ CardArgs a) {
+    const kvp_card_header *hdr = reinterpret_cast<const kvp_card_header *>(a.card);
+    if (hdr->error & (FLAG_BITS | FLAG_SIZE)) return;
+    const uint64_t stride = hdr->layer_stride;  // depends on the device-resident bitwidths
+    const int lane = threadIdx.x & 31;
+    const int cpr = a.d / 8;                        // chunks per head row
+    const int nchunks = a.H * cpr;                  // chunks per (token, K|V)
+    const uint64_t tasks = uint64_t(a.L) * uint64_t(a.T) * 2u;
+    const uint8_t *bits = a.card + CARD_HEADER_BYTES;
+    const uint32_t *offs = reinterpret_cast<const uint32_t *>(a.card + a.off_offsets);
+    uint32_t flags = 0;
+
+    for (uint64_t task = uint64_t(blockIdx.x) * CARD_WARPS + (threadIdx.x >> 5); task < tasks;
+         task += uint64_t(gridDim.x) * CARD_WARPS) {
+        const int kv = int(task & 1u);
+        const uint64_t lt = task >> 1;
+        const int t = int(lt % uint64_t(a.T));
+        const int l = int(lt / uint64_t(a.T));
+        const int b = bits[t];
+        uint8_t *rec = a.card + a.off_layers + uint64_t(l) * stride + offs[t];
+        const uint4 *src = a.src[kv][l];
+        if (b == 16) {
+            uint4 *out = reinterpret_cast<uint4 *>(rec + uint64_t(kv) * a.H * a.d * 2);
+            for (int c = lane; c < nchunks; c += 32) {
+                const int h = c / cpr, ch = c % cpr;
+                out[c] = ld_stream_v4(src + (uint64_t(h) * a.T + t) * cpr + ch);
+            }
+            continue;
+        }
+        const float qmax = float((1 << b) - 1);
+        const uint64_t code_bytes = uint64_t(a.H) * a.d * b / 8;
+        uint8_t *codes = rec + uint64_t(kv) * code_bytes;
+        uint32_t *par = reinterpret_cast<uint32_t *>(rec + 2 * code_bytes + uint64_t(kv) * a.H * (a.d / 32) * 4);
+        for (int c0 = 0; c0 < nchunks; c0 += 32) {
+            const int c = c0 + lane;
+            const bool act = c < nchunks;  // whole groups: nchunks is a multiple of 4
+            uint4 w = make_uint4(0, 0, 0, 0);
+            if (act) {
+                const int h = c / cpr, ch = c % cpr;
+                w = ld_stream_v4(src + (uint64_t(h) * a.T + t) * cpr + ch);
+            }
+            const float x[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
+                                bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
+            // non-finite detection on the bit patterns (NaN escapes fminf/fmaxf)
+            bool nf = false;
+            {
+                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    nf |= ((ws[i] & 0x7F80u) == 0x7F80u) | ((ws[i] & 0x7F800000u) == 0x7F800000u);
+            }
+            float mn = x[0], mx = x[0];
+#pragma unroll
+            for (int e = 1; e < 8; ++e) {
+                mn = fminf(mn, x[e]);
+                mx = fmaxf(mx, x[e]);
+            }
+#pragma unroll
+            for (int m = 1; m < 4; m <<= 1) {
+                mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, m));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
+            }
+            const uint16_t sb = group_scale_f16(mx, mn, qmax);
+            const uint16_t zb = __half_as_ushort(__float2half_rn(mn));
+            if (act && (((sb & 0x7C00u) == 0x7C00u) || ((zb & 0x7C00u) == 0x7C00u))) flags |= FLAG_RANGE;
+            if (act && nf) flags |= FLAG_NONFINITE;
+            const float sf = __half2float(__ushort_as_half(sb)), zf = __half2float(__ushort_as_half(zb));
+            const float inv = (sf > 0.0f && sf <= 65504.0f) ? 1.0f / sf : 0.0f;
+            const int qm = (1 << b) - 1;
+            uint32_t q[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float tf = fmaf(x[e] - zf, inv, RNE_MAGIC_C);
+                const int qi = int(__float_as_uint(tf)) - 0x4B400000;
+                q[e] = uint32_t(min(max(qi, 0), qm));
+            }
+            if (act) {
+                if (b == 2) {
+                    uint32_t v = 0;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) v |= q[e] << (2 * e);
+                    reinterpret_cast<uint16_t *>(codes)[c] = uint16_t(v);
+                } else if (b == 4) {
+                    uint32_t v = 0;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) v |= q[e] << (4 * e);
+                    reinterpret_cast<uint32_t *>(codes)[c] = v;
+                } else {
+                    uint2 v;
+                    v.x = __byte_perm(__byte_perm(q[0], q[1], 0x0040), __byte_perm(q[2], q[3], 0x0040), 0x5410);
+                    v.y = __byte_perm(__byte_perm(q[4], q[5], 0x0040), __byte_perm(q[6], q[7], 0x0040), 0x5410);
+                    reinterpret_cast<uint2 *>(codes)[c] = v;
+                }
+                if ((lane & 3) == 0) par[c >> 2] = uint32_t(sb) | (uint32_t(zb) << 16);
+            }
+        }
+        // zero the record's padding (sizes are multiples of 8, records of 16)
+        if (kv == 1 && lane == 0) {
+            const uint64_t used = 2 * code_bytes + 2ull * a.H * (a.d / 32) * 4;
+            const uint64_t padded = card_record_bytes(b, a.H, a.d);
+            if (padded > used) *reinterpret_cast<uint2 *>(rec + used) = make_uint2(0, 0);
+        }
+    }
+    flags = __reduce_or_sync(0xffffffffu, flags);
+    if (lane == 0 && flags) atomicOr(const_cast<uint32_t *>(&hdr->error), flags);
+}
+
+// Zero each layer's tail after its last record (layer_stride is 256-aligned),
+// one block per layer, so the card image is fully determined.
+__global__ void card_zero_tails(const __grid_constant__ CardArgs a) {
+    const kvp_card_header *hdr = reinterpret_cast<const kvp_card_header *>(a.card);
+    if (hdr->error & (FLAG_BITS | FLAG_SIZE)) return;
+    const uint64_t stride = hdr->layer_stride;
+    const uint8_t *bits = a.card + CARD_HEADER_BYTES;
+    const uint32_t *offs = reinterpret_cast<const uint32_t *>(a.card + a.off_offsets);
+    const uint64_t used = uint64_t(offs[a.T - 1]) + card_record_bytes(bits[a.T - 1], a.H, a.d);
+    for (uint64_t i = used + threadIdx.x; i < stride; i += blockDim.x)
+        a.card[a.off_layers + uint64_t(blockIdx.x) * stride + i] = 0;
+}
+
+// ---------------------------------------------------------------------------
+// Unpack ("QKVShare" Methodology 3): x = bf16(q * s_h + z_h); 16-bit tokens
+// verbatim.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(CARD_THREADS) card_unpack(const __grid_constant__ CardArgs a) {
+    const int lane = threadIdx.x & 31;
+    const int cpr = a.d / 8;
+    const int nchunks = a.H * cpr;
+    const uint64_t tasks = uint64_t(a.L) * uint64_t(a.T) * 2u;
+    const uint8_t *bits = a.card + CARD_HEADER_BYTES;
+    const uint32_t *offs = reinterpret_cast<const uint32_t *>(a.card + a.off_offsets);
+    for (uint64_t task = uint64_t(blockIdx.x) * CARD_WARPS + (threadIdx.x >> 5); task < tasks;
+         task += uint64_t(gridDim.x) * CARD_WARPS) {
+        const int kv = int(task & 1u);
+        const uint64_t lt = task >> 1;
+        const int t = int(lt % uint64_t(a.T));
+        const int l = int(lt / uint64_t(a.T));
+        const int b = bits[t];
+        // a card whose bitwidths or offsets do not fit its own layer stride
+        // is not decoded (and is reported through cachecard_status)
+        if (!valid_bits(b) || uint64_t(offs[t]) + card_record_bytes(b, a.H, a.d) > a.layer_stride) {
+            if (lane == 0) atomicOr(&reinterpret_cast<kvp_card_header *>(a.card)->error, FLAG_HEADER);
+            continue;
+        }
+        const uint8_t *rec = a.card + a.off_layers + uint64_t(l) * a.layer_stride + offs[t];
+        uint4 *dst = a.dst[kv][l];
+        if (b == 16) {
+            const uint4 *in = reinterpret_cast<const uint4 *>(rec + uint64_t(kv) * a.H * a.d * 2);
+            for (int c = lane; c < nchunks; c += 32) {
+                const int h = c / cpr, ch = c % cpr;
+                st_stream_v4(dst + (uint64_t(h) * a.T + t) * cpr + ch, ld_stream_v4(in + c));
+            }
+            continue;
+        }
+        const uint64_t code_bytes = uint64_t(a.H) * a.d * b / 8;
+        const uint8_t *codes = rec + uint64_t(kv) * code_bytes;
+        const uint32_t *par = reinterpret_cast<const uint32_t *>(rec + 2 * code_bytes + uint64_t(kv) * a.H * (a.d / 32) * 4);
+        for (int c = lane; c < nchunks; c += 32) {
+            uint32_t q[8];
+            if (b == 2) {
+                const uint32_t v = reinterpret_cast<const uint16_t *>(codes)[c];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) q[e] = (v >> (2 * e)) & 3u;
+            } else if (b == 4) {
+                const uint32_t v = reinterpret_cast<const uint32_t *>(codes)[c];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) q[e] = (v >> (4 * e)) & 15u;
+            } else {
+                const uint2 v = reinterpret_cast<const uint2 *>(codes)[c];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    q[e] = (v.x >> (8 * e)) & 255u;
+                    q[4 + e] = (v.y >> (8 * e)) & 255u;
+                }
+            }
+            const uint32_t p = par[c >> 2];
+            const float sf = __half2float(__ushort_as_half(uint16_t(p & 0xFFFFu)));
+            const float zf = __half2float(__ushort_as_half(uint16_t(p >> 16)));
+            float y[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) y[e] = fmaf(__uint_as_float(0x4B000000u | q[e]) - 8388608.0f, sf, zf);
+            const int h = c / cpr, ch = c % cpr;
+            st_stream_v4(dst + (uint64_t(h) * a.T + t) * cpr + ch,
+                         make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
+                                    pack_bf16x2(y[6], y[7])));
+        }
+    }
+}
+
+template <typename K>
+static int card_grid(K kernel, uint64_t tasks) {
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, CARD_THREADS, 0) != cudaSuccess || occ < 1) occ = 1;
+    const uint64_t want = (tasks + CARD_WARPS - 1) / CARD_WARPS;
+    const uint64_t cap = uint64_t(sm_count()) * uint64_t(occ);
+    return int(want < cap ? (want < 1 ? 1 : want) : cap);
+}
+
+}  // namespace kvp
+
+using namespace kvp;
+
+extern "C" int cachecard_pack(const kvp_shape *s, uint64_t model_id, int64_t pos_offset, const uint8_t *bits_dev,
+                              const void *const *k_layers, const void *const *v_layers, void *card, size_t card_bytes,
+                              void *stream) {
+    int rc = shape_ok(s);
+    if (rc != KVP_OK) return rc;
+    if (!bits_dev || !k_layers || !v_layers || !card) return KVP_ERR_ARG;
+    const int L = s->n_layers;
+    for (int l = 0; l < L; ++l) {
+        if (!k_layers[l] || !v_layers[l]) return KVP_ERR_ARG;
+        if (!aligned(k_layers[l], 16) || !aligned(v_layers[l], 16)) return KVP_ERR_ALIGN;
+    }
+    if (!aligned(card, 256)) return KVP_ERR_ALIGN;
+    // the header, bits and offsets must fit whatever the bitwidths are
+    if (card_bytes < card_off_layers(s->n_tokens)) return KVP_ERR_SIZE;
+    // record offsets are 32-bit: the largest possible layer must fit
+    if (uint64_t(s->n_tokens) * card_record_bytes(16, s->n_kv_heads, s->head_dim) >= (1ull << 32)) return KVP_ERR_SIZE;
+
+    CardArgs a;
+    for (int l = 0; l < L; ++l) {
+        a.src[0][l] = static_cast<const uint4 *>(k_layers[l]);
+        a.src[1][l] = static_cast<const uint4 *>(v_layers[l]);
+    }
+    a.card = static_cast<uint8_t *>(card);
+    a.bits_dev = bits_dev;
+    a.card_bytes = card_bytes;
+    a.model_id = model_id;
+    a.pos_offset = pos_offset;
+    a.L = L;
+    a.H = s->n_kv_heads;
+    a.T = s->n_tokens;
+    a.d = s->head_dim;
+    a.off_offsets = card_off_offsets(a.T);
+    a.off_layers = card_off_layers(a.T);
+    a.layer_stride = 0;  // depends on device-resident bits: kernels read it from the header
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    card_scan<<<1, SCAN_THREADS, 0, st>>>(a);
+    const uint64_t tasks = uint64_t(L) * uint64_t(a.T) * 2u;
+    card_pack<<<card_grid(card_pack, tasks), CARD_THREADS, 0, st>>>(a);
+    card_zero_tails<<<L, CARD_THREADS, 0, st>>>(a);
+    count_launch(3);
+    return launch_status();
+}
+
+extern "C" int cachecard_unpack(const void *card, const kvp_card_header *hdr, void *const *k_dst, void *const *v_dst,
+                                void *stream) {
+    if (!card || !hdr || !k_dst || !v_dst) return KVP_ERR_ARG;
+    if (hdr->magic != CARD_MAGIC || hdr->version != CARD_VERSION || hdr->group_size != CARD_GROUP || hdr->dtype != 1)
+        return KVP_ERR_HEADER;
+    kvp_shape s = {hdr->n_layers, hdr->n_kv_heads, hdr->head_dim, hdr->seq_len};
+    int rc = shape_ok(&s);
+    if (rc != KVP_OK) return rc == KVP_ERR_ARG ? KVP_ERR_HEADER : rc;
+    if (hdr->error & (FLAG_BITS | FLAG_SIZE)) return KVP_ERR_HEADER;
+    if (hdr->off_offsets != card_off_offsets(s.n_tokens) || hdr->off_layers != card_off_layers(s.n_tokens) ||
+        hdr->off_bits != CARD_HEADER_BYTES || (hdr->layer_stride & 255u) != 0 ||
+        hdr->total_bytes != hdr->off_layers + uint64_t(s.n_layers) * hdr->layer_stride)
+        return KVP_ERR_HEADER;
+    if (!aligned(card, 256)) return KVP_ERR_ALIGN;
+    const int L = s.n_layers;
+    CardArgs a;
+    for (int l = 0; l < L; ++l) {
+        if (!k_dst[l] || !v_dst[l]) return KVP_ERR_ARG;
+        if (!aligned(k_dst[l], 16) || !aligned(v_dst[l], 16)) return KVP_ERR_ALIGN;
+        a.dst[0][l] = static_cast<uint4 *>(k_dst[l]);
+        a.dst[1][l] = static_cast<uint4 *>(v_dst[l]);
+    }
+    a.card = static_cast<uint8_t *>(const_cast<void *>(card));
+    a.bits_dev = nullptr;
+    a.card_bytes = hdr->total_bytes;
+    a.model_id = hdr->model_id;
+    a.pos_offset = hdr->pos_offset;
+    a.off_offsets = hdr->off_offsets;
+    a.off_layers = hdr->off_layers;
+    a.layer_stride = hdr->layer_stride;
+    a.L = L;
+    a.H = s.n_kv_heads;
+    a.T = s.n_tokens;
+    a.d = s.head_dim;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const uint64_t tasks = uint64_t(L) * uint64_t(a.T) * 2u;
+    card_unpack<<<card_grid(card_unpack, tasks), CARD_THREADS, 0, st>>>(a);
+    count_launch(1);
+    return launch_status();
+}

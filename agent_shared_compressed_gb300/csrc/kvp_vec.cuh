@@ -1,0 +1,98 @@
+// kvp_vec.cuh -- per-warp vector machinery shared by the pool encoder and
+// decoder: the register / warp-shuffle Walsh-Hadamard transform and the
+// 3-bit Lloyd-Max codebook.
+//
+// Lane mapping.  A value vector of d = 64 or 128 coordinates is held by
+// LPV = d/32 lanes, 32 coordinates per lane, as 4 chunks of 8 consecutive
+// coordinates: lane l of the vector holds chunks c = j*LPV + l (j = 0..3),
+// coordinate i = 8c + e (e = 0..7).  So coordinate bits 0-2 live in
+// registers (e), the next log2(LPV) bits in the lane index (l) and the top 2
+// bits in registers again (j); a warp holds 32/LPV vectors.  With this
+// mapping every 16-byte access of a warp instruction is part of a fully used
+// 32-byte sector (chunk j of the LPV lanes of a vector is contiguous).
+#pragma once
+
+#include "kvp_internal.cuh"
+
+namespace kvp {
+
+// Unnormalised Sylvester-order Walsh-Hadamard transform of the vector held
+// in x by the LPV lanes of each vector ("PolyKV" 2.B.2 rotation):
+// y_i = sum_j (-1)^popcount(i & j) x_j, one butterfly stage per index bit.
+template <int LPV>
+__device__ __forceinline__ void fwht(float (&x)[4][8], int lane) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+#pragma unroll
+        for (int h = 1; h < 8; h <<= 1) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if ((i & h) == 0) {
+                    const float p = x[j][i], q = x[j][i + h];
+                    x[j][i] = p + q;
+                    x[j][i + h] = p - q;
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int h = 1; h < 4; h <<= 1) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if ((j & h) == 0) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float p = x[j][i], q = x[j + h][i];
+                    x[j][i] = p + q;
+                    x[j + h][i] = p - q;
+                }
+            }
+        }
+    }
+    // Lane bits: the lane holding the lower index keeps p + q, the upper
+    // one p - q, i.e. new = partner + sgn * own with sgn = -1 on the upper.
+#pragma unroll
+    for (int m = 1; m < LPV; m <<= 1) {
+        const float sgn = (lane & m) ? -1.0f : 1.0f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float o = __shfl_xor_sync(0xffffffffu, x[j][i], m);
+                x[j][i] = fmaf(sgn, x[j][i], o);
+            }
+        }
+    }
+}
+
+// Lloyd-Max 8-level codebook for N(0,1) (+-0.2451, 0.7560, 1.3440, 2.1520)
+// and its decision thresholds (midpoints of adjacent centroids), positive
+// half.  Codes 0..7 index the centroids in ascending order.
+constexpr float THR1 = 0.50055f;  // (0.2451 + 0.7560) / 2
+constexpr float THR2 = 1.05f;     // (0.7560 + 1.3440) / 2
+constexpr float THR3 = 1.748f;    // (1.3440 + 2.1520) / 2
+
+// Code of a rotated coordinate y given the scaled thresholds T_k = t_k*||v||
+// (u = y/||v|| compared with t_k without a division): the number of
+// thresholds not above u.  For y >= 0 that is 4 + #{T_k <= |y|}; for y < 0
+// it is 3 - #{T_k < |y|}, taken here as 3 - #{T_k <= |y|} (the two differ
+// only when |y| equals a threshold exactly).
+__device__ __forceinline__ uint32_t v_code(float y, float T1, float T2, float T3) {
+    const float a = fabsf(y);
+    const uint32_t cnt = uint32_t(a >= T1) + uint32_t(a >= T2) + uint32_t(a >= T3);
+    return cnt ^ (y >= 0.0f ? 4u : 3u);
+}
+
+// Centroid of a code scaled by 10^4 -- the codebook's values are integers at
+// that scale (2451, 7560, 13440, 21520), so a Walsh-Hadamard transform of
+// them is exact in fp32 (|sum| <= 128 * 21520 < 2^24); the 10^-4 is folded
+// into the final rescale.
+__device__ __forceinline__ float centroid_e4(uint32_t code) {
+    const uint32_t up = code >> 2;                  // 1 for the positive half
+    const uint32_t rank = (code ^ (up - 1u)) & 3u;  // 0..3 by magnitude
+    const float m = (rank & 2u) ? ((rank & 1u) ? 21520.0f : 13440.0f)
+                                : ((rank & 1u) ? 7560.0f : 2451.0f);
+    return up ? m : -m;
+}
+
+}  // namespace kvp

@@ -1,0 +1,203 @@
+// kvpool_decode.cu -- fan-out decode of a SharedKVPool ("PolyKV" 2.A: each
+// PooledAgent receives the decompressed KV layer by layer in its own cache;
+// 2.B.2 dequantization: centroid lookup, inverse Walsh-Hadamard transform,
+// rescale).  The pool is read once per launch; every decoded tile is stored
+// to all agents' caches from registers, so HBM traffic is the pool plus
+// N x the bf16 cache -- the write side is the roofline.
+#include "kvp_vec.cuh"
+
+namespace kvp {
+
+constexpr int DEC_THREADS = 256;
+constexpr int DEC_WARPS = DEC_THREADS / 32;
+constexpr int DEC_MAX_PTRS = 1024;  // (agent, layer) destinations per launch
+
+struct DecodeArgs {
+    uint4 *kd[DEC_MAX_PTRS];  // index a * nl + r: agent a, layer lb + r
+    uint4 *vd[DEC_MAX_PTRS];
+    const uint8_t *pool;
+    PoolGeom geo;
+    int L, H, T, d;
+    int lb, nl, na;
+};
+
+// 8 int8 key codes -> 8 bf16 values q*s.  A code byte c is turned into the
+// float 2^23 + (c + 128) by byte permutation (exact), then offset and scaled.
+__device__ __forceinline__ uint4 k_decode8(uint2 raw, float s) {
+    const uint32_t a0 = raw.x ^ 0x80808080u, a1 = raw.y ^ 0x80808080u;
+    float f[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[i] = (__uint_as_float(__byte_perm(a0, 0x4B000000u, 0x7650u | i)) - 8388736.0f) * s;
+        f[4 + i] = (__uint_as_float(__byte_perm(a1, 0x4B000000u, 0x7650u | i)) - 8388736.0f) * s;
+    }
+    return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                      pack_bf16x2(f[6], f[7]));
+}
+
+template <int D>
+__global__ void __launch_bounds__(DEC_THREADS) decode_fanout(const __grid_constant__ DecodeArgs a) {
+    constexpr int LPV = D / 32;
+    constexpr int VPW = 32 / LPV;
+    constexpr int CPV = D / 8;
+    constexpr int CB = 3 * D / 8;
+    constexpr int KCH = VPW * D / 8 / 32;  // 8-byte key chunks per lane per step (4)
+    // 1 / (sqrt(d) * 10^4): the orthonormal 1/sqrt(d) and the codebook's 10^4.
+    constexpr float KS = D == 128 ? 8.838834764831845e-6f : 1.25e-5f;
+    __shared__ __align__(16) uint8_t stage[DEC_WARPS][384 + 16];
+
+    const uint32_t *hdr = reinterpret_cast<const uint32_t *>(a.pool);
+    if (hdr[0] != POOL_MAGIC || hdr[1] != POOL_VERSION) return;
+    if (hdr[2] != uint32_t(a.L) || hdr[3] != uint32_t(a.H) || hdr[4] != uint32_t(a.d) || hdr[5] != uint32_t(a.T)) {
+        if (blockIdx.x == 0 && threadIdx.x == 0)
+            atomicOr(const_cast<uint32_t *>(hdr) + POOL_ERR_WORD, FLAG_HEADER);
+        return;
+    }
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane / LPV, l = lane % LPV;
+    const uint64_t nvec = uint64_t(a.H) * uint64_t(a.T);
+    const uint64_t upl = (nvec + VPW - 1) / VPW;
+    const uint64_t total = upl * uint64_t(a.nl);
+    const float *scales = reinterpret_cast<const float *>(a.pool + a.geo.off_scales);
+
+    for (uint64_t u = uint64_t(blockIdx.x) * DEC_WARPS + warp; u < total; u += uint64_t(gridDim.x) * DEC_WARPS) {
+        const int r = int(u / upl);
+        const int layer = a.lb + r;
+        const uint64_t n0 = (u % upl) * VPW;
+        const uint32_t cnt = uint32_t(min(uint64_t(VPW), nvec - n0));
+        const uint8_t *lay = a.pool + a.geo.off_layers + uint64_t(layer) * a.geo.layer_stride;
+        const float s = scales[layer];
+
+        // keys: VPW*d int8 codes, 8 per lane-chunk
+        const uint2 *kc = reinterpret_cast<const uint2 *>(lay) + n0 * (D / 8);
+        const uint32_t kvalid = cnt * (D / 8);
+        uint4 kout[KCH];
+#pragma unroll
+        for (int it = 0; it < KCH; ++it) {
+            const uint32_t k = uint32_t(it) * 32u + uint32_t(lane);
+            kout[it] = k < kvalid ? k_decode8(ld_stream_v2(kc + k), s) : make_uint4(0, 0, 0, 0);
+        }
+
+        // values: stage the step's 384 code bytes, then each lane takes the
+        // 24-bit words of its 4 chunks
+        {
+            const uint32_t bytes = cnt * CB;
+            const uint32_t off = uint32_t(lane) * 16u;
+            const uint8_t *src = lay + a.geo.sec_v + n0 * CB;
+            if (off + 16u <= bytes)
+                *reinterpret_cast<uint4 *>(stage[warp] + off) = ld_stream_v4(src + off);
+            else if (off < bytes)
+                *reinterpret_cast<uint2 *>(stage[warp] + off) = ld_stream_v2(src + off);
+        }
+        const uint64_t n = n0 + g;
+        const bool valid = n < nvec;
+        const uint16_t sh = valid ? reinterpret_cast<const uint16_t *>(lay + a.geo.sec_sigma)[n] : uint16_t(0);
+        __syncwarp();
+        float x[4][8];
+        const uint32_t *st32 = reinterpret_cast<const uint32_t *>(stage[warp]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t o = uint32_t(g * CB + 3 * (j * LPV + l));
+            const uint32_t w = __funnelshift_r(st32[o >> 2], st32[(o >> 2) + 1], (o & 3u) * 8u);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[j][e] = centroid_e4((w >> (3 * e)) & 7u);
+        }
+        __syncwarp();
+        fwht<LPV>(x, lane);
+        const float f = __half2float(__ushort_as_half(sh)) * KS;
+        uint4 vout[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            vout[j] = make_uint4(pack_bf16x2(x[j][0] * f, x[j][1] * f), pack_bf16x2(x[j][2] * f, x[j][3] * f),
+                                 pack_bf16x2(x[j][4] * f, x[j][5] * f), pack_bf16x2(x[j][6] * f, x[j][7] * f));
+
+        // fan out: the same registers to every agent's cache
+        for (int ag = 0; ag < a.na; ++ag) {
+            uint4 *kd = a.kd[ag * a.nl + r] + n0 * (D / 8);
+#pragma unroll
+            for (int it = 0; it < KCH; ++it) {
+                const uint32_t k = uint32_t(it) * 32u + uint32_t(lane);
+                if (k < kvalid) st_stream_v4(kd + k, kout[it]);
+            }
+            if (valid) {
+                uint4 *vd = a.vd[ag * a.nl + r] + n * CPV;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) st_stream_v4(vd + j * LPV + l, vout[j]);
+            }
+        }
+    }
+}
+
+template <int D>
+static int decode_grid(uint64_t total_units) {
+    static int occ[2] = {0, 0};
+    int &o = occ[D == 128 ? 1 : 0];
+    if (o == 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, decode_fanout<D>, DEC_THREADS, 0) != cudaSuccess || o < 1)
+            o = 1;
+    }
+    const uint64_t want = (total_units + DEC_WARPS - 1) / DEC_WARPS;
+    const uint64_t cap = uint64_t(sm_count()) * uint64_t(o);
+    return int(want < cap ? (want < 1 ? 1 : want) : cap);
+}
+
+}  // namespace kvp
+
+using namespace kvp;
+
+extern "C" int kvpool_decode_into(const void *pool, const kvp_shape *s, int lb, int le, int na,
+                                  void *const *k_dst, void *const *v_dst, void *stream) {
+    int rc = shape_ok(s);
+    if (rc != KVP_OK) return rc;
+    if (!pool || !k_dst || !v_dst) return KVP_ERR_ARG;
+    const int L = s->n_layers;
+    if (lb < 0 || le > L || lb >= le || na < 1) return KVP_ERR_ARG;
+    if (!aligned(pool, 256)) return KVP_ERR_ALIGN;
+    for (int ag = 0; ag < na; ++ag)
+        for (int l = lb; l < le; ++l) {
+            const void *kp = k_dst[size_t(ag) * L + l], *vp = v_dst[size_t(ag) * L + l];
+            if (!kp || !vp) return KVP_ERR_ARG;
+            if (!aligned(kp, 16) || !aligned(vp, 16)) return KVP_ERR_ALIGN;
+        }
+
+    DecodeArgs a;
+    a.pool = static_cast<const uint8_t *>(pool);
+    a.geo = pool_geom(L, s->n_kv_heads, s->head_dim, s->n_tokens);
+    a.L = L;
+    a.H = s->n_kv_heads;
+    a.T = s->n_tokens;
+    a.d = s->head_dim;
+    const uint64_t nvec = uint64_t(a.H) * uint64_t(a.T);
+    const int vpw = a.d == 128 ? 8 : 16;
+    const uint64_t upl = (nvec + vpw - 1) / vpw;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    // Split (agent, layer) destinations into launches of at most
+    // DEC_MAX_PTRS pointers each (one launch for every shape in practice).
+    const int ac = na < DEC_MAX_PTRS ? na : DEC_MAX_PTRS;
+    const int lc_max = DEC_MAX_PTRS / ac;
+    int launches = 0;
+    for (int a0 = 0; a0 < na; a0 += ac) {
+        const int nag = (na - a0) < ac ? (na - a0) : ac;
+        for (int l0 = lb; l0 < le; l0 += lc_max) {
+            const int nl = (le - l0) < lc_max ? (le - l0) : lc_max;
+            a.lb = l0;
+            a.nl = nl;
+            a.na = nag;
+            for (int ag = 0; ag < nag; ++ag)
+                for (int r = 0; r < nl; ++r) {
+                    a.kd[ag * nl + r] = static_cast<uint4 *>(k_dst[size_t(a0 + ag) * L + l0 + r]);
+                    a.vd[ag * nl + r] = static_cast<uint4 *>(v_dst[size_t(a0 + ag) * L + l0 + r]);
+                }
+            const uint64_t units = upl * uint64_t(nl);
+            if (a.d == 128)
+                decode_fanout<128><<<decode_grid<128>(units), DEC_THREADS, 0, st>>>(a);
+            else
+                decode_fanout<64><<<decode_grid<64>(units), DEC_THREADS, 0, st>>>(a);
+            ++launches;
+        }
+    }
+    count_launch(launches);
+    return launch_status();
+}

@@ -1,0 +1,461 @@
+"""Benchmark of the GB300 KV codec: one step = the whole hot path on one
+batch of synthetic KV cache --
+  1. kvpool_encode      (int8 K per-tensor scale; V FWHT + Lloyd-Max 3 bit)
+  2. kvpool_decode_into (fan-out of every layer into N agent caches)
+  3. cachecard_pack     (per-token {2,4,8,16}-bit groups + metadata)
+  4. cachecard_unpack   (back to bf16 past_key_values)
+Metric: bf16-equivalent GB/s of the step (bytes of bf16 KV consumed or
+produced: encode raw + decode N*raw + pack raw + unpack raw) and its
+fraction of the GB300 HBM roofline.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                       [--workload NAME] [--agents N] [--tokens T] [--layers L]
+Under torchrun (N > 1) every rank runs its own replica (independent pools:
+weak scaling, no collective on the data path); rank 0 prints one JSON line.
+"""
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import agent_shared_compressed_gb300 as kv  # noqa: E402
+from agent_shared_compressed_gb300 import synth  # noqa: E402
+
+METRIC = "KV codec encode/decode GB/s (bf16-equivalent) and % of GB300 HBM peak"
+DEFAULT_WORKLOAD = "llama3-8b-4k-15agents"
+L2_BYTES = 129 * 1024 * 1024
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+DECODE_SOURCES = ["agent_shared_compressed_gb300/csrc/kvpool_decode.cu",
+                  "agent_shared_compressed_gb300/csrc/kvp_vec.cuh",
+                  "agent_shared_compressed_gb300/csrc/kvp_internal.cuh"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_fanout_traffic.json")
+
+
+# ----------------------------------------------------------------------------
+# environment helpers
+# ----------------------------------------------------------------------------
+
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_hash(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload, agents, tokens, layers):
+    """DRAM bytes per decode launch from a committed ncu summary, if it was
+    taken on the current decode kernel source (else None)."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    if rec.get("source_hash") != source_hash(DECODE_SOURCES):
+        return None
+    per_unit = rec.get("dram_bytes_per_output_byte")
+    if per_unit is None:
+        return None
+    return per_unit
+
+
+class ClockSampler:
+    """Samples SM clock and clock-event reasons through NVML (driver library,
+    read-only queries) on a background thread."""
+    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+               0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
+
+    def __init__(self, index, period=0.005):
+        self.period = period
+        self.samples = []
+        self.reasons = 0
+        self.max_mhz = None
+        self.ok = False
+        try:
+            self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nvml.nvmlInit_v2() != 0:
+                return
+            self.h = ctypes.c_void_p()
+            if self.nvml.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.h)) != 0:
+                return
+            m = ctypes.c_uint()
+            if self.nvml.nvmlDeviceGetMaxClockInfo(self.h, ctypes.c_int(1), ctypes.byref(m)) == 0:
+                self.max_mhz = m.value
+            self.ok = True
+        except OSError:
+            self.ok = False
+
+    def _run(self):
+        clk = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        fn = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self.stop.is_set():
+            if self.nvml.nvmlDeviceGetClockInfo(self.h, ctypes.c_int(1), ctypes.byref(clk)) == 0:
+                self.samples.append(clk.value)
+            if fn(self.h, ctypes.byref(rs)) == 0:
+                self.reasons |= rs.value
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.ok:
+            self.stop = threading.Event()
+            self.t = threading.Thread(target=self._run, daemon=True)
+            self.t.start()
+        return self
+
+    def __exit__(self, *a):
+        if self.ok:
+            self.stop.set()
+            self.t.join()
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unavailable"]}
+        return {"sm_mhz": float(statistics.median(self.samples)), "sm_max_mhz": self.max_mhz,
+                "reasons": [n for b, n in sorted(self.REASONS.items()) if self.reasons & b],
+                "samples": len(self.samples)}
+
+
+# ----------------------------------------------------------------------------
+# workload
+# ----------------------------------------------------------------------------
+
+def workload(args):
+    w = dict(synth.WORKLOADS[args.workload])
+    if args.agents:
+        w["N"] = args.agents
+    if args.tokens:
+        w["T"] = args.tokens
+    if args.layers:
+        w["L"] = args.layers
+    return w
+
+
+def step_bytes(w, pool_bytes, card_bytes):
+    raw = 2 * w["L"] * w["H"] * w["T"] * w["d"] * 2
+    return {
+        "raw": raw,
+        "bf16_equiv": raw * (w["N"] + 3),
+        "encode_alg": raw + pool_bytes,
+        "decode_alg": pool_bytes + w["N"] * raw,
+        "pack_alg": raw + card_bytes,
+        "unpack_alg": card_bytes + raw,
+    }
+
+
+class Codec:
+    """Device buffers for one replica of the step and the calls that run it."""
+
+    def __init__(self, w, device, seed=0):
+        L, H, d, T, N = w["L"], w["H"], w["d"], w["T"], w["N"]
+        self.w = w
+        self.shape = kv.Shape(L, H, d, T)
+        self.k, self.v = synth.kv_layers(L, H, T, d, seed=seed, device=device)
+        self.bits_host = synth.card_bits(T, seed=seed).numpy()
+        self.bits = torch.from_numpy(self.bits_host).to(device)
+        self.pool_bytes = kv.kvpool_pool_bytes(self.shape)
+        self.ws_bytes = kv.kvpool_workspace_bytes(self.shape)
+        self.card_bytes = kv.cachecard_bytes(self.shape, self.bits_host)
+        self.pool = torch.empty(self.pool_bytes, dtype=torch.uint8, device=device)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
+        self.card = torch.empty(self.card_bytes, dtype=torch.uint8, device=device)
+        self.caches_k = [torch.empty((H, T, d), dtype=torch.bfloat16, device=device) for _ in range(N * L)]
+        self.caches_v = [torch.empty((H, T, d), dtype=torch.bfloat16, device=device) for _ in range(N * L)]
+        self.out_k = [torch.empty((H, T, d), dtype=torch.bfloat16, device=device) for _ in range(L)]
+        self.out_v = [torch.empty((H, T, d), dtype=torch.bfloat16, device=device) for _ in range(L)]
+        self.hdr = None
+
+    def encode(self, st):
+        kv.check(kv.kvpool_encode(self.shape, self.k, self.v, self.pool, self.pool_bytes, self.ws,
+                                  self.ws_bytes, st), "encode")
+
+    def decode(self, st):
+        kv.check(kv.kvpool_decode_into(self.pool, self.shape, 0, self.w["L"], self.w["N"], self.caches_k,
+                                       self.caches_v, st), "decode")
+
+    def pack(self, st):
+        kv.check(kv.cachecard_pack(self.shape, 0x8B, 0, self.bits, self.k, self.v, self.card, self.card_bytes,
+                                   st), "pack")
+
+    def unpack(self, st):
+        if self.hdr is None:
+            self.hdr = kv.CardHeader()
+            kv.check(kv.cachecard_read_header(self.card, self.hdr, st), "read_header")
+        kv.check(kv.cachecard_unpack(self.card, self.hdr, self.out_k, self.out_v, st), "unpack")
+
+
+# ----------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------
+
+def run_ours(args, rank, world, local_rank):
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    kv.load()
+    w = workload(args)
+    c = Codec(w, device, seed=rank)
+    st = torch.cuda.current_stream(device)
+    sb = step_bytes(w, c.pool_bytes, c.card_bytes)
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=device) if sb["raw"] < 4 * L2_BYTES else None
+
+    # warm-up (also reads the card header once: the unpack's host metadata)
+    for _ in range(args.warmup):
+        c.encode(st); c.decode(st); c.pack(st); c.unpack(st)
+    torch.cuda.synchronize(device)
+    for rc, what in ((kv.kvpool_status(c.pool, st), "pool"), (kv.cachecard_status(c.card, st), "card")):
+        if rc != kv.KVP_OK:
+            raise RuntimeError("%s status after warm-up: %s" % (what, kv.kvp_strerror(rc)))
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(device)
+    launches0 = kv.kvp_launch_count()
+    sampler = ClockSampler(local_rank)
+    with sampler:
+        for i in range(args.steps):
+            if flush is not None:
+                flush.zero_()
+            e = ev[i]
+            e[0].record(st)
+            c.encode(st)
+            e[1].record(st)
+            c.decode(st)
+            e[2].record(st)
+            c.pack(st)
+            e[3].record(st)
+            c.unpack(st)
+            e[4].record(st)
+        torch.cuda.synchronize(device)
+    launches = kv.kvp_launch_count() - launches0
+    if world > 1:
+        torch.distributed.barrier()
+    phase = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(4)] for e in ev])  # ms
+    step_ms = phase.sum(1)
+    total_ms = float(step_ms.sum())
+    if world > 1:
+        t = torch.tensor([total_ms], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * sb["bf16_equiv"] / (ms_per_step * 1e-3) / 1e9
+
+    # end to end through the C ABI with host buffers: H2D of the step's K/V
+    # (and bitwidths) from pinned memory, the four calls, D2H of the pool and
+    # the card (the two shareable artefacts) and their status words.
+    e2e = run_e2e(c, st, device, args, sb)
+
+    peak, peak_kind = hbm_peak()
+    dec_ms = float(phase[:, 1].mean())
+    achieved = sb["decode_alg"] / (dec_ms * 1e-3) / 1e9
+    per_unit = recorded_traffic(args.workload, w["N"], w["T"], w["L"])
+    traffic = None if per_unit is None else int(per_unit * (w["N"] * sb["raw"]))
+    names = ("encode", "decode", "pack", "unpack")
+    algs = (sb["encode_alg"], sb["decode_alg"], sb["pack_alg"], sb["unpack_alg"])
+    breakdown = {}
+    for j, (n, b) in enumerate(zip(names, algs)):
+        ms = float(phase[:, j].mean())
+        breakdown[n] = {"ms": round(ms, 4), "alg_bytes": int(b), "alg_GBps": round(b / (ms * 1e-3) / 1e9, 1),
+                        "frac_of_measured_peak": round(b / (ms * 1e-3) / 1e9 / peak, 4),
+                        "frac_of_8TBps": round(b / (ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 4)}
+    breakdown["encode"]["implemented_bytes"] = int(sb["encode_alg"] + sb["raw"] // 2)  # K is read twice
+
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "io_dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "layers": w["L"], "kv_heads": w["H"], "head_dim": w["d"],
+                   "tokens": w["T"], "agents": w["N"],
+                   "card_bits": "iid {2,4,8,16} p={.25,.40,.25,.10}",
+                   "l2": ("flushed between steps (2x L2 write)" if flush is not None
+                          else "inputs larger than L2 (%d MB K/V per step)" % (sb["raw"] // 10 ** 6)),
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "roofline": {"kernel": "decode_fanout", "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "frac_nominal_8000": round(achieved / NOMINAL_HBM_GBS, 4),
+                     "alg_bytes_per_launch": int(sb["decode_alg"]), "traffic": traffic},
+        "e2e": e2e,
+        "gpu_launches": int(launches),
+        "clocks": sampler.summary(),
+        "breakdown": breakdown,
+    }
+    return out, c, sb
+
+
+def run_e2e(c, st, device, args, sb):
+    L = c.w["L"]
+    hk = [t.cpu().pin_memory() for t in c.k]
+    hv = [t.cpu().pin_memory() for t in c.v]
+    hbits = torch.from_numpy(c.bits_host).pin_memory()
+    hpool = torch.empty(c.pool_bytes, dtype=torch.uint8).pin_memory()
+    hcard = torch.empty(c.card_bytes, dtype=torch.uint8).pin_memory()
+    steps = max(1, min(args.steps, 20))
+
+    def one():
+        for i in range(L):
+            c.k[i].copy_(hk[i], non_blocking=True)
+            c.v[i].copy_(hv[i], non_blocking=True)
+        c.bits.copy_(hbits, non_blocking=True)
+        c.encode(st); c.decode(st); c.pack(st); c.unpack(st)
+        hpool.copy_(c.pool, non_blocking=True)
+        hcard.copy_(c.card, non_blocking=True)
+    one()
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(steps):
+        one()
+    e1.record(st)
+    torch.cuda.synchronize(device)
+    ms = e0.elapsed_time(e1) / steps
+    if kv.kvpool_status(c.pool, st) != kv.KVP_OK or kv.cachecard_status(c.card, st) != kv.KVP_OK:
+        raise RuntimeError("e2e status")
+    return {"value": round(sb["bf16_equiv"] / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "ms_per_step": round(ms, 4), "steps": steps,
+            "h2d_bytes_per_step": int(sb["raw"] + c.bits_host.size),
+            "d2h_bytes_per_step": int(c.pool_bytes + c.card_bytes)}
+
+
+# ----------------------------------------------------------------------------
+# the fp64 oracle on the host: CPU baseline and reference arm
+# ----------------------------------------------------------------------------
+
+def oracle_step(layers_k, layers_v, bits, n_agents):
+    """The whole step on the oracle for the given layers; returns seconds."""
+    import oracle as O
+    t0 = time.perf_counter()
+    pool, _, _ = O.pool_encode(layers_k, layers_v)
+    O.pool_decode_into(pool, 0, len(layers_k), n_agents)
+    card, _, _ = O.card_pack(layers_k, layers_v, bits)
+    O.card_unpack(card)
+    return time.perf_counter() - t0
+
+
+def oracle_sample(w, seed, budget_s, layer_fn):
+    """Time the oracle on the first n layers of the workload, n grown until
+    about budget_s of CPU work (and at most 4 GB of decoded agent caches on
+    the host); layer_fn(i) gives layer i's (K, V) bf16 bits.  Returns
+    (GB/s, cores, description, seconds)."""
+    import oracle as O
+    L, H, d, T, N = w["L"], w["H"], w["d"], w["T"], w["N"]
+    bits = synth.card_bits(T, seed=seed).numpy()
+    k0, v0 = layer_fn(0)
+    t1 = oracle_step([k0], [v0], bits, N)
+    raw1 = 2 * H * T * d * 2
+    n_mem = max(1, int(4e9 // (N * raw1)))
+    n = int(max(1, min(L, n_mem, budget_s / max(t1, 1e-3))))
+    if n > 1:
+        ks, vs = [k0], [v0]
+        for i in range(1, n):
+            k, v = layer_fn(i)
+            ks.append(k)
+            vs.append(v)
+        t = oracle_step(ks, vs, bits, N)
+    else:
+        t = t1
+    gbs = raw1 * n * (N + 3) / t / 1e9
+    desc = "layers 0..%d of %d, all %d agents, whole step (encode, fan-out decode, card pack, unpack)" % (
+        n - 1, L, N)
+    return gbs, O.get_threads(), desc, t
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: each step is a bounded sample (one
+    layer of the workload) timed on the host cores."""
+    import oracle as O
+    w = workload(args)
+    H, d, T, N = w["H"], w["d"], w["T"], w["N"]
+    ks, vs = synth.kv_layers(1, H, T, d, seed=0, device="cpu")
+    k1, v1 = [synth.bits16(ks[0])], [synth.bits16(vs[0])]
+    bits = synth.card_bits(T, seed=0).numpy()
+    for _ in range(args.warmup):
+        oracle_step(k1, v1, bits, N)
+    secs = [oracle_step(k1, v1, bits, N) for _ in range(args.steps)]
+    raw1 = 2 * H * T * d * 2
+    tot = sum(secs)
+    value = raw1 * (N + 3) * args.steps / tot / 1e9
+    sample = "one layer of %d per step (L=%d H=%d d=%d T=%d), all %d agents" % (w["L"], w["L"], H, d, T, N)
+    return {
+        "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(1e3 * tot / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "io_dtype": "bf16", "data": "synthetic",
+        "impl": "reference",
+        "config": {"workload": args.workload, "layers": w["L"], "kv_heads": H, "head_dim": d, "tokens": T,
+                   "agents": N, "card_bits": "iid {2,4,8,16} p={.25,.40,.25,.10}", "l2": "host (CPU)",
+                   "parallelism": "single"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": O.get_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+# ----------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--agents", type=int, default=0)
+    ap.add_argument("--tokens", type=int, default=0)
+    ap.add_argument("--layers", type=int, default=0)
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return
+
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    out, c, sb = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        if args.no_cpu_baseline:
+            out["cpu_baseline"] = None
+        else:
+            gbs, cores, desc, secs = oracle_sample(
+                c.w, 0, args.cpu_budget, lambda i: (synth.bits16(c.k[i]), synth.bits16(c.v[i])))
+            out["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                                   "sample": desc, "seconds": round(secs, 2)}
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

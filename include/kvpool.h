@@ -1,0 +1,218 @@
+/*
+ * kvpool.h -- C ABI of the GB300 (sm_103a) KV-cache codec for multi-agent
+ * KV sharing.
+ *
+ * Two containers, both position-independent byte blobs in device memory:
+ *
+ *  SharedKVPool -- "PolyKV: A Shared Asymmetrically-Compressed KV Cache Pool
+ *    for Multi-Agent LLM Inference", 2.A (write once, read many; one object
+ *    whose size does not depend on the number of agents) and 2.B (keys int8
+ *    with one symmetric scale per layer tensor; values rotated by a fast
+ *    Walsh-Hadamard transform, normalised, mapped to the 8-level Lloyd-Max
+ *    codebook for N(0,1) and packed at 3 bits).
+ *
+ *  CacheCard -- "QKVShare: Quantized KV-Cache Handoff for Multi-Agent
+ *    On-Device LLMs", Methodology 1-3 (per-token bitwidth from {2,4,8,16},
+ *    quantized KV groups plus metadata seq_len / model_id / position offset;
+ *    the receiver rebuilds 16-bit past_key_values from it).
+ *
+ * Conventions shared by every entry point
+ * ----------------------------------------
+ *  - KV tensors are bf16, one tensor per layer, layout [H][T][d] contiguous
+ *    (the Hugging Face past_key_values layout at batch 1).  head_dim d must
+ *    be 64 or 128.
+ *  - Arrays of per-layer tensor pointers (k_layers, k_dst, ...) are HOST
+ *    arrays of DEVICE pointers; the library reads them during the call only
+ *    (they are copied into the kernel launch), so the caller may reuse them
+ *    as soon as the call returns.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Every compute call only enqueues work on that stream and
+ *    returns; it never allocates, frees or synchronises device memory.  The
+ *    only synchronising calls are kvpool_status, cachecard_status and
+ *    cachecard_read_header, which say so.
+ *  - The caller owns every buffer.  Device pointers to KV tensors must be
+ *    16-byte aligned; pool and card buffers 256-byte aligned; workspaces
+ *    16-byte aligned.
+ *  - Errors: 0 is success, negative values are KVP_ERR_*.  Everything the
+ *    host can check (null pointers, shapes, alignment, buffer sizes) is
+ *    checked before any work is enqueued, and nothing is enqueued on error.
+ *    Conditions only the device can see (non-finite input, a value whose
+ *    fp16 scale overflows, an invalid bitwidth in device memory) are
+ *    recorded in an error word inside the pool / card header and returned
+ *    by the *_status calls.  No kernel traps, asserts or waits on another
+ *    block.
+ */
+#ifndef KVPOOL_H
+#define KVPOOL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+#define KVP_OK 0
+#define KVP_ERR_ARG (-1)            /* null pointer, bad count or range      */
+#define KVP_ERR_UNSUPPORTED_D (-2)  /* head_dim other than 64 or 128         */
+#define KVP_ERR_ALIGN (-3)          /* pointer not aligned as required       */
+#define KVP_ERR_SIZE (-4)           /* buffer too small / shape too large    */
+#define KVP_ERR_CUDA (-5)           /* a CUDA call or kernel launch failed   */
+#define KVP_ERR_NONFINITE (-6)      /* input held Inf or NaN                 */
+#define KVP_ERR_RANGE (-7)          /* a scale or zero point overflowed fp16 */
+#define KVP_ERR_BITS (-8)           /* CacheCard bitwidth not in {2,4,8,16}  */
+#define KVP_ERR_HEADER (-9)         /* not a pool / card, or shape mismatch  */
+
+/* Largest layer count one call accepts. */
+#define KVP_MAX_LAYERS 512
+
+/* Shape of one KV cache: n_layers tensors of [n_kv_heads][n_tokens][head_dim]. */
+typedef struct kvp_shape {
+    int32_t n_layers;
+    int32_t n_kv_heads;
+    int32_t head_dim;
+    int32_t n_tokens;
+} kvp_shape;
+
+/* CacheCard header, byte-for-byte the first 128 bytes of a card. */
+typedef struct kvp_card_header {
+    uint32_t magic;         /* 0x4343564B, bytes "KVCC"                        */
+    uint32_t version;       /* 1                                              */
+    int32_t seq_len;        /* T                                              */
+    int32_t n_layers;       /* L                                              */
+    int32_t n_kv_heads;     /* H                                              */
+    int32_t head_dim;       /* d                                              */
+    int32_t group_size;     /* 32                                             */
+    int32_t dtype;          /* 1 = bf16                                       */
+    uint64_t model_id;      /* opaque id of the model that produced the cache */
+    int64_t pos_offset;     /* position of token 0 in the sender's sequence   */
+    uint64_t off_bits;      /* byte offset of uint8 bits[T]                    */
+    uint64_t off_offsets;   /* byte offset of uint32 off[T] (record offsets)   */
+    uint64_t off_layers;    /* byte offset of layer 0's records                */
+    uint64_t layer_stride;  /* bytes per layer                                 */
+    uint64_t total_bytes;   /* bytes of the whole card                         */
+    uint32_t error;         /* device-detected error bits                      */
+    uint32_t reserved[9];
+} kvp_card_header;
+
+/* ---------------------------------------------------------------------- */
+/* SharedKVPool                                                            */
+/* ---------------------------------------------------------------------- */
+
+/* Exact byte size of the pool for this shape, or 0 for an invalid shape.
+ * Independent of how many agents will read it ("PolyKV" 2.A).
+ * Pool layout (every section 256-byte aligned): 256-byte header (magic
+ * "KVPL", version 1, L, H, d, T, error word, section offsets), fp32 K scale
+ * per layer, then per layer: int8 K codes [H][T][d], 3-bit V codes
+ * [H][T][3d/8] (8 codes c_0..c_7 = the 24-bit little-endian word
+ * sum c_j << 3j), fp16 sigma [H][T]. */
+size_t kvpool_pool_bytes(const kvp_shape *shape);
+
+/* Bytes of device workspace kvpool_encode needs for this shape (0 for an
+ * invalid shape).  The workspace holds per-block partial maxima and
+ * per-layer quantization parameters; its contents need no initialisation
+ * and are dead after the encode's kernels finish. */
+size_t kvpool_workspace_bytes(const kvp_shape *shape);
+
+/* Encode a whole KV cache into a pool ("PolyKV" 2.B).
+ *  k_layers, v_layers: host arrays of n_layers device pointers, each a bf16
+ *    [H][T][d] tensor (16-byte aligned).
+ *  Keys: per layer, s = max|k| / 127 rounded once to fp32; code = the
+ *    integer nearest to the exact k/s (ties to even), in [-127,127]; s = 0
+ *    gives all-zero codes.
+ *  Values: per (token, head) vector v, y = H_d v (Sylvester-order
+ *    Walsh-Hadamard), sigma = ||v||/sqrt(d) stored as fp16, u = y/||v||, and
+ *    code = number of Lloyd-Max thresholds (midpoints of
+ *    +-0.2451/0.7560/1.3440/2.1520) not above u; a zero vector codes as 4.
+ *  pool: pool_bytes >= kvpool_pool_bytes(shape), 256-byte aligned; fully
+ *    overwritten.  ws: ws_bytes >= kvpool_workspace_bytes(shape).
+ * Non-finite input or a sigma above the fp16 range is reported by
+ * kvpool_status (the affected codes are then unspecified). */
+int kvpool_encode(const kvp_shape *shape, const void *const *k_layers,
+                  const void *const *v_layers, void *pool, size_t pool_bytes,
+                  void *ws, size_t ws_bytes, void *stream);
+
+/* Fan-out decode ("PolyKV" 2.A PooledAgent, 2.B.2 dequantization): read
+ * layers [layer_begin, layer_end) of the pool once and write the decoded
+ * bf16 K and V into each of n_agents caches.
+ *  K: bf16(q * s_l).  V: bf16(sigma_h * (H_d c) / sqrt(d)) with c the
+ *    centroids of the codes (the orthonormal transform is its own inverse).
+ *  shape must equal the shape the pool was encoded with.
+ *  k_dst, v_dst: host arrays of n_agents * n_layers device pointers,
+ *    agent-major (entry a * n_layers + l is agent a's layer l, a bf16
+ *    [H][T][d] tensor, 16-byte aligned).  Only entries of layers in the
+ *    range are read; the others may be NULL.
+ * The pool is only read, so decodes of one pool may run concurrently on
+ * several streams.  A pool whose header does not match `shape` is left
+ * undecoded and kvpool_status reports KVP_ERR_HEADER. */
+int kvpool_decode_into(const void *pool, const kvp_shape *shape, int layer_begin,
+                       int layer_end, int n_agents, void *const *k_dst,
+                       void *const *v_dst, void *stream);
+
+/* Synchronises `stream`, then returns KVP_OK or the first device-detected
+ * error recorded in the pool's header (KVP_ERR_HEADER if `pool` does not
+ * hold a version-1 pool). */
+int kvpool_status(const void *pool, void *stream);
+
+/* ---------------------------------------------------------------------- */
+/* CacheCard                                                               */
+/* ---------------------------------------------------------------------- */
+
+/* Exact byte size of a card for these per-token bitwidths (host array of
+ * n_tokens values), or 0 if the shape or any bitwidth is invalid.
+ * Card layout: 128-byte header (kvp_card_header), uint8 bits[T], uint32
+ * off[T] (16-byte aligned; exclusive prefix sum of record sizes), then
+ * n_layers layers of layer_stride bytes (256-byte aligned).  A token's
+ * record in one layer, b in {2,4,8}: K codes [H][d] then V codes [H][d] at b
+ * bits (each group of 32 coordinates a little-endian bit string, code j at
+ * bits j*b..j*b+b-1), then K (fp16 scale, fp16 zero) [H][d/32], then V
+ * (scale, zero) [H][d/32]; b = 16: K then V verbatim.  Records are padded to
+ * 16 bytes. */
+size_t cachecard_bytes(const kvp_shape *shape, const uint8_t *bits_host);
+
+/* Pack a CacheCard ("QKVShare" Methodology 1-2).
+ *  bits_dev: device array of n_tokens bitwidths in {2,4,8,16}.
+ *  For b < 16, per group of 32 coordinates of one (layer, token, K|V, head):
+ *    s_h = fp16((max-min)/(2^b-1)), z_h = fp16(min), code =
+ *    clamp(nearest integer to (x - z_h)/s_h, 0, 2^b-1) (0 when s_h = 0).
+ *    b = 16 copies the bf16 values.
+ *  card: card_bytes bytes, 256-byte aligned; must hold cachecard_bytes()
+ *    for these bits, otherwise nothing but the header is written and
+ *    cachecard_status reports KVP_ERR_SIZE (KVP_ERR_BITS for an invalid
+ *    bitwidth). */
+int cachecard_pack(const kvp_shape *shape, uint64_t model_id, int64_t pos_offset,
+                   const uint8_t *bits_dev, const void *const *k_layers,
+                   const void *const *v_layers, void *card, size_t card_bytes,
+                   void *stream);
+
+/* Copy the card's 128-byte header to *out (synchronises `stream`).  Returns
+ * KVP_ERR_HEADER if the magic or version is wrong. */
+int cachecard_read_header(const void *card, kvp_card_header *out, void *stream);
+
+/* Receiver injection ("QKVShare" Methodology 3): rebuild every layer's bf16
+ * K and V ([H][T][d]) from the card: x = bf16(q * s_h + z_h), 16-bit tokens
+ * verbatim.  hdr is the header read by cachecard_read_header.  k_dst, v_dst:
+ * host arrays of n_layers device pointers (16-byte aligned). */
+int cachecard_unpack(const void *card, const kvp_card_header *hdr,
+                     void *const *k_dst, void *const *v_dst, void *stream);
+
+/* Synchronises `stream`, then returns KVP_OK or the first device-detected
+ * error recorded in the card's header. */
+int cachecard_status(const void *card, void *stream);
+
+/* ---------------------------------------------------------------------- */
+/* Diagnostics                                                             */
+/* ---------------------------------------------------------------------- */
+
+/* Static, human-readable text for a status code. */
+const char *kvp_strerror(int status);
+
+/* Number of kernels this library has launched in this process. */
+uint64_t kvp_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVPOOL_H */

@@ -1,0 +1,121 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads and
+exports every function include/kvpool.h declares; host-computed sizes agree
+with the oracle's byte formats; every error the host can detect is returned
+before any work is enqueued (each call below fails validation, so nothing
+reaches the device even on a GPU machine)."""
+import ctypes as C
+
+import numpy as np
+import pytest
+
+import agent_shared_compressed_gb300 as kv
+from agent_shared_compressed_gb300 import build as kvbuild
+import oracle as O
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    kvbuild.build()
+    kv.load()
+
+
+def test_exports_every_declared_function():
+    names = kv.declared_functions()
+    assert set(names) >= {"kvpool_pool_bytes", "kvpool_workspace_bytes", "kvpool_encode", "kvpool_decode_into",
+                          "kvpool_status", "cachecard_bytes", "cachecard_pack", "cachecard_read_header",
+                          "cachecard_unpack", "cachecard_status", "kvp_strerror", "kvp_launch_count"}
+    lib = C.CDLL(kv.binding.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+SHAPES = [(1, 8, 128, 512), (24, 32, 64, 1851), (32, 8, 128, 4096), (32, 8, 128, 32768),
+          (3, 5, 64, 37), (1, 1, 64, 1), (2, 3, 128, 7), (512, 1, 64, 3)]
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+def test_pool_bytes_match_oracle_format(shape):
+    L, H, d, T = shape
+    assert kv.kvpool_pool_bytes((L, H, d, T)) == O.pool_bytes(L, H, d, T)
+    assert kv.kvpool_workspace_bytes((L, H, d, T)) > 0
+
+
+def test_pool_bytes_of_the_named_configurations():
+    # per layer: K H*T*d + V H*T*3d/8 + sigma 2*H*T, each section 256-aligned
+    assert kv.kvpool_pool_bytes((1, 8, 128, 512)) == 512 + 729088
+    assert kv.kvpool_pool_bytes((32, 8, 128, 4096)) - 512 == 186646528
+    # payload bytes independent of agents; achieved ratio 2.8764 at d=128
+    assert abs(2 * 32 * 8 * 4096 * 128 * 2 / (kv.kvpool_pool_bytes((32, 8, 128, 4096)) - 512) - 2.8764) < 1e-4
+
+
+@pytest.mark.parametrize("shape", [(3, 5, 64, 37), (32, 8, 128, 8192), (2, 1, 64, 1), (4, 3, 128, 100)])
+def test_card_bytes_match_oracle_format(shape):
+    L, H, d, T = shape
+    rng = np.random.default_rng(T)
+    bits = rng.choice(np.array([2, 4, 8, 16], np.uint8), T, p=[0.25, 0.4, 0.25, 0.1])
+    assert kv.cachecard_bytes((L, H, d, T), bits) == O.card_bytes(L, H, d, T, bits)
+    bad = bits.copy()
+    bad[-1] = 6
+    assert kv.cachecard_bytes((L, H, d, T), bad) == 0
+
+
+@pytest.mark.parametrize("shape,code", [((0, 8, 128, 16), kv.KVP_ERR_ARG), ((1, 0, 128, 16), kv.KVP_ERR_ARG),
+                                        ((1, 8, 96, 16), kv.KVP_ERR_UNSUPPORTED_D),
+                                        ((1, 8, 128, 0), kv.KVP_ERR_ARG), ((513, 8, 128, 16), kv.KVP_ERR_SIZE)])
+def test_invalid_shapes(shape, code):
+    assert kv.kvpool_pool_bytes(shape) == 0
+    assert kv.kvpool_workspace_bytes(shape) == 0
+    assert kv.kvpool_encode(shape, [0x1000], [0x1000], 0x1000, 1 << 30, 0x1000, 1 << 20) == code
+    assert kv.kvpool_decode_into(0x1000, shape, 0, 1, 1, [0x1000], [0x1000]) == code
+    assert kv.cachecard_pack(shape, 0, 0, 0x1000, [0x1000], [0x1000], 0x1000, 1 << 30) == code
+
+
+def test_encode_argument_errors():
+    s = (2, 8, 128, 64)
+    pb, wb = kv.kvpool_pool_bytes(s), kv.kvpool_workspace_bytes(s)
+    ok = 0x10000
+    assert kv.kvpool_encode(s, [ok, None], [ok, ok], ok, pb, ok, wb) == kv.KVP_ERR_ARG
+    assert kv.kvpool_encode(s, [ok, ok], [ok, ok], None, pb, ok, wb) == kv.KVP_ERR_ARG
+    assert kv.kvpool_encode(s, [ok, ok + 8], [ok, ok], ok, pb, ok, wb) == kv.KVP_ERR_ALIGN
+    assert kv.kvpool_encode(s, [ok, ok], [ok, ok], ok + 16, pb, ok, wb) == kv.KVP_ERR_ALIGN
+    assert kv.kvpool_encode(s, [ok, ok], [ok, ok], ok, pb - 1, ok, wb) == kv.KVP_ERR_SIZE
+    assert kv.kvpool_encode(s, [ok, ok], [ok, ok], ok, pb, ok, wb - 1) == kv.KVP_ERR_SIZE
+
+
+def test_decode_argument_errors():
+    s = (3, 8, 128, 64)
+    ok = 0x10000
+    dst = [ok] * 6
+    assert kv.kvpool_decode_into(ok, s, 0, 4, 2, dst, dst) == kv.KVP_ERR_ARG      # layer range
+    assert kv.kvpool_decode_into(ok, s, 2, 2, 2, dst, dst) == kv.KVP_ERR_ARG      # empty range
+    assert kv.kvpool_decode_into(ok, s, 0, 3, 0, dst, dst) == kv.KVP_ERR_ARG      # no agents
+    assert kv.kvpool_decode_into(ok + 128, s, 0, 3, 2, dst, dst) == kv.KVP_ERR_ALIGN
+    bad = list(dst)
+    bad[4] = ok + 2                                                               # agent 1, layer 1
+    assert kv.kvpool_decode_into(ok, s, 0, 3, 2, bad, dst) == kv.KVP_ERR_ALIGN
+    bad[4] = None
+    assert kv.kvpool_decode_into(ok, s, 0, 3, 2, dst, bad) == kv.KVP_ERR_ARG
+    # layers outside the range are not read: a NULL there is fine up to validation
+    # (range [1,2) with an unaligned pool still fails on the pool, before launch)
+    assert kv.kvpool_decode_into(ok + 64, s, 1, 2, 2, [None, ok, None] * 2, [None, ok, None] * 2) == kv.KVP_ERR_ALIGN
+
+
+def test_card_argument_errors():
+    s = (2, 8, 128, 64)
+    ok = 0x10000
+    assert kv.cachecard_pack(s, 1, 2, None, [ok, ok], [ok, ok], ok, 1 << 24) == kv.KVP_ERR_ARG
+    assert kv.cachecard_pack(s, 1, 2, ok, [ok, ok], [ok, ok], ok + 16, 1 << 24) == kv.KVP_ERR_ALIGN
+    assert kv.cachecard_pack(s, 1, 2, ok, [ok, ok], [ok, ok], ok, 128) == kv.KVP_ERR_SIZE
+    h = kv.CardHeader()
+    h.magic = 0x12345678
+    assert kv.cachecard_unpack(ok, h, [ok, ok], [ok, ok]) == kv.KVP_ERR_HEADER
+    assert kv.cachecard_unpack(None, h, [ok], [ok]) == kv.KVP_ERR_ARG
+    assert kv.kvpool_status(None) == kv.KVP_ERR_ARG
+    assert kv.cachecard_status(None) == kv.KVP_ERR_ARG
+
+
+def test_strerror_and_counter():
+    for code in range(-9, 1):
+        assert kv.kvp_strerror(code) and kv.kvp_strerror(code) != "unknown status"
+    assert kv.kvp_strerror(-100) == "unknown status"
+    assert kv.kvp_launch_count() >= 0
