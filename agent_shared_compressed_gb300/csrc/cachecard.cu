@@ -202,8 +202,13 @@ __global__ void __launch_bounds__(CARD_THREADS) card_pack(const __grid_constant_
             }
             const uint16_t sb = group_scale_f16(mx, mn, qmax);
             const uint16_t zb = __half_as_ushort(__float2half_rn(mn));
-            if (act && (((sb & 0x7C00u) == 0x7C00u) || ((zb & 0x7C00u) == 0x7C00u))) flags |= FLAG_RANGE;
-            if (act && nf) flags |= FLAG_NONFINITE;
+            // non-finite anywhere in the group -> NONFINITE; otherwise an fp16
+            // overflow of the scale or zero point -> RANGE
+            bool gnf = nf;
+            gnf |= __shfl_xor_sync(0xffffffffu, gnf, 1);
+            gnf |= __shfl_xor_sync(0xffffffffu, gnf, 2);
+            if (act && gnf) flags |= FLAG_NONFINITE;
+            else if (act && (((sb & 0x7C00u) == 0x7C00u) || ((zb & 0x7C00u) == 0x7C00u))) flags |= FLAG_RANGE;
             const float sf = __half2float(__ushort_as_half(sb)), zf = __half2float(__ushort_as_half(zb));
             const float inv = (sf > 0.0f && sf <= 65504.0f) ? 1.0f / sf : 0.0f;
             const int qm = (1 << b) - 1;

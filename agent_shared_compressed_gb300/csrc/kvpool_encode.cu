@@ -190,8 +190,12 @@ __device__ void v_encode_blocks(const EncodeArgs &a, int vb) {
                 sig_bits = 0;
             }
         }
-        if (valid && !(n2 <= 3.0e38f)) flags |= classify_nonfinite(vec - 0, CPV);
-        if (valid && (sig_bits & 0x7C00u) == 0x7C00u) flags |= FLAG_RANGE;
+        // RANGE: finite input whose sigma exceeds fp16; non-finite input is
+        // NONFINITE only.
+        if (valid && !(n2 <= 3.0e38f))
+            flags |= classify_nonfinite(vec, CPV);
+        else if (valid && (sig_bits & 0x7C00u) == 0x7C00u)
+            flags |= FLAG_RANGE;
 
         float T1 = THR1 * nrm, T2 = THR2 * nrm, T3 = THR3 * nrm;
         if (nrm == 0.0f) T1 = T2 = T3 = __int_as_float(0x7F800000);  // zero vector: all codes 4

@@ -312,7 +312,9 @@ uint32_t orc_v_encode_vec(const uint16_t *v, int d, uint8_t *codes,
     orc_fwht(y, d);
     double sigma = nrm / sqrt((double)d);
     uint16_t sh = orc_f64_to_f16(sigma);
-    if ((sh & 0x7C00) == 0x7C00) flags |= ORC_FLAG_RANGE;
+    /* RANGE: a finite vector whose sigma is beyond fp16; a non-finite input
+     * is reported as NONFINITE only. */
+    if (!(flags & ORC_FLAG_NONFINITE) && (sh & 0x7C00) == 0x7C00) flags |= ORC_FLAG_RANGE;
     *sigma_h = sh;
     for (int i = 0; i < d; i++) {
         double u = (nrm > 0.0 && isfinite(nrm)) ? y[i] / nrm : 0.0;
@@ -589,7 +591,8 @@ uint32_t orc_group_quant(const double *x, int b, uint8_t *q, uint16_t *s_h, uint
     double qmax = (double)((1 << b) - 1);
     uint16_t sb = orc_f64_to_f16((mx - mn) / qmax);
     uint16_t zb = orc_f64_to_f16(mn);
-    if ((sb & 0x7C00) == 0x7C00 || (zb & 0x7C00) == 0x7C00) flags |= ORC_FLAG_RANGE;
+    if (!(flags & ORC_FLAG_NONFINITE) && ((sb & 0x7C00) == 0x7C00 || (zb & 0x7C00) == 0x7C00))
+        flags |= ORC_FLAG_RANGE;
     *s_h = sb;
     *z_h = zb;
     double s = orc_f16_to_f64(sb), z = orc_f16_to_f64(zb);

@@ -299,12 +299,27 @@ def test_v_one_hot_and_hadamard_row_closed_forms(d):
 
 
 def test_v_flags():
+    """Non-finite input is NONFINITE only; a finite vector whose sigma exceeds
+    the fp16 range is RANGE only."""
     d = 64
-    v = np.zeros(d)
-    v[3] = np.inf
-    assert O.v_encode_vec(_bf16(v))[3] & O.FLAG_NONFINITE
+    for bad in (np.inf, -np.inf, np.nan):
+        v = np.zeros(d)
+        v[3] = bad
+        assert O.v_encode_vec(_bf16(v))[3] == O.FLAG_NONFINITE
     v = np.full(d, 70000.0)          # sigma = 70000 > fp16 max
-    assert O.v_encode_vec(_bf16(v))[3] & O.FLAG_RANGE
+    assert O.v_encode_vec(_bf16(v))[3] == O.FLAG_RANGE
+    v = np.full(d, 65000.0)          # sigma = 65000 fits
+    assert O.v_encode_vec(_bf16(v))[3] == 0
+
+
+def test_group_flags():
+    x = np.linspace(-1, 1, 32)
+    x[4] = np.nan
+    assert O.group_quant(x, 4)[4] == O.FLAG_NONFINITE
+    x[4] = np.inf
+    assert O.group_quant(x, 4)[4] == O.FLAG_NONFINITE
+    x = np.linspace(-70000.0, 0.0, 32)      # zero point below -65504
+    assert O.group_quant(x, 4)[4] == O.FLAG_RANGE
 
 
 def test_pack3_layout():
