@@ -30,6 +30,7 @@ KVP_ERR_RANGE = -7
 KVP_ERR_BITS = -8
 KVP_ERR_HEADER = -9
 KVP_MAX_LAYERS = 512
+KVP_NOALLOC_SCRATCH_BYTES = 262144
 
 
 class Shape(C.Structure):
@@ -62,6 +63,7 @@ _SIGS = {
     "kvpool_decode_into": (C.c_int, [_vp, C.POINTER(Shape), C.c_int, C.c_int, C.c_int,
                                      C.POINTER(_vp), C.POINTER(_vp), _vp]),
     "kvpool_status": (C.c_int, [_vp, _vp]),
+    "kvpool_encode_noalloc": (C.c_int, [C.POINTER(Shape), C.POINTER(_vp), C.POINTER(_vp), _vp, C.c_size_t, _vp]),
     "cachecard_bytes": (C.c_size_t, [C.POINTER(Shape), C.POINTER(C.c_uint8)]),
     "cachecard_pack": (C.c_int, [C.POINTER(Shape), C.c_uint64, C.c_int64, _vp, C.POINTER(_vp),
                                  C.POINTER(_vp), _vp, C.c_size_t, _vp]),
@@ -148,6 +150,13 @@ def kvpool_workspace_bytes(shape):
 def kvpool_encode(shape, k_layers, v_layers, pool, pool_bytes, ws, ws_bytes, stream=None):
     return load().kvpool_encode(C.byref(_shape(shape)), _ptrs(k_layers), _ptrs(v_layers), _addr(pool),
                                 int(pool_bytes), _addr(ws), int(ws_bytes), _stream(stream))
+
+
+def kvpool_encode_noalloc(shape, k_layers, v_layers, pool, pool_bytes, stream=None):
+    """kvpool_encode with the library's own scratch array as workspace (for
+    callers that cannot allocate device memory)."""
+    return load().kvpool_encode_noalloc(C.byref(_shape(shape)), _ptrs(k_layers), _ptrs(v_layers), _addr(pool),
+                                        int(pool_bytes), _stream(stream))
 
 
 def kvpool_decode_into(pool, shape, layer_begin, layer_end, n_agents, k_dst, v_dst, stream=None):

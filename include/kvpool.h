@@ -155,6 +155,33 @@ int kvpool_decode_into(const void *pool, const kvp_shape *shape, int layer_begin
  * hold a version-1 pool). */
 int kvpool_status(const void *pool, void *stream);
 
+/* Size of the library's own device scratch array used by
+ * kvpool_encode_noalloc (256 KiB on every GPU that loads the library, held
+ * until the process exits). */
+#define KVP_NOALLOC_SCRATCH_BYTES 262144
+
+/* kvpool_encode without a caller workspace.  This entry point has no
+ * counterpart in the papers; it exists for callers that cannot allocate
+ * device memory -- e.g. a plug-in inside another program's process that must
+ * not allocate behind its host's memory manager, or a latency-critical caller
+ * for which a cudaMalloc could synchronise the device.  It allocates nothing
+ * (no cudaMalloc, cudaFree or allocating library call): the workspace is a
+ * fixed array of KVP_NOALLOC_SCRATCH_BYTES in the library's device memory.
+ *  Arguments and results are those of kvpool_encode minus ws / ws_bytes.
+ *  Shapes whose kvpool_workspace_bytes() exceeds KVP_NOALLOC_SCRATCH_BYTES
+ *    (about 240 layers at the largest per-layer partial count) are rejected
+ *    with KVP_ERR_SIZE before anything is enqueued.
+ *  The first call on a device looks up the array's device address (with
+ *    that device current) and caches it; make that first call before any
+ *    stream capture.
+ *  Every call on a device shares the one array.  The encoder overwrites
+ *    everything it reads from it, so nothing needs clearing between calls,
+ *    but calls that overlap on the GPU (other streams, no ordering between
+ *    them) race on the array: order them on one stream or with events. */
+int kvpool_encode_noalloc(const kvp_shape *shape, const void *const *k_layers,
+                          const void *const *v_layers, void *pool, size_t pool_bytes,
+                          void *stream);
+
 /* ---------------------------------------------------------------------- */
 /* CacheCard                                                               */
 /* ---------------------------------------------------------------------- */
