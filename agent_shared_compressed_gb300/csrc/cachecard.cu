@@ -116,11 +116,12 @@ __device__ __forceinline__ int cmp_mid(float hi, float lo, float m, float qmax) 
     return r > 0.0f ? 1 : (r < 0.0f ? -1 : 0);
 }
 
-__device__ uint16_t group_scale_f16(float mx, float mn, float qmax) {
+__device__ uint16_t group_scale_f16(float mx, float mn, float qmax, float rcp_qmax) {
     const float hi = mx - mn;
     const float bb = hi - mx;
     const float lo = (mx - (hi - bb)) + (-mn - bb);
-    uint16_t h = __half_as_ushort(__float2half_rn(hi / qmax));
+    // estimate within one fp16 step of the answer; the checks below make it exact
+    uint16_t h = __half_as_ushort(__float2half_rn(hi * rcp_qmax));
     if (h == 0x7C00u) return cmp_mid(hi, lo, 65520.0f, qmax) < 0 ? uint16_t(0x7BFFu) : h;
     const float vh = __half2float(__ushort_as_half(h));
     const float vn = h == 0x7BFFu ? 65536.0f : __half2float(__ushort_as_half(uint16_t(h + 1)));
@@ -168,75 +169,87 @@ __global__ void __launch_bounds__(CARD_THREADS) card_pack(const __grid_constant_
             continue;
         }
         const float qmax = float((1 << b) - 1);
+        const float rcp_qmax = 1.0f / qmax;
+        const int qm = (1 << b) - 1;
         const uint64_t code_bytes = uint64_t(a.H) * a.d * b / 8;
         uint8_t *codes = rec + uint64_t(kv) * code_bytes;
         uint32_t *par = reinterpret_cast<uint32_t *>(rec + 2 * code_bytes + uint64_t(kv) * a.H * (a.d / 32) * 4);
-        for (int c0 = 0; c0 < nchunks; c0 += 32) {
-            const int c = c0 + lane;
-            const bool act = c < nchunks;  // whole groups: nchunks is a multiple of 4
-            uint4 w = make_uint4(0, 0, 0, 0);
-            if (act) {
-                const int h = c / cpr, ch = c % cpr;
-                w = ld_stream_v4(src + (uint64_t(h) * a.T + t) * cpr + ch);
-            }
-            const float x[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
-                                bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
-            // non-finite detection on the bit patterns (NaN escapes fminf/fmaxf)
-            bool nf = false;
-            {
-                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+        for (int c0 = 0; c0 < nchunks; c0 += 4 * 32) {
+            // up to 4 chunks per lane in flight before any arithmetic
+            uint4 wv[4];
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    nf |= ((ws[i] & 0x7F80u) == 0x7F80u) | ((ws[i] & 0x7F800000u) == 0x7F800000u);
-            }
-            float mn = x[0], mx = x[0];
-#pragma unroll
-            for (int e = 1; e < 8; ++e) {
-                mn = fminf(mn, x[e]);
-                mx = fmaxf(mx, x[e]);
-            }
-#pragma unroll
-            for (int m = 1; m < 4; m <<= 1) {
-                mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, m));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
-            }
-            const uint16_t sb = group_scale_f16(mx, mn, qmax);
-            const uint16_t zb = __half_as_ushort(__float2half_rn(mn));
-            // non-finite anywhere in the group -> NONFINITE; otherwise an fp16
-            // overflow of the scale or zero point -> RANGE
-            bool gnf = nf;
-            gnf |= __shfl_xor_sync(0xffffffffu, gnf, 1);
-            gnf |= __shfl_xor_sync(0xffffffffu, gnf, 2);
-            if (act && gnf) flags |= FLAG_NONFINITE;
-            else if (act && (((sb & 0x7C00u) == 0x7C00u) || ((zb & 0x7C00u) == 0x7C00u))) flags |= FLAG_RANGE;
-            const float sf = __half2float(__ushort_as_half(sb)), zf = __half2float(__ushort_as_half(zb));
-            const float inv = (sf > 0.0f && sf <= 65504.0f) ? 1.0f / sf : 0.0f;
-            const int qm = (1 << b) - 1;
-            uint32_t q[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const float tf = fmaf(x[e] - zf, inv, RNE_MAGIC_C);
-                const int qi = int(__float_as_uint(tf)) - 0x4B400000;
-                q[e] = uint32_t(min(max(qi, 0), qm));
-            }
-            if (act) {
-                if (b == 2) {
-                    uint32_t v = 0;
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) v |= q[e] << (2 * e);
-                    reinterpret_cast<uint16_t *>(codes)[c] = uint16_t(v);
-                } else if (b == 4) {
-                    uint32_t v = 0;
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) v |= q[e] << (4 * e);
-                    reinterpret_cast<uint32_t *>(codes)[c] = v;
-                } else {
-                    uint2 v;
-                    v.x = __byte_perm(__byte_perm(q[0], q[1], 0x0040), __byte_perm(q[2], q[3], 0x0040), 0x5410);
-                    v.y = __byte_perm(__byte_perm(q[4], q[5], 0x0040), __byte_perm(q[6], q[7], 0x0040), 0x5410);
-                    reinterpret_cast<uint2 *>(codes)[c] = v;
+            for (int it = 0; it < 4; ++it) {
+                const int c = c0 + it * 32 + lane;
+                wv[it] = make_uint4(0, 0, 0, 0);
+                if (c < nchunks) {
+                    const int h = c / cpr, ch = c % cpr;
+                    wv[it] = ld_stream_v4(src + (uint64_t(h) * a.T + t) * cpr + ch);
                 }
-                if ((lane & 3) == 0) par[c >> 2] = uint32_t(sb) | (uint32_t(zb) << 16);
+            }
+#pragma unroll
+            for (int it = 0; it < 4; ++it) {
+                if (c0 + it * 32 >= nchunks) break;  // warp-uniform
+                const int c = c0 + it * 32 + lane;
+                const bool act = c < nchunks;  // whole groups: nchunks is a multiple of 4
+                const uint4 w = wv[it];
+                const float x[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
+                                    bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
+                // non-finite detection on the bit patterns (NaN escapes fminf/fmaxf)
+                bool nf = false;
+                {
+                    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        nf |= ((ws[i] & 0x7F80u) == 0x7F80u) | ((ws[i] & 0x7F800000u) == 0x7F800000u);
+                }
+                float mn = x[0], mx = x[0];
+#pragma unroll
+                for (int e = 1; e < 8; ++e) {
+                    mn = fminf(mn, x[e]);
+                    mx = fmaxf(mx, x[e]);
+                }
+#pragma unroll
+                for (int m = 1; m < 4; m <<= 1) {
+                    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, m));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
+                }
+                const uint16_t sb = group_scale_f16(mx, mn, qmax, rcp_qmax);
+                const uint16_t zb = __half_as_ushort(__float2half_rn(mn));
+                // non-finite anywhere in the group -> NONFINITE; otherwise an fp16
+                // overflow of the scale or zero point -> RANGE
+                bool gnf = nf;
+                gnf |= __shfl_xor_sync(0xffffffffu, gnf, 1);
+                gnf |= __shfl_xor_sync(0xffffffffu, gnf, 2);
+                if (act && gnf) flags |= FLAG_NONFINITE;
+                else if (act && (((sb & 0x7C00u) == 0x7C00u) || ((zb & 0x7C00u) == 0x7C00u))) flags |= FLAG_RANGE;
+                const float sf = __half2float(__ushort_as_half(sb)), zf = __half2float(__ushort_as_half(zb));
+                const float inv = (sf > 0.0f && sf <= 65504.0f) ? __frcp_rn(sf) : 0.0f;
+                uint32_t q[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float tf = fmaf(x[e] - zf, inv, RNE_MAGIC_C);
+                    const int qi = int(__float_as_uint(tf)) - 0x4B400000;
+                    q[e] = uint32_t(min(max(qi, 0), qm));
+                }
+                if (act) {
+                    if (b == 2) {
+                        uint32_t v = 0;
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) v |= q[e] << (2 * e);
+                        reinterpret_cast<uint16_t *>(codes)[c] = uint16_t(v);
+                    } else if (b == 4) {
+                        uint32_t v = 0;
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) v |= q[e] << (4 * e);
+                        reinterpret_cast<uint32_t *>(codes)[c] = v;
+                    } else {
+                        uint2 v;
+                        v.x = __byte_perm(__byte_perm(q[0], q[1], 0x0040), __byte_perm(q[2], q[3], 0x0040), 0x5410);
+                        v.y = __byte_perm(__byte_perm(q[4], q[5], 0x0040), __byte_perm(q[6], q[7], 0x0040), 0x5410);
+                        reinterpret_cast<uint2 *>(codes)[c] = v;
+                    }
+                    if ((lane & 3) == 0) par[c >> 2] = uint32_t(sb) | (uint32_t(zb) << 16);
+                }
             }
         }
         // zero the record's padding (sizes are multiples of 8, records of 16)
@@ -300,34 +313,50 @@ __global__ void __launch_bounds__(CARD_THREADS) card_unpack(const __grid_constan
         const uint64_t code_bytes = uint64_t(a.H) * a.d * b / 8;
         const uint8_t *codes = rec + uint64_t(kv) * code_bytes;
         const uint32_t *par = reinterpret_cast<const uint32_t *>(rec + 2 * code_bytes + uint64_t(kv) * a.H * (a.d / 32) * 4);
-        for (int c = lane; c < nchunks; c += 32) {
-            uint32_t q[8];
-            if (b == 2) {
-                const uint32_t v = reinterpret_cast<const uint16_t *>(codes)[c];
+        for (int c0 = 0; c0 < nchunks; c0 += 4 * 32) {
+            // up to 4 chunks' codes and group parameters per lane in flight
+            uint2 cw[4];
+            uint32_t pw[4];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) q[e] = (v >> (2 * e)) & 3u;
-            } else if (b == 4) {
-                const uint32_t v = reinterpret_cast<const uint32_t *>(codes)[c];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) q[e] = (v >> (4 * e)) & 15u;
-            } else {
-                const uint2 v = reinterpret_cast<const uint2 *>(codes)[c];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    q[e] = (v.x >> (8 * e)) & 255u;
-                    q[4 + e] = (v.y >> (8 * e)) & 255u;
+            for (int it = 0; it < 4; ++it) {
+                const int c = c0 + it * 32 + lane;
+                cw[it] = make_uint2(0, 0);
+                pw[it] = 0;
+                if (c < nchunks) {
+                    if (b == 2) cw[it].x = reinterpret_cast<const uint16_t *>(codes)[c];
+                    else if (b == 4) cw[it].x = reinterpret_cast<const uint32_t *>(codes)[c];
+                    else cw[it] = reinterpret_cast<const uint2 *>(codes)[c];
+                    pw[it] = par[c >> 2];
                 }
             }
-            const uint32_t p = par[c >> 2];
-            const float sf = __half2float(__ushort_as_half(uint16_t(p & 0xFFFFu)));
-            const float zf = __half2float(__ushort_as_half(uint16_t(p >> 16)));
-            float y[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) y[e] = fmaf(__uint_as_float(0x4B000000u | q[e]) - 8388608.0f, sf, zf);
-            const int h = c / cpr, ch = c % cpr;
-            st_stream_v4(dst + (uint64_t(h) * a.T + t) * cpr + ch,
-                         make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
-                                    pack_bf16x2(y[6], y[7])));
+            for (int it = 0; it < 4; ++it) {
+                const int c = c0 + it * 32 + lane;
+                if (c >= nchunks) break;
+                uint32_t q[8];
+                if (b == 2) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) q[e] = (cw[it].x >> (2 * e)) & 3u;
+                } else if (b == 4) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) q[e] = (cw[it].x >> (4 * e)) & 15u;
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        q[e] = (cw[it].x >> (8 * e)) & 255u;
+                        q[4 + e] = (cw[it].y >> (8 * e)) & 255u;
+                    }
+                }
+                const float sf = __half2float(__ushort_as_half(uint16_t(pw[it] & 0xFFFFu)));
+                const float zf = __half2float(__ushort_as_half(uint16_t(pw[it] >> 16)));
+                float y[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) y[e] = fmaf(__uint_as_float(0x4B000000u | q[e]) - 8388608.0f, sf, zf);
+                const int h = c / cpr, ch = c % cpr;
+                st_stream_v4(dst + (uint64_t(h) * a.T + t) * cpr + ch,
+                             make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
+                                        pack_bf16x2(y[6], y[7])));
+            }
         }
     }
 }

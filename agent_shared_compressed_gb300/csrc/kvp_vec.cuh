@@ -65,6 +65,61 @@ __device__ __forceinline__ void fwht(float (&x)[4][8], int lane) {
     }
 }
 
+// The same transform on packed pairs: x[j][p] holds coordinates (8c + 2p,
+// 8c + 2p + 1) of chunk c = j*LPV + l, and the caller has already applied the
+// butterfly of coordinate bit 0 (x[j][p] = (a + b, a - b)).  The remaining
+// stages run as f32x2 operations; a - b is fma(b, -1, a), rounded once like
+// the subtraction.
+__device__ __forceinline__ float2 f2add(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 f2sub(float2 a, float2 b) { return __ffma2_rn(b, make_float2(-1.0f, -1.0f), a); }
+
+template <int LPV>
+__device__ __forceinline__ void fwht_pairs(float2 (&x)[4][4], int lane) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+#pragma unroll
+        for (int h = 1; h < 4; h <<= 1) {       // coordinate bits 1, 2
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                if ((p & h) == 0) {
+                    const float2 a = x[j][p], b = x[j][p + h];
+                    x[j][p] = f2add(a, b);
+                    x[j][p + h] = f2sub(a, b);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int h = 1; h < 4; h <<= 1) {           // the two register-held top bits
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if ((j & h) == 0) {
+#pragma unroll
+                for (int p = 0; p < 4; ++p) {
+                    const float2 a = x[j][p], b = x[j + h][p];
+                    x[j][p] = f2add(a, b);
+                    x[j + h][p] = f2sub(a, b);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int m = 1; m < LPV; m <<= 1) {         // lane bits
+        const float sg = (lane & m) ? -1.0f : 1.0f;
+        const float2 sgn = make_float2(sg, sg);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                float2 o;
+                o.x = __shfl_xor_sync(0xffffffffu, x[j][p].x, m);
+                o.y = __shfl_xor_sync(0xffffffffu, x[j][p].y, m);
+                x[j][p] = __ffma2_rn(sgn, x[j][p], o);
+            }
+        }
+    }
+}
+
 // Lloyd-Max 8-level codebook for N(0,1) (+-0.2451, 0.7560, 1.3440, 2.1520)
 // and its decision thresholds (midpoints of adjacent centroids), positive
 // half.  Codes 0..7 index the centroids in ascending order.

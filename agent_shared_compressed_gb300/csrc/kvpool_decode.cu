@@ -22,21 +22,34 @@ struct DecodeArgs {
 };
 
 // 8 int8 key codes -> 8 bf16 values q*s.  A code byte c is turned into the
-// float 2^23 + (c + 128) by byte permutation (exact), then offset and scaled.
+// float 2^23 + (c + 128) by byte permutation (exact), then offset (exact) and
+// scaled, two lanes of f32x2 at a time.
 __device__ __forceinline__ uint4 k_decode8(uint2 raw, float s) {
     const uint32_t a0 = raw.x ^ 0x80808080u, a1 = raw.y ^ 0x80808080u;
-    float f[8];
+    const float2 off = make_float2(8388736.0f, 8388736.0f), ss = make_float2(s, s);
+    float2 f[4];
+    f[0] = make_float2(__uint_as_float(__byte_perm(a0, 0x4B000000u, 0x7650u)),
+                       __uint_as_float(__byte_perm(a0, 0x4B000000u, 0x7651u)));
+    f[1] = make_float2(__uint_as_float(__byte_perm(a0, 0x4B000000u, 0x7652u)),
+                       __uint_as_float(__byte_perm(a0, 0x4B000000u, 0x7653u)));
+    f[2] = make_float2(__uint_as_float(__byte_perm(a1, 0x4B000000u, 0x7650u)),
+                       __uint_as_float(__byte_perm(a1, 0x4B000000u, 0x7651u)));
+    f[3] = make_float2(__uint_as_float(__byte_perm(a1, 0x4B000000u, 0x7652u)),
+                       __uint_as_float(__byte_perm(a1, 0x4B000000u, 0x7653u)));
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        f[i] = (__uint_as_float(__byte_perm(a0, 0x4B000000u, 0x7650u | i)) - 8388736.0f) * s;
-        f[4 + i] = (__uint_as_float(__byte_perm(a1, 0x4B000000u, 0x7650u | i)) - 8388736.0f) * s;
-    }
-    return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
-                      pack_bf16x2(f[6], f[7]));
+    for (int i = 0; i < 4; ++i) f[i] = __fmul2_rn(f2sub(f[i], off), ss);
+    return make_uint4(pack_bf16x2(f[0].x, f[0].y), pack_bf16x2(f[1].x, f[1].y), pack_bf16x2(f[2].x, f[2].y),
+                      pack_bf16x2(f[3].x, f[3].y));
 }
 
+// One warp step ("unit"): VPW consecutive vectors of one layer.  The pool
+// bytes of the unit are loaded up front (keys 4 x 8 B per lane, value codes
+// 16 B on 24 lanes, sigma 2 B); keys are decoded and stored to every agent,
+// then values.  Value codes are staged in shared memory and each pair of
+// codes (a, b) is looked up in a 64-entry table of (c_a + c_b, c_a - c_b),
+// which is also the transform's first butterfly stage.
 template <int D>
-__global__ void __launch_bounds__(DEC_THREADS) decode_fanout(const __grid_constant__ DecodeArgs a) {
+__global__ void __launch_bounds__(DEC_THREADS, 4) decode_fanout(const __grid_constant__ DecodeArgs a) {
     constexpr int LPV = D / 32;
     constexpr int VPW = 32 / LPV;
     constexpr int CPV = D / 8;
@@ -45,6 +58,13 @@ __global__ void __launch_bounds__(DEC_THREADS) decode_fanout(const __grid_consta
     // 1 / (sqrt(d) * 10^4): the orthonormal 1/sqrt(d) and the codebook's 10^4.
     constexpr float KS = D == 128 ? 8.838834764831845e-6f : 1.25e-5f;
     __shared__ __align__(16) uint8_t stage[DEC_WARPS][384 + 16];
+    __shared__ float2 pair_lut[64];
+
+    if (threadIdx.x < 64) {
+        const float ca = centroid_e4(threadIdx.x & 7u), cb = centroid_e4(threadIdx.x >> 3);
+        pair_lut[threadIdx.x] = make_float2(ca + cb, ca - cb);  // exact: integers < 2^16
+    }
+    __syncthreads();
 
     const uint32_t *hdr = reinterpret_cast<const uint32_t *>(a.pool);
     if (hdr[0] != POOL_MAGIC || hdr[1] != POOL_VERSION) return;
@@ -67,60 +87,73 @@ __global__ void __launch_bounds__(DEC_THREADS) decode_fanout(const __grid_consta
         const uint64_t n0 = (u % upl) * VPW;
         const uint32_t cnt = uint32_t(min(uint64_t(VPW), nvec - n0));
         const uint8_t *lay = a.pool + a.geo.off_layers + uint64_t(layer) * a.geo.layer_stride;
-        const float s = scales[layer];
 
-        // keys: VPW*d int8 codes, 8 per lane-chunk
+        // --- all loads of the unit first
         const uint2 *kc = reinterpret_cast<const uint2 *>(lay) + n0 * (D / 8);
         const uint32_t kvalid = cnt * (D / 8);
-        uint4 kout[KCH];
+        uint2 kraw[KCH];
 #pragma unroll
         for (int it = 0; it < KCH; ++it) {
             const uint32_t k = uint32_t(it) * 32u + uint32_t(lane);
-            kout[it] = k < kvalid ? k_decode8(ld_stream_v2(kc + k), s) : make_uint4(0, 0, 0, 0);
+            kraw[it] = k < kvalid ? ld_stream_v2(kc + k) : make_uint2(0x80808080u, 0x80808080u);
         }
-
-        // values: stage the step's 384 code bytes, then each lane takes the
-        // 24-bit words of its 4 chunks
-        {
-            const uint32_t bytes = cnt * CB;
-            const uint32_t off = uint32_t(lane) * 16u;
-            const uint8_t *src = lay + a.geo.sec_v + n0 * CB;
-            if (off + 16u <= bytes)
-                *reinterpret_cast<uint4 *>(stage[warp] + off) = ld_stream_v4(src + off);
-            else if (off < bytes)
-                *reinterpret_cast<uint2 *>(stage[warp] + off) = ld_stream_v2(src + off);
+        const uint32_t bytes = cnt * CB;
+        const uint32_t off = uint32_t(lane) * 16u;
+        const uint8_t *vsrc = lay + a.geo.sec_v + n0 * CB;
+        uint4 vraw = make_uint4(0, 0, 0, 0);
+        if (off + 16u <= bytes) {
+            vraw = ld_stream_v4(vsrc + off);
+        } else if (off < bytes) {
+            const uint2 h = ld_stream_v2(vsrc + off);
+            vraw.x = h.x;
+            vraw.y = h.y;
         }
         const uint64_t n = n0 + g;
         const bool valid = n < nvec;
         const uint16_t sh = valid ? reinterpret_cast<const uint16_t *>(lay + a.geo.sec_sigma)[n] : uint16_t(0);
+        const float s = scales[layer];
+
+        // --- keys: decode, fan out
+        {
+            uint4 kout[KCH];
+#pragma unroll
+            for (int it = 0; it < KCH; ++it) kout[it] = k_decode8(kraw[it], s);
+            for (int ag = 0; ag < a.na; ++ag) {
+                uint4 *kd = a.kd[ag * a.nl + r] + n0 * (D / 8);
+#pragma unroll
+                for (int it = 0; it < KCH; ++it) {
+                    const uint32_t k = uint32_t(it) * 32u + uint32_t(lane);
+                    if (k < kvalid) st_stream_v4(kd + k, kout[it]);
+                }
+            }
+        }
+
+        // --- values: stage codes, look up pairs, transform, rescale, fan out
+        if (off < 384u) *reinterpret_cast<uint4 *>(stage[warp] + off) = vraw;
         __syncwarp();
-        float x[4][8];
+        float2 x[4][4];
         const uint32_t *st32 = reinterpret_cast<const uint32_t *>(stage[warp]);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const uint32_t o = uint32_t(g * CB + 3 * (j * LPV + l));
             const uint32_t w = __funnelshift_r(st32[o >> 2], st32[(o >> 2) + 1], (o & 3u) * 8u);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) x[j][e] = centroid_e4((w >> (3 * e)) & 7u);
+            for (int p = 0; p < 4; ++p) x[j][p] = pair_lut[(w >> (6 * p)) & 63u];
         }
         __syncwarp();
-        fwht<LPV>(x, lane);
+        fwht_pairs<LPV>(x, lane);
         const float f = __half2float(__ushort_as_half(sh)) * KS;
+        const float2 ff = make_float2(f, f);
         uint4 vout[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-            vout[j] = make_uint4(pack_bf16x2(x[j][0] * f, x[j][1] * f), pack_bf16x2(x[j][2] * f, x[j][3] * f),
-                                 pack_bf16x2(x[j][4] * f, x[j][5] * f), pack_bf16x2(x[j][6] * f, x[j][7] * f));
-
-        // fan out: the same registers to every agent's cache
-        for (int ag = 0; ag < a.na; ++ag) {
-            uint4 *kd = a.kd[ag * a.nl + r] + n0 * (D / 8);
-#pragma unroll
-            for (int it = 0; it < KCH; ++it) {
-                const uint32_t k = uint32_t(it) * 32u + uint32_t(lane);
-                if (k < kvalid) st_stream_v4(kd + k, kout[it]);
-            }
-            if (valid) {
+        for (int j = 0; j < 4; ++j) {
+            const float2 y0 = __fmul2_rn(x[j][0], ff), y1 = __fmul2_rn(x[j][1], ff);
+            const float2 y2 = __fmul2_rn(x[j][2], ff), y3 = __fmul2_rn(x[j][3], ff);
+            vout[j] = make_uint4(pack_bf16x2(y0.x, y0.y), pack_bf16x2(y1.x, y1.y), pack_bf16x2(y2.x, y2.y),
+                                 pack_bf16x2(y3.x, y3.y));
+        }
+        if (valid) {
+            for (int ag = 0; ag < a.na; ++ag) {
                 uint4 *vd = a.vd[ag * a.nl + r] + n * CPV;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) st_stream_v4(vd + j * LPV + l, vout[j]);

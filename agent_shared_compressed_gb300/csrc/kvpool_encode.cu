@@ -5,10 +5,10 @@
 // bytes.
 //
 // Three launches on the caller's stream:
-//   1. encode_phase1: blocks [0, L*P) reduce max|k| over a slice of one
-//      layer into a partial; the remaining G blocks encode every value vector
-//      of every layer (independent of the key scale), recording error bits in
-//      one slot per block.
+//   1. encode_phase1: a persistent grid of G blocks works through L*P key
+//      slices (max|k| of one slice of one layer -> a partial) interleaved
+//      with the value batches (every value vector of every layer: it does not
+//      depend on the key scale), recording error bits in one slot per block.
 //   2. encode_finalize: one block per layer folds its P partials into the
 //      layer's maximum, writes the fp32 scale s = m/127 into the pool and the
 //      key-quantizer parameters into the workspace; block 0 writes the pool
@@ -67,7 +67,7 @@ static inline WsLayout ws_layout(int L, uint64_t chunks) {
 // patterns is the order of the magnitudes; Inf/NaN patterns sort above
 // every finite one, so they flag themselves).
 // ---------------------------------------------------------------------------
-__device__ void absmax_block(const EncodeArgs &a, int bid) {
+__device__ void absmax_slice(const EncodeArgs &a, int bid) {
     const int l = bid / a.P, p = bid % a.P;
     const uint64_t c0 = uint64_t(p) * a.chunks_per_block;
     const uint64_t c1 = min(c0 + a.chunks_per_block, a.chunks);
@@ -101,6 +101,7 @@ __device__ void absmax_block(const EncodeArgs &a, int bid) {
         for (int i = 1; i < ENC_WARPS; ++i) r = max(r, red[i]);
         a.partials[bid] = r;
     }
+    __syncthreads();  // red[] is reused by the block's next slice
 }
 
 // ---------------------------------------------------------------------------
@@ -120,113 +121,157 @@ __device__ uint32_t classify_nonfinite(const uint4 *vec, int nchunks) {
     return FLAG_RANGE;
 }
 
+// One warp step: VPW consecutive vectors of one layer (see kvp_vec.cuh for
+// the lane mapping).  Returns error bits.
 template <int D>
-__device__ void v_encode_blocks(const EncodeArgs &a, int vb) {
+__device__ uint32_t v_encode_step(const EncodeArgs &a, uint64_t step, uint64_t steps_per_layer, uint8_t *stage) {
     constexpr int LPV = D / 32;      // lanes per vector
     constexpr int VPW = 32 / LPV;    // vectors per warp step
     constexpr int CPV = D / 8;       // 16-byte chunks per vector
     constexpr int CB = 3 * D / 8;    // code bytes per vector
-    constexpr int STAGE = VPW * CB;  // 384 bytes
-    static_assert(STAGE == 384, "a warp step stages 384 code bytes");
-    __shared__ __align__(16) uint8_t stage[ENC_WARPS][STAGE];
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    static_assert(VPW * CB == 384, "a warp step stages 384 code bytes");
+    const int lane = threadIdx.x & 31;
     const int g = lane / LPV, l = lane % LPV;
     const uint64_t nvec = uint64_t(a.H) * uint64_t(a.T);
-    const uint64_t steps_per_layer = (nvec + VPW - 1) / VPW;
-    const uint64_t total = steps_per_layer * uint64_t(a.L);
     const float inv_d = 1.0f / float(D);
     uint32_t flags = 0;
 
-    for (uint64_t step = uint64_t(vb) * ENC_WARPS + warp; step < total; step += uint64_t(a.G) * ENC_WARPS) {
-        const int layer = int(step / steps_per_layer);
-        const uint64_t n0 = (step % steps_per_layer) * VPW;
-        const uint64_t n = n0 + g;
-        const bool valid = n < nvec;
-        const uint4 *vec = a.v[layer] + n * CPV;
+    const int layer = int(step / steps_per_layer);
+    const uint64_t n0 = (step % steps_per_layer) * VPW;
+    const uint64_t n = n0 + g;
+    const bool valid = n < nvec;
+    const uint4 *vec = a.v[layer] + n * CPV;
 
-        float x[4][8];
-        float n2a = 0.0f, n2b = 0.0f;
+    // x[j][p] = (v_a + v_b, v_a - v_b) for the coordinate pair (a, b) = (2p, 2p+1)
+    // of chunk j: the first butterfly stage is applied while unpacking.
+    uint4 w[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const uint4 w = valid ? ld_stream_v4(vec + j * LPV + l) : make_uint4(0, 0, 0, 0);
-            x[j][0] = bf16_lo(w.x); x[j][1] = bf16_hi(w.x);
-            x[j][2] = bf16_lo(w.y); x[j][3] = bf16_hi(w.y);
-            x[j][4] = bf16_lo(w.z); x[j][5] = bf16_hi(w.z);
-            x[j][6] = bf16_lo(w.w); x[j][7] = bf16_hi(w.w);
+    for (int j = 0; j < 4; ++j) w[j] = valid ? ld_stream_v4(vec + j * LPV + l) : make_uint4(0, 0, 0, 0);
+    float2 x[4][4];
+    float2 n2v = make_float2(0.0f, 0.0f);
 #pragma unroll
-            for (int e = 0; e < 8; e += 2) {
-                n2a = fmaf(x[j][e], x[j][e], n2a);
-                n2b = fmaf(x[j][e + 1], x[j][e + 1], n2b);
-            }
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t ws[4] = {w[j].x, w[j].y, w[j].z, w[j].w};
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            const float2 v = make_float2(bf16_lo(ws[p]), bf16_hi(ws[p]));
+            n2v = __ffma2_rn(v, v, n2v);
+            x[j][p] = make_float2(v.x + v.y, v.x - v.y);
         }
-        float n2 = n2a + n2b;
-#pragma unroll
-        for (int m = 1; m < LPV; m <<= 1) n2 += __shfl_xor_sync(0xffffffffu, n2, m);
-
-        fwht<LPV>(x, lane);
-
-        // Thresholds t_k * ||v|| in the unnormalised rotated domain.
-        float nrm = sqrtf(n2);
-        uint16_t sig_bits = __half_as_ushort(__float2half_rn(sqrtf(n2 * inv_d)));
-        // A norm below 2^-50 loses precision to underflow in n2: rescale the
-        // rotated vector by 2^60 (exact) and take the norm from it through
-        // Parseval (||y||^2 = d ||v||^2).  sigma is below 2^-53: fp16 zero.
-        const bool tiny = n2 < 0x1p-100f;
-        if (__any_sync(0xffffffffu, tiny)) {
-            float s2 = 0.0f;
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float ys = x[j][e] * 0x1p60f;
-                    if (tiny) x[j][e] = ys;
-                    s2 = fmaf(ys, ys, s2);
-                }
-#pragma unroll
-            for (int m = 1; m < LPV; m <<= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, m);
-            if (tiny) {
-                nrm = sqrtf(s2 * inv_d);
-                sig_bits = 0;
-            }
-        }
-        // RANGE: finite input whose sigma exceeds fp16; non-finite input is
-        // NONFINITE only.
-        if (valid && !(n2 <= 3.0e38f))
-            flags |= classify_nonfinite(vec, CPV);
-        else if (valid && (sig_bits & 0x7C00u) == 0x7C00u)
-            flags |= FLAG_RANGE;
-
-        float T1 = THR1 * nrm, T2 = THR2 * nrm, T3 = THR3 * nrm;
-        if (nrm == 0.0f) T1 = T2 = T3 = __int_as_float(0x7F800000);  // zero vector: all codes 4
-
-        uint8_t *st = stage[warp] + g * CB;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            uint32_t w = 0;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) w |= v_code(x[j][e], T1, T2, T3) << (3 * e);
-            const int c = j * LPV + l;
-            st[3 * c + 0] = uint8_t(w);
-            st[3 * c + 1] = uint8_t(w >> 8);
-            st[3 * c + 2] = uint8_t(w >> 16);
-        }
-        __syncwarp();
-
-        uint8_t *lay = a.pool + a.geo.off_layers + uint64_t(layer) * a.geo.layer_stride;
-        const uint64_t nv_here = min(uint64_t(VPW), nvec - n0);
-        const uint32_t bytes = uint32_t(nv_here) * CB;
-        uint8_t *vdst = lay + a.geo.sec_v + n0 * CB;
-        const uint32_t off = uint32_t(lane) * 16u;
-        if (off + 16u <= bytes) {
-            *reinterpret_cast<uint4 *>(vdst + off) = *reinterpret_cast<const uint4 *>(stage[warp] + off);
-        } else if (off < bytes) {  // bytes is a multiple of 8
-            *reinterpret_cast<uint2 *>(vdst + off) = *reinterpret_cast<const uint2 *>(stage[warp] + off);
-        }
-        if (valid && l == 0) reinterpret_cast<uint16_t *>(lay + a.geo.sec_sigma)[n] = sig_bits;
-        __syncwarp();
     }
+    float n2 = n2v.x + n2v.y;
+#pragma unroll
+    for (int m = 1; m < LPV; m <<= 1) n2 += __shfl_xor_sync(0xffffffffu, n2, m);
 
+    fwht_pairs<LPV>(x, lane);
+
+    // Thresholds t_k * ||v|| in the unnormalised rotated domain.
+    float nrm = sqrtf(n2);
+    uint16_t sig_bits = __half_as_ushort(__float2half_rn(sqrtf(n2 * inv_d)));
+    // A norm below 2^-50 loses precision to underflow in n2: rescale the
+    // rotated vector by 2^60 (exact) and take the norm from it through
+    // Parseval (||y||^2 = d ||v||^2).  sigma is below 2^-53: fp16 zero.
+    const bool tiny = n2 < 0x1p-100f;
+    if (__any_sync(0xffffffffu, tiny)) {
+        float s2 = 0.0f;
+        const float2 sc = make_float2(0x1p60f, 0x1p60f);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                const float2 ys = __fmul2_rn(x[j][p], sc);
+                if (tiny) x[j][p] = ys;
+                s2 = fmaf(ys.x, ys.x, fmaf(ys.y, ys.y, s2));
+            }
+#pragma unroll
+        for (int m = 1; m < LPV; m <<= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, m);
+        if (tiny) {
+            nrm = sqrtf(s2 * inv_d);
+            sig_bits = 0;
+        }
+    }
+    // RANGE: finite input whose sigma exceeds fp16; non-finite input is
+    // NONFINITE only.
+    if (valid && !(n2 <= 3.0e38f))
+        flags |= classify_nonfinite(vec, CPV);
+    else if (valid && (sig_bits & 0x7C00u) == 0x7C00u)
+        flags |= FLAG_RANGE;
+
+    float T1 = THR1 * nrm, T2 = THR2 * nrm, T3 = THR3 * nrm;
+    if (nrm == 0.0f) T1 = T2 = T3 = __int_as_float(0x7F800000);  // zero vector: all codes 4
+
+    uint8_t *st = stage + g * CB;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint32_t cw = 0;
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            cw |= v_code(x[j][p].x, T1, T2, T3) << (6 * p);
+            cw |= v_code(x[j][p].y, T1, T2, T3) << (6 * p + 3);
+        }
+        const int c = j * LPV + l;
+        st[3 * c + 0] = uint8_t(cw);
+        st[3 * c + 1] = uint8_t(cw >> 8);
+        st[3 * c + 2] = uint8_t(cw >> 16);
+    }
+    __syncwarp();
+
+    uint8_t *lay = a.pool + a.geo.off_layers + uint64_t(layer) * a.geo.layer_stride;
+    const uint64_t nv_here = min(uint64_t(VPW), nvec - n0);
+    const uint32_t bytes = uint32_t(nv_here) * CB;
+    uint8_t *vdst = lay + a.geo.sec_v + n0 * CB;
+    const uint32_t off = uint32_t(lane) * 16u;
+    if (off + 16u <= bytes) {
+        *reinterpret_cast<uint4 *>(vdst + off) = *reinterpret_cast<const uint4 *>(stage + off);
+    } else if (off < bytes) {  // bytes is a multiple of 8
+        *reinterpret_cast<uint2 *>(vdst + off) = *reinterpret_cast<const uint2 *>(stage + off);
+    }
+    if (valid && l == 0) reinterpret_cast<uint16_t *>(lay + a.geo.sec_sigma)[n] = sig_bits;
+    __syncwarp();
+    return flags;
+}
+
+// Phase 1 work items: L*P key-absmax slices and ceil(value steps / 8)
+// value batches (8 warp steps, one per warp), interleaved so that both kinds
+// run on every SM at once (key reads overlap the value transform's ALU work).
+struct Phase1Items {
+    uint64_t na, nv, total;
+    __device__ __forceinline__ void at(uint64_t t, bool &is_abs, uint64_t &id) const {
+        const uint64_t both = 2 * min(na, nv);
+        if (t < both) {
+            is_abs = (t & 1u) == 0;
+            id = t >> 1;
+        } else {
+            is_abs = na > nv;
+            id = t - both + min(na, nv);
+        }
+    }
+};
+
+template <int D>
+__global__ void __launch_bounds__(ENC_THREADS, 3) encode_phase1(const __grid_constant__ EncodeArgs a) {
+    constexpr int VPW = 32 / (D / 32);
+    __shared__ __align__(16) uint8_t stage[ENC_WARPS][384];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint64_t nvec = uint64_t(a.H) * uint64_t(a.T);
+    const uint64_t steps_per_layer = (nvec + VPW - 1) / VPW;
+    const uint64_t vsteps = steps_per_layer * uint64_t(a.L);
+    Phase1Items items;
+    items.na = uint64_t(a.L) * uint64_t(a.P);
+    items.nv = (vsteps + ENC_WARPS - 1) / ENC_WARPS;
+    items.total = items.na + items.nv;
+    uint32_t flags = 0;
+    for (uint64_t t = blockIdx.x; t < items.total; t += gridDim.x) {
+        bool is_abs;
+        uint64_t id;
+        items.at(t, is_abs, id);
+        if (is_abs) {
+            absmax_slice(a, int(id));
+        } else {
+            const uint64_t step = id * ENC_WARPS + warp;
+            if (step < vsteps) flags |= v_encode_step<D>(a, step, steps_per_layer, stage[warp]);
+        }
+    }
     flags = __reduce_or_sync(0xffffffffu, flags);
     __shared__ uint32_t fl[ENC_WARPS];
     if (lane == 0) fl[warp] = flags;
@@ -235,17 +280,8 @@ __device__ void v_encode_blocks(const EncodeArgs &a, int vb) {
         uint32_t f = 0;
 #pragma unroll
         for (int i = 0; i < ENC_WARPS; ++i) f |= fl[i];
-        a.vflags[vb] = f;
+        a.vflags[blockIdx.x] = f;
     }
-}
-
-template <int D>
-__global__ void __launch_bounds__(ENC_THREADS) encode_phase1(const __grid_constant__ EncodeArgs a) {
-    const int nabs = a.L * a.P;
-    if (int(blockIdx.x) < nabs)
-        absmax_block(a, int(blockIdx.x));
-    else
-        v_encode_blocks<D>(a, int(blockIdx.x) - nabs);
 }
 
 // ---------------------------------------------------------------------------
@@ -411,6 +447,17 @@ __global__ void __launch_bounds__(ENC_THREADS) encode_keys(const __grid_constant
     }
 }
 
+template <int D>
+static int phase1_occupancy() {
+    static int occ = 0;
+    if (occ == 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, encode_phase1<D>, ENC_THREADS, 0) != cudaSuccess ||
+            occ < 1)
+            occ = 1;
+    }
+    return occ;
+}
+
 }  // namespace kvp
 
 using namespace kvp;
@@ -460,17 +507,18 @@ extern "C" int kvpool_encode(const kvp_shape *s, const void *const *k_layers, co
     const int sms = sm_count();
     const uint64_t nvec = uint64_t(a.H) * uint64_t(a.T);
     const uint64_t vsteps = (nvec + (a.d == 128 ? 8 : 16) - 1) / (a.d == 128 ? 8 : 16) * uint64_t(L);
-    uint64_t g = (vsteps + ENC_WARPS - 1) / ENC_WARPS;
-    const uint64_t gmax = uint64_t(sms) * 4;
-    a.G = int(g < 1 ? 1 : (g > gmax ? gmax : g));
-    if (a.G > VFLAG_SLOTS) a.G = VFLAG_SLOTS;
+    // persistent phase-1 grid: one block per resident slot, one flag slot per block
+    const uint64_t items = uint64_t(a.L) * uint64_t(a.P) + (vsteps + ENC_WARPS - 1) / ENC_WARPS;
+    const uint64_t gmax = uint64_t(sms) * uint64_t(a.d == 128 ? phase1_occupancy<128>() : phase1_occupancy<64>());
+    uint64_t g = items < gmax ? items : gmax;
+    if (g > VFLAG_SLOTS) g = VFLAG_SLOTS;
+    a.G = int(g < 1 ? 1 : g);
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const unsigned grid1 = unsigned(a.L * a.P + a.G);
     if (a.d == 128)
-        encode_phase1<128><<<grid1, ENC_THREADS, 0, st>>>(a);
+        encode_phase1<128><<<unsigned(a.G), ENC_THREADS, 0, st>>>(a);
     else
-        encode_phase1<64><<<grid1, ENC_THREADS, 0, st>>>(a);
+        encode_phase1<64><<<unsigned(a.G), ENC_THREADS, 0, st>>>(a);
     encode_finalize<<<L, ENC_THREADS, 0, st>>>(a);
     uint64_t bpl = (chunks + 2ull * ENC_THREADS * 4 - 1) / (2ull * ENC_THREADS * 4);
     const uint64_t bmax = (uint64_t(sms) * 8 + L - 1) / L;
