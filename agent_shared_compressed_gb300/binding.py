@@ -29,6 +29,7 @@ KVP_ERR_NONFINITE = -6
 KVP_ERR_RANGE = -7
 KVP_ERR_BITS = -8
 KVP_ERR_HEADER = -9
+KVP_ERR_TIMEOUT = -10
 KVP_MAX_LAYERS = 512
 KVP_NOALLOC_SCRATCH_BYTES = 262144
 
@@ -72,6 +73,7 @@ _SIGS = {
     "cachecard_status": (C.c_int, [_vp, _vp]),
     "kvp_strerror": (C.c_char_p, [C.c_int]),
     "kvp_launch_count": (C.c_uint64, []),
+    "kvp_test_fail_next_encode": (C.c_int, [C.c_int, C.c_uint32]),
 }
 
 _lib = None
@@ -200,6 +202,10 @@ def kvp_strerror(status):
 
 def kvp_launch_count():
     return int(load().kvp_launch_count())
+
+
+def kvp_test_fail_next_encode(layer, spin_iters):
+    return load().kvp_test_fail_next_encode(int(layer), int(spin_iters))
 
 
 class KVPError(RuntimeError):

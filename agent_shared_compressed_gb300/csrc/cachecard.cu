@@ -112,8 +112,14 @@ __global__ void __launch_bounds__(SCAN_THREADS) card_scan(const __grid_constant_
 // factor 2, and dominates lo otherwise).
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ int cmp_mid(float hi, float lo, float m, float qmax) {
-    const float r = (hi - m * qmax) + lo;
+    const float r = fmaf(-m, qmax, hi) + lo;
     return r > 0.0f ? 1 : (r < 0.0f ? -1 : 0);
+}
+
+// fp32 value of the midpoint between normal fp16 h and the next fp16 value
+// (65520 above 65504): h's bits widened to fp32 with the rounding bit set.
+__device__ __forceinline__ float f16_mid_above(uint32_t h) {
+    return __uint_as_float(((h << 13) | 0x1000u) + 0x38000000u);
 }
 
 __device__ uint16_t group_scale_f16(float mx, float mn, float qmax, float rcp_qmax) {
@@ -121,136 +127,152 @@ __device__ uint16_t group_scale_f16(float mx, float mn, float qmax, float rcp_qm
     const float bb = hi - mx;
     const float lo = (mx - (hi - bb)) + (-mn - bb);
     // estimate within one fp16 step of the answer; the checks below make it exact
-    uint16_t h = __half_as_ushort(__float2half_rn(hi * rcp_qmax));
-    if (h == 0x7C00u) return cmp_mid(hi, lo, 65520.0f, qmax) < 0 ? uint16_t(0x7BFFu) : h;
-    const float vh = __half2float(__ushort_as_half(h));
+    uint32_t h = __half_as_ushort(__float2half_rn(hi * rcp_qmax));
+    if (h >= 0x0401u && h <= 0x7BFFu) {  // h and h - 1 normal: midpoints by bit arithmetic
+        int c = cmp_mid(hi, lo, f16_mid_above(h), qmax);
+        if (c > 0 || (c == 0 && (h & 1u))) return uint16_t(h + 1);
+        c = cmp_mid(hi, lo, f16_mid_above(h - 1), qmax);
+        if (c < 0 || (c == 0 && (h & 1u))) return uint16_t(h - 1);
+        return uint16_t(h);
+    }
+    if (h == 0x7C00u) return cmp_mid(hi, lo, 65520.0f, qmax) < 0 ? uint16_t(0x7BFFu) : uint16_t(h);
+    const float vh = __half2float(__ushort_as_half(uint16_t(h)));
     const float vn = h == 0x7BFFu ? 65536.0f : __half2float(__ushort_as_half(uint16_t(h + 1)));
     int c = cmp_mid(hi, lo, 0.5f * (vh + vn), qmax);
     if (c > 0 || (c == 0 && (h & 1u))) return uint16_t(h + 1);
-    if (h == 0) return h;
+    if (h == 0) return uint16_t(h);
     const float vp = __half2float(__ushort_as_half(uint16_t(h - 1)));
     c = cmp_mid(hi, lo, 0.5f * (vp + vh), qmax);
     if (c < 0 || (c == 0 && (h & 1u))) return uint16_t(h - 1);
-    return h;
+    return uint16_t(h);
 }
 
 // ---------------------------------------------------------------------------
-// Pack: one warp per (layer, token, K|V).  Lane chunk c covers coordinates
-// 8c..8c+7 of the token's [H][d] row set (head c / (d/8)); 4 consecutive
-// lanes form one group of 32.
+// Pack: one warp per (layer, token, K|V); one thread per group of 32
+// coordinates.  A thread loads its group's 64 contiguous bytes (L1-cached, so
+// the warp's 2 KB are fetched once), reduces min / max, takes the exactly
+// rounded fp16 scale, quantizes and packs its 32 codes (4b bytes) and stores
+// them with the group's (s_h, z_h).
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t pack_bytes4(uint32_t b0, uint32_t b1, uint32_t b2, uint32_t b3) {
+    return __byte_perm(__byte_perm(b0, b1, 0x0040), __byte_perm(b2, b3, 0x0040), 0x5410);
+}
+
 __global__ void __launch_bounds__(CARD_THREADS) card_pack(const __grid_constant__ CardArgs a) {
     const kvp_card_header *hdr = reinterpret_cast<const kvp_card_header *>(a.card);
     if (hdr->error & (FLAG_BITS | FLAG_SIZE)) return;
     const uint64_t stride = hdr->layer_stride;  // depends on the device-resident bitwidths
     const int lane = threadIdx.x & 31;
-    const int cpr = a.d / 8;                        // chunks per head row
-    const int nchunks = a.H * cpr;                  // chunks per (token, K|V)
-    const uint64_t tasks = uint64_t(a.L) * uint64_t(a.T) * 2u;
+    const int cpr = a.d / 8;                     // 16-byte chunks per head row (8 or 16)
+    const int cshift = a.d == 128 ? 4 : 3;
+    const int gpr = a.d / 32;                    // groups per head row (2 or 4)
+    const int gshift = a.d == 128 ? 2 : 1;
+    const int nchunks = a.H * cpr;               // 16-byte chunks per (token, K|V)
+    const int ngroups = a.H * gpr;
+    const uint32_t T = uint32_t(a.T);
+    const uint32_t tasks = uint32_t(a.L) * T * 2u;  // fits: checked on the host
     const uint8_t *bits = a.card + CARD_HEADER_BYTES;
     const uint32_t *offs = reinterpret_cast<const uint32_t *>(a.card + a.off_offsets);
     uint32_t flags = 0;
 
-    for (uint64_t task = uint64_t(blockIdx.x) * CARD_WARPS + (threadIdx.x >> 5); task < tasks;
-         task += uint64_t(gridDim.x) * CARD_WARPS) {
+    for (uint32_t task = blockIdx.x * CARD_WARPS + (threadIdx.x >> 5); task < tasks;
+         task += gridDim.x * CARD_WARPS) {
         const int kv = int(task & 1u);
-        const uint64_t lt = task >> 1;
-        const int t = int(lt % uint64_t(a.T));
-        const int l = int(lt / uint64_t(a.T));
+        const uint32_t lt = task >> 1;
+        const uint32_t t = lt % T;
+        const int l = int(lt / T);
         const int b = bits[t];
         uint8_t *rec = a.card + a.off_layers + uint64_t(l) * stride + offs[t];
         const uint4 *src = a.src[kv][l];
         if (b == 16) {
             uint4 *out = reinterpret_cast<uint4 *>(rec + uint64_t(kv) * a.H * a.d * 2);
             for (int c = lane; c < nchunks; c += 32) {
-                const int h = c / cpr, ch = c % cpr;
-                out[c] = ld_stream_v4(src + (uint64_t(h) * a.T + t) * cpr + ch);
+                const int h = c >> cshift, ch = c & (cpr - 1);
+                out[c] = ld_stream_v4(src + (uint64_t(h) * T + t) * cpr + ch);
             }
             continue;
         }
         const float qmax = float((1 << b) - 1);
         const float rcp_qmax = 1.0f / qmax;
-        const int qm = (1 << b) - 1;
         const uint64_t code_bytes = uint64_t(a.H) * a.d * b / 8;
         uint8_t *codes = rec + uint64_t(kv) * code_bytes;
         uint32_t *par = reinterpret_cast<uint32_t *>(rec + 2 * code_bytes + uint64_t(kv) * a.H * (a.d / 32) * 4);
-        for (int c0 = 0; c0 < nchunks; c0 += 4 * 32) {
-            // up to 4 chunks per lane in flight before any arithmetic
-            uint4 wv[4];
+        for (int gi = lane; gi < ngroups; gi += 32) {
+            const int h = gi >> gshift, gg = gi & (gpr - 1);
+            const uint4 *p = src + (uint64_t(h) * T + t) * cpr + gg * 4;
+            uint32_t w[16];
 #pragma unroll
-            for (int it = 0; it < 4; ++it) {
-                const int c = c0 + it * 32 + lane;
-                wv[it] = make_uint4(0, 0, 0, 0);
-                if (c < nchunks) {
-                    const int h = c / cpr, ch = c % cpr;
-                    wv[it] = ld_stream_v4(src + (uint64_t(h) * a.T + t) * cpr + ch);
-                }
+            for (int q = 0; q < 4; ++q) {
+                const uint4 v = __ldg(p + q);
+                w[4 * q] = v.x;
+                w[4 * q + 1] = v.y;
+                w[4 * q + 2] = v.z;
+                w[4 * q + 3] = v.w;
             }
+            float2 x[16];
+            float mn0 = bf16_lo(w[0]), mx0 = mn0, mn1 = bf16_hi(w[0]), mx1 = mn1;
+            float2 nfacc = make_float2(0.0f, 0.0f);
 #pragma unroll
-            for (int it = 0; it < 4; ++it) {
-                if (c0 + it * 32 >= nchunks) break;  // warp-uniform
-                const int c = c0 + it * 32 + lane;
-                const bool act = c < nchunks;  // whole groups: nchunks is a multiple of 4
-                const uint4 w = wv[it];
-                const float x[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
-                                    bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
-                // non-finite detection on the bit patterns (NaN escapes fminf/fmaxf)
-                bool nf = false;
-                {
-                    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        nf |= ((ws[i] & 0x7F80u) == 0x7F80u) | ((ws[i] & 0x7F800000u) == 0x7F800000u);
-                }
-                float mn = x[0], mx = x[0];
-#pragma unroll
-                for (int e = 1; e < 8; ++e) {
-                    mn = fminf(mn, x[e]);
-                    mx = fmaxf(mx, x[e]);
-                }
-#pragma unroll
-                for (int m = 1; m < 4; m <<= 1) {
-                    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, m));
-                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
-                }
-                const uint16_t sb = group_scale_f16(mx, mn, qmax, rcp_qmax);
-                const uint16_t zb = __half_as_ushort(__float2half_rn(mn));
-                // non-finite anywhere in the group -> NONFINITE; otherwise an fp16
-                // overflow of the scale or zero point -> RANGE
-                bool gnf = nf;
-                gnf |= __shfl_xor_sync(0xffffffffu, gnf, 1);
-                gnf |= __shfl_xor_sync(0xffffffffu, gnf, 2);
-                if (act && gnf) flags |= FLAG_NONFINITE;
-                else if (act && (((sb & 0x7C00u) == 0x7C00u) || ((zb & 0x7C00u) == 0x7C00u))) flags |= FLAG_RANGE;
-                const float sf = __half2float(__ushort_as_half(sb)), zf = __half2float(__ushort_as_half(zb));
-                const float inv = (sf > 0.0f && sf <= 65504.0f) ? __frcp_rn(sf) : 0.0f;
-                uint32_t q[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float tf = fmaf(x[e] - zf, inv, RNE_MAGIC_C);
-                    const int qi = int(__float_as_uint(tf)) - 0x4B400000;
-                    q[e] = uint32_t(min(max(qi, 0), qm));
-                }
-                if (act) {
-                    if (b == 2) {
-                        uint32_t v = 0;
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) v |= q[e] << (2 * e);
-                        reinterpret_cast<uint16_t *>(codes)[c] = uint16_t(v);
-                    } else if (b == 4) {
-                        uint32_t v = 0;
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) v |= q[e] << (4 * e);
-                        reinterpret_cast<uint32_t *>(codes)[c] = v;
-                    } else {
-                        uint2 v;
-                        v.x = __byte_perm(__byte_perm(q[0], q[1], 0x0040), __byte_perm(q[2], q[3], 0x0040), 0x5410);
-                        v.y = __byte_perm(__byte_perm(q[4], q[5], 0x0040), __byte_perm(q[6], q[7], 0x0040), 0x5410);
-                        reinterpret_cast<uint2 *>(codes)[c] = v;
-                    }
-                    if ((lane & 3) == 0) par[c >> 2] = uint32_t(sb) | (uint32_t(zb) << 16);
-                }
+            for (int i = 0; i < 16; ++i) {
+                x[i] = make_float2(bf16_lo(w[i]), bf16_hi(w[i]));
+                mn0 = fminf(mn0, x[i].x);
+                mx0 = fmaxf(mx0, x[i].x);
+                mn1 = fminf(mn1, x[i].y);
+                mx1 = fmaxf(mx1, x[i].y);
+                nfacc = __ffma2_rn(x[i], make_float2(0.0f, 0.0f), nfacc);  // NaN iff Inf/NaN seen
             }
+            const float mn = fminf(mn0, mn1), mx = fmaxf(mx0, mx1);
+            const bool nf = (nfacc.x != nfacc.x) || (nfacc.y != nfacc.y);
+            const uint32_t sb = group_scale_f16(mx, mn, qmax, rcp_qmax);
+            const uint32_t zb = __half_as_ushort(__float2half_rn(mn));
+            if (nf)
+                flags |= FLAG_NONFINITE;
+            else if (((sb & 0x7C00u) == 0x7C00u) || ((zb & 0x7C00u) == 0x7C00u))
+                flags |= FLAG_RANGE;
+            const float sf = __half2float(__ushort_as_half(uint16_t(sb)));
+            const float zf = __half2float(__ushort_as_half(uint16_t(zb)));
+            const float inv = (sf > 0.0f && sf <= 65504.0f) ? __frcp_rn(sf) : 0.0f;
+            // code = clamp(round((x - z_h) / s_h), 0, 2^b - 1): the low mantissa bits
+            // of (x - z_h) * (1/s_h) + 1.5*2^23.  The map is monotone, so the clamp is
+            // needed only if the group's extremes fall outside the code range.
+            const float lo_c = RNE_MAGIC_C, hi_c = RNE_MAGIC_C + qmax;
+            const float tmn = fmaf(mn - zf, inv, RNE_MAGIC_C), tmx = fmaf(mx - zf, inv, RNE_MAGIC_C);
+            const bool clamp = !(tmn >= lo_c && tmx <= hi_c);
+            const float2 negz = make_float2(-zf, -zf), inv2 = make_float2(inv, inv);
+            const float2 mg = make_float2(RNE_MAGIC_C, RNE_MAGIC_C);
+            uint32_t q[32];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                float2 tf = __ffma2_rn(__fadd2_rn(x[i], negz), inv2, mg);
+                if (clamp) {
+                    tf.x = fminf(fmaxf(tf.x, lo_c), hi_c);
+                    tf.y = fminf(fmaxf(tf.y, lo_c), hi_c);
+                }
+                q[2 * i] = __float_as_uint(tf.x) & 0xFFu;
+                q[2 * i + 1] = __float_as_uint(tf.y) & 0xFFu;
+            }
+            if (b == 8) {
+                uint4 *o = reinterpret_cast<uint4 *>(codes) + 2 * gi;
+                o[0] = make_uint4(pack_bytes4(q[0], q[1], q[2], q[3]), pack_bytes4(q[4], q[5], q[6], q[7]),
+                                  pack_bytes4(q[8], q[9], q[10], q[11]), pack_bytes4(q[12], q[13], q[14], q[15]));
+                o[1] = make_uint4(pack_bytes4(q[16], q[17], q[18], q[19]), pack_bytes4(q[20], q[21], q[22], q[23]),
+                                  pack_bytes4(q[24], q[25], q[26], q[27]), pack_bytes4(q[28], q[29], q[30], q[31]));
+            } else if (b == 4) {
+                uint32_t by[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) by[i] = q[2 * i] | (q[2 * i + 1] << 4);
+                reinterpret_cast<uint4 *>(codes)[gi] =
+                    make_uint4(pack_bytes4(by[0], by[1], by[2], by[3]), pack_bytes4(by[4], by[5], by[6], by[7]),
+                               pack_bytes4(by[8], by[9], by[10], by[11]), pack_bytes4(by[12], by[13], by[14], by[15]));
+            } else {
+                uint32_t by[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    by[i] = q[4 * i] | (q[4 * i + 1] << 2) | (q[4 * i + 2] << 4) | (q[4 * i + 3] << 6);
+                reinterpret_cast<uint2 *>(codes)[gi] =
+                    make_uint2(pack_bytes4(by[0], by[1], by[2], by[3]), pack_bytes4(by[4], by[5], by[6], by[7]));
+            }
+            par[gi] = sb | (zb << 16);
         }
         // zero the record's padding (sizes are multiples of 8, records of 16)
         if (kv == 1 && lane == 0) {
@@ -283,16 +305,18 @@ __global__ void card_zero_tails(const __grid_constant__ CardArgs a) {
 __global__ void __launch_bounds__(CARD_THREADS) card_unpack(const __grid_constant__ CardArgs a) {
     const int lane = threadIdx.x & 31;
     const int cpr = a.d / 8;
+    const int cshift = a.d == 128 ? 4 : 3;
     const int nchunks = a.H * cpr;
-    const uint64_t tasks = uint64_t(a.L) * uint64_t(a.T) * 2u;
+    const uint32_t T = uint32_t(a.T);
+    const uint32_t tasks = uint32_t(a.L) * T * 2u;  // fits: checked on the host
     const uint8_t *bits = a.card + CARD_HEADER_BYTES;
     const uint32_t *offs = reinterpret_cast<const uint32_t *>(a.card + a.off_offsets);
-    for (uint64_t task = uint64_t(blockIdx.x) * CARD_WARPS + (threadIdx.x >> 5); task < tasks;
-         task += uint64_t(gridDim.x) * CARD_WARPS) {
+    for (uint32_t task = blockIdx.x * CARD_WARPS + (threadIdx.x >> 5); task < tasks;
+         task += gridDim.x * CARD_WARPS) {
         const int kv = int(task & 1u);
-        const uint64_t lt = task >> 1;
-        const int t = int(lt % uint64_t(a.T));
-        const int l = int(lt / uint64_t(a.T));
+        const uint32_t lt = task >> 1;
+        const uint32_t t = lt % T;
+        const int l = int(lt / T);
         const int b = bits[t];
         // a card whose bitwidths or offsets do not fit its own layer stride
         // is not decoded (and is reported through cachecard_status)
@@ -305,8 +329,8 @@ __global__ void __launch_bounds__(CARD_THREADS) card_unpack(const __grid_constan
         if (b == 16) {
             const uint4 *in = reinterpret_cast<const uint4 *>(rec + uint64_t(kv) * a.H * a.d * 2);
             for (int c = lane; c < nchunks; c += 32) {
-                const int h = c / cpr, ch = c % cpr;
-                st_stream_v4(dst + (uint64_t(h) * a.T + t) * cpr + ch, ld_stream_v4(in + c));
+                const int h = c >> cshift, ch = c & (cpr - 1);
+                st_stream_v4(dst + (uint64_t(h) * T + t) * cpr + ch, ld_stream_v4(in + c));
             }
             continue;
         }
@@ -352,8 +376,8 @@ __global__ void __launch_bounds__(CARD_THREADS) card_unpack(const __grid_constan
                 float y[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) y[e] = fmaf(__uint_as_float(0x4B000000u | q[e]) - 8388608.0f, sf, zf);
-                const int h = c / cpr, ch = c % cpr;
-                st_stream_v4(dst + (uint64_t(h) * a.T + t) * cpr + ch,
+                const int h = c >> cshift, ch = c & (cpr - 1);
+                st_stream_v4(dst + (uint64_t(h) * T + t) * cpr + ch,
                              make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
                                         pack_bf16x2(y[6], y[7])));
             }
@@ -390,6 +414,8 @@ extern "C" int cachecard_pack(const kvp_shape *s, uint64_t model_id, int64_t pos
     if (card_bytes < card_off_layers(s->n_tokens)) return KVP_ERR_SIZE;
     // record offsets are 32-bit: the largest possible layer must fit
     if (uint64_t(s->n_tokens) * card_record_bytes(16, s->n_kv_heads, s->head_dim) >= (1ull << 32)) return KVP_ERR_SIZE;
+    // (layer, token, K|V) tasks are counted in 32 bits
+    if (uint64_t(s->n_layers) * uint64_t(s->n_tokens) * 2ull >= (1ull << 32)) return KVP_ERR_SIZE;
 
     CardArgs a;
     for (int l = 0; l < L; ++l) {
@@ -431,6 +457,7 @@ extern "C" int cachecard_unpack(const void *card, const kvp_card_header *hdr, vo
         hdr->total_bytes != hdr->off_layers + uint64_t(s.n_layers) * hdr->layer_stride)
         return KVP_ERR_HEADER;
     if (!aligned(card, 256)) return KVP_ERR_ALIGN;
+    if (uint64_t(s.n_layers) * uint64_t(s.n_tokens) * 2ull >= (1ull << 32)) return KVP_ERR_SIZE;
     const int L = s.n_layers;
     CardArgs a;
     for (int l = 0; l < L; ++l) {

@@ -57,6 +57,7 @@ const char *kvp_strerror(int st) {
         case KVP_ERR_RANGE: return "a scale or zero point overflowed fp16";
         case KVP_ERR_BITS: return "CacheCard bitwidth not in {2,4,8,16}";
         case KVP_ERR_HEADER: return "not a pool / card, or its shape does not match";
+        case KVP_ERR_TIMEOUT: return "a bounded device-side wait ran out";
         default: return "unknown status";
     }
 }
@@ -65,6 +66,7 @@ uint64_t kvp_launch_count(void) { return g_launches.load(std::memory_order_relax
 
 static int flags_to_status(uint32_t f) {
     if (f & FLAG_HEADER) return KVP_ERR_HEADER;
+    if (f & FLAG_TIMEOUT) return KVP_ERR_TIMEOUT;
     if (f & FLAG_BITS) return KVP_ERR_BITS;
     if (f & FLAG_SIZE) return KVP_ERR_SIZE;
     if (f & FLAG_NONFINITE) return KVP_ERR_NONFINITE;

@@ -20,6 +20,7 @@ constexpr uint32_t FLAG_RANGE = 2u;      // a scale / zero point overflowed fp16
 constexpr uint32_t FLAG_BITS = 4u;       // a CacheCard bitwidth not in {2,4,8,16}
 constexpr uint32_t FLAG_SIZE = 8u;       // card buffer smaller than the bits need
 constexpr uint32_t FLAG_HEADER = 16u;    // decode asked for a shape the pool lacks
+constexpr uint32_t FLAG_TIMEOUT = 32u;   // a bounded wait on another block ran out
 
 // ---------------------------------------------------------------------------
 // SharedKVPool geometry ("PolyKV" 2.A: one object, size independent of the
@@ -107,6 +108,35 @@ __device__ __forceinline__ uint32_t ld_stream_u32(const void *p) {
     uint32_t r;
     asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(r) : "l"(p));
     return r;
+}
+
+// L2 eviction-priority policies for loads: keep (evict_last) data that is read
+// again soon, drop (evict_first) data read for the last time.
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint4 ld_v4_policy(const void *p, uint64_t pol) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p), "l"(pol));
+    return r;
+}
+
+// Acquire / release on a 32-bit flag in global memory (GPU scope).
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_u32(uint32_t *p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 // 16-byte store of write-once output (evict-first in L2).

@@ -4,109 +4,316 @@
 // (fp16), quantized to the 8-level Lloyd-Max codebook and packed 8 codes to 3
 // bytes.
 //
-// Three launches on the caller's stream:
-//   1. encode_phase1: a persistent grid of G blocks works through L*P key
-//      slices (max|k| of one slice of one layer -> a partial) interleaved
-//      with the value batches (every value vector of every layer: it does not
-//      depend on the key scale), recording error bits in one slot per block.
-//   2. encode_finalize: one block per layer folds its P partials into the
-//      layer's maximum, writes the fp32 scale s = m/127 into the pool and the
-//      key-quantizer parameters into the workspace; block 0 writes the pool
-//      header (with the OR of every error bit) and zeroes alignment gaps.
-//   3. encode_keys: int8 codes = the integer nearest to the exact k/s.
-// No block waits on another; the workspace needs no initialisation.
+// One persistent kernel, encode_pool, works through an ordered queue of
+// items.  For every layer l (queue order in item_of):
+//   1. P key slices "absmax": max|k| over one slice of K_l -> a partial.  The
+//      block that finishes the layer's last slice folds the P partials into
+//      the layer's scale s = m/127, writes it to the pool and the key
+//      quantizer's parameters to the workspace, and releases ready[l].
+//   2. the layer's value batches (4 warp steps of VPW vectors per warp),
+//      interleaved with P key slices "quantize": each waits (bounded) for
+//      ready[l], then writes the int8 codes = the integer nearest to the
+//      exact k/s.  The key slice is re-read soon after its first read, from
+//      L2 (first read marked evict-last, second evict-first).
+// Items are taken in queue order by running blocks, so every item a wait
+// depends on was taken earlier by a block that does not wait: no deadlock,
+// whatever the number of resident blocks.  The last block to finish writes
+// the pool header with the OR of every error bit.  The workspace's control
+// block is zeroed on the stream before the kernel.
 #include "kvp_vec.cuh"
 
 namespace kvp {
 
 constexpr int ENC_THREADS = 256;
 constexpr int ENC_WARPS = ENC_THREADS / 32;
-constexpr uint64_t ABSMAX_MIN_CHUNKS = 2048;  // 16-byte chunks per absmax block, at least
-constexpr int ABSMAX_MAX_BLOCKS = 256;        // per layer
-constexpr int VFLAG_SLOTS = 1024;             // value-encode blocks, at most
-constexpr float RNE_MAGIC = 12582912.0f;      // 1.5 * 2^23
+constexpr uint64_t SLICE_MIN_CHUNKS = 4096;  // 16-byte chunks (64 KB of keys) per slice, at least
+constexpr int MAX_SLICES = 256;              // per layer
+constexpr float RNE_MAGIC = 12582912.0f;     // 1.5 * 2^23
+constexpr uint32_t SPIN_LIMIT = 1u << 24;    // ~1.7 s of 100 ns sleeps
+constexpr int VSTEPS = 4;                    // value warp steps per warp per item
+
+enum : int { ITEM_ABSMAX = 0, ITEM_KEYS = 1, ITEM_VALUES = 2 };
+
+// Start of the workspace; zeroed before every encode.
+struct EncodeCtl {
+    uint32_t next_item;                    // work queue head
+    uint32_t flags;                        // OR of every block's error bits
+    uint32_t blocks_done;                  // last-block ticket
+    uint32_t pad;
+    uint32_t slices_done[KVP_MAX_LAYERS];  // absmax slices finished, per layer
+    uint32_t ready[KVP_MAX_LAYERS];        // 1 once the layer's key parameters are written
+};
 
 struct EncodeArgs {
     const uint4 *k[KVP_MAX_LAYERS];
     const uint4 *v[KVP_MAX_LAYERS];
     uint8_t *pool;
+    EncodeCtl *ctl;
     uint32_t *partials;  // [L][P]
-    uint32_t *vflags;    // [G]
     float4 *kparams;     // [L]: s_eff, 1/s_eff, prescale1, prescale2
     PoolGeom geo;
-    uint64_t chunks;           // 16-byte chunks per layer of K (H*T*d/8)
-    uint64_t chunks_per_block; // per absmax block
-    int L, H, T, d, P, G;
+    uint64_t chunks;            // 16-byte chunks per layer of K (H*T*d/8)
+    uint64_t chunks_per_slice;  // per absmax / quantize slice
+    uint64_t nvec;              // vectors per layer (H*T)
+    uint64_t steps_per_layer;   // value warp steps per layer
+    uint32_t vitems;            // value batches per layer
+    uint32_t vhead;             // value batches of a layer queued before its first quantize slice
+    uint32_t lag;               // layer l's value/quantize items follow layer l+lag's absmax items
+    uint32_t seg0, seg1;        // queue positions where the middle / last stretch of rounds begin
+    uint32_t total_items;
+    uint32_t spin_limit;
+    int L, H, T, d, P;
+    int fail_layer;             // failure-path testing: this layer's flag is never released
 };
 
-// Workspace: partials, value flags, key parameters (each 16-byte aligned).
 struct WsLayout {
-    uint64_t partials, vflags, kparams, total;
+    uint64_t ctl, partials, kparams, total;
 };
 
-static inline int absmax_blocks(uint64_t chunks) {
-    uint64_t p = (chunks + ABSMAX_MIN_CHUNKS - 1) / ABSMAX_MIN_CHUNKS;
+static inline int slices_per_layer(uint64_t chunks) {
+    uint64_t p = (chunks + SLICE_MIN_CHUNKS - 1) / SLICE_MIN_CHUNKS;
     if (p < 1) p = 1;
-    if (p > ABSMAX_MAX_BLOCKS) p = ABSMAX_MAX_BLOCKS;
+    if (p > MAX_SLICES) p = MAX_SLICES;
     return int(p);
 }
 
 static inline WsLayout ws_layout(int L, uint64_t chunks) {
     WsLayout w;
-    const int P = absmax_blocks(chunks);
-    w.partials = 0;
-    w.vflags = align16(4ull * uint64_t(L) * uint64_t(P));
-    w.kparams = align16(w.vflags + 4ull * VFLAG_SLOTS);
+    const int P = slices_per_layer(chunks);
+    w.ctl = 0;
+    w.partials = align256(sizeof(EncodeCtl));
+    w.kparams = align16(w.partials + 4ull * uint64_t(L) * uint64_t(P));
     w.total = align16(w.kparams + 16ull * uint64_t(L));
     return w;
 }
 
+// Item t of the queue.  The queue is a sequence of rounds r = 0 .. L+lag-1;
+// round r holds layer r's P absmax slices (if r < L), then the mixed items of
+// layer r - lag (if that layer exists): its value batches with its P quantize
+// slices spread evenly among them after a head of vhead value batches.  The
+// lag (0-2 layers, chosen so that the keys of the layers in between still fit
+// in L2) and the head put enough items between a layer's absmax slices and
+// its quantize slices that the latter rarely wait.
+__device__ __forceinline__ void mixed_item(const EncodeArgs &a, uint32_t o, int &kind, uint32_t &id) {
+    if (o < a.vhead) {
+        kind = ITEM_VALUES;
+        id = o;
+        return;
+    }
+    const uint64_t k = o - a.vhead;
+    const uint64_t n = uint64_t(a.P) + a.vitems - a.vhead;
+    const uint64_t qb = (k * uint64_t(a.P)) / n, qa = ((k + 1) * uint64_t(a.P)) / n;
+    if (qa > qb) {
+        kind = ITEM_KEYS;
+        id = uint32_t(qb);
+    } else {
+        kind = ITEM_VALUES;
+        id = uint32_t(a.vhead + k - qb);
+    }
+}
+
+__device__ __forceinline__ void item_of(const EncodeArgs &a, uint32_t t, int &kind, int &layer, uint32_t &id) {
+    const uint32_t P = uint32_t(a.P), M = P + a.vitems;
+    if (t < a.seg0) {  // rounds 0 .. lag-1: absmax only
+        layer = int(t / P);
+        kind = ITEM_ABSMAX;
+        id = t % P;
+        return;
+    }
+    if (t < a.seg1) {  // rounds lag .. L-1: absmax of layer r, mixed of layer r - lag
+        const uint32_t u = t - a.seg0;
+        const uint32_t r = a.lag + u / (P + M), o = u % (P + M);
+        if (o < P) {
+            layer = int(r);
+            kind = ITEM_ABSMAX;
+            id = o;
+        } else {
+            layer = int(r - a.lag);
+            mixed_item(a, o - P, kind, id);
+        }
+        return;
+    }
+    const uint32_t u = t - a.seg1;  // rounds L .. L+lag-1: mixed only
+    layer = int(uint32_t(a.L) - a.lag + u / M);
+    mixed_item(a, u % M, kind, id);
+}
+
 // ---------------------------------------------------------------------------
-// Phase 1a: partial max|k| of one slice of one layer, on the bf16 bit
-// patterns with the sign cleared (for finite values the order of the
-// patterns is the order of the magnitudes; Inf/NaN patterns sort above
-// every finite one, so they flag themselves).
+// Keys, pass 1: partial max|k| of one slice, on the bf16 bit patterns with the
+// sign cleared (for finite values their order is the order of the magnitudes;
+// Inf/NaN patterns sort above every finite one, so they flag themselves).
 // ---------------------------------------------------------------------------
-__device__ void absmax_slice(const EncodeArgs &a, int bid) {
-    const int l = bid / a.P, p = bid % a.P;
-    const uint64_t c0 = uint64_t(p) * a.chunks_per_block;
-    const uint64_t c1 = min(c0 + a.chunks_per_block, a.chunks);
+__device__ void absmax_slice(const EncodeArgs &a, int l, uint32_t p, uint64_t pol, uint32_t *red) {
+    const uint64_t c0 = uint64_t(p) * a.chunks_per_slice;
+    const uint64_t c1 = min(c0 + a.chunks_per_slice, a.chunks);
     const uint4 *src = a.k[l];
     uint32_t mlo = 0, mhi = 0;
     uint64_t c = c0 + threadIdx.x;
-    for (; c + 3 * ENC_THREADS < c1; c += 4 * ENC_THREADS) {
-        uint4 w[4];
+    for (; c + 7 * ENC_THREADS < c1; c += 8 * ENC_THREADS) {
+        uint4 w[8];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) w[u] = ld_stream_v4(src + c + u * ENC_THREADS);
+        for (int u = 0; u < 8; ++u) w[u] = ld_v4_policy(src + c + u * ENC_THREADS, pol);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < 8; ++u) {
             mlo = max(mlo, max(max(w[u].x & 0x7FFFu, w[u].y & 0x7FFFu), max(w[u].z & 0x7FFFu, w[u].w & 0x7FFFu)));
             mhi = max(mhi, max(max(w[u].x & 0x7FFF0000u, w[u].y & 0x7FFF0000u),
                                max(w[u].z & 0x7FFF0000u, w[u].w & 0x7FFF0000u)));
         }
     }
     for (; c < c1; c += ENC_THREADS) {
-        const uint4 w = ld_stream_v4(src + c);
+        const uint4 w = ld_v4_policy(src + c, pol);
         mlo = max(mlo, max(max(w.x & 0x7FFFu, w.y & 0x7FFFu), max(w.z & 0x7FFFu, w.w & 0x7FFFu)));
         mhi = max(mhi, max(max(w.x & 0x7FFF0000u, w.y & 0x7FFF0000u), max(w.z & 0x7FFF0000u, w.w & 0x7FFF0000u)));
     }
     uint32_t m = max(mlo, mhi >> 16);
     m = __reduce_max_sync(0xffffffffu, m);
-    __shared__ uint32_t red[ENC_WARPS];
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
     __syncthreads();
     if (threadIdx.x == 0) {
         uint32_t r = red[0];
 #pragma unroll
         for (int i = 1; i < ENC_WARPS; ++i) r = max(r, red[i]);
-        a.partials[bid] = r;
+        a.partials[uint64_t(l) * a.P + p] = r;
     }
-    __syncthreads();  // red[] is reused by the block's next slice
+    __syncthreads();
+}
+
+// Layer l's absmax slices are all done: its scale, quantizer parameters and
+// alignment gaps; then release ready[l].  Whole block.
+__device__ void finalize_layer(const EncodeArgs &a, int l, uint32_t *red) {
+    __threadfence();  // the other blocks' partials (written before their counter increments)
+    uint32_t m = 0;
+    const volatile uint32_t *part = a.partials + uint64_t(l) * a.P;
+    for (int i = threadIdx.x; i < a.P; i += ENC_THREADS) m = max(m, part[i]);
+    m = __reduce_max_sync(0xffffffffu, m);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t r = red[0];
+        for (int i = 1; i < ENC_WARPS; ++i) r = max(r, red[i]);
+        const bool finite = r < 0x7F80u;
+        if (!finite) atomicOr(&a.ctl->flags, FLAG_NONFINITE);
+        const float mk = __uint_as_float(r << 16);  // max|k|, exact
+        // s = m/127, IEEE division: the correctly rounded fp32 quotient.
+        const float s = finite ? mk / 127.0f : 0.0f;
+        float4 kp = make_float4(0.f, 0.f, 1.f, 1.f);
+        if (s > 0.0f) {
+            if (s >= 0x1p-100f) {
+                kp = make_float4(s, 1.0f / s, 1.0f, 1.0f);
+            } else {
+                // Tiny scale: quantize k*2^p against s*2^p with s*2^p in [1,2)
+                // (both scalings exact), so 1/s cannot overflow and the exact
+                // tie test cannot underflow.
+                int e;
+                frexpf(s, &e);
+                const int p = 1 - e;
+                const int p1 = p > 120 ? 120 : p;
+                const float f1 = ldexpf(1.0f, p1), f2 = ldexpf(1.0f, p - p1);
+                const float se = (s * f1) * f2;
+                kp = make_float4(se, 1.0f / se, f1, f2);
+            }
+        }
+        a.kparams[l] = kp;
+        reinterpret_cast<float *>(a.pool + a.geo.off_scales)[l] = s;
+    }
+    {   // zero the layer's alignment gaps so the pool image is deterministic
+        uint8_t *lay = a.pool + a.geo.off_layers + uint64_t(l) * a.geo.layer_stride;
+        const uint64_t gaps[3][2] = {{a.nvec * uint64_t(a.d), a.geo.sec_v},
+                                     {a.geo.sec_v + a.nvec * uint64_t(3 * a.d / 8), a.geo.sec_sigma},
+                                     {a.geo.sec_sigma + 2 * a.nvec, a.geo.layer_stride}};
+        for (int gi = 0; gi < 3; ++gi)
+            for (uint64_t i = gaps[gi][0] + threadIdx.x; i < gaps[gi][1]; i += ENC_THREADS) lay[i] = 0;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (l != a.fail_layer) st_release_u32(&a.ctl->ready[l], 1u);
+    }
 }
 
 // ---------------------------------------------------------------------------
-// Phase 1b: value vectors ("PolyKV" 2.B.2).  One warp handles VPW vectors per
-// step; see kvp_vec.cuh for the lane mapping.
+// Keys, pass 2: int8 codes ("PolyKV" 2.B.1).  q = the integer nearest to the
+// real k/s, ties to even.  Fast path: t = fma(k, 1/s, 1.5*2^23) rounds k/s'
+// (k/s within 1.6e-5) to an integer held in t's low mantissa bits, whose low
+// byte is the two's-complement code.  Only when that estimate is within 1e-4
+// of a half-integer is the decision taken exactly: the sign of
+// k - (q0 +- 1/2) s is exact under one fma rounding.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t k_code_exact(float k, float s, float q0) {
+    const float hi = fmaf(-(q0 + 0.5f), s, k);
+    const float lo = fmaf(-(q0 - 0.5f), s, k);
+    int q = int(q0);
+    if (hi > 0.0f)
+        q += 1;
+    else if (hi == 0.0f)
+        q += (q & 1);
+    else if (lo < 0.0f)
+        q -= 1;
+    else if (lo == 0.0f)
+        q -= (q & 1);
+    return uint32_t(q) & 0xFFu;
+}
+
+template <bool PRESCALE>
+__device__ __forceinline__ uint2 k_quant8(uint4 w, float4 kp) {
+    float k[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
+                  bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
+    if (PRESCALE) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) k[i] = (k[i] * kp.z) * kp.w;
+    }
+    uint32_t t[8];
+    bool near = false;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float tf = fmaf(k[i], kp.y, RNE_MAGIC);
+        const float q0 = tf - RNE_MAGIC;
+        const float e = fmaf(k[i], kp.y, -q0);
+        near |= fabsf(e) > 0.4999f;
+        t[i] = __float_as_uint(tf);
+    }
+    if (near) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float q0 = __uint_as_float(t[i]) - RNE_MAGIC;
+            t[i] = k_code_exact(k[i], kp.x, q0);
+        }
+    }
+    uint2 r;
+    r.x = __byte_perm(__byte_perm(t[0], t[1], 0x0040), __byte_perm(t[2], t[3], 0x0040), 0x5410);
+    r.y = __byte_perm(__byte_perm(t[4], t[5], 0x0040), __byte_perm(t[6], t[7], 0x0040), 0x5410);
+    return r;
+}
+
+__device__ void quant_slice(const EncodeArgs &a, int l, uint32_t p, uint64_t pol) {
+    // written by another block in this kernel: plain (coherent) loads
+    const volatile float *kpv = reinterpret_cast<const volatile float *>(a.kparams + l);
+    const float4 kp = make_float4(kpv[0], kpv[1], kpv[2], kpv[3]);
+    const bool pre = kp.z != 1.0f || kp.w != 1.0f;
+    const uint64_t c0 = uint64_t(p) * a.chunks_per_slice;
+    const uint64_t c1 = min(c0 + a.chunks_per_slice, a.chunks);
+    const uint4 *src = a.k[l];
+    uint2 *dst = reinterpret_cast<uint2 *>(a.pool + a.geo.off_layers + uint64_t(l) * a.geo.layer_stride);
+    uint64_t c = c0 + threadIdx.x;
+    for (; c + ENC_THREADS < c1; c += 2 * ENC_THREADS) {
+        const uint4 w0 = ld_v4_policy(src + c, pol), w1 = ld_v4_policy(src + c + ENC_THREADS, pol);
+        if (pre) {
+            dst[c] = k_quant8<true>(w0, kp);
+            dst[c + ENC_THREADS] = k_quant8<true>(w1, kp);
+        } else {
+            dst[c] = k_quant8<false>(w0, kp);
+            dst[c + ENC_THREADS] = k_quant8<false>(w1, kp);
+        }
+    }
+    for (; c < c1; c += ENC_THREADS) {
+        const uint4 w0 = ld_v4_policy(src + c, pol);
+        dst[c] = pre ? k_quant8<true>(w0, kp) : k_quant8<false>(w0, kp);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Values ("PolyKV" 2.B.2): one warp step, VPW consecutive vectors of one layer
+// (see kvp_vec.cuh for the lane mapping).  Returns error bits.
 // ---------------------------------------------------------------------------
 
 // Slow path for the rare vector whose squared norm is not finite: Inf/NaN in
@@ -121,10 +328,8 @@ __device__ uint32_t classify_nonfinite(const uint4 *vec, int nchunks) {
     return FLAG_RANGE;
 }
 
-// One warp step: VPW consecutive vectors of one layer (see kvp_vec.cuh for
-// the lane mapping).  Returns error bits.
 template <int D>
-__device__ uint32_t v_encode_step(const EncodeArgs &a, uint64_t step, uint64_t steps_per_layer, uint8_t *stage) {
+__device__ uint32_t v_encode_step(const EncodeArgs &a, int layer, uint64_t step, uint8_t *stage, uint64_t pol) {
     constexpr int LPV = D / 32;      // lanes per vector
     constexpr int VPW = 32 / LPV;    // vectors per warp step
     constexpr int CPV = D / 8;       // 16-byte chunks per vector
@@ -132,12 +337,11 @@ __device__ uint32_t v_encode_step(const EncodeArgs &a, uint64_t step, uint64_t s
     static_assert(VPW * CB == 384, "a warp step stages 384 code bytes");
     const int lane = threadIdx.x & 31;
     const int g = lane / LPV, l = lane % LPV;
-    const uint64_t nvec = uint64_t(a.H) * uint64_t(a.T);
+    const uint64_t nvec = a.nvec;
     const float inv_d = 1.0f / float(D);
     uint32_t flags = 0;
 
-    const int layer = int(step / steps_per_layer);
-    const uint64_t n0 = (step % steps_per_layer) * VPW;
+    const uint64_t n0 = step * VPW;
     const uint64_t n = n0 + g;
     const bool valid = n < nvec;
     const uint4 *vec = a.v[layer] + n * CPV;
@@ -146,7 +350,7 @@ __device__ uint32_t v_encode_step(const EncodeArgs &a, uint64_t step, uint64_t s
     // of chunk j: the first butterfly stage is applied while unpacking.
     uint4 w[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) w[j] = valid ? ld_stream_v4(vec + j * LPV + l) : make_uint4(0, 0, 0, 0);
+    for (int j = 0; j < 4; ++j) w[j] = valid ? ld_v4_policy(vec + j * LPV + l, pol) : make_uint4(0, 0, 0, 0);
     float2 x[4][4];
     float2 n2v = make_float2(0.0f, 0.0f);
 #pragma unroll
@@ -231,236 +435,125 @@ __device__ uint32_t v_encode_step(const EncodeArgs &a, uint64_t step, uint64_t s
     return flags;
 }
 
-// Phase 1 work items: L*P key-absmax slices and ceil(value steps / 8)
-// value batches (8 warp steps, one per warp), interleaved so that both kinds
-// run on every SM at once (key reads overlap the value transform's ALU work).
-struct Phase1Items {
-    uint64_t na, nv, total;
-    __device__ __forceinline__ void at(uint64_t t, bool &is_abs, uint64_t &id) const {
-        const uint64_t both = 2 * min(na, nv);
-        if (t < both) {
-            is_abs = (t & 1u) == 0;
-            id = t >> 1;
-        } else {
-            is_abs = na > nv;
-            id = t - both + min(na, nv);
-        }
+// The pool header, written by the last block (all error bits are in).
+__device__ void write_header(const EncodeArgs &a) {
+    __threadfence();
+    for (uint64_t i = 80 + threadIdx.x; i < POOL_HEADER_BYTES; i += ENC_THREADS) a.pool[i] = 0;
+    for (uint64_t i = a.geo.off_scales + 4ull * a.L + threadIdx.x; i < a.geo.off_layers; i += ENC_THREADS)
+        a.pool[i] = 0;
+    if (threadIdx.x == 0) {
+        uint32_t *h = reinterpret_cast<uint32_t *>(a.pool);
+        h[0] = POOL_MAGIC;
+        h[1] = POOL_VERSION;
+        h[2] = uint32_t(a.L);
+        h[3] = uint32_t(a.H);
+        h[4] = uint32_t(a.d);
+        h[5] = uint32_t(a.T);
+        h[POOL_ERR_WORD] = *reinterpret_cast<volatile uint32_t *>(&a.ctl->flags);
+        h[7] = 0;
+        uint64_t *h64 = reinterpret_cast<uint64_t *>(a.pool);
+        h64[4] = a.geo.off_scales;
+        h64[5] = a.geo.off_layers;
+        h64[6] = a.geo.layer_stride;
+        h64[7] = a.geo.sec_v;
+        h64[8] = a.geo.sec_sigma;
+        h64[9] = a.geo.total;
     }
-};
+}
 
 template <int D>
-__global__ void __launch_bounds__(ENC_THREADS, 3) encode_phase1(const __grid_constant__ EncodeArgs a) {
-    constexpr int VPW = 32 / (D / 32);
+__global__ void __launch_bounds__(ENC_THREADS, 3) encode_pool(const __grid_constant__ EncodeArgs a) {
     __shared__ __align__(16) uint8_t stage[ENC_WARPS][384];
+    __shared__ uint32_t red[ENC_WARPS];
+    __shared__ uint32_t s_item[2], s_flag;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint64_t nvec = uint64_t(a.H) * uint64_t(a.T);
-    const uint64_t steps_per_layer = (nvec + VPW - 1) / VPW;
-    const uint64_t vsteps = steps_per_layer * uint64_t(a.L);
-    Phase1Items items;
-    items.na = uint64_t(a.L) * uint64_t(a.P);
-    items.nv = (vsteps + ENC_WARPS - 1) / ENC_WARPS;
-    items.total = items.na + items.nv;
+    const uint64_t keep = l2_evict_last_policy(), drop = l2_evict_first_policy();
     uint32_t flags = 0;
-    for (uint64_t t = blockIdx.x; t < items.total; t += gridDim.x) {
-        bool is_abs;
-        uint64_t id;
-        items.at(t, is_abs, id);
-        if (is_abs) {
-            absmax_slice(a, int(id));
+    // The next queue index is fetched while the current item runs (thread 0
+    // holds it in a register); the broadcast slot alternates between two
+    // words so one barrier per item suffices.
+    uint32_t next = 0;
+    if (threadIdx.x == 0) next = atomicAdd(&a.ctl->next_item, 1u);
+    for (uint32_t k = 0;; ++k) {
+        if (threadIdx.x == 0) s_item[k & 1u] = next;
+        __syncthreads();
+        const uint32_t t = s_item[k & 1u];
+        if (t >= a.total_items) break;
+        if (threadIdx.x == 0) next = atomicAdd(&a.ctl->next_item, 1u);
+        int kind, layer;
+        uint32_t id;
+        item_of(a, t, kind, layer, id);
+        if (kind == ITEM_ABSMAX) {
+            absmax_slice(a, layer, id, keep, red);
+            if (threadIdx.x == 0) {
+                __threadfence();  // this slice's partial before the count
+                s_flag = atomicAdd(&a.ctl->slices_done[layer], 1u) == uint32_t(a.P) - 1u;
+            }
+            __syncthreads();
+            if (s_flag) finalize_layer(a, layer, red);
+        } else if (kind == ITEM_KEYS) {
+            if (threadIdx.x == 0) {
+                // bounded wait for the layer's scale (released by another block)
+                uint32_t ok = 1, i = 0;
+                while (ld_acquire_u32(&a.ctl->ready[layer]) == 0u) {
+                    if (++i >= a.spin_limit) {
+                        ok = 0;
+                        break;
+                    }
+                    __nanosleep(100);
+                }
+                __threadfence();
+                s_flag = ok;
+            }
+            __syncthreads();
+            if (s_flag)
+                quant_slice(a, layer, id, drop);
+            else if (threadIdx.x == 0)
+                flags |= FLAG_TIMEOUT;
         } else {
-            const uint64_t step = id * ENC_WARPS + warp;
-            if (step < vsteps) flags |= v_encode_step<D>(a, step, steps_per_layer, stage[warp]);
+#pragma unroll 1
+            for (int vs = 0; vs < VSTEPS; ++vs) {
+                const uint64_t step = (uint64_t(id) * VSTEPS + vs) * ENC_WARPS + warp;
+                if (step < a.steps_per_layer) flags |= v_encode_step<D>(a, layer, step, stage[warp], drop);
+            }
         }
     }
     flags = __reduce_or_sync(0xffffffffu, flags);
-    __shared__ uint32_t fl[ENC_WARPS];
-    if (lane == 0) fl[warp] = flags;
+    if (lane == 0 && flags) atomicOr(&a.ctl->flags, flags);
     __syncthreads();
     if (threadIdx.x == 0) {
-        uint32_t f = 0;
-#pragma unroll
-        for (int i = 0; i < ENC_WARPS; ++i) f |= fl[i];
-        a.vflags[blockIdx.x] = f;
+        __threadfence();
+        s_flag = atomicAdd(&a.ctl->blocks_done, 1u) == gridDim.x - 1u;
     }
-}
-
-// ---------------------------------------------------------------------------
-// Phase 2: per-layer scale and key-quantizer parameters; the pool header.
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(ENC_THREADS) encode_finalize(const __grid_constant__ EncodeArgs a) {
-    const int l = blockIdx.x;
-    __shared__ uint32_t red[ENC_WARPS];
-    uint32_t m = 0;
-    for (int i = threadIdx.x; i < a.P; i += ENC_THREADS) m = max(m, a.partials[l * a.P + i]);
-    m = __reduce_max_sync(0xffffffffu, m);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
     __syncthreads();
-    if (threadIdx.x == 0) {
-        uint32_t r = red[0];
-        for (int i = 1; i < ENC_WARPS; ++i) r = max(r, red[i]);
-        const bool finite = r < 0x7F80u;
-        const float mk = __uint_as_float(r << 16);  // max|k|, exact
-        // s = m/127, IEEE division: the correctly rounded fp32 quotient.
-        const float s = finite ? mk / 127.0f : 0.0f;
-        float4 kp = make_float4(0.f, 0.f, 1.f, 1.f);
-        if (s > 0.0f) {
-            if (s >= 0x1p-100f) {
-                kp = make_float4(s, 1.0f / s, 1.0f, 1.0f);
-            } else {
-                // Tiny scale: quantize k*2^p against s*2^p with s*2^p in [1,2)
-                // (both scalings exact), so 1/s cannot overflow and the exact
-                // tie test below cannot underflow.
-                int e;
-                frexpf(s, &e);
-                const int p = 1 - e;
-                const int p1 = p > 120 ? 120 : p;
-                const float f1 = ldexpf(1.0f, p1), f2 = ldexpf(1.0f, p - p1);
-                const float se = (s * f1) * f2;
-                kp = make_float4(se, 1.0f / se, f1, f2);
-            }
-        }
-        a.kparams[l] = kp;
-        reinterpret_cast<float *>(a.pool + a.geo.off_scales)[l] = s;
-    }
-    // Zero this layer's alignment gaps so the pool image is deterministic.
-    {
-        uint8_t *lay = a.pool + a.geo.off_layers + uint64_t(l) * a.geo.layer_stride;
-        const uint64_t nv = uint64_t(a.H) * uint64_t(a.T);
-        const uint64_t gaps[3][2] = {{nv * uint64_t(a.d), a.geo.sec_v},
-                                     {a.geo.sec_v + nv * uint64_t(3 * a.d / 8), a.geo.sec_sigma},
-                                     {a.geo.sec_sigma + 2 * nv, a.geo.layer_stride}};
-        for (int gi = 0; gi < 3; ++gi)
-            for (uint64_t i = gaps[gi][0] + threadIdx.x; i < gaps[gi][1]; i += ENC_THREADS) lay[i] = 0;
-    }
-    if (l == 0) {
-        // Error bits: every value-encode slot and every key partial.
-        uint32_t f = 0;
-        for (int i = threadIdx.x; i < a.G; i += ENC_THREADS) f |= a.vflags[i];
-        for (int i = threadIdx.x; i < a.L * a.P; i += ENC_THREADS)
-            if (a.partials[i] >= 0x7F80u) f |= FLAG_NONFINITE;
-        f = __reduce_or_sync(0xffffffffu, f);
-        __syncthreads();
-        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = f;
-        __syncthreads();
-        uint32_t *h = reinterpret_cast<uint32_t *>(a.pool);
-        // bytes 80..(off_layers): header tail and the gap after the scales
-        for (uint64_t i = 80 + threadIdx.x; i < POOL_HEADER_BYTES; i += ENC_THREADS) a.pool[i] = 0;
-        for (uint64_t i = a.geo.off_scales + 4ull * a.L + threadIdx.x; i < a.geo.off_layers; i += ENC_THREADS)
-            a.pool[i] = 0;
-        if (threadIdx.x == 0) {
-            uint32_t ff = 0;
-            for (int i = 0; i < ENC_WARPS; ++i) ff |= red[i];
-            h[0] = POOL_MAGIC;
-            h[1] = POOL_VERSION;
-            h[2] = uint32_t(a.L);
-            h[3] = uint32_t(a.H);
-            h[4] = uint32_t(a.d);
-            h[5] = uint32_t(a.T);
-            h[POOL_ERR_WORD] = ff;
-            h[7] = 0;
-            uint64_t *h64 = reinterpret_cast<uint64_t *>(a.pool);
-            h64[4] = a.geo.off_scales;
-            h64[5] = a.geo.off_layers;
-            h64[6] = a.geo.layer_stride;
-            h64[7] = a.geo.sec_v;
-            h64[8] = a.geo.sec_sigma;
-            h64[9] = a.geo.total;
-        }
-    }
-}
-
-// ---------------------------------------------------------------------------
-// Phase 3: int8 key codes ("PolyKV" 2.B.1).  q = the integer nearest to the
-// real k/s, ties to even.  Fast path: t = fma(k, 1/s, 1.5*2^23) rounds k/s'
-// (k/s within 1.6e-5) to an integer held in t's low mantissa bits, whose low
-// byte is the two's-complement code.  Only when that estimate is within 1e-4
-// of a half-integer is the decision taken exactly: the sign of
-// k - (q0 +- 1/2) s is exact under one fma rounding.
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t k_code_exact(float k, float s, float q0) {
-    const float hi = fmaf(-(q0 + 0.5f), s, k);
-    const float lo = fmaf(-(q0 - 0.5f), s, k);
-    int q = int(q0);
-    if (hi > 0.0f)
-        q += 1;
-    else if (hi == 0.0f)
-        q += (q & 1);
-    else if (lo < 0.0f)
-        q -= 1;
-    else if (lo == 0.0f)
-        q -= (q & 1);
-    return uint32_t(q) & 0xFFu;
-}
-
-template <bool PRESCALE>
-__device__ __forceinline__ uint2 k_quant8(uint4 w, float4 kp) {
-    float k[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
-                  bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
-    if (PRESCALE) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) k[i] = (k[i] * kp.z) * kp.w;
-    }
-    uint32_t t[8];
-    bool near = false;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const float tf = fmaf(k[i], kp.y, RNE_MAGIC);
-        const float q0 = tf - RNE_MAGIC;
-        const float e = fmaf(k[i], kp.y, -q0);
-        near |= fabsf(e) > 0.4999f;
-        t[i] = __float_as_uint(tf);
-    }
-    if (near) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float q0 = __uint_as_float(t[i]) - RNE_MAGIC;
-            t[i] = k_code_exact(k[i], kp.x, q0);
-        }
-    }
-    uint2 r;
-    r.x = __byte_perm(__byte_perm(t[0], t[1], 0x0040), __byte_perm(t[2], t[3], 0x0040), 0x5410);
-    r.y = __byte_perm(__byte_perm(t[4], t[5], 0x0040), __byte_perm(t[6], t[7], 0x0040), 0x5410);
-    return r;
-}
-
-__global__ void __launch_bounds__(ENC_THREADS) encode_keys(const __grid_constant__ EncodeArgs a, int blocks_per_layer) {
-    const int l = blockIdx.x / blocks_per_layer, b = blockIdx.x % blocks_per_layer;
-    const float4 kp = a.kparams[l];
-    const uint4 *src = a.k[l];
-    uint2 *dst = reinterpret_cast<uint2 *>(a.pool + a.geo.off_layers + uint64_t(l) * a.geo.layer_stride);
-    const uint64_t stride = uint64_t(blocks_per_layer) * ENC_THREADS;
-    const bool pre = kp.z != 1.0f || kp.w != 1.0f;
-    uint64_t c = uint64_t(b) * ENC_THREADS + threadIdx.x;
-    for (; c + stride < a.chunks; c += 2 * stride) {
-        const uint4 w0 = ld_stream_v4(src + c), w1 = ld_stream_v4(src + c + stride);
-        if (pre) {
-            dst[c] = k_quant8<true>(w0, kp);
-            dst[c + stride] = k_quant8<true>(w1, kp);
-        } else {
-            dst[c] = k_quant8<false>(w0, kp);
-            dst[c + stride] = k_quant8<false>(w1, kp);
-        }
-    }
-    for (; c < a.chunks; c += stride) {
-        const uint4 w0 = ld_stream_v4(src + c);
-        dst[c] = pre ? k_quant8<true>(w0, kp) : k_quant8<false>(w0, kp);
-    }
+    if (s_flag) write_header(a);
 }
 
 template <int D>
-static int phase1_occupancy() {
+static int encode_occupancy() {
     static int occ = 0;
     if (occ == 0) {
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, encode_phase1<D>, ENC_THREADS, 0) != cudaSuccess ||
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, encode_pool<D>, ENC_THREADS, 0) != cudaSuccess ||
             occ < 1)
             occ = 1;
     }
     return occ;
 }
 
+// Failure-path testing (kvp_test_fail_next_encode): consumed by the next
+// encode on the calling thread.
+static thread_local int t_fail_layer = -1;
+static thread_local uint32_t t_fail_spin = SPIN_LIMIT;
+
 }  // namespace kvp
 
 using namespace kvp;
+
+extern "C" int kvp_test_fail_next_encode(int layer, uint32_t spin_iters) {
+    t_fail_layer = layer < 0 ? -1 : layer;
+    t_fail_spin = layer < 0 ? SPIN_LIMIT : (spin_iters > 0 ? spin_iters : 1u);
+    return KVP_OK;
+}
 
 extern "C" size_t kvpool_workspace_bytes(const kvp_shape *s) {
     if (shape_ok(s) != KVP_OK) return 0;
@@ -493,8 +586,8 @@ extern "C" int kvpool_encode(const kvp_shape *s, const void *const *k_layers, co
     for (int l = L; l < KVP_MAX_LAYERS; ++l) a.k[l] = a.v[l] = nullptr;
     a.pool = static_cast<uint8_t *>(pool);
     uint8_t *w = static_cast<uint8_t *>(ws);
+    a.ctl = reinterpret_cast<EncodeCtl *>(w + wl.ctl);
     a.partials = reinterpret_cast<uint32_t *>(w + wl.partials);
-    a.vflags = reinterpret_cast<uint32_t *>(w + wl.vflags);
     a.kparams = reinterpret_cast<float4 *>(w + wl.kparams);
     a.geo = geo;
     a.chunks = chunks;
@@ -502,29 +595,47 @@ extern "C" int kvpool_encode(const kvp_shape *s, const void *const *k_layers, co
     a.H = s->n_kv_heads;
     a.T = s->n_tokens;
     a.d = s->head_dim;
-    a.P = absmax_blocks(chunks);
-    a.chunks_per_block = (chunks + a.P - 1) / a.P;
-    const int sms = sm_count();
-    const uint64_t nvec = uint64_t(a.H) * uint64_t(a.T);
-    const uint64_t vsteps = (nvec + (a.d == 128 ? 8 : 16) - 1) / (a.d == 128 ? 8 : 16) * uint64_t(L);
-    // persistent phase-1 grid: one block per resident slot, one flag slot per block
-    const uint64_t items = uint64_t(a.L) * uint64_t(a.P) + (vsteps + ENC_WARPS - 1) / ENC_WARPS;
-    const uint64_t gmax = uint64_t(sms) * uint64_t(a.d == 128 ? phase1_occupancy<128>() : phase1_occupancy<64>());
-    uint64_t g = items < gmax ? items : gmax;
-    if (g > VFLAG_SLOTS) g = VFLAG_SLOTS;
-    a.G = int(g < 1 ? 1 : g);
+    a.P = slices_per_layer(chunks);
+    a.chunks_per_slice = (chunks + a.P - 1) / a.P;
+    a.nvec = uint64_t(a.H) * uint64_t(a.T);
+    const int vpw = a.d == 128 ? 8 : 16;
+    a.steps_per_layer = (a.nvec + vpw - 1) / vpw;
+    const uint64_t vitems = (a.steps_per_layer + ENC_WARPS * VSTEPS - 1) / (ENC_WARPS * VSTEPS);
+    const uint64_t ipl = 2ull * uint64_t(a.P) + vitems;
+    if (ipl * uint64_t(L) >= (1ull << 32)) return KVP_ERR_SIZE;
+    a.vitems = uint32_t(vitems);
+    a.total_items = uint32_t(ipl * uint64_t(L));
+    const uint64_t resident =
+        uint64_t(sm_count()) * uint64_t(a.d == 128 ? encode_occupancy<128>() : encode_occupancy<64>());
+    const unsigned grid = unsigned(resident < a.total_items ? resident : a.total_items);
+    // Between a layer's last absmax slice and its first quantize slice the
+    // queue holds about two grids' worth of items, so the absmax slices are
+    // done by then: `lag` whole rounds (as many as needed, while the keys of
+    // lag+1 layers fit in 48 MB of L2), then a head of value batches for the
+    // rest.
+    const uint64_t kbytes = chunks * 16u;
+    const uint64_t want = 2ull * grid;
+    const uint64_t lag_l2 = kbytes >= (48ull << 20) ? 0 : (48ull << 20) / kbytes - 1;
+    uint64_t lag = (want + ipl - 1) / ipl;
+    if (lag > lag_l2) lag = lag_l2;
+    if (lag > uint64_t(L)) lag = uint64_t(L);
+    a.lag = uint32_t(lag);
+    const uint64_t covered = lag * ipl;
+    const uint64_t head = covered >= want ? 0 : want - covered;
+    a.vhead = uint32_t(head < vitems ? head : vitems);
+    a.seg0 = lag * uint32_t(a.P);
+    a.seg1 = a.seg0 + (uint32_t(L) - lag) * uint32_t(ipl);
+    a.fail_layer = t_fail_layer;
+    a.spin_limit = t_fail_spin;
+    t_fail_layer = -1;
+    t_fail_spin = SPIN_LIMIT;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(a.ctl, 0, sizeof(EncodeCtl), st) != cudaSuccess) return KVP_ERR_CUDA;
     if (a.d == 128)
-        encode_phase1<128><<<unsigned(a.G), ENC_THREADS, 0, st>>>(a);
+        encode_pool<128><<<grid, ENC_THREADS, 0, st>>>(a);
     else
-        encode_phase1<64><<<unsigned(a.G), ENC_THREADS, 0, st>>>(a);
-    encode_finalize<<<L, ENC_THREADS, 0, st>>>(a);
-    uint64_t bpl = (chunks + 2ull * ENC_THREADS * 4 - 1) / (2ull * ENC_THREADS * 4);
-    const uint64_t bmax = (uint64_t(sms) * 8 + L - 1) / L;
-    if (bpl > bmax) bpl = bmax;
-    if (bpl < 1) bpl = 1;
-    encode_keys<<<unsigned(uint64_t(L) * bpl), ENC_THREADS, 0, st>>>(a, int(bpl));
-    count_launch(3);
+        encode_pool<64><<<grid, ENC_THREADS, 0, st>>>(a);
+    count_launch(1);
     return launch_status();
 }

@@ -63,6 +63,7 @@ extern "C" {
 #define KVP_ERR_RANGE (-7)          /* a scale or zero point overflowed fp16 */
 #define KVP_ERR_BITS (-8)           /* CacheCard bitwidth not in {2,4,8,16}  */
 #define KVP_ERR_HEADER (-9)         /* not a pool / card, or shape mismatch  */
+#define KVP_ERR_TIMEOUT (-10)       /* a bounded device-side wait ran out    */
 
 /* Largest layer count one call accepts. */
 #define KVP_MAX_LAYERS 512
@@ -237,6 +238,16 @@ const char *kvp_strerror(int status);
 
 /* Number of kernels this library has launched in this process. */
 uint64_t kvp_launch_count(void);
+
+/* Failure-path testing.  The pool encoder's key-quantization work waits, with
+ * an iteration limit, for a per-layer "scale ready" flag set by other blocks
+ * of the same kernel; a wait that runs out is reported by kvpool_status as
+ * KVP_ERR_TIMEOUT and leaves the CUDA context usable.  Calling this with
+ * layer >= 0 makes the NEXT kvpool_encode on this thread leave that layer's
+ * flag unset and wait at most spin_iters iterations (about 100 ns each), so
+ * a test can exercise that path; layer < 0 restores normal operation.
+ * Returns KVP_OK. */
+int kvp_test_fail_next_encode(int layer, uint32_t spin_iters);
 
 #ifdef __cplusplus
 }

@@ -276,3 +276,20 @@ def test_full_size_sampled(name):
     for a in range(N - 1):
         for l in range(L):
             assert torch.equal(ck[a][l], ck[N - 1][l]) and torch.equal(cv[a][l], cv[N - 1][l])
+
+
+def test_encode_wait_timeout_is_reported_and_context_survives():
+    """The key-quantize work waits (bounded) for its layer's scale, released by
+    another block.  With that release withheld for one layer, the wait runs out
+    after a short limit, kvpool_status reports KVP_ERR_TIMEOUT, and the next
+    encode on the same context is correct."""
+    shape = (3, 4, 128, 64)
+    L, H, d, T = shape
+    ks, vs = cpu_inputs(L, H, T, d, seed=31)
+    assert kv.kvp_test_fail_next_encode(1, 20000) == kv.KVP_OK   # ~2-3 ms per waiting slice
+    pool, status, _ = gpu_encode(ks, vs, shape)
+    assert status == kv.KVP_ERR_TIMEOUT
+    pool2, status2, _ = gpu_encode(ks, vs, shape)                 # the hook applies to one call only
+    assert status2 == kv.KVP_OK
+    ora, flags, u = O.pool_encode(ks, vs, want_u=True)
+    assert_pool_parity(pool2.host(), ora, u, L, H, d, T)
