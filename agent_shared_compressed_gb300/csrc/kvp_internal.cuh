@@ -129,6 +129,18 @@ __device__ __forceinline__ uint4 ld_v4_policy(const void *p, uint64_t pol) {
     return r;
 }
 
+// Asynchronous 16-byte global -> shared copies (completion tracked per thread
+// with commit / wait groups).  src_bytes = 0 fills the 16 bytes with zeros
+// and reads nothing.
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem, uint32_t src_bytes, uint64_t pol) {
+    const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;"
+                 ::"r"(s), "l"(gmem), "r"(src_bytes), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
 // Acquire / release on a 32-bit flag in global memory (GPU scope).
 __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t *p) {
     uint32_t v;

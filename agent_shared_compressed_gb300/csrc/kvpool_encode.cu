@@ -10,7 +10,8 @@
 //      block that finishes the layer's last slice folds the P partials into
 //      the layer's scale s = m/127, writes it to the pool and the key
 //      quantizer's parameters to the workspace, and releases ready[l].
-//   2. the layer's value batches (4 warp steps of VPW vectors per warp),
+//   2. the layer's value batches (4 warp steps of VPW vectors per warp, each
+//      warp prefetching its next step into shared memory with cp.async),
 //      interleaved with P key slices "quantize": each waits (bounded) for
 //      ready[l], then writes the int8 codes = the integer nearest to the
 //      exact k/s.  The key slice is re-read soon after its first read, from
@@ -295,14 +296,16 @@ __device__ void quant_slice(const EncodeArgs &a, int l, uint32_t p, uint64_t pol
     const uint4 *src = a.k[l];
     uint2 *dst = reinterpret_cast<uint2 *>(a.pool + a.geo.off_layers + uint64_t(l) * a.geo.layer_stride);
     uint64_t c = c0 + threadIdx.x;
-    for (; c + ENC_THREADS < c1; c += 2 * ENC_THREADS) {
-        const uint4 w0 = ld_v4_policy(src + c, pol), w1 = ld_v4_policy(src + c + ENC_THREADS, pol);
+    for (; c + 3 * ENC_THREADS < c1; c += 4 * ENC_THREADS) {
+        uint4 w[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) w[u] = ld_v4_policy(src + c + u * ENC_THREADS, pol);
         if (pre) {
-            dst[c] = k_quant8<true>(w0, kp);
-            dst[c + ENC_THREADS] = k_quant8<true>(w1, kp);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) dst[c + u * ENC_THREADS] = k_quant8<true>(w[u], kp);
         } else {
-            dst[c] = k_quant8<false>(w0, kp);
-            dst[c + ENC_THREADS] = k_quant8<false>(w1, kp);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) dst[c + u * ENC_THREADS] = k_quant8<false>(w[u], kp);
         }
     }
     for (; c < c1; c += ENC_THREADS) {
@@ -328,8 +331,29 @@ __device__ uint32_t classify_nonfinite(const uint4 *vec, int nchunks) {
     return FLAG_RANGE;
 }
 
+// Issue the cp.async copies of one warp step's value data into a lane-private
+// buffer: lane l's 4 chunks at buf[j][lane] (chunk-major, so the later 16-byte
+// reads of a warp are conflict-free).  Lanes past the layer's last vector get
+// zeros.  Always commits one group.
 template <int D>
-__device__ uint32_t v_encode_step(const EncodeArgs &a, int layer, uint64_t step, uint8_t *stage, uint64_t pol) {
+__device__ __forceinline__ void v_prefetch(const EncodeArgs &a, int layer, uint64_t step, uint4 (*buf)[32],
+                                           uint64_t pol) {
+    constexpr int LPV = D / 32;
+    constexpr int VPW = 32 / LPV;
+    constexpr int CPV = D / 8;
+    const int lane = threadIdx.x & 31;
+    const int g = lane / LPV, l = lane % LPV;
+    const uint64_t n = step * VPW + g;
+    const bool valid = step < a.steps_per_layer && n < a.nvec;
+    const uint4 *vec = a.v[layer] + (valid ? n * CPV : 0);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) cp_async16(&buf[j][lane], vec + j * LPV + l, valid ? 16u : 0u, pol);
+    cp_async_commit();
+}
+
+template <int D>
+__device__ uint32_t v_encode_step(const EncodeArgs &a, int layer, uint64_t step, uint8_t *stage,
+                                  const uint4 (*buf)[32]) {
     constexpr int LPV = D / 32;      // lanes per vector
     constexpr int VPW = 32 / LPV;    // vectors per warp step
     constexpr int CPV = D / 8;       // 16-byte chunks per vector
@@ -350,7 +374,7 @@ __device__ uint32_t v_encode_step(const EncodeArgs &a, int layer, uint64_t step,
     // of chunk j: the first butterfly stage is applied while unpacking.
     uint4 w[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) w[j] = valid ? ld_v4_policy(vec + j * LPV + l, pol) : make_uint4(0, 0, 0, 0);
+    for (int j = 0; j < 4; ++j) w[j] = buf[j][lane];
     float2 x[4][4];
     float2 n2v = make_float2(0.0f, 0.0f);
 #pragma unroll
@@ -464,6 +488,7 @@ __device__ void write_header(const EncodeArgs &a) {
 template <int D>
 __global__ void __launch_bounds__(ENC_THREADS, 3) encode_pool(const __grid_constant__ EncodeArgs a) {
     __shared__ __align__(16) uint8_t stage[ENC_WARPS][384];
+    __shared__ __align__(16) uint4 vbuf[ENC_WARPS][2][4][32];  // per warp: two steps of value data
     __shared__ uint32_t red[ENC_WARPS];
     __shared__ uint32_t s_item[2], s_flag;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -511,11 +536,21 @@ __global__ void __launch_bounds__(ENC_THREADS, 3) encode_pool(const __grid_const
             else if (threadIdx.x == 0)
                 flags |= FLAG_TIMEOUT;
         } else {
+            // the warp's VSTEPS steps, each prefetched while the previous one is encoded
+            const uint64_t step0 = uint64_t(id) * VSTEPS * ENC_WARPS + warp;
+            v_prefetch<D>(a, layer, step0, vbuf[warp][0], drop);
 #pragma unroll 1
             for (int vs = 0; vs < VSTEPS; ++vs) {
-                const uint64_t step = (uint64_t(id) * VSTEPS + vs) * ENC_WARPS + warp;
-                if (step < a.steps_per_layer) flags |= v_encode_step<D>(a, layer, step, stage[warp], drop);
+                const uint64_t step = step0 + uint64_t(vs) * ENC_WARPS;
+                if (vs + 1 < VSTEPS)
+                    v_prefetch<D>(a, layer, step + ENC_WARPS, vbuf[warp][(vs + 1) & 1], drop);
+                else
+                    cp_async_commit();  // keep one group per iteration
+                cp_async_wait<1>();     // this step's group has landed
+                if (step < a.steps_per_layer)
+                    flags |= v_encode_step<D>(a, layer, step, stage[warp], vbuf[warp][vs & 1]);
             }
+            cp_async_wait<0>();
         }
     }
     flags = __reduce_or_sync(0xffffffffu, flags);
