@@ -66,8 +66,9 @@ def source_hash(paths):
 
 
 def recorded_traffic(workload, agents, tokens, layers):
-    """DRAM bytes per decode launch from a committed ncu summary, if it was
-    taken on the current decode kernel source (else None)."""
+    """DRAM bytes (read + write) of one decode launch from the committed ncu
+    capture, if it was taken on this workload and on the current decode
+    kernel source; else None."""
     try:
         with open(TRAFFIC_FILE) as f:
             rec = json.load(f)
@@ -75,10 +76,9 @@ def recorded_traffic(workload, agents, tokens, layers):
         return None
     if rec.get("source_hash") != source_hash(DECODE_SOURCES):
         return None
-    per_unit = rec.get("dram_bytes_per_output_byte")
-    if per_unit is None:
+    if (rec.get("workload"), rec.get("agents"), rec.get("tokens"), rec.get("layers")) != (workload, agents, tokens, layers):
         return None
-    return per_unit
+    return rec.get("dram_bytes_per_launch")
 
 
 class ClockSampler:
@@ -272,8 +272,7 @@ def run_ours(args, rank, world, local_rank):
     peak, peak_kind = hbm_peak()
     dec_ms = float(phase[:, 1].mean())
     achieved = sb["decode_alg"] / (dec_ms * 1e-3) / 1e9
-    per_unit = recorded_traffic(args.workload, w["N"], w["T"], w["L"])
-    traffic = None if per_unit is None else int(per_unit * (w["N"] * sb["raw"]))
+    traffic = recorded_traffic(args.workload, w["N"], w["T"], w["L"])
     names = ("encode", "decode", "pack", "unpack")
     algs = (sb["encode_alg"], sb["decode_alg"], sb["pack_alg"], sb["unpack_alg"])
     breakdown = {}
