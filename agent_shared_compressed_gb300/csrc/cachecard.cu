@@ -386,11 +386,11 @@ __global__ void __launch_bounds__(CARD_THREADS) card_unpack(const __grid_constan
 }
 
 template <typename K>
-static int card_grid(K kernel, uint64_t tasks) {
+static int card_grid(K kernel, uint64_t tasks, int waves) {
     int occ = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, CARD_THREADS, 0) != cudaSuccess || occ < 1) occ = 1;
     const uint64_t want = (tasks + CARD_WARPS - 1) / CARD_WARPS;
-    const uint64_t cap = uint64_t(sm_count()) * uint64_t(occ);
+    const uint64_t cap = uint64_t(sm_count()) * uint64_t(occ) * uint64_t(waves);
     return int(want < cap ? (want < 1 ? 1 : want) : cap);
 }
 
@@ -437,7 +437,7 @@ extern "C" int cachecard_pack(const kvp_shape *s, uint64_t model_id, int64_t pos
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     card_scan<<<1, SCAN_THREADS, 0, st>>>(a);
     const uint64_t tasks = uint64_t(L) * uint64_t(a.T) * 2u;
-    card_pack<<<card_grid(card_pack, tasks), CARD_THREADS, 0, st>>>(a);
+    card_pack<<<card_grid(card_pack, tasks, 1), CARD_THREADS, 0, st>>>(a);
     card_zero_tails<<<L, CARD_THREADS, 0, st>>>(a);
     count_launch(3);
     return launch_status();
@@ -480,7 +480,9 @@ extern "C" int cachecard_unpack(const void *card, const kvp_card_header *hdr, vo
     a.d = s.head_dim;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const uint64_t tasks = uint64_t(L) * uint64_t(a.T) * 2u;
-    card_unpack<<<card_grid(card_unpack, tasks), CARD_THREADS, 0, st>>>(a);
+    // store-heavy: several resident grids' worth of blocks spread the
+    // concurrent stores (as in the pool decoder)
+    card_unpack<<<card_grid(card_unpack, tasks, 3), CARD_THREADS, 0, st>>>(a);
     count_launch(1);
     return launch_status();
 }
