@@ -212,6 +212,19 @@ class Codec:
 # our arm
 # ----------------------------------------------------------------------------
 
+def aggregate_ranks(local_ms, steps, bytes_per_step, world, device):
+    """Whole-job throughput of N independent replicas: the slowest rank's
+    time (max over ranks) and the bytes all ranks processed.  Returns
+    (ms per step, GB/s)."""
+    total_ms = float(local_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / steps
+    return ms_per_step, world * bytes_per_step / (ms_per_step * 1e-3) / 1e9
+
+
 def run_ours(args, rank, world, local_rank):
     device = torch.device("cuda", local_rank)
     torch.cuda.set_device(device)
@@ -255,14 +268,7 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         torch.distributed.barrier()
     phase = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(4)] for e in ev])  # ms
-    step_ms = phase.sum(1)
-    total_ms = float(step_ms.sum())
-    if world > 1:
-        t = torch.tensor([total_ms], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
-    ms_per_step = total_ms / args.steps
-    value = world * sb["bf16_equiv"] / (ms_per_step * 1e-3) / 1e9
+    ms_per_step, value = aggregate_ranks(float(phase.sum()), args.steps, sb["bf16_equiv"], world, device)
 
     # end to end through the C ABI with host buffers: H2D of the step's K/V
     # (and bitwidths) from pinned memory, the four calls, D2H of the pool and

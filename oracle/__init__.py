@@ -31,11 +31,14 @@ _u64p = C.POINTER(C.c_uint64)
 
 
 def lib():
-    """Load (building first if needed) the oracle shared object."""
+    """Load (building first if needed) the oracle shared object.  The
+    KV_ORACLE_LIB environment variable points at another build of the same
+    source (used by the mutation test to load deliberately broken copies)."""
     global _lib
     if _lib is not None:
         return _lib
-    path = _build.build()
+    import os
+    path = os.environ.get("KV_ORACLE_LIB") or _build.build()
     L = C.CDLL(path)
     sig = {
         "orc_set_threads": (None, [C.c_int]),

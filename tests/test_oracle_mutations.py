@@ -1,0 +1,68 @@
+"""Mutation check of the oracle's pins: plant one plausible mistake at a time
+in a copy of the oracle's C source (a flipped sign, a wrong tie rule, a
+transposed index, a wrong constant, a wrong layout size ...), build it, and
+run the pin suite against it in a child process.  Every mutant must fail at
+least one pin; a mutant that passes would mean the pins cannot tell that
+mistake from the method.  Mistakes are planted on the CPU, in the oracle
+only."""
+import os
+import subprocess
+import sys
+import tempfile
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "kv_oracle.c")
+
+# (name, text in the oracle, replacement)
+MUTANTS = [
+    ("fwht sign", "x[j + h] = a - b;", "x[j + h] = b - a;"),
+    ("fwht pairing", "double a = x[j], b = x[j + h];", "double a = x[j], b = x[(j + h) % d];\n                (void)0; a = x[j]; b = x[j ^ h ^ (h > 1 ? 1 : 0)];"),
+    ("threshold tie to lower cell", "if (t[j] <= u) code++;", "if (t[j] < u) code++;"),
+    ("centroid typo", "-0.7560, -0.2451, 0.2451, 0.7560,", "-0.7560, -0.2451, 0.2451, 0.7650,"),
+    ("sigma normaliser", "double sigma = nrm / sqrt((double)d);", "double sigma = nrm / (double)d;"),
+    ("u normalised by sigma", "? y[i] / nrm : 0.0;", "? y[i] / (nrm / sqrt((double)d)) : 0.0;"),
+    ("k scale 128", "return (float)(m / 127.0);", "return (float)(m / 128.0);"),
+    ("k rounding ties away", "double q = nearbyint(k / (double)s);", "double q = round(k / (double)s);"),
+    # (A -128 lower clamp would be an equivalent mutant: with s = fl(m/127),
+    # |k/s| <= 127.00001, so no input reaches it.)
+    ("k decode divides", "return orc_f64_to_bf16((double)q * (double)s);", "return orc_f64_to_bf16((double)q / (double)s);"),
+    ("pack3 bit order", "w |= (uint32_t)(codes[8 * g + j] & 7u) << (3 * j);", "w |= (uint32_t)(codes[8 * g + j] & 7u) << (3 * (7 - j));"),
+    ("decode rescale", "out[i] = orc_f64_to_bf16(sig * z[i] / rs);", "out[i] = orc_f64_to_bf16(sig * z[i] / (double)d);"),
+    ("bf16 ties away", "double r = nearbyint(scaled);", "double r = floor(scaled + 0.5);"),
+    ("fp16 subnormal scale", "return sign | (uint16_t)ldexp(r, 24);", "return sign | (uint16_t)ldexp(r, 23);"),
+    ("lloyd mean sign", "double m = (pa - pb) / (Phi(b) - Phi(a));", "double m = (pb - pa) / (Phi(b) - Phi(a));"),
+    ("group scale levels", "double qmax = (double)((1 << b) - 1);", "double qmax = (double)(1 << b);"),
+    ("group zero point max", "uint16_t zb = orc_f64_to_f16(mn);", "uint16_t zb = orc_f64_to_f16(mx);"),
+    ("group bit order", "int bit = j * b + k;\n                out[bit >> 3]", "int bit = j * b + (b - 1 - k);\n                out[bit >> 3]"),
+    ("card params per group", "+ (uint64_t)H * (uint64_t)(d / 32) * 4ull);", "+ (uint64_t)H * (uint64_t)(d / 32) * 2ull);"),
+    ("pool sigma offset", "g.sec_sigma = al256(g.sec_v + nv * (uint64_t)(3 * d / 8));", "g.sec_sigma = al256(g.sec_v + nv * (uint64_t)(d / 2));"),
+    ("k absmax skips sign", "double a = fabs(orc_bf16_to_f64(k[i]));", "double a = orc_bf16_to_f64(k[i]);"),
+]
+
+
+def _build(text, out):
+    src = out + ".c"
+    with open(src, "w") as f:
+        f.write(text)
+    r = subprocess.run(["gcc", "-O2", "-std=gnu11", "-fPIC", "-shared", "-ffp-contract=off", "-fopenmp", src,
+                        "-o", out, "-lm"], capture_output=True, text=True)
+    if r.returncode != 0:  # no OpenMP on this host
+        r = subprocess.run(["gcc", "-O2", "-std=gnu11", "-fPIC", "-shared", "-ffp-contract=off", src, "-o", out,
+                            "-lm"], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_mutant(name, old, new):
+    text = open(SRC).read()
+    assert text.count(old) == 1, "mutation site not found exactly once: %r" % old
+    with tempfile.TemporaryDirectory() as tmp:
+        lib = os.path.join(tmp, "mutant.so")
+        _build(text.replace(old, new), lib)
+        env = dict(os.environ, KV_ORACLE_LIB=lib, PYTHONPATH=ROOT)
+        r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                            os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                           capture_output=True, text=True, env=env, cwd=ROOT, timeout=600)
+    assert r.returncode != 0, "mutant '%s' passed every pin:\n%s" % (name, r.stdout[-2000:])
