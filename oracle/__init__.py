@@ -71,6 +71,7 @@ def lib():
         "orc_card_pack": (C.c_uint32, [C.c_int] * 4 + [C.c_uint64, C.c_int64, _u8p,
                                                       C.POINTER(_u16p), C.POINTER(_u16p), _u8p, _dp]),
         "orc_card_unpack": (C.c_int, [_u8p, C.POINTER(_u16p), C.POINTER(_u16p)]),
+        "orc_pool_attend": (C.c_int, [_u8p, C.c_int, C.c_int, C.c_int, _u16p, C.c_double, _dp, _dp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -314,3 +315,20 @@ def card_unpack(card):
     if rc != 0:
         raise ValueError("oracle: not a version-1 card")
     return k, v
+
+
+# --- attention over the pool -------------------------------------------------
+
+def pool_attend(pool, layer, q_bits, scale):
+    """q_bits: uint16 [n_agents, n_q_heads, d] (bf16).  Returns (out fp64
+    [n_agents, n_q_heads, d], lse fp64 [n_agents, n_q_heads])."""
+    pool = _c(pool, np.uint8)
+    q = _c(q_bits, np.uint16)
+    na, nq, d = q.shape
+    out = np.zeros((na, nq, d), np.float64)
+    lse = np.zeros((na, nq), np.float64)
+    rc = lib().orc_pool_attend(_p(pool, _u8p), int(layer), na, nq, _p(q, _u16p), float(scale),
+                               _p(out, _dp), _p(lse, _dp))
+    if rc != 0:
+        raise ValueError("oracle: bad pool header, layer or head count")
+    return out, lse

@@ -751,3 +751,81 @@ int orc_card_unpack(const uint8_t *card, uint16_t *const *k_out, uint16_t *const
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------------- */
+/* Attention over the pool without materialising the caches.                  */
+/* [QKVShare] "Significance": a fully fused attention kernel over the          */
+/* quantized cache, deferred by the page; [PolyKV] 2.A: agents read the one    */
+/* shared pool.                                                                */
+/* ------------------------------------------------------------------------- */
+
+/* One decode step of attention for n_agents agents against layer `layer` of
+ * the pool: for agent a and query head j (GQA: query head j reads KV head
+ * j / (n_q_heads / H)),
+ *   s_t   = scale * (q . k_t),        k_t = q_t * s_l          (exact, fp64)
+ *   p_t   = exp(s_t - max s) / sum,   v_t = sigma_h * (H_d c_t) / sqrt(d)
+ *   out   = sum_t p_t v_t,            lse = log(sum_t exp(s_t))
+ * over the T pooled tokens.  q: bf16 [n_agents][n_q_heads][d]; out:
+ * [n_agents][n_q_heads][d]; lse: [n_agents][n_q_heads].  Keys and values are
+ * dequantized exactly (no bf16 rounding).  Returns 0, or -1 on a bad header
+ * or head count. */
+int orc_pool_attend(const uint8_t *pool, int layer, int n_agents, int n_q_heads, const uint16_t *q,
+                    double scale, double *out, double *lse)
+{
+    if (get32(pool) != 0x4C50564Bu || get32(pool + 4) != 1u) return -1;
+    int L = (int)get32(pool + 8), H = (int)get32(pool + 12);
+    int d = (int)get32(pool + 16), T = (int)get32(pool + 20);
+    if (layer < 0 || layer >= L || n_q_heads % H != 0) return -1;
+    orc_pool_geom g = pool_geom(L, H, d, T);
+    const uint8_t *lay = pool + g.off_layers + (uint64_t)layer * g.layer_stride;
+    float s;
+    memcpy(&s, pool + g.off_scales + 4u * (uint64_t)layer, 4);
+    const int8_t *kc = (const int8_t *)lay;
+    const uint8_t *vc = lay + g.sec_v;
+    const uint8_t *sg = lay + g.sec_sigma;
+    const int grp = n_q_heads / H;
+    /* dequantized values of every KV head, exact */
+    double *kf = (double *)malloc(sizeof(double) * (size_t)H * T * d);
+    double *vf = (double *)malloc(sizeof(double) * (size_t)H * T * d);
+    for (int64_t n = 0; n < (int64_t)H * T; n++) {
+        uint8_t codes[128];
+        uint16_t sh;
+        double z[128];
+        for (int i = 0; i < d; i++) kf[n * d + i] = (double)kc[n * d + i] * (double)s;
+        orc_unpack3(vc + (uint64_t)n * (uint64_t)(3 * d / 8), d, codes);
+        memcpy(&sh, sg + 2u * (uint64_t)n, 2);
+        for (int i = 0; i < d; i++) z[i] = CENTROID[codes[i]];
+        orc_fwht(z, d);
+        double sig = orc_f16_to_f64(sh);
+        for (int i = 0; i < d; i++) vf[n * d + i] = sig * z[i] / sqrt((double)d);
+    }
+#pragma omp parallel for schedule(static)
+    for (int aj = 0; aj < n_agents * n_q_heads; aj++) {
+        const int j = aj % n_q_heads;
+        const int h = j / grp;
+        const uint16_t *qv = q + (uint64_t)aj * d;
+        double *sc = (double *)malloc(sizeof(double) * (size_t)T);
+        double mx = -INFINITY;
+        for (int t = 0; t < T; t++) {
+            const double *kt = kf + ((uint64_t)h * T + t) * d;
+            double dot = 0.0;
+            for (int i = 0; i < d; i++) dot += orc_bf16_to_f64(qv[i]) * kt[i];
+            sc[t] = scale * dot;
+            if (sc[t] > mx) mx = sc[t];
+        }
+        double sum = 0.0;
+        for (int t = 0; t < T; t++) { sc[t] = exp(sc[t] - mx); sum += sc[t]; }
+        double *o = out + (uint64_t)aj * d;
+        for (int i = 0; i < d; i++) o[i] = 0.0;
+        for (int t = 0; t < T; t++) {
+            const double *vt = vf + ((uint64_t)h * T + t) * d;
+            const double p = sc[t] / sum;
+            for (int i = 0; i < d; i++) o[i] += p * vt[i];
+        }
+        lse[aj] = mx + log(sum);
+        free(sc);
+    }
+    free(kf);
+    free(vf);
+    return 0;
+}

@@ -39,6 +39,8 @@ MUTANTS = [
     ("card params per group", "+ (uint64_t)H * (uint64_t)(d / 32) * 4ull);", "+ (uint64_t)H * (uint64_t)(d / 32) * 2ull);"),
     ("pool sigma offset", "g.sec_sigma = al256(g.sec_v + nv * (uint64_t)(3 * d / 8));", "g.sec_sigma = al256(g.sec_v + nv * (uint64_t)(d / 2));"),
     ("k absmax skips sign", "double a = fabs(orc_bf16_to_f64(k[i]));", "double a = orc_bf16_to_f64(k[i]);"),
+    ("attend GQA head map", "const int h = j / grp;", "const int h = j % H;"),
+    ("attend lse drops max", "lse[aj] = mx + log(sum);", "lse[aj] = log(sum);"),
 ]
 
 

@@ -572,3 +572,65 @@ def test_card_invalid_bits():
     ks, vs = _tiny_kv(1, 1, 3, 64, 17)
     _, flags, _ = O.card_pack(ks, vs, np.array([2, 5, 4], np.uint8))
     assert flags == O.FLAG_BITS
+
+
+# --------------------------------------------------------------------------
+# attention over the pool (next row: fused attention on the quantized cache)
+# --------------------------------------------------------------------------
+
+def _decoded_fp64(pool, L, H, d, T, layer):
+    """Exact dequantized K and V of one layer, from the oracle's pieces."""
+    g = O.pool_geometry(L, H, d, T)
+    base = g["off_layers"] + layer * g["layer_stride"]
+    s = float(pool[g["off_scales"] + 4 * layer: g["off_scales"] + 4 * layer + 4].view(np.float32)[0])
+    kc = pool[base: base + H * T * d].view(np.int8).astype(np.float64).reshape(H, T, d) * s
+    vp = pool[base + g["sec_v"]: base + g["sec_v"] + H * T * 3 * d // 8].reshape(H * T, 3 * d // 8)
+    sig = pool[base + g["sec_sigma"]: base + g["sec_sigma"] + 2 * H * T].view(np.uint16)
+    Hm = scipy.linalg.hadamard(d).astype(np.float64)
+    c = O.centroids()
+    v = np.zeros((H * T, d))
+    for n in range(H * T):
+        codes = O.unpack3(vp[n], d)
+        v[n] = O.f16_to_f64(int(sig[n])) * (Hm @ c[codes]) / math.sqrt(d)
+    return kc, v.reshape(H, T, d)
+
+
+def test_pool_attend_against_library_softmax():
+    """Against numpy matmuls and scipy's softmax / logsumexp over the exactly
+    dequantized caches, with GQA (4 query heads per KV head) and 3 agents."""
+    import scipy.special
+    L, H, T, d = 2, 2, 37, 64
+    ks, vs = _tiny_kv(L, H, T, d, 21)
+    pool, _, _ = O.pool_encode(ks, vs)
+    rng = np.random.default_rng(22)
+    na, nq = 3, 8
+    q = _bf16(rng.normal(size=(na, nq, d)))
+    qf = _f(q)
+    for layer in range(L):
+        out, lse = O.pool_attend(pool, layer, q, 0.125)
+        kf, vf = _decoded_fp64(pool, L, H, d, T, layer)
+        for a in range(na):
+            for j in range(nq):
+                h = j // (nq // H)
+                sc = 0.125 * (kf[h] @ qf[a, j])
+                np.testing.assert_allclose(out[a, j], scipy.special.softmax(sc) @ vf[h], rtol=1e-10, atol=1e-12)
+                assert abs(lse[a, j] - scipy.special.logsumexp(sc)) < 1e-10
+
+
+def test_pool_attend_closed_forms():
+    L, H, T, d = 1, 1, 16, 128
+    ks, vs = _tiny_kv(L, H, T, d, 23)
+    pool, _, _ = O.pool_encode(ks, vs)
+    kf, vf = _decoded_fp64(pool, L, H, d, T, 0)
+    # q = 0: uniform weights -> the mean of the values, lse = log T
+    out, lse = O.pool_attend(pool, 0, np.zeros((1, 1, d), np.uint16), 1.0)
+    np.testing.assert_allclose(out[0, 0], vf[0].mean(0), rtol=1e-12, atol=1e-14)
+    assert abs(lse[0, 0] - math.log(T)) < 1e-12
+    # a large scale makes the softmax one-hot on the top-scoring token
+    q = _bf16(kf[0, 5][None, None, :] / np.abs(kf[0, 5]).max())
+    sc = kf[0] @ _f(q)[0, 0]
+    top = np.sort(sc)
+    scale = 60.0 / (top[-1] - top[-2])          # the runner-up weighs < e^-60
+    out, lse = O.pool_attend(pool, 0, q, scale)
+    np.testing.assert_allclose(out[0, 0], vf[0, int(np.argmax(sc))], rtol=1e-9, atol=1e-12)
+    assert abs(lse[0, 0] - scale * top[-1]) < 1e-9 * scale * abs(top[-1])
