@@ -64,6 +64,9 @@ _SIGS = {
     "kvpool_decode_into": (C.c_int, [_vp, C.POINTER(Shape), C.c_int, C.c_int, C.c_int,
                                      C.POINTER(_vp), C.POINTER(_vp), _vp]),
     "kvpool_status": (C.c_int, [_vp, _vp]),
+    "kvpool_attend_workspace_bytes": (C.c_size_t, [C.POINTER(Shape), C.c_int, C.c_int]),
+    "kvpool_attend": (C.c_int, [_vp, C.POINTER(Shape), C.c_int, C.c_int, C.c_int, _vp, C.c_float, _vp, _vp, _vp,
+                                C.c_size_t, _vp]),
     "kvpool_encode_noalloc": (C.c_int, [C.POINTER(Shape), C.POINTER(_vp), C.POINTER(_vp), _vp, C.c_size_t, _vp]),
     "cachecard_bytes": (C.c_size_t, [C.POINTER(Shape), C.POINTER(C.c_uint8)]),
     "cachecard_pack": (C.c_int, [C.POINTER(Shape), C.c_uint64, C.c_int64, _vp, C.POINTER(_vp),
@@ -165,6 +168,16 @@ def kvpool_decode_into(pool, shape, layer_begin, layer_end, n_agents, k_dst, v_d
     """k_dst/v_dst: n_agents * n_layers pointers, agent-major (a*L + l)."""
     return load().kvpool_decode_into(_addr(pool), C.byref(_shape(shape)), int(layer_begin), int(layer_end),
                                      int(n_agents), _ptrs(k_dst), _ptrs(v_dst), _stream(stream))
+
+
+def kvpool_attend_workspace_bytes(shape, n_agents, n_q_heads):
+    return int(load().kvpool_attend_workspace_bytes(C.byref(_shape(shape)), int(n_agents), int(n_q_heads)))
+
+
+def kvpool_attend(pool, shape, layer, n_agents, n_q_heads, q, scale, out, lse, ws, ws_bytes, stream=None):
+    return load().kvpool_attend(_addr(pool), C.byref(_shape(shape)), int(layer), int(n_agents), int(n_q_heads),
+                                _addr(q), C.c_float(scale), _addr(out), _addr(lse), _addr(ws), int(ws_bytes),
+                                _stream(stream))
 
 
 def kvpool_status(pool, stream=None):

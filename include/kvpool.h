@@ -184,6 +184,34 @@ int kvpool_encode_noalloc(const kvp_shape *shape, const void *const *k_layers,
                           void *stream);
 
 /* ---------------------------------------------------------------------- */
+/* Attention over the pool                                                 */
+/* ---------------------------------------------------------------------- */
+
+/* Bytes of device workspace kvpool_attend needs (0 for an invalid shape or
+ * head count).  Holds per-split partial results; no initialisation. */
+size_t kvpool_attend_workspace_bytes(const kvp_shape *shape, int n_agents, int n_q_heads);
+
+/* One decode step of attention of n_agents agents' queries over layer
+ * `layer` of the pool, computed from the compressed bytes without writing any
+ * bf16 cache: the fused attention over the quantized cache that "QKVShare"
+ * (Significance) leaves as future work, on "PolyKV" 2.A's shared pool.
+ *  q: device bf16 [n_agents][n_q_heads][head_dim], 16-byte aligned; query head
+ *    j reads KV head j / (n_q_heads / n_kv_heads) (n_q_heads a multiple of
+ *    n_kv_heads: grouped-query attention).
+ *  For each (agent, head): s_t = scale * (q . k_t) over the T pooled tokens
+ *    with k_t = code_t * s_layer; out = sum_t softmax(s)_t v_t with v_t the
+ *    decoded value (sigma_t * H_d c_t / sqrt(d), accumulated in the rotated
+ *    domain and transformed once); lse = log sum_t exp(s_t) (natural log), so a
+ *    caller can merge with attention over its own further tokens.
+ *  out: device fp32 [n_agents][n_q_heads][head_dim] (16-byte aligned); lse:
+ *    device fp32 [n_agents][n_q_heads].  ws: kvpool_attend_workspace_bytes.
+ *  Precision: scores are exact products accumulated in fp32; probabilities
+ *  times sigma enter the value product as fp16. */
+int kvpool_attend(const void *pool, const kvp_shape *shape, int layer, int n_agents, int n_q_heads,
+                  const void *q, float scale, float *out, float *lse, void *ws, size_t ws_bytes,
+                  void *stream);
+
+/* ---------------------------------------------------------------------- */
 /* CacheCard                                                               */
 /* ---------------------------------------------------------------------- */
 
