@@ -337,6 +337,22 @@ __global__ void __launch_bounds__(256) attend_combine(const __grid_constant__ At
     if (lane == 0) a.lse[uint64_t(ag) * a.NQ + j] = m + __logf(l);
 }
 
+// The split kernel's dynamic shared memory exceeds the default 48 KB: raise
+// the limit once per device (the first call on a device does it).
+template <int D>
+static bool attend_smem_ready() {
+    static bool done[64] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    if (!done[dev]) {
+        if (cudaFuncSetAttribute(attend_split<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(AttendSmem<D>::bytes)) != cudaSuccess)
+            return false;
+        done[dev] = true;
+    }
+    return true;
+}
+
 struct AttendPlan {
     int G, QH, QHP, nsub, per_split, nsplit;
     uint64_t part_off, stats_off, total;
@@ -407,18 +423,12 @@ extern "C" int kvpool_attend(const void *pool, const kvp_shape *s, int layer, in
     const dim3 grid(unsigned(a.H), unsigned(a.nsplit));
     const unsigned cgrid = unsigned((uint64_t(n_agents) * n_q_heads * 32 + 255) / 256);
     if (s->head_dim == 128) {
-        const size_t sm = AttendSmem<128>::bytes;
-        if (cudaFuncSetAttribute(attend_split<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm)) !=
-            cudaSuccess)
-            return KVP_ERR_CUDA;
-        attend_split<128><<<grid, ATT_THREADS, sm, st>>>(a);
+        if (!attend_smem_ready<128>()) return KVP_ERR_CUDA;
+        attend_split<128><<<grid, ATT_THREADS, AttendSmem<128>::bytes, st>>>(a);
         attend_combine<128><<<cgrid, 256, 0, st>>>(a);
     } else {
-        const size_t sm = AttendSmem<64>::bytes;
-        if (cudaFuncSetAttribute(attend_split<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm)) !=
-            cudaSuccess)
-            return KVP_ERR_CUDA;
-        attend_split<64><<<grid, ATT_THREADS, sm, st>>>(a);
+        if (!attend_smem_ready<64>()) return KVP_ERR_CUDA;
+        attend_split<64><<<grid, ATT_THREADS, AttendSmem<64>::bytes, st>>>(a);
         attend_combine<64><<<cgrid, 256, 0, st>>>(a);
     }
     count_launch(2);

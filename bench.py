@@ -17,6 +17,7 @@ import argparse
 import ctypes
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -470,6 +471,79 @@ def run_reference(args, rank, world):
 
 # ----------------------------------------------------------------------------
 
+def run_attend(args):
+    """Pool attention for one decode step of every agent over every layer
+    (a forward pass's worth of attention over the shared context), straight
+    from the compressed pool.  Llama-3-8B has 32 query heads over 8 KV heads;
+    SmolLM2-1.7B 32 over 32."""
+    torch.cuda.set_device(0)
+    kv.load()
+    w = workload(args)
+    L, H, d, T, N = w["L"], w["H"], w["d"], w["T"], w["N"]
+    nq = 32
+    c = Codec(w, torch.device("cuda", 0), seed=0)
+    st = torch.cuda.current_stream()
+    c.encode(st)
+    kv.check(kv.kvpool_status(c.pool, st), "encode")
+    g = torch.Generator(device="cuda").manual_seed(1)
+    q = torch.randn(N, nq, d, generator=g, device="cuda").to(torch.bfloat16)
+    out = torch.empty(N, nq, d, dtype=torch.float32, device="cuda")
+    lse = torch.empty(N, nq, dtype=torch.float32, device="cuda")
+    wsb = kv.kvpool_attend_workspace_bytes(c.shape, N, nq)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    scale = 1.0 / math.sqrt(d)
+
+    def step():
+        cur = torch.cuda.current_stream()
+        for l in range(L):
+            kv.check(kv.kvpool_attend(c.pool, c.shape, l, N, nq, q, scale, out, lse, ws, wsb, cur), "attend")
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    # the 2*L launches of a step are replayed from a CUDA graph, so the host's
+    # per-call cost does not pace the GPU
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = kv.kvp_launch_count()
+    e0.record(st)
+    for _ in range(args.steps):
+        graph.replay()
+    e1.record(st)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    launches = 2 * L * args.steps  # replayed graph nodes (the counter sees only direct launches)
+    pool_bytes = c.pool_bytes
+    io = N * nq * d * 2 + N * nq * (d + 1) * 4
+    flops = 2.0 * 2.0 * N * nq * T * d * L
+    peak, kind = hbm_peak()
+    gbs = (pool_bytes + L * io) / (ms * 1e-3) / 1e9
+    # what the agents would otherwise read: N bf16 caches of every layer
+    caches = N * 2 * L * H * T * d * 2
+    return {
+        "metric": "pool attention: agents' decode-step attention over all layers from the compressed pool",
+        "value": round(ms * 1e3 / L, 2), "unit": "us per layer", "higher_is_better": False,
+        "ms_per_step": round(ms, 4), "steps": args.steps, "warmup": args.warmup, "n_gpus": 1,
+        "dtype": "bf16 q / int8 k / 3-bit v", "data": "synthetic",
+        "config": {"workload": args.workload, "layers": L, "kv_heads": H, "q_heads": nq, "head_dim": d,
+                   "tokens": T, "agents": N},
+        "pool_GBps": round(gbs, 1), "frac_of_measured_peak": round(gbs / peak, 4), "peak_kind": kind,
+        "tensor_TFLOPs": round(flops / (ms * 1e-3) / 1e12, 2),
+        "bytes_read_vs_bf16_caches": round((pool_bytes + L * io) / caches, 4),
+        "gpu_launches": int(launches),
+        "graph": True,
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -482,12 +556,19 @@ def main():
     ap.add_argument("--layers", type=int, default=0)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--mode", choices=["step", "attend"], default="step",
+                    help="step: the whole codec path (default); attend: attention over the pool")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.mode == "attend":
+        if rank == 0:
+            print(json.dumps(run_attend(args)), flush=True)
+        return
 
     if args.impl == "reference":
         if rank != 0:
