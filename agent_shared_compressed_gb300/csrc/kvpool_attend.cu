@@ -11,20 +11,25 @@
 // so values are accumulated in the rotated domain and transformed once per
 // query at the end.
 //
-// attend_split: one block per (KV head, token split); the split's 64-token
-// sub-chunks are staged in shared memory (keys as exact bf16 integers,
-// centroids as fp16 hi + lo parts, transposed), and two warp-level tensor-core
-// products run per sub-chunk: S = Q K^T (bf16 in, fp32 accumulate: exact
-// products) and A += P' C (P' = p * sigma in fp16; C = C_hi + C_lo), with an
-// online softmax across sub-chunks.  attend_combine merges the splits
-// (log-sum-exp), applies the inverse transform and writes out / lse.
+// attend_split: one block per (KV head, token split).  The split's 64-token
+// sub-chunks are staged in shared memory, double-buffered (keys as exact bf16
+// integers, centroids as fp16, both [token][dim]), with the next sub-chunk's
+// raw bytes already in registers while the current one is multiplied.  Warp
+// (mi, th) owns query rows mi*16.. and a token slice th of every sub-chunk; it
+// runs its own online softmax over that slice with warp-level tensor-core
+// products: S = Q K^T (bf16 in, fp32 accumulate: exact products) and
+// A += P' C (P' = p * sigma, fp16, kept in registers as the next product's
+// A operand).  The warps' states are merged in shared memory at the end.
+// attend_combine merges the splits (log-sum-exp), applies the inverse
+// transform and writes out / lse.  Exponentials are base 2 throughout.
 #include "kvp_vec.cuh"
 
 namespace kvp {
 
 constexpr int ATT_THREADS = 256;
+constexpr int ATT_WARPS = ATT_THREADS / 32;
 constexpr int ATT_TC = 64;  // tokens per sub-chunk
-constexpr int ATT_MT = 64;  // query rows per tile
+constexpr int ATT_MT = 64;  // query rows per tile (the Q buffer)
 constexpr int ATT_TARGET_BLOCKS = 304;
 
 struct AttendArgs {
@@ -33,286 +38,385 @@ struct AttendArgs {
     float *out;         // [NA][NQ][d]
     float *lse;         // [NA][NQ]
     float *part;        // [H][nsplit][QHP][d] rotated-domain partial sums
-    float2 *stats;      // [H][nsplit][QHP]: (running max, running sum)
+    float2 *stats;      // [H][nsplit][QHP]: (running max, running sum), base 2
     PoolGeom geo;
     float scale;
     int L, H, T, layer, NA, NQ, G, QH, QHP, nsub, per_split, nsplit;
 };
 
-__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
+__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%0,%1,%2,%3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
-__device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                        uint32_t b0, uint32_t b1) {
+__device__ __forceinline__ void mma_f16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%0,%1,%2,%3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// Four 8x8 b16 tiles from shared memory; lane l supplies the row address of
+// tile l/8, row l%8.  .trans delivers each tile transposed.
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void *p) {
+    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(a));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void *p) {
+    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(a));
+}
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&h);
 }
 
 template <int D>
 struct AttendSmem {
-    static constexpr int KW = D / 2 + 4;       // 32-bit words per Q / K row (padded: conflict-free fragments)
-    static constexpr int CW = ATT_TC / 2 + 4;  // words per P / C row
-    static constexpr size_t words = size_t(ATT_MT) * KW + size_t(ATT_TC) * KW + size_t(ATT_MT) * CW +
-                                    2 * size_t(D) * CW + ATT_TC + 4 * ATT_MT + 2 * ATT_MT;
-    static constexpr size_t bytes = words * 4 + 16 * 4;  // + the centroid table
+    static constexpr int RW = D / 2 + 4;  // 32-bit words per Q / K / C row (16-B multiple, conflict-free ldmatrix)
+    static constexpr int MS = D + 8;      // floats per row of a warp's merge slot (conflict-free float2 stores)
+    static constexpr size_t q_words = size_t(ATT_MT) * RW;
+    static constexpr size_t tile_words = size_t(ATT_TC) * RW;  // one K or C buffer
+    static constexpr size_t stage_words = q_words + 4 * tile_words + 2 * ATT_TC + 64;  // Q, K[2], C[2], sig[2], lut
+    static constexpr size_t merge_words = size_t(ATT_WARPS) * (16 * MS + 32);
+    static constexpr size_t bytes = 4 * (stage_words > merge_words ? stage_words : merge_words);
+};
+
+// Raw bytes of one sub-chunk held by one thread between load and staging.
+template <int D>
+struct RawChunk {
+    uint4 k[D / 64];  // codes of token tid/4, bytes (tid%4)*D/4 ..
+    uint32_t v[3];    // 32 value codes (12 bytes) of one token
+    uint32_t sig;     // fp16 bits of token tid's sigma (tid < 64)
 };
 
 template <int D>
+__device__ __forceinline__ void load_chunk(RawChunk<D> &r, const uint8_t *lay, const PoolGeom &geo, uint64_t vbase,
+                                           int t0, int T, int tid) {
+    constexpr int VPT = D / 32;  // 32-code value items per token
+    const int tk = t0 + (tid >> 2);
+    if (tk < T) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(lay + (vbase + tk) * D + (tid & 3) * (D / 4));
+#pragma unroll
+        for (int u = 0; u < D / 64; ++u) r.k[u] = ld_stream_v4(src + u);
+    } else {
+#pragma unroll
+        for (int u = 0; u < D / 64; ++u) r.k[u] = make_uint4(0, 0, 0, 0);
+    }
+    const int tv = t0 + tid / VPT;
+    if (tid < ATT_TC * VPT && tv < T) {
+        const uint8_t *src = lay + geo.sec_v + (vbase + tv) * (3 * D / 8) + (tid % VPT) * 12;
+#pragma unroll
+        for (int u = 0; u < 3; ++u) r.v[u] = ld_stream_u32(src + 4 * u);
+    } else {
+        r.v[0] = r.v[1] = r.v[2] = 0u;
+    }
+    r.sig = 0u;
+    if (tid < ATT_TC && t0 + tid < T)
+        r.sig = reinterpret_cast<const uint16_t *>(lay + geo.sec_sigma)[vbase + t0 + tid];
+}
+
+// Registers -> shared tiles: keys int8 -> exact bf16 (|q| <= 127 has at most
+// 7 significant bits); value codes -> fp16 centroids, two dims per word via
+// the pair table.
+template <int D>
+__device__ __forceinline__ void stage_chunk(const RawChunk<D> &r, uint32_t *Kb, uint32_t *Cs, float *sig,
+                                            const uint32_t *lut, int tid) {
+    constexpr int RW = AttendSmem<D>::RW, VPT = D / 32;
+    {
+        uint32_t *row = Kb + (tid >> 2) * RW + (tid & 3) * (D / 8);
+#pragma unroll
+        for (int u = 0; u < D / 64; ++u) {
+            const uint32_t w4[4] = {r.k[u].x, r.k[u].y, r.k[u].z, r.k[u].w};
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                const uint32_t x = w4[b] ^ 0x80808080u;
+                float f[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    f[i] = __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7650u | i)) - 8388736.0f;
+                row[8 * u + 2 * b] = __byte_perm(__float_as_uint(f[0]), __float_as_uint(f[1]), 0x7632u);
+                row[8 * u + 2 * b + 1] = __byte_perm(__float_as_uint(f[2]), __float_as_uint(f[3]), 0x7632u);
+            }
+        }
+    }
+    if (tid < ATT_TC * VPT) {
+        uint32_t *row = Cs + (tid / VPT) * RW + (tid % VPT) * 16;
+        const uint32_t w[4] = {r.v[0], r.v[1], r.v[2], 0u};
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {  // codes 2k, 2k+1: bits 6k .. 6k+5
+            const int bit = 6 * k, wi = bit >> 5, sh = bit & 31;
+            row[k] = lut[__funnelshift_r(w[wi], w[wi + 1], sh) & 63u];
+        }
+    }
+    if (tid < ATT_TC) sig[tid] = __half2float(__ushort_as_half(static_cast<uint16_t>(r.sig)));
+}
+
+// TPW: tokens of a sub-chunk per warp (32: four 16-row tiles per pass; 16:
+// two 16-row tiles per pass, for blocks with at most 32 query rows).
+template <int D, int TPW>
 __global__ void __launch_bounds__(ATT_THREADS, 2) attend_split(const __grid_constant__ AttendArgs a) {
     using SM = AttendSmem<D>;
-    constexpr int KW = SM::KW, CW = SM::CW;
-    constexpr int NT_S = 32 / 8;         // S: a warp covers 32 tokens (4 n8 tiles)
-    constexpr int NT_V = D / 2 / 8;      // PV: a warp covers D/2 dims
+    constexpr int RW = SM::RW, MSW = SM::MS;
+    constexpr int MS = TPW / 8;       // 16-row tiles per pass
+    constexpr int RP = 16 * MS;       // query rows per pass
+    constexpr int NS = TPW / 8;       // S n-tiles per warp
+    constexpr int NV = D / 8;         // PV n-tiles per warp (all dims)
     extern __shared__ __align__(16) uint32_t smem[];
-    uint32_t *Qs = smem;                  // [ATT_MT][KW]  bf16 pairs
-    uint32_t *Kb = Qs + ATT_MT * KW;      // [ATT_TC][KW]  bf16 pairs
-    uint32_t *Ps = Kb + ATT_TC * KW;      // [ATT_MT][CW]  fp16 pairs
-    uint32_t *Ch = Ps + ATT_MT * CW;      // [D][CW]       fp16 pairs, token-contiguous
-    uint32_t *Cl = Ch + D * CW;           // [D][CW]
-    float *sig = reinterpret_cast<float *>(Cl + D * CW);  // [ATT_TC]
-    float *rmax = sig + ATT_TC;           // [2][ATT_MT] per-half row maxima
-    float *rsum = rmax + 2 * ATT_MT;      // [2][ATT_MT] per-half row sums
-    float *row_m = rsum + 2 * ATT_MT;     // [ATT_MT] running max
-    float *row_l = row_m + ATT_MT;        // [ATT_MT] running sum
-    __half2 *ctab = reinterpret_cast<__half2 *>(row_l + ATT_MT);  // [8] (hi, lo) per code
+    uint32_t *Qs = smem;                       // [ATT_MT][RW] bf16 pairs
+    uint32_t *Kb = Qs + SM::q_words;           // [2][ATT_TC][RW] bf16 pairs
+    uint32_t *Cs = Kb + 2 * SM::tile_words;    // [2][ATT_TC][RW] fp16 pairs
+    float *sig = reinterpret_cast<float *>(Cs + 2 * SM::tile_words);  // [2][ATT_TC]
+    uint32_t *lut = reinterpret_cast<uint32_t *>(sig + 2 * ATT_TC);   // [64] (c[lo], c[hi]) fp16 pairs
+    float *mrg = reinterpret_cast<float *>(smem);  // after the loop: [warps][16][MSW] acc, then [warps][32] m, l
 
     const int h = blockIdx.x, split = blockIdx.y;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, tig = lane & 3;
-    const int mi = warp & 3, nh = warp >> 2;  // m16 tile; half (tokens for S, dims for PV)
-    const int r0 = mi * 16;
+    const int mi = warp % MS, th = warp / MS;
     const uint8_t *lay = a.pool + a.geo.off_layers + uint64_t(a.layer) * a.geo.layer_stride;
-    const float qk = a.scale * reinterpret_cast<const float *>(a.pool + a.geo.off_scales)[a.layer];
-    const uint64_t vbase = uint64_t(h) * uint64_t(a.T);  // first vector of this KV head
+    const float qk2 = a.scale * 1.4426950408889634f *
+                      reinterpret_cast<const float *>(a.pool + a.geo.off_scales)[a.layer];  // base-2 score scale
+    const uint64_t vbase = uint64_t(h) * uint64_t(a.T);
     const int sub0 = split * a.per_split, sub1 = min(a.nsub, sub0 + a.per_split);
 
-    if (tid < 8) {  // centroids as fp16 hi + lo parts: c = hi + lo to ~2^-22 relative
-        const float c = centroid_e4(uint32_t(tid)) * 1e-4f;
-        const __half hi = __float2half_rn(c);
-        ctab[tid] = __halves2half2(hi, __float2half_rn(c - __half2float(hi)));
-    }
-
-    for (int m0 = 0; m0 < a.QH; m0 += ATT_MT) {
-        __syncthreads();
-        // query rows m0..m0+63 of this KV head: agent r / G, head h*G + r % G
-        for (int e = tid; e < ATT_MT * (D / 8); e += ATT_THREADS) {
+    for (int m0 = 0; m0 < a.QH; m0 += RP) {
+        __syncthreads();  // the previous pass's merge slots are read
+        RawChunk<D> raw;  // the first sub-chunk's bytes are requested before the query tile
+        load_chunk<D>(raw, lay, a.geo, vbase, sub0 * ATT_TC, a.T, tid);
+        if (tid < 64) {
+            const float c0 = centroid_e4(uint32_t(tid & 7)) * 1e-4f, c1 = centroid_e4(uint32_t(tid >> 3)) * 1e-4f;
+            lut[tid] = pack_half2(c0, c1);
+        }
+        for (int e = tid; e < RP * (D / 8); e += ATT_THREADS) {
             const int r = e / (D / 8), c8 = e % (D / 8);
             uint4 v = make_uint4(0, 0, 0, 0);
             if (m0 + r < a.QH) {
                 const int ag = (m0 + r) / a.G, j = h * a.G + (m0 + r) % a.G;
                 v = *reinterpret_cast<const uint4 *>(a.q + (uint64_t(ag) * a.NQ + j) * D + c8 * 8);
             }
-            *reinterpret_cast<uint4 *>(Qs + r * KW + c8 * 4) = v;
+            *reinterpret_cast<uint4 *>(Qs + r * RW + c8 * 4) = v;
         }
-        if (tid < ATT_MT) {
-            row_m[tid] = -INFINITY;
-            row_l[tid] = 0.0f;
-        }
-        float acc[NT_V][4];
+        const bool active = m0 + mi * 16 < a.QH;  // warp-uniform: this tile has real rows
+        float acc[NV][4];
 #pragma unroll
-        for (int nt = 0; nt < NT_V; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.0f;
+        for (int nt = 0; nt < NV; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.0f;
+        float mx[2] = {-INFINITY, -INFINITY}, ls[2] = {0.0f, 0.0f};
 
+        __syncthreads();  // the pair table and the query tile are in
         for (int sub = sub0; sub < sub1; ++sub) {
-            const int t0 = sub * ATT_TC;
-            __syncthreads();  // (1) the previous sub-chunk's tiles and statistics are settled
-            {   // keys: int8 codes -> exact bf16 (|q| <= 127: at most 7 significant bits)
-                const int t = tid >> 2, part = tid & 3;  // 64 tokens x 4 quarters of d
-                constexpr int DQ = D / 4;                // codes per quarter (32 or 16)
-                uint32_t wds[DQ / 4];
-                if (t0 + t < a.T) {
-                    const uint4 *src = reinterpret_cast<const uint4 *>(lay + (vbase + t0 + t) * D + part * DQ);
-#pragma unroll
-                    for (int u = 0; u < DQ / 16; ++u) {
-                        const uint4 w = ld_stream_v4(src + u);
-                        wds[4 * u] = w.x;
-                        wds[4 * u + 1] = w.y;
-                        wds[4 * u + 2] = w.z;
-                        wds[4 * u + 3] = w.w;
-                    }
-                } else {
-#pragma unroll
-                    for (int u = 0; u < DQ / 4; ++u) wds[u] = 0u;  // codes 0 (scores are masked anyway)
-                }
-                uint32_t *row = Kb + t * KW + part * (DQ / 2);
-#pragma unroll
-                for (int u = 0; u < DQ / 4; ++u) {
-                    const uint32_t x = wds[u] ^ 0x80808080u;
-                    float f[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        f[i] = __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7650u | i)) - 8388736.0f;
-                    row[2 * u] = __byte_perm(__float_as_uint(f[0]), __float_as_uint(f[1]), 0x7632u);
-                    row[2 * u + 1] = __byte_perm(__float_as_uint(f[2]), __float_as_uint(f[3]), 0x7632u);
-                }
-            }
-            // values: 3-bit codes -> centroid hi / lo, transposed [dim][token]; each
-            // work item is 32 codes (12 bytes) of one token
-            for (int e = tid; e < ATT_TC * (D / 32); e += ATT_THREADS) {
-                const int t = e & (ATT_TC - 1), ig = e / ATT_TC;
-                const bool ok = t0 + t < a.T;
-                uint32_t w[4];
-#pragma unroll
-                for (int u = 0; u < 3; ++u)
-                    w[u] = ok ? ld_stream_u32(lay + a.geo.sec_v + (vbase + t0 + t) * (3 * D / 8) + ig * 12 + 4 * u)
-                              : 0u;
-                w[3] = 0u;
-                __half *chh = reinterpret_cast<__half *>(Ch), *cll = reinterpret_cast<__half *>(Cl);
-#pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    const int bit = 3 * c, wi = bit >> 5, sh = bit & 31;
-                    uint32_t code = w[wi] >> sh;
-                    if (sh > 29) code |= w[wi + 1] << (32 - sh);
-                    const __half2 cv = ctab[code & 7u];
-                    const int dim = ig * 32 + c;
-                    chh[dim * (2 * CW) + t] = ok ? __low2half(cv) : __float2half_rn(0.0f);
-                    cll[dim * (2 * CW) + t] = ok ? __high2half(cv) : __float2half_rn(0.0f);
-                }
-            }
-            if (tid < ATT_TC)
-                sig[tid] = (t0 + tid < a.T) ? __half2float(__ushort_as_half(reinterpret_cast<const uint16_t *>(
-                                                  lay + a.geo.sec_sigma)[vbase + t0 + tid]))
-                                            : 0.0f;
-            __syncthreads();  // (2) tiles staged
+            const int buf = (sub - sub0) & 1;
+            uint32_t *Kt = Kb + buf * SM::tile_words, *Ct = Cs + buf * SM::tile_words;
+            float *st = sig + buf * ATT_TC;
+            stage_chunk<D>(raw, Kt, Ct, st, lut, tid);
+            if (sub + 1 < sub1) load_chunk<D>(raw, lay, a.geo, vbase, (sub + 1) * ATT_TC, a.T, tid);
+            __syncthreads();  // this buffer is staged; every warp is done with the other one
+            if (!active) continue;
 
-            // S = Q K^T: rows r0.., tokens nh*32..
-            float s[NT_S][4];
+            // S = Q K^T for rows mi*16.., tokens th*TPW..
+            float s[NS][4];
 #pragma unroll
-            for (int nt = 0; nt < NT_S; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.0f;
+            for (int nt = 0; nt < NS; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.0f;
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks) {
-                const int kw = ks * 8;
-                const uint32_t a0 = Qs[(r0 + g) * KW + kw + tig], a1 = Qs[(r0 + g + 8) * KW + kw + tig];
-                const uint32_t a2 = Qs[(r0 + g) * KW + kw + tig + 4], a3 = Qs[(r0 + g + 8) * KW + kw + tig + 4];
+                uint32_t qa[4];
+                ldsm_x4(qa, Qs + (mi * 16 + (lane & 15)) * RW + ks * 8 + (lane >> 4) * 4);
 #pragma unroll
-                for (int nt = 0; nt < NT_S; ++nt) {
-                    const int n0 = nh * 32 + nt * 8;
-                    mma_bf16(s[nt], a0, a1, a2, a3, Kb[(n0 + g) * KW + kw + tig], Kb[(n0 + g) * KW + kw + tig + 4]);
+                for (int np = 0; np < NS; np += 2) {
+                    uint32_t kb[4];
+                    const int tok = th * TPW + np * 8 + (lane & 7) + ((lane >> 4) << 3);
+                    ldsm_x4(kb, Kt + tok * RW + ks * 8 + ((lane >> 3) & 1) * 4);
+                    mma_bf16(s[np], qa, kb[0], kb[1]);
+                    mma_bf16(s[np + 1], qa, kb[2], kb[3]);
                 }
             }
-            float mx0 = -INFINITY, mx1 = -INFINITY;
+            // online softmax over this warp's slice (rows g and g+8 of the tile)
+            const int tbase = sub * ATT_TC + th * TPW;
+            float cm[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-            for (int nt = 0; nt < NT_S; ++nt) {
-                const int tk = t0 + nh * 32 + nt * 8 + 2 * tig;
-                s[nt][0] = tk < a.T ? s[nt][0] * qk : -INFINITY;
-                s[nt][1] = tk + 1 < a.T ? s[nt][1] * qk : -INFINITY;
-                s[nt][2] = tk < a.T ? s[nt][2] * qk : -INFINITY;
-                s[nt][3] = tk + 1 < a.T ? s[nt][3] * qk : -INFINITY;
-                mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
-                mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
+            for (int nt = 0; nt < NS; ++nt) {
+                const int tk = tbase + nt * 8 + 2 * tig;
+                s[nt][0] = tk < a.T ? s[nt][0] * qk2 : -INFINITY;
+                s[nt][1] = tk + 1 < a.T ? s[nt][1] * qk2 : -INFINITY;
+                s[nt][2] = tk < a.T ? s[nt][2] * qk2 : -INFINITY;
+                s[nt][3] = tk + 1 < a.T ? s[nt][3] * qk2 : -INFINITY;
+                cm[0] = fmaxf(cm[0], fmaxf(s[nt][0], s[nt][1]));
+                cm[1] = fmaxf(cm[1], fmaxf(s[nt][2], s[nt][3]));
+            }
+            float ref[2], al[2];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                cm[i] = fmaxf(cm[i], __shfl_xor_sync(0xffffffffu, cm[i], 1));
+                cm[i] = fmaxf(cm[i], __shfl_xor_sync(0xffffffffu, cm[i], 2));
+                const float nm = fmaxf(mx[i], cm[i]);
+                ref[i] = nm == -INFINITY ? 0.0f : nm;  // a slice with no token yet: p = 0, nothing to rescale
+                al[i] = exp2f(mx[i] - ref[i]);
+                mx[i] = nm;
+                ls[i] *= al[i];
             }
 #pragma unroll
-            for (int m = 1; m < 4; m <<= 1) {
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, m));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, m));
+            for (int nt = 0; nt < NV; ++nt) {
+                acc[nt][0] *= al[0];
+                acc[nt][1] *= al[0];
+                acc[nt][2] *= al[1];
+                acc[nt][3] *= al[1];
             }
-            if (tig == 0) {
-                rmax[nh * ATT_MT + r0 + g] = mx0;
-                rmax[nh * ATT_MT + r0 + g + 8] = mx1;
-            }
-            __syncthreads();  // (3) both halves' maxima in
-
-            // new running max of the warp's two rows (every sub-chunk has a valid token)
-            const float om0 = row_m[r0 + g], om1 = row_m[r0 + g + 8];
-            const float nm0 = fmaxf(om0, fmaxf(rmax[r0 + g], rmax[ATT_MT + r0 + g]));
-            const float nm1 = fmaxf(om1, fmaxf(rmax[r0 + g + 8], rmax[ATT_MT + r0 + g + 8]));
-            float sm0 = 0.0f, sm1 = 0.0f;
+            // P' = p * sigma as fp16 A fragments: the S accumulator of n-tiles
+            // 2kk, 2kk+1 is the A operand of k-step kk
 #pragma unroll
-            for (int nt = 0; nt < NT_S; ++nt) {
-                const int tl = nh * 32 + nt * 8 + 2 * tig;
-                const float p0 = __expf(s[nt][0] - nm0), p1 = __expf(s[nt][1] - nm0);
-                const float p2 = __expf(s[nt][2] - nm1), p3 = __expf(s[nt][3] - nm1);
-                sm0 += p0 + p1;
-                sm1 += p2 + p3;
-                const __half2 u = __floats2half2_rn(p0 * sig[tl], p1 * sig[tl + 1]);
-                const __half2 v = __floats2half2_rn(p2 * sig[tl], p3 * sig[tl + 1]);
-                Ps[(r0 + g) * CW + tl / 2] = *reinterpret_cast<const uint32_t *>(&u);
-                Ps[(r0 + g + 8) * CW + tl / 2] = *reinterpret_cast<const uint32_t *>(&v);
-            }
+            for (int kk = 0; kk < NS / 2; ++kk) {
+                uint32_t pa[4];
 #pragma unroll
-            for (int m = 1; m < 4; m <<= 1) {
-                sm0 += __shfl_xor_sync(0xffffffffu, sm0, m);
-                sm1 += __shfl_xor_sync(0xffffffffu, sm1, m);
-            }
-            if (tig == 0) {
-                rsum[nh * ATT_MT + r0 + g] = sm0;
-                rsum[nh * ATT_MT + r0 + g + 8] = sm1;
-            }
-            __syncthreads();  // (4) P' and the partial sums in
-
-            // rescale to the new max, then A += P' (C_hi + C_lo): rows r0.., dims nh*D/2..
-            const float al0 = __expf(om0 - nm0), al1 = __expf(om1 - nm1);  // 0 on the first sub-chunk
+                for (int hf = 0; hf < 2; ++hf) {
+                    const int nt = 2 * kk + hf;
+                    const int tl = th * TPW + nt * 8 + 2 * tig;
+                    const float s0 = st[tl], s1 = st[tl + 1];
+                    const float p0 = exp2f(s[nt][0] - ref[0]), p1 = exp2f(s[nt][1] - ref[0]);
+                    const float p2 = exp2f(s[nt][2] - ref[1]), p3 = exp2f(s[nt][3] - ref[1]);
+                    ls[0] += p0 + p1;
+                    ls[1] += p2 + p3;
+                    pa[2 * hf] = pack_half2(p0 * s0, p1 * s1);
+                    pa[2 * hf + 1] = pack_half2(p2 * s0, p3 * s1);
+                }
+                // A += P' C over tokens th*TPW + kk*16 .. +15, every dim
 #pragma unroll
-            for (int nt = 0; nt < NT_V; ++nt) {
-                acc[nt][0] *= al0;
-                acc[nt][1] *= al0;
-                acc[nt][2] *= al1;
-                acc[nt][3] *= al1;
-            }
-#pragma unroll
-            for (int ks = 0; ks < ATT_TC / 16; ++ks) {
-                const int kw = ks * 8;
-                const uint32_t a0 = Ps[(r0 + g) * CW + kw + tig], a1 = Ps[(r0 + g + 8) * CW + kw + tig];
-                const uint32_t a2 = Ps[(r0 + g) * CW + kw + tig + 4], a3 = Ps[(r0 + g + 8) * CW + kw + tig + 4];
-#pragma unroll
-                for (int nt = 0; nt < NT_V; ++nt) {
-                    const int n0 = nh * (D / 2) + nt * 8;
-                    mma_f16(acc[nt], a0, a1, a2, a3, Ch[(n0 + g) * CW + kw + tig], Ch[(n0 + g) * CW + kw + tig + 4]);
-                    mma_f16(acc[nt], a0, a1, a2, a3, Cl[(n0 + g) * CW + kw + tig], Cl[(n0 + g) * CW + kw + tig + 4]);
+                for (int np = 0; np < NV; np += 2) {
+                    uint32_t cb[4];
+                    const int tok = th * TPW + kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+                    ldsm_x4_t(cb, Ct + tok * RW + np * 4 + (lane >> 4) * 4);
+                    mma_f16(acc[np], pa, cb[0], cb[1]);
+                    mma_f16(acc[np + 1], pa, cb[2], cb[3]);
                 }
             }
-            __syncthreads();  // (5) every warp has read the old statistics and P'
-            if (tid < ATT_MT) {
-                const float om = row_m[tid];
-                const float nm = fmaxf(om, fmaxf(rmax[tid], rmax[ATT_MT + tid]));
-                row_l[tid] = row_l[tid] * __expf(om - nm) + rsum[tid] + rsum[ATT_MT + tid];
-                row_m[tid] = nm;
+        }
+        // merge the token slices of each row tile
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            ls[i] += __shfl_xor_sync(0xffffffffu, ls[i], 1);
+            ls[i] += __shfl_xor_sync(0xffffffffu, ls[i], 2);
+        }
+        __syncthreads();  // every warp is done with the staged tiles
+        {
+            float *slot = mrg + warp * (16 * MSW);
+#pragma unroll
+            for (int nt = 0; nt < NV; ++nt) {
+                *reinterpret_cast<float2 *>(slot + g * MSW + nt * 8 + 2 * tig) = make_float2(acc[nt][0], acc[nt][1]);
+                *reinterpret_cast<float2 *>(slot + (g + 8) * MSW + nt * 8 + 2 * tig) =
+                    make_float2(acc[nt][2], acc[nt][3]);
+            }
+            float *ms = mrg + ATT_WARPS * 16 * MSW + warp * 32;
+            if (tig == 0) {
+                ms[g] = mx[0];
+                ms[g + 8] = mx[1];
+                ms[16 + g] = ls[0];
+                ms[16 + g + 8] = ls[1];
             }
         }
         __syncthreads();
-        // this split's partial sums and statistics for the tile's real rows
         const uint64_t pbase = (uint64_t(h) * a.nsplit + split) * uint64_t(a.QHP);
+        for (int e = tid; e < RP * (D / 4); e += ATT_THREADS) {
+            const int r = e / (D / 4), c4 = e % (D / 4);
+            if (m0 + r >= a.QH) continue;
+            const int ti = r >> 4, rr = r & 15;
+            const float *ms = mrg + ATT_WARPS * 16 * MSW;
+            float M = -INFINITY;
 #pragma unroll
-        for (int nt = 0; nt < NT_V; ++nt) {
-            const int dim = nh * (D / 2) + nt * 8 + 2 * tig;
-            const int ra = m0 + r0 + g, rb = ra + 8;
-            if (ra < a.QH)
-                *reinterpret_cast<float2 *>(a.part + (pbase + ra) * D + dim) = make_float2(acc[nt][0], acc[nt][1]);
-            if (rb < a.QH)
-                *reinterpret_cast<float2 *>(a.part + (pbase + rb) * D + dim) = make_float2(acc[nt][2], acc[nt][3]);
+            for (int w = ti; w < ATT_WARPS; w += MS) M = fmaxf(M, ms[w * 32 + rr]);
+            float4 o = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            float l = 0.0f;
+#pragma unroll
+            for (int w = ti; w < ATT_WARPS; w += MS) {
+                const float f = exp2f(ms[w * 32 + rr] - M);  // 0 for a slice that saw no token
+                const float4 x = *reinterpret_cast<const float4 *>(mrg + w * (16 * MSW) + rr * MSW + c4 * 4);
+                o.x = fmaf(f, x.x, o.x);
+                o.y = fmaf(f, x.y, o.y);
+                o.z = fmaf(f, x.z, o.z);
+                o.w = fmaf(f, x.w, o.w);
+                l = fmaf(f, ms[w * 32 + 16 + rr], l);
+            }
+            *reinterpret_cast<float4 *>(a.part + (pbase + m0 + r) * D + c4 * 4) = o;
+            if (c4 == 0) a.stats[pbase + m0 + r] = make_float2(M, l);
         }
-        if (tid < ATT_MT && m0 + tid < a.QH) a.stats[pbase + m0 + tid] = make_float2(row_m[tid], row_l[tid]);
     }
 }
 
-// One warp per (agent, query head): merge the splits, inverse transform.
+// One 128-thread block per (agent, query head): merge the splits, inverse
+// transform.  Warp w merges splits w, w+4, ... online, with the statistics
+// and partial rows of up to eight splits in flight at once; the four warps'
+// states are then merged in shared memory and warp 0 applies the transform.
+constexpr int CMB_THREADS = 128;
+constexpr int CMB_WARPS = CMB_THREADS / 32;
+
 template <int D>
-__global__ void __launch_bounds__(256) attend_combine(const __grid_constant__ AttendArgs a) {
+__global__ void __launch_bounds__(CMB_THREADS) attend_combine(const __grid_constant__ AttendArgs a) {
     constexpr int PL = D / 32;  // dims per lane, indices lane*PL + e
-    const int wq = int((blockIdx.x * blockDim.x + threadIdx.x) >> 5), lane = threadIdx.x & 31;
-    if (wq >= a.NA * a.NQ) return;
-    const int ag = wq / a.NQ, j = wq % a.NQ;
+    constexpr int UN = 8;       // splits in flight per warp
+    __shared__ float wacc[CMB_WARPS][D];
+    __shared__ float wml[CMB_WARPS][2];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ag = blockIdx.x / a.NQ, j = blockIdx.x % a.NQ;
     const int h = j / a.G, r = ag * a.G + j % a.G;
+    const uint64_t row0 = uint64_t(h) * a.nsplit * uint64_t(a.QHP) + r;  // split sp: row0 + sp * QHP
     float m = -INFINITY, l = 0.0f, acc[PL];
 #pragma unroll
     for (int e = 0; e < PL; ++e) acc[e] = 0.0f;
-    for (int sp = 0; sp < a.nsplit; ++sp) {
-        const uint64_t row = (uint64_t(h) * a.nsplit + sp) * uint64_t(a.QHP) + r;
-        const float2 st = a.stats[row];
-        const float nm = fmaxf(m, st.x);
-        const float a1 = __expf(m - nm), a2 = __expf(st.x - nm);
-        l = l * a1 + st.y * a2;
-        const float *pp = a.part + row * D + lane * PL;
+    for (int sp0 = warp; sp0 < a.nsplit; sp0 += CMB_WARPS * UN) {
+        float2 st[UN];
+        float v[UN][PL];
 #pragma unroll
-        for (int e = 0; e < PL; ++e) acc[e] = acc[e] * a1 + pp[e] * a2;
-        m = nm;
+        for (int u = 0; u < UN; ++u) {
+            const int sp = sp0 + u * CMB_WARPS;
+            st[u] = make_float2(-INFINITY, 0.0f);
+#pragma unroll
+            for (int e = 0; e < PL; ++e) v[u][e] = 0.0f;
+            if (sp < a.nsplit) {
+                const uint64_t row = row0 + uint64_t(sp) * a.QHP;
+                st[u] = a.stats[row];
+                const float *pp = a.part + row * D + lane * PL;
+                if constexpr (PL == 4) {
+                    const float4 x = *reinterpret_cast<const float4 *>(pp);
+                    v[u][0] = x.x, v[u][1] = x.y, v[u][2] = x.z, v[u][3] = x.w;
+                } else {
+                    const float2 x = *reinterpret_cast<const float2 *>(pp);
+                    v[u][0] = x.x, v[u][1] = x.y;
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < UN; ++u) {
+            if (st[u].x == -INFINITY) continue;  // past the last split
+            const float nm = fmaxf(m, st[u].x);
+            const float f0 = exp2f(m - nm), f1 = exp2f(st[u].x - nm);
+            l = l * f0 + st[u].y * f1;
+#pragma unroll
+            for (int e = 0; e < PL; ++e) acc[e] = acc[e] * f0 + v[u][e] * f1;
+            m = nm;
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < PL; ++e) wacc[warp][lane * PL + e] = acc[e];
+    if (lane == 0) {
+        wml[warp][0] = m;
+        wml[warp][1] = l;
+    }
+    __syncthreads();
+    if (warp != 0) return;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < CMB_WARPS; ++w) M = fmaxf(M, wml[w][0]);
+    l = 0.0f;
+#pragma unroll
+    for (int e = 0; e < PL; ++e) acc[e] = 0.0f;
+#pragma unroll
+    for (int w = 0; w < CMB_WARPS; ++w) {
+        const float f = wml[w][0] == -INFINITY ? 0.0f : exp2f(wml[w][0] - M);  // a warp with no split
+        l = fmaf(f, wml[w][1], l);
+#pragma unroll
+        for (int e = 0; e < PL; ++e) acc[e] = fmaf(f, wacc[w][lane * PL + e], acc[e]);
     }
     // unnormalised Walsh-Hadamard transform over d: register bits, then lane bits
 #pragma unroll
@@ -334,23 +438,31 @@ __global__ void __launch_bounds__(256) attend_combine(const __grid_constant__ At
     float *o = a.out + (uint64_t(ag) * a.NQ + j) * D + lane * PL;
 #pragma unroll
     for (int e = 0; e < PL; ++e) o[e] = acc[e] * f;
-    if (lane == 0) a.lse[uint64_t(ag) * a.NQ + j] = m + __logf(l);
+    if (lane == 0) a.lse[uint64_t(ag) * a.NQ + j] = (M + __log2f(l)) * 0.6931471805599453f;
 }
 
 // The split kernel's dynamic shared memory exceeds the default 48 KB: raise
 // the limit once per device (the first call on a device does it).
-template <int D>
+template <int D, int TPW>
 static bool attend_smem_ready() {
     static bool done[64] = {false};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
     if (!done[dev]) {
-        if (cudaFuncSetAttribute(attend_split<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(attend_split<D, TPW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  int(AttendSmem<D>::bytes)) != cudaSuccess)
             return false;
         done[dev] = true;
     }
     return true;
+}
+
+template <int D, int TPW>
+static int attend_launch(const AttendArgs &a, dim3 grid, unsigned cgrid, cudaStream_t st) {
+    if (!attend_smem_ready<D, TPW>()) return KVP_ERR_CUDA;
+    attend_split<D, TPW><<<grid, ATT_THREADS, AttendSmem<D>::bytes, st>>>(a);
+    attend_combine<D><<<cgrid, CMB_THREADS, 0, st>>>(a);
+    return KVP_OK;
 }
 
 struct AttendPlan {
@@ -421,16 +533,14 @@ extern "C" int kvpool_attend(const void *pool, const kvp_shape *s, int layer, in
     a.nsplit = p.nsplit;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const dim3 grid(unsigned(a.H), unsigned(a.nsplit));
-    const unsigned cgrid = unsigned((uint64_t(n_agents) * n_q_heads * 32 + 255) / 256);
-    if (s->head_dim == 128) {
-        if (!attend_smem_ready<128>()) return KVP_ERR_CUDA;
-        attend_split<128><<<grid, ATT_THREADS, AttendSmem<128>::bytes, st>>>(a);
-        attend_combine<128><<<cgrid, 256, 0, st>>>(a);
-    } else {
-        if (!attend_smem_ready<64>()) return KVP_ERR_CUDA;
-        attend_split<64><<<grid, ATT_THREADS, AttendSmem<64>::bytes, st>>>(a);
-        attend_combine<64><<<cgrid, 256, 0, st>>>(a);
-    }
+    const unsigned cgrid = unsigned(n_agents) * unsigned(n_q_heads);  // one block per query
+    // at most 32 query rows per KV head: two 16-row tiles, four 16-token slices
+    const bool narrow = p.QH <= 32;
+    if (s->head_dim == 128)
+        rc = narrow ? attend_launch<128, 16>(a, grid, cgrid, st) : attend_launch<128, 32>(a, grid, cgrid, st);
+    else
+        rc = narrow ? attend_launch<64, 16>(a, grid, cgrid, st) : attend_launch<64, 32>(a, grid, cgrid, st);
+    if (rc != KVP_OK) return rc;
     count_launch(2);
     return launch_status();
 }

@@ -171,7 +171,7 @@ def step_bytes(w, pool_bytes, card_bytes):
 class Codec:
     """Device buffers for one replica of the step and the calls that run it."""
 
-    def __init__(self, w, device, seed=0):
+    def __init__(self, w, device, seed=0, outputs=True):
         L, H, d, T, N = w["L"], w["H"], w["d"], w["T"], w["N"]
         self.w = w
         self.shape = kv.Shape(L, H, d, T)
@@ -184,10 +184,12 @@ class Codec:
         self.pool = torch.empty(self.pool_bytes, dtype=torch.uint8, device=device)
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
         self.card = torch.empty(self.card_bytes, dtype=torch.uint8, device=device)
-        self.caches_k = [torch.empty((H, T, d), dtype=torch.bfloat16, device=device) for _ in range(N * L)]
-        self.caches_v = [torch.empty((H, T, d), dtype=torch.bfloat16, device=device) for _ in range(N * L)]
-        self.out_k = [torch.empty((H, T, d), dtype=torch.bfloat16, device=device) for _ in range(L)]
-        self.out_v = [torch.empty((H, T, d), dtype=torch.bfloat16, device=device) for _ in range(L)]
+        # agent caches and card output (skipped when only the pool is needed)
+        n_out = N * L if outputs else 0
+        self.caches_k = [torch.empty((H, T, d), dtype=torch.bfloat16, device=device) for _ in range(n_out)]
+        self.caches_v = [torch.empty((H, T, d), dtype=torch.bfloat16, device=device) for _ in range(n_out)]
+        self.out_k = [torch.empty((H, T, d), dtype=torch.bfloat16, device=device) for _ in range(L if outputs else 0)]
+        self.out_v = [torch.empty((H, T, d), dtype=torch.bfloat16, device=device) for _ in range(L if outputs else 0)]
         self.hdr = None
 
     def encode(self, st):
@@ -481,7 +483,7 @@ def run_attend(args):
     w = workload(args)
     L, H, d, T, N = w["L"], w["H"], w["d"], w["T"], w["N"]
     nq = 32
-    c = Codec(w, torch.device("cuda", 0), seed=0)
+    c = Codec(w, torch.device("cuda", 0), seed=0, outputs=False)
     st = torch.cuda.current_stream()
     c.encode(st)
     kv.check(kv.kvpool_status(c.pool, st), "encode")

@@ -5,7 +5,7 @@ over the same pool image (exact dequantization).
 
 Criteria: out within 1e-3 of the largest |value| of the KV head's tokens
 (probabilities times sigma enter the value product as fp16, relative 2^-11;
-centroids as fp16 hi + lo); lse within 1e-4 (1 + |lse|)."""
+centroids as fp16, relative 2.5e-4 at most); lse within 1e-4 (1 + |lse|)."""
 import math
 
 import numpy as np
@@ -57,10 +57,13 @@ def _check(pool_img, shape, layer, q_bits, scale, out, lse):
     vmax = np.abs((vref[0][layer].astype(np.uint32) << 16).view(np.float32)).reshape(H, -1).max(1)
     na, nq, _ = q_bits.shape
     G = nq // H
+    worst = 0.0
     for j in range(nq):
         tol = 1e-3 * vmax[j // G] + 1e-6
         err = np.abs(out[:, j] - ref[:, j]).max()
         assert err <= tol, "head %d: max error %g > %g" % (j, err, tol)
+        worst = max(worst, err / tol)
+    print("attend %s layer %d: worst out error / tolerance %.3f" % (tuple(shape), layer, worst))
     assert np.all(np.abs(lse - ref_lse) <= 1e-4 * (1 + np.abs(ref_lse)))
 
 
@@ -71,6 +74,7 @@ CASES = [  # (L, H, d, T, n_agents, n_q_heads)
     (1, 32, 64, 300, 3, 32),     # SmolLM2-like: no grouping (1 query head per KV head)
     (1, 1, 128, 1, 1, 1),        # one token
     (1, 2, 128, 4096, 2, 8),     # many sub-chunks per split
+    (1, 4, 128, 1000, 4, 32),    # 32 rows per KV head: two 16-row tiles, four token slices
 ]
 
 
