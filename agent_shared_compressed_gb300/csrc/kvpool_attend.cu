@@ -87,29 +87,35 @@ struct AttendSmem {
 };
 
 // Raw bytes of one sub-chunk held by one thread between load and staging.
+// Thread mapping: the eight lanes of a quarter-warp take eight consecutive
+// tokens of the same part of the row, so their 16-byte shared stores fall on
+// eight distinct bank groups (row strides are 4 words mod 32).
+//   keys:   token (tid & 7) + 8 * (tid >> 5), part (tid >> 3) & 3 of 4 (D/4 codes)
+//   values: token (tid & 7) + 8 * ((tid >> 3) / VPT), item (tid >> 3) % VPT (32 codes)
 template <int D>
 struct RawChunk {
-    uint4 k[D / 64];  // codes of token tid/4, bytes (tid%4)*D/4 ..
-    uint32_t v[3];    // 32 value codes (12 bytes) of one token
-    uint32_t sig;     // fp16 bits of token tid's sigma (tid < 64)
+    uint4 k[D / 64];
+    uint32_t v[3];
+    uint32_t sig;  // fp16 bits of token tid's sigma (tid < 64)
 };
 
 template <int D>
 __device__ __forceinline__ void load_chunk(RawChunk<D> &r, const uint8_t *lay, const PoolGeom &geo, uint64_t vbase,
                                            int t0, int T, int tid) {
     constexpr int VPT = D / 32;  // 32-code value items per token
-    const int tk = t0 + (tid >> 2);
+    const int q = tid >> 3, l8 = tid & 7;
+    const int tk = t0 + l8 + 8 * (q >> 2);
     if (tk < T) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(lay + (vbase + tk) * D + (tid & 3) * (D / 4));
+        const uint4 *src = reinterpret_cast<const uint4 *>(lay + (vbase + tk) * D + (q & 3) * (D / 4));
 #pragma unroll
         for (int u = 0; u < D / 64; ++u) r.k[u] = ld_stream_v4(src + u);
     } else {
 #pragma unroll
         for (int u = 0; u < D / 64; ++u) r.k[u] = make_uint4(0, 0, 0, 0);
     }
-    const int tv = t0 + tid / VPT;
-    if (tid < ATT_TC * VPT && tv < T) {
-        const uint8_t *src = lay + geo.sec_v + (vbase + tv) * (3 * D / 8) + (tid % VPT) * 12;
+    const int tv = t0 + l8 + 8 * (q / VPT);
+    if (q < 8 * VPT && tv < T) {
+        const uint8_t *src = lay + geo.sec_v + (vbase + tv) * (3 * D / 8) + (q % VPT) * 12;
 #pragma unroll
         for (int u = 0; u < 3; ++u) r.v[u] = ld_stream_u32(src + 4 * u);
     } else {
@@ -127,11 +133,13 @@ template <int D>
 __device__ __forceinline__ void stage_chunk(const RawChunk<D> &r, uint32_t *Kb, uint32_t *Cs, float *sig,
                                             const uint32_t *lut, int tid) {
     constexpr int RW = AttendSmem<D>::RW, VPT = D / 32;
+    const int q = tid >> 3, l8 = tid & 7;
     {
-        uint32_t *row = Kb + (tid >> 2) * RW + (tid & 3) * (D / 8);
+        uint32_t *row = Kb + (l8 + 8 * (q >> 2)) * RW + (q & 3) * (D / 8);
 #pragma unroll
         for (int u = 0; u < D / 64; ++u) {
             const uint32_t w4[4] = {r.k[u].x, r.k[u].y, r.k[u].z, r.k[u].w};
+            uint32_t o[8];
 #pragma unroll
             for (int b = 0; b < 4; ++b) {
                 const uint32_t x = w4[b] ^ 0x80808080u;
@@ -139,19 +147,24 @@ __device__ __forceinline__ void stage_chunk(const RawChunk<D> &r, uint32_t *Kb, 
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
                     f[i] = __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7650u | i)) - 8388736.0f;
-                row[8 * u + 2 * b] = __byte_perm(__float_as_uint(f[0]), __float_as_uint(f[1]), 0x7632u);
-                row[8 * u + 2 * b + 1] = __byte_perm(__float_as_uint(f[2]), __float_as_uint(f[3]), 0x7632u);
+                o[2 * b] = __byte_perm(__float_as_uint(f[0]), __float_as_uint(f[1]), 0x7632u);
+                o[2 * b + 1] = __byte_perm(__float_as_uint(f[2]), __float_as_uint(f[3]), 0x7632u);
             }
+            *reinterpret_cast<uint4 *>(row + 8 * u) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4 *>(row + 8 * u + 4) = make_uint4(o[4], o[5], o[6], o[7]);
         }
     }
-    if (tid < ATT_TC * VPT) {
-        uint32_t *row = Cs + (tid / VPT) * RW + (tid % VPT) * 16;
+    if (q < 8 * VPT) {
+        uint32_t *row = Cs + (l8 + 8 * (q / VPT)) * RW + (q % VPT) * 16;
         const uint32_t w[4] = {r.v[0], r.v[1], r.v[2], 0u};
+        uint32_t o[16];
 #pragma unroll
         for (int k = 0; k < 16; ++k) {  // codes 2k, 2k+1: bits 6k .. 6k+5
             const int bit = 6 * k, wi = bit >> 5, sh = bit & 31;
-            row[k] = lut[__funnelshift_r(w[wi], w[wi + 1], sh) & 63u];
+            o[k] = lut[__funnelshift_r(w[wi], w[wi + 1], sh) & 63u];
         }
+#pragma unroll
+        for (int k = 0; k < 16; k += 4) *reinterpret_cast<uint4 *>(row + k) = make_uint4(o[k], o[k + 1], o[k + 2], o[k + 3]);
     }
     if (tid < ATT_TC) sig[tid] = __half2float(__ushort_as_half(static_cast<uint16_t>(r.sig)));
 }
