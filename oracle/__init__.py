@@ -71,6 +71,8 @@ def lib():
         "orc_card_pack": (C.c_uint32, [C.c_int] * 4 + [C.c_uint64, C.c_int64, _u8p,
                                                       C.POINTER(_u16p), C.POINTER(_u16p), _u8p, _dp]),
         "orc_card_unpack": (C.c_int, [_u8p, C.POINTER(_u16p), C.POINTER(_u16p)]),
+        "orc_card_unpack_at": (C.c_int, [_u8p, C.c_int64, C.POINTER(C.c_float), C.POINTER(_u16p),
+                                         C.POINTER(_u16p)]),
         "orc_pool_attend": (C.c_int, [_u8p, C.c_int, C.c_int, C.c_int, _u16p, C.c_double, _dp, _dp]),
     }
     for name, (res, args) in sig.items():
@@ -312,6 +314,24 @@ def card_unpack(card):
     k = [np.zeros((H, T, d), np.uint16) for _ in range(L)]
     v = [np.zeros((H, T, d), np.uint16) for _ in range(L)]
     rc = lib().orc_card_unpack(_p(card, _u8p), _ptr_table(k, _u16p), _ptr_table(v, _u16p))
+    if rc != 0:
+        raise ValueError("oracle: not a version-1 card")
+    return k, v
+
+
+def card_unpack_at(card, pos_dst, inv_freq):
+    """Unpack with K re-aligned from the card's position offset to pos_dst
+    (rotary pairs (i, i + d/2), frequencies inv_freq[d/2] in radians per
+    position)."""
+    card = _c(card, np.uint8)
+    hdr = card[:32].view(np.int32)
+    T, L, H, d = int(hdr[2]), int(hdr[3]), int(hdr[4]), int(hdr[5])
+    w = _c(inv_freq, np.float32)
+    assert w.size == d // 2
+    k = [np.zeros((H, T, d), np.uint16) for _ in range(L)]
+    v = [np.zeros((H, T, d), np.uint16) for _ in range(L)]
+    rc = lib().orc_card_unpack_at(_p(card, _u8p), C.c_int64(pos_dst), _p(w, C.POINTER(C.c_float)),
+                                  _ptr_table(k, _u16p), _ptr_table(v, _u16p))
     if rc != 0:
         raise ValueError("oracle: not a version-1 card")
     return k, v

@@ -752,6 +752,86 @@ int orc_card_unpack(const uint8_t *card, uint16_t *const *k_out, uint16_t *const
     return 0;
 }
 
+/* Receiver injection at other positions.  A CacheCard carries the position
+ * of its first token in the sender's sequence ([QKVShare] "CacheCard
+ * representation": sequence length, model id, position offset), and a
+ * shared segment's keys are moved to the receiving agent's positions before
+ * reuse ([KVCMAS] "How it is used": the source cache's key positions are
+ * re-aligned to the target's).  With rotary position embedding -- dims i and
+ * i + d/2 form a pair turned through the angle p * w_i at position p, as the
+ * Hugging Face Llama implementation pairs them -- a key turned for position
+ * p0 + t becomes the key for p1 + t by one further turn through
+ * (p1 - p0) * w_i, because plane rotations add their angles.
+ *
+ * K of every layer, head and token is dequantized exactly (16-bit tokens:
+ * their bf16 value), turned in fp64 and rounded to bf16 once; V is decoded
+ * exactly as orc_card_unpack does.  w: d/2 frequencies in radians per
+ * position.  Returns 0, or -1 on a bad header. */
+int orc_card_unpack_at(const uint8_t *card, int64_t pos_dst, const float *w, uint16_t *const *k_out,
+                       uint16_t *const *v_out)
+{
+    if (get32(card) != 0x4343564Bu || get32(card + 4) != 1u) return -1;
+    int T = (int)get32(card + 8), L = (int)get32(card + 12);
+    int H = (int)get32(card + 16), d = (int)get32(card + 20);
+    int64_t pos_src = (int64_t)get64(card + 40);
+    uint64_t off_bits = get64(card + 48), off_offsets = get64(card + 56);
+    uint64_t off_layers = get64(card + 64), stride = get64(card + 72);
+    const int ng = d / 32, half = d / 2;
+    double cs[64], sn[64];
+    const double delta = (double)(pos_dst - pos_src);
+    for (int i = 0; i < half; i++) {
+        double phi = delta * (double)w[i];
+        cs[i] = cos(phi);
+        sn[i] = sin(phi);
+    }
+    for (int l = 0; l < L; l++) {
+        const uint8_t *lay = card + off_layers + (uint64_t)l * stride;
+#pragma omp parallel for schedule(static)
+        for (int t = 0; t < T; t++) {
+            int b = card[off_bits + (uint64_t)t];
+            const uint8_t *rec = lay + get32(card + off_offsets + 4ull * (uint64_t)t);
+            for (int kv = 0; kv < 2; kv++) {
+                uint16_t *dst = kv ? v_out[l] : k_out[l];
+                for (int h = 0; h < H; h++) {
+                    double x[128];
+                    if (b == 16) {
+                        const uint8_t *src = rec + (uint64_t)kv * (uint64_t)H * (uint64_t)d * 2u + (uint64_t)h * d * 2u;
+                        for (int i = 0; i < d; i++) {
+                            uint16_t u;
+                            memcpy(&u, src + 2 * i, 2);
+                            x[i] = orc_bf16_to_f64(u);
+                        }
+                    } else {
+                        uint64_t code_bytes = (uint64_t)H * (uint64_t)d * (uint64_t)b / 8u;
+                        const uint8_t *codes = rec + (uint64_t)kv * code_bytes;
+                        const uint8_t *par = rec + 2u * code_bytes + (uint64_t)kv * (uint64_t)H * (uint64_t)ng * 4u;
+                        for (int gi = 0; gi < ng; gi++) {
+                            uint8_t q[32];
+                            uint16_t sb, zb;
+                            unpack_group(codes + ((uint64_t)h * ng + (uint64_t)gi) * 4u * (uint64_t)b, b, q);
+                            memcpy(&sb, par + ((uint64_t)h * ng + (uint64_t)gi) * 4u, 2);
+                            memcpy(&zb, par + ((uint64_t)h * ng + (uint64_t)gi) * 4u + 2, 2);
+                            double sc = orc_f16_to_f64(sb), z = orc_f16_to_f64(zb);
+                            for (int i = 0; i < 32; i++) x[32 * gi + i] = (double)q[i] * sc + z;
+                        }
+                    }
+                    uint16_t *row = dst + ((uint64_t)h * T + (uint64_t)t) * d;
+                    if (kv == 0) {
+                        for (int i = 0; i < half; i++) {
+                            double a = x[i], c = x[i + half];
+                            row[i] = orc_f64_to_bf16(a * cs[i] - c * sn[i]);
+                            row[i + half] = orc_f64_to_bf16(a * sn[i] + c * cs[i]);
+                        }
+                    } else {
+                        for (int i = 0; i < d; i++) row[i] = orc_f64_to_bf16(x[i]);
+                    }
+                }
+            }
+        }
+    }
+    return 0;
+}
+
 /* ------------------------------------------------------------------------- */
 /* Attention over the pool without materialising the caches.                  */
 /* [QKVShare] "Significance": a fully fused attention kernel over the          */

@@ -41,6 +41,13 @@ MUTANTS = [
     ("k absmax skips sign", "double a = fabs(orc_bf16_to_f64(k[i]));", "double a = orc_bf16_to_f64(k[i]);"),
     ("attend GQA head map", "const int h = j / grp;", "const int h = j % H;"),
     ("attend lse drops max", "lse[aj] = mx + log(sum);", "lse[aj] = log(sum);"),
+    ("realign shift reversed", "const double delta = (double)(pos_dst - pos_src);",
+     "const double delta = (double)(pos_src - pos_dst);"),
+    ("realign sine sign", "row[i] = orc_f64_to_bf16(a * cs[i] - c * sn[i]);",
+     "row[i] = orc_f64_to_bf16(a * cs[i] + c * sn[i]);"),
+    ("realign adjacent pairs", "double a = x[i], c = x[i + half];", "double a = x[i], c = x[i ^ 1];"),
+    ("realign frequency order", "double phi = delta * (double)w[i];", "double phi = delta * (double)w[half - 1 - i];"),
+    ("realign drops zero point", "x[32 * gi + i] = (double)q[i] * sc + z;", "x[32 * gi + i] = (double)q[i] * sc;"),
 ]
 
 

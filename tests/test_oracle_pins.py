@@ -634,3 +634,109 @@ def test_pool_attend_closed_forms():
     out, lse = O.pool_attend(pool, 0, q, scale)
     np.testing.assert_allclose(out[0, 0], vf[0, int(np.argmax(sc))], rtol=1e-9, atol=1e-12)
     assert abs(lse[0, 0] - scale * top[-1]) < 1e-9 * scale * abs(top[-1])
+
+
+# --------------------------------------------------------------------------
+# card unpack re-aligned to other positions (next row: rotary realignment)
+# --------------------------------------------------------------------------
+
+def _rope_complex(x, pos, w):
+    """Rotary embedding written as complex multiplication, independently of
+    the oracle's real 2x2 form: pair (i, i + d/2) is z = x_i + 1j x_{i+d/2},
+    turned by exp(1j * pos * w_i).  x [..., T, d], pos [T] (int), w [d/2]."""
+    half = x.shape[-1] // 2
+    z = x[..., :half] + 1j * x[..., half:]
+    ang = np.multiply.outer(np.asarray(pos, np.float64), np.asarray(w, np.float64))
+    z = z * np.exp(1j * ang)
+    return np.concatenate([z.real, z.imag], axis=-1)
+
+
+def _bf16_rne(x):
+    import torch
+    return torch.from_numpy(np.asarray(x, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def _llama_inv_freq(d, base=500000.0):
+    return (1.0 / base ** (np.arange(0, d, 2, dtype=np.float64) / d)).astype(np.float32)
+
+
+def _pair_norm(x):
+    half = x.shape[-1] // 2
+    n = np.sqrt(x[..., :half] ** 2 + x[..., half:] ** 2)
+    return np.concatenate([n, n], axis=-1)
+
+
+def test_card_unpack_at_zero_shift_is_plain_unpack():
+    L, H, T, d = 2, 3, 9, 128
+    ks, vs = _tiny_kv(L, H, T, d, 21)
+    bits = np.array([2, 4, 8, 16, 16, 8, 4, 2, 4], np.uint8)
+    card, flags, _ = O.card_pack(ks, vs, bits, pos_offset=300)
+    assert flags == 0
+    k0, v0 = O.card_unpack(card)
+    k1, v1 = O.card_unpack_at(card, 300, _llama_inv_freq(d))
+    for l in range(L):
+        np.testing.assert_array_equal(k1[l], k0[l])
+        np.testing.assert_array_equal(v1[l], v0[l])
+
+
+@pytest.mark.parametrize("d,p_src,p_dst,w", [
+    (64, -77, 1000, "llama"), (128, 5000, 12, "llama"), (128, 0, 30000, "unit"), (64, 7, 8, "ramp")])
+def test_card_unpack_at_matches_complex_rotation(d, p_src, p_dst, w):
+    """Keys embedded at p_src + t, carried verbatim (16-bit tokens), come out
+    as the keys embedded at p_dst + t; values are untouched."""
+    L, H, T = 2, 3, 7
+    rng = np.random.default_rng(d + p_dst)
+    freq = {"llama": _llama_inv_freq(d), "unit": np.ones(d // 2, np.float32),
+            "ramp": np.linspace(0.01, 3.0, d // 2).astype(np.float32)}[w]
+    k0 = [rng.normal(size=(H, T, d)) * 2.0 for _ in range(L)]
+    ks = [_bf16_rne(_rope_complex(k, p_src + np.arange(T), freq)) for k in k0]
+    vs = [_bf16_rne(rng.normal(size=(H, T, d))) for _ in range(L)]
+    card, flags, _ = O.card_pack(ks, vs, np.full(T, 16, np.uint8), pos_offset=p_src)
+    assert flags == 0
+    ko, vo = O.card_unpack_at(card, p_dst, freq)
+    for l in range(L):
+        want = _rope_complex(k0[l], p_dst + np.arange(T), freq)
+        assert np.all(np.abs(_f(ko[l]) - want) <= 2.0 ** -7 * _pair_norm(want) + 1e-12)
+        np.testing.assert_array_equal(vo[l], vs[l])
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_card_unpack_at_quarter_and_half_turns(d):
+    """w_i = pi/2 per position: a shift of 1 maps (a, b) to (-b, a), a shift
+    of 2 negates every key and a shift of -1 maps (a, b) to (b, -a)."""
+    L, H, T = 1, 2, 5
+    rng = np.random.default_rng(3)
+    ks = [_bf16_rne(rng.normal(size=(H, T, d)) + np.sign(rng.normal(size=(H, T, d))))]
+    vs = [_bf16_rne(rng.normal(size=(H, T, d)))]
+    card, _, _ = O.card_pack(ks, vs, np.full(T, 16, np.uint8), pos_offset=10)
+    x = _f(ks[0])
+    half = d // 2
+    freq = np.full(half, np.pi / 2, np.float32)
+    k1, _ = O.card_unpack_at(card, 11, freq)
+    np.testing.assert_array_equal(_f(k1[0]), np.concatenate([-x[..., half:], x[..., :half]], -1))
+    k2, _ = O.card_unpack_at(card, 12, freq)
+    np.testing.assert_array_equal(_f(k2[0]), -x)
+    k3, _ = O.card_unpack_at(card, 9, freq)
+    np.testing.assert_array_equal(_f(k3[0]), np.concatenate([x[..., half:], -x[..., :half]], -1))
+
+
+def test_card_unpack_at_quantized_tokens_and_round_trip():
+    """Quantized tokens: the re-aligned key is the turned dequantized key (to
+    the bf16 rounding of the plain unpack); re-packing the result at the new
+    offset and re-aligning back restores the plain unpack."""
+    L, H, T, d = 2, 2, 8, 128
+    ks, vs = _tiny_kv(L, H, T, d, 22)
+    bits = np.array([2, 4, 8, 16, 2, 4, 8, 16], np.uint8)
+    freq = _llama_inv_freq(d, base=10000.0)
+    card, _, _ = O.card_pack(ks, vs, bits, pos_offset=-1234)
+    k0, v0 = O.card_unpack(card)
+    k1, v1 = O.card_unpack_at(card, 4321, freq)
+    for l in range(L):
+        want = _rope_complex(_f(k0[l]), 5555 + np.zeros(T), freq)
+        assert np.all(np.abs(_f(k1[l]) - want) <= 2.0 ** -7 * _pair_norm(want) + 1e-12)
+        np.testing.assert_array_equal(v1[l], v0[l])
+    card2, _, _ = O.card_pack(k1, v1, np.full(T, 16, np.uint8), pos_offset=4321)
+    k2, _ = O.card_unpack_at(card2, -1234, freq)
+    for l in range(L):
+        ref = _f(k0[l])
+        assert np.all(np.abs(_f(k2[l]) - ref) <= 2.0 ** -7 * _pair_norm(ref) + 1e-12)
