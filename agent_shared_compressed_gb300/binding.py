@@ -73,6 +73,8 @@ _SIGS = {
                                  C.POINTER(_vp), _vp, C.c_size_t, _vp]),
     "cachecard_read_header": (C.c_int, [_vp, C.POINTER(CardHeader), _vp]),
     "cachecard_unpack": (C.c_int, [_vp, C.POINTER(CardHeader), C.POINTER(_vp), C.POINTER(_vp), _vp]),
+    "cachecard_unpack_at": (C.c_int, [_vp, C.POINTER(CardHeader), C.c_int64, C.POINTER(C.c_float), C.POINTER(_vp),
+                                      C.POINTER(_vp), _vp]),
     "cachecard_status": (C.c_int, [_vp, _vp]),
     "kvp_strerror": (C.c_char_p, [C.c_int]),
     "kvp_launch_count": (C.c_uint64, []),
@@ -203,6 +205,17 @@ def cachecard_read_header(card, out, stream=None):
 
 def cachecard_unpack(card, hdr, k_dst, v_dst, stream=None):
     return load().cachecard_unpack(_addr(card), C.byref(hdr), _ptrs(k_dst), _ptrs(v_dst), _stream(stream))
+
+
+def cachecard_unpack_at(card, hdr, pos_dst, inv_freq, k_dst, v_dst, stream=None):
+    """inv_freq: head_dim/2 host floats (any sequence; None passes NULL)."""
+    if inv_freq is None:
+        w = None
+    else:
+        vals = [float(x) for x in inv_freq]
+        w = (C.c_float * max(1, len(vals)))(*vals)
+    return load().cachecard_unpack_at(_addr(card), C.byref(hdr), C.c_int64(int(pos_dst)), w, _ptrs(k_dst),
+                                      _ptrs(v_dst), _stream(stream))
 
 
 def cachecard_status(card, stream=None):

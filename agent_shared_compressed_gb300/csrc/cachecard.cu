@@ -6,6 +6,8 @@
 // cachecard_pack: card_scan (one block: bitwidths -> record offsets, header)
 // then card_pack (one warp per (layer, token, K|V) record half).
 // cachecard_unpack: card_unpack, the inverse, one warp per record half.
+#include <cmath>
+
 #include "kvp_internal.cuh"
 
 namespace kvp {
@@ -25,6 +27,8 @@ struct CardArgs {
     int64_t pos_offset;
     uint64_t off_offsets, off_layers, layer_stride;
     int L, H, T, d;
+    int64_t shift;      // unpack_at: target offset - card offset
+    float inv_freq[64]; // unpack_at: rotary frequencies, d/2 of them
 };
 
 // ---------------------------------------------------------------------------
@@ -302,84 +306,219 @@ __global__ void card_zero_tails(const __grid_constant__ CardArgs a) {
 // Unpack ("QKVShare" Methodology 3): x = bf16(q * s_h + z_h); 16-bit tokens
 // verbatim.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(CARD_THREADS) card_unpack(const __grid_constant__ CardArgs a) {
-    const int lane = threadIdx.x & 31;
+
+// The 8 values of one chunk (8 consecutive dims) of a b-bit group record:
+// codes cw (2, 4 or 8 bits each, low bits first), group parameters pw
+// (fp16 scale | fp16 zero point << 16).
+__device__ __forceinline__ void card_chunk_values(int b, uint2 cw, uint32_t pw, float (&y)[8]) {
+    uint32_t q[8];
+    if (b == 2) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) q[e] = (cw.x >> (2 * e)) & 3u;
+    } else if (b == 4) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) q[e] = (cw.x >> (4 * e)) & 15u;
+    } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            q[e] = (cw.x >> (8 * e)) & 255u;
+            q[4 + e] = (cw.y >> (8 * e)) & 255u;
+        }
+    }
+    const float sf = __half2float(__ushort_as_half(uint16_t(pw & 0xFFFFu)));
+    const float zf = __half2float(__ushort_as_half(uint16_t(pw >> 16)));
+#pragma unroll
+    for (int e = 0; e < 8; ++e) y[e] = fmaf(__uint_as_float(0x4B000000u | q[e]) - 8388608.0f, sf, zf);
+}
+
+// Codes of chunk c of a b-bit record part.
+__device__ __forceinline__ uint2 card_chunk_codes(int b, const uint8_t *codes, int c) {
+    if (b == 2) return make_uint2(reinterpret_cast<const uint16_t *>(codes)[c], 0u);
+    if (b == 4) return make_uint2(reinterpret_cast<const uint32_t *>(codes)[c], 0u);
+    return reinterpret_cast<const uint2 *>(codes)[c];
+}
+
+__device__ __forceinline__ uint4 pack_bf16x8(const float (&y)[8]) {
+    return make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
+                      pack_bf16x2(y[6], y[7]));
+}
+
+// One (layer, token, K|V) task of a plain unpack, by one warp: lanes over
+// the H * d/8 chunks of the token.
+__device__ __forceinline__ void unpack_task_plain(const CardArgs &a, const uint8_t *rec, uint4 *dst, int b, int kv,
+                                                  uint32_t t, int lane) {
     const int cpr = a.d / 8;
     const int cshift = a.d == 128 ? 4 : 3;
     const int nchunks = a.H * cpr;
     const uint32_t T = uint32_t(a.T);
-    const uint32_t tasks = uint32_t(a.L) * T * 2u;  // fits: checked on the host
+    if (b == 16) {
+        const uint4 *in = reinterpret_cast<const uint4 *>(rec + uint64_t(kv) * a.H * a.d * 2);
+        for (int c = lane; c < nchunks; c += 32) {
+            const int h = c >> cshift, ch = c & (cpr - 1);
+            st_stream_v4(dst + (uint64_t(h) * T + t) * cpr + ch, ld_stream_v4(in + c));
+        }
+        return;
+    }
+    const uint64_t code_bytes = uint64_t(a.H) * a.d * b / 8;
+    const uint8_t *codes = rec + uint64_t(kv) * code_bytes;
+    const uint32_t *par = reinterpret_cast<const uint32_t *>(rec + 2 * code_bytes + uint64_t(kv) * a.H * (a.d / 32) * 4);
+    for (int c0 = 0; c0 < nchunks; c0 += 4 * 32) {
+        // up to 4 chunks' codes and group parameters per lane in flight
+        uint2 cw[4];
+        uint32_t pw[4];
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+            const int c = c0 + it * 32 + lane;
+            cw[it] = make_uint2(0, 0);
+            pw[it] = 0;
+            if (c < nchunks) {
+                cw[it] = card_chunk_codes(b, codes, c);
+                pw[it] = par[c >> 2];
+            }
+        }
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+            const int c = c0 + it * 32 + lane;
+            if (c >= nchunks) break;
+            float y[8];
+            card_chunk_values(b, cw[it], pw[it], y);
+            const int h = c >> cshift, ch = c & (cpr - 1);
+            st_stream_v4(dst + (uint64_t(h) * T + t) * cpr + ch, pack_bf16x8(y));
+        }
+    }
+}
+
+// The record of (layer l, token t), or null (and the card's error flag set)
+// when its bitwidth or offset does not fit the card's own layer stride.
+__device__ __forceinline__ const uint8_t *unpack_record(const CardArgs &a, int l, uint32_t t, int &b, int lane) {
     const uint8_t *bits = a.card + CARD_HEADER_BYTES;
     const uint32_t *offs = reinterpret_cast<const uint32_t *>(a.card + a.off_offsets);
+    b = bits[t];
+    if (!valid_bits(b) || uint64_t(offs[t]) + card_record_bytes(b, a.H, a.d) > a.layer_stride) {
+        if (lane == 0) atomicOr(&reinterpret_cast<kvp_card_header *>(a.card)->error, FLAG_HEADER);
+        return nullptr;
+    }
+    return a.card + a.off_layers + uint64_t(l) * a.layer_stride + offs[t];
+}
+
+__global__ void __launch_bounds__(CARD_THREADS) card_unpack(const __grid_constant__ CardArgs a) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t T = uint32_t(a.T);
+    const uint32_t tasks = uint32_t(a.L) * T * 2u;  // fits: checked on the host
     for (uint32_t task = blockIdx.x * CARD_WARPS + (threadIdx.x >> 5); task < tasks;
          task += gridDim.x * CARD_WARPS) {
         const int kv = int(task & 1u);
         const uint32_t lt = task >> 1;
         const uint32_t t = lt % T;
         const int l = int(lt / T);
-        const int b = bits[t];
-        // a card whose bitwidths or offsets do not fit its own layer stride
-        // is not decoded (and is reported through cachecard_status)
-        if (!valid_bits(b) || uint64_t(offs[t]) + card_record_bytes(b, a.H, a.d) > a.layer_stride) {
-            if (lane == 0) atomicOr(&reinterpret_cast<kvp_card_header *>(a.card)->error, FLAG_HEADER);
-            continue;
-        }
-        const uint8_t *rec = a.card + a.off_layers + uint64_t(l) * a.layer_stride + offs[t];
+        int b;
+        const uint8_t *rec = unpack_record(a, l, t, b, lane);
+        if (rec) unpack_task_plain(a, rec, a.dst[kv][l], b, kv, t, lane);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Unpack with the keys moved to other positions: rotary position embedding
+// turns dims (i, i + d/2) through p * w_i at position p, and turns compose,
+// so keys embedded at (card offset + t) become the keys at (pos_dst + t) by a
+// turn through shift * w_i, shift = pos_dst - card offset ("KVCMAS", How it
+// is used: the source cache's key positions are re-aligned to the target's;
+// "QKVShare", Methodology 2: the card carries the position offset).  The
+// angle is formed and its sine / cosine taken in fp64 once per block; each
+// key is dequantized and turned in fp32 and rounded to bf16 once.  Values
+// are unpacked as by card_unpack.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(CARD_THREADS, 4) card_unpack_rope(const __grid_constant__ CardArgs a) {
+    __shared__ float2 rot[64];  // (cos, sin) per frequency
+    for (int i = threadIdx.x; i < a.d / 2; i += CARD_THREADS) {
+        double sv, cv;
+        sincos(double(a.shift) * double(a.inv_freq[i]), &sv, &cv);
+        rot[i] = make_float2(float(cv), float(sv));
+    }
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    const int cpr = a.d / 8, half = cpr / 2;  // chunks per row, per half row
+    const int hshift = a.d == 128 ? 3 : 2;     // log2(half)
+    const int npairs = a.H * half;
+    // a lane's chunk within the half row is the same for every pair it takes
+    const int chl = lane & (half - 1);
+    float rc[8], rs[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const float2 r = rot[chl * 8 + e];
+        rc[e] = r.x;
+        rs[e] = r.y;
+    }
+    const uint32_t T = uint32_t(a.T);
+    const uint32_t tasks = uint32_t(a.L) * T * 2u;
+    for (uint32_t task = blockIdx.x * CARD_WARPS + (threadIdx.x >> 5); task < tasks;
+         task += gridDim.x * CARD_WARPS) {
+        const int kv = int(task & 1u);
+        const uint32_t lt = task >> 1;
+        const uint32_t t = lt % T;
+        const int l = int(lt / T);
+        int b;
+        const uint8_t *rec = unpack_record(a, l, t, b, lane);
+        if (!rec) continue;
         uint4 *dst = a.dst[kv][l];
-        if (b == 16) {
-            const uint4 *in = reinterpret_cast<const uint4 *>(rec + uint64_t(kv) * a.H * a.d * 2);
-            for (int c = lane; c < nchunks; c += 32) {
-                const int h = c >> cshift, ch = c & (cpr - 1);
-                st_stream_v4(dst + (uint64_t(h) * T + t) * cpr + ch, ld_stream_v4(in + c));
-            }
+        if (kv == 1) {
+            unpack_task_plain(a, rec, dst, b, kv, t, lane);
             continue;
         }
         const uint64_t code_bytes = uint64_t(a.H) * a.d * b / 8;
-        const uint8_t *codes = rec + uint64_t(kv) * code_bytes;
-        const uint32_t *par = reinterpret_cast<const uint32_t *>(rec + 2 * code_bytes + uint64_t(kv) * a.H * (a.d / 32) * 4);
-        for (int c0 = 0; c0 < nchunks; c0 += 4 * 32) {
-            // up to 4 chunks' codes and group parameters per lane in flight
-            uint2 cw[4];
-            uint32_t pw[4];
+        const uint32_t *par = reinterpret_cast<const uint32_t *>(rec + 2 * code_bytes);
+        for (int p0 = 0; p0 < npairs; p0 += 2 * 32) {
+            // two pairs (four chunks) per lane in flight
+            uint4 ra[2], rb[2];
+            uint32_t pa[2], pb[2];
 #pragma unroll
-            for (int it = 0; it < 4; ++it) {
-                const int c = c0 + it * 32 + lane;
-                cw[it] = make_uint2(0, 0);
-                pw[it] = 0;
-                if (c < nchunks) {
-                    if (b == 2) cw[it].x = reinterpret_cast<const uint16_t *>(codes)[c];
-                    else if (b == 4) cw[it].x = reinterpret_cast<const uint32_t *>(codes)[c];
-                    else cw[it] = reinterpret_cast<const uint2 *>(codes)[c];
-                    pw[it] = par[c >> 2];
+            for (int it = 0; it < 2; ++it) {
+                const int p = p0 + it * 32 + lane;
+                ra[it] = rb[it] = make_uint4(0, 0, 0, 0);
+                pa[it] = pb[it] = 0;
+                if (p < npairs) {
+                    const int ca = (p >> hshift) * cpr + (p & (half - 1)), cb = ca + half;
+                    if (b == 16) {
+                        ra[it] = ld_stream_v4(reinterpret_cast<const uint4 *>(rec) + ca);
+                        rb[it] = ld_stream_v4(reinterpret_cast<const uint4 *>(rec) + cb);
+                    } else {
+                        const uint2 x = card_chunk_codes(b, rec, ca), y = card_chunk_codes(b, rec, cb);
+                        ra[it] = make_uint4(x.x, x.y, 0, 0);
+                        rb[it] = make_uint4(y.x, y.y, 0, 0);
+                        pa[it] = par[ca >> 2];
+                        pb[it] = par[cb >> 2];
+                    }
                 }
             }
 #pragma unroll
-            for (int it = 0; it < 4; ++it) {
-                const int c = c0 + it * 32 + lane;
-                if (c >= nchunks) break;
-                uint32_t q[8];
-                if (b == 2) {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) q[e] = (cw[it].x >> (2 * e)) & 3u;
-                } else if (b == 4) {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) q[e] = (cw[it].x >> (4 * e)) & 15u;
-                } else {
+            for (int it = 0; it < 2; ++it) {
+                const int p = p0 + it * 32 + lane;
+                if (p >= npairs) break;
+                const int h = p >> hshift;
+                const int ca = h * cpr + chl, cb = ca + half;
+                float ya[8], yb[8];
+                if (b == 16) {
+                    const uint32_t wa[4] = {ra[it].x, ra[it].y, ra[it].z, ra[it].w};
+                    const uint32_t wb[4] = {rb[it].x, rb[it].y, rb[it].z, rb[it].w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        q[e] = (cw[it].x >> (8 * e)) & 255u;
-                        q[4 + e] = (cw[it].y >> (8 * e)) & 255u;
+                        ya[2 * e] = bf16_lo(wa[e]);
+                        ya[2 * e + 1] = bf16_hi(wa[e]);
+                        yb[2 * e] = bf16_lo(wb[e]);
+                        yb[2 * e + 1] = bf16_hi(wb[e]);
                     }
+                } else {
+                    card_chunk_values(b, make_uint2(ra[it].x, ra[it].y), pa[it], ya);
+                    card_chunk_values(b, make_uint2(rb[it].x, rb[it].y), pb[it], yb);
                 }
-                const float sf = __half2float(__ushort_as_half(uint16_t(pw[it] & 0xFFFFu)));
-                const float zf = __half2float(__ushort_as_half(uint16_t(pw[it] >> 16)));
-                float y[8];
+                float oa[8], ob[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) y[e] = fmaf(__uint_as_float(0x4B000000u | q[e]) - 8388608.0f, sf, zf);
-                const int h = c >> cshift, ch = c & (cpr - 1);
-                st_stream_v4(dst + (uint64_t(h) * T + t) * cpr + ch,
-                             make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
-                                        pack_bf16x2(y[6], y[7])));
+                for (int e = 0; e < 8; ++e) {
+                    oa[e] = fmaf(ya[e], rc[e], -yb[e] * rs[e]);
+                    ob[e] = fmaf(ya[e], rs[e], yb[e] * rc[e]);
+                }
+                st_stream_v4(dst + (uint64_t(h) * T + t) * cpr + (ca - h * cpr), pack_bf16x8(oa));
+                st_stream_v4(dst + (uint64_t(h) * T + t) * cpr + (cb - h * cpr), pack_bf16x8(ob));
             }
         }
     }
@@ -443,8 +582,9 @@ extern "C" int cachecard_pack(const kvp_shape *s, uint64_t model_id, int64_t pos
     return launch_status();
 }
 
-extern "C" int cachecard_unpack(const void *card, const kvp_card_header *hdr, void *const *k_dst, void *const *v_dst,
-                                void *stream) {
+// Host checks and launch arguments shared by both unpack entry points.
+static int unpack_setup(const void *card, const kvp_card_header *hdr, void *const *k_dst, void *const *v_dst,
+                        CardArgs &a) {
     if (!card || !hdr || !k_dst || !v_dst) return KVP_ERR_ARG;
     if (hdr->magic != CARD_MAGIC || hdr->version != CARD_VERSION || hdr->group_size != CARD_GROUP || hdr->dtype != 1)
         return KVP_ERR_HEADER;
@@ -459,7 +599,6 @@ extern "C" int cachecard_unpack(const void *card, const kvp_card_header *hdr, vo
     if (!aligned(card, 256)) return KVP_ERR_ALIGN;
     if (uint64_t(s.n_layers) * uint64_t(s.n_tokens) * 2ull >= (1ull << 32)) return KVP_ERR_SIZE;
     const int L = s.n_layers;
-    CardArgs a;
     for (int l = 0; l < L; ++l) {
         if (!k_dst[l] || !v_dst[l]) return KVP_ERR_ARG;
         if (!aligned(k_dst[l], 16) || !aligned(v_dst[l], 16)) return KVP_ERR_ALIGN;
@@ -478,11 +617,38 @@ extern "C" int cachecard_unpack(const void *card, const kvp_card_header *hdr, vo
     a.H = s.n_kv_heads;
     a.T = s.n_tokens;
     a.d = s.head_dim;
+    a.shift = 0;
+    return KVP_OK;
+}
+
+extern "C" int cachecard_unpack(const void *card, const kvp_card_header *hdr, void *const *k_dst, void *const *v_dst,
+                                void *stream) {
+    CardArgs a;
+    const int rc = unpack_setup(card, hdr, k_dst, v_dst, a);
+    if (rc != KVP_OK) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const uint64_t tasks = uint64_t(L) * uint64_t(a.T) * 2u;
+    const uint64_t tasks = uint64_t(a.L) * uint64_t(a.T) * 2u;
     // store-heavy: several resident grids' worth of blocks spread the
     // concurrent stores (as in the pool decoder)
     card_unpack<<<card_grid(card_unpack, tasks, 3), CARD_THREADS, 0, st>>>(a);
+    count_launch(1);
+    return launch_status();
+}
+
+extern "C" int cachecard_unpack_at(const void *card, const kvp_card_header *hdr, int64_t pos_dst,
+                                   const float *inv_freq, void *const *k_dst, void *const *v_dst, void *stream) {
+    if (!inv_freq) return KVP_ERR_ARG;
+    CardArgs a;
+    const int rc = unpack_setup(card, hdr, k_dst, v_dst, a);
+    if (rc != KVP_OK) return rc;
+    if (__builtin_sub_overflow(pos_dst, hdr->pos_offset, &a.shift)) return KVP_ERR_ARG;
+    for (int i = 0; i < a.d / 2; ++i) {
+        if (!std::isfinite(inv_freq[i])) return KVP_ERR_ARG;
+        a.inv_freq[i] = inv_freq[i];
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const uint64_t tasks = uint64_t(a.L) * uint64_t(a.T) * 2u;
+    card_unpack_rope<<<card_grid(card_unpack_rope, tasks, 3), CARD_THREADS, 0, st>>>(a);
     count_launch(1);
     return launch_status();
 }

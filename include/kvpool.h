@@ -253,6 +253,27 @@ int cachecard_read_header(const void *card, kvp_card_header *out, void *stream);
 int cachecard_unpack(const void *card, const kvp_card_header *hdr,
                      void *const *k_dst, void *const *v_dst, void *stream);
 
+/* Receiver injection at other positions: as cachecard_unpack, but every key
+ * is moved from its position in the sender's sequence (hdr->pos_offset + t)
+ * to pos_dst + t.  The card's metadata carries the position offset
+ * ("QKVShare" Methodology 2), and a reused segment's key positions are
+ * re-aligned to the target agent's ("KVCMAS", How it is used).  Under rotary
+ * position embedding -- dims i and i + d/2 turned through p * w_i at
+ * position p, the Hugging Face Llama pairing -- that is one further turn of
+ * every pair through (pos_dst - hdr->pos_offset) * w_i.
+ *   inv_freq: HOST array of head_dim/2 fp32 frequencies w_i (radians per
+ *     position; the model's rotary inverse frequencies, any scaling already
+ *     applied).  Copied into the launch, so it may be freed on return.
+ *   The angle is formed and its sine and cosine taken in fp64; each key is
+ *   dequantized and turned in fp32 and rounded to bf16 once.  Values are
+ *   unpacked exactly as by cachecard_unpack.  pos_dst == hdr->pos_offset
+ *   gives cachecard_unpack's output bit for bit.
+ * Returns KVP_ERR_ARG for a null inv_freq, a non-finite frequency or a shift
+ * that overflows int64; otherwise as cachecard_unpack. */
+int cachecard_unpack_at(const void *card, const kvp_card_header *hdr, int64_t pos_dst,
+                        const float *inv_freq, void *const *k_dst, void *const *v_dst,
+                        void *stream);
+
 /* Synchronises `stream`, then returns KVP_OK or the first device-detected
  * error recorded in the card's header. */
 int cachecard_status(const void *card, void *stream);

@@ -23,7 +23,8 @@ def test_exports_every_declared_function():
     names = kv.declared_functions()
     assert set(names) >= {"kvpool_pool_bytes", "kvpool_workspace_bytes", "kvpool_encode", "kvpool_decode_into",
                           "kvpool_status", "cachecard_bytes", "cachecard_pack", "cachecard_read_header",
-                          "cachecard_unpack", "cachecard_status", "kvp_strerror", "kvp_launch_count"}
+                          "cachecard_unpack", "cachecard_unpack_at", "cachecard_status", "kvp_strerror",
+                          "kvp_launch_count"}
     lib = C.CDLL(kv.binding.LIB_PATH)
     for n in names:
         assert hasattr(lib, n), n
@@ -112,6 +113,33 @@ def test_card_argument_errors():
     assert kv.cachecard_unpack(None, h, [ok], [ok]) == kv.KVP_ERR_ARG
     assert kv.kvpool_status(None) == kv.KVP_ERR_ARG
     assert kv.cachecard_status(None) == kv.KVP_ERR_ARG
+
+
+def _consistent_header(L, H, d, T, bits):
+    g = O.card_geometry(L, H, d, T, bits)
+    h = kv.CardHeader()
+    h.magic, h.version, h.seq_len, h.n_layers, h.n_kv_heads, h.head_dim = 0x4343564B, 1, T, L, H, d
+    h.group_size, h.dtype, h.pos_offset = 32, 1, -5
+    h.off_bits, h.off_offsets, h.off_layers = g["off_bits"], g["off_offsets"], g["off_layers"]
+    h.layer_stride = g["layer_stride"]
+    h.total_bytes = g["off_layers"] + L * g["layer_stride"]
+    return h
+
+
+def test_card_unpack_at_argument_errors():
+    """Host-side checks of the re-aligning unpack, all before any launch."""
+    L, H, d, T = 2, 8, 128, 64
+    ok = 0x10000
+    h = _consistent_header(L, H, d, T, np.full(T, 4, np.uint8))
+    w = [1.0] * (d // 2)
+    assert kv.cachecard_unpack_at(ok, h, 0, None, [ok] * L, [ok] * L) == kv.KVP_ERR_ARG
+    assert kv.cachecard_unpack_at(ok, h, 0, w[:-1] + [float("nan")], [ok] * L, [ok] * L) == kv.KVP_ERR_ARG
+    assert kv.cachecard_unpack_at(ok, h, 0, w[:-1] + [float("inf")], [ok] * L, [ok] * L) == kv.KVP_ERR_ARG
+    assert kv.cachecard_unpack_at(ok, h, 2 ** 63 - 1, w, [ok] * L, [ok] * L) == kv.KVP_ERR_ARG  # shift overflows
+    assert kv.cachecard_unpack_at(ok + 16, h, 0, w, [ok] * L, [ok] * L) == kv.KVP_ERR_ALIGN
+    assert kv.cachecard_unpack_at(ok, h, 0, w, [ok + 2] * L, [ok] * L) == kv.KVP_ERR_ALIGN
+    h.magic = 1
+    assert kv.cachecard_unpack_at(ok, h, 0, w, [ok] * L, [ok] * L) == kv.KVP_ERR_HEADER
 
 
 def test_strerror_and_counter():
