@@ -56,6 +56,9 @@ def lib():
         "orc_k_scale": (C.c_float, [C.c_double]),
         "orc_k_code": (C.c_int, [C.c_uint16, C.c_float]),
         "orc_k_decode": (C.c_uint16, [C.c_int, C.c_float]),
+        "orc_k_block_scale": (C.c_uint16, [_u16p, C.POINTER(C.c_int), C.POINTER(C.c_int)]),
+        "orc_k_block_code": (C.c_int, [C.c_uint16, C.c_uint16]),
+        "orc_k_block_decode": (C.c_uint16, [C.c_int, C.c_uint16]),
         "orc_v_encode_vec": (C.c_uint32, [_u16p, C.c_int, _u8p, _u16p, _dp]),
         "orc_pack3": (None, [_u8p, C.c_int, _u8p]),
         "orc_unpack3": (None, [_u8p, C.c_int, _u8p]),
@@ -63,6 +66,9 @@ def lib():
         "orc_pool_bytes": (C.c_size_t, [C.c_int] * 4),
         "orc_pool_geometry": (None, [C.c_int] * 4 + [_u64p]),
         "orc_pool_encode": (C.c_uint32, [C.c_int] * 4 + [C.POINTER(_u16p), C.POINTER(_u16p), _u8p, _dp]),
+        "orc_pool_encode_mode": (C.c_uint32, [C.c_int] * 5 + [C.POINTER(_u16p), C.POINTER(_u16p), _u8p, _dp]),
+        "orc_pool_bytes_mode": (C.c_size_t, [C.c_int] * 5),
+        "orc_pool_geometry_q8": (None, [C.c_int] * 4 + [_u64p]),
         "orc_pool_decode_into": (C.c_int, [_u8p, C.c_int, C.c_int, C.c_int, C.POINTER(_u16p), C.POINTER(_u16p)]),
         "orc_card_record_bytes": (C.c_uint64, [C.c_int, C.c_int, C.c_int]),
         "orc_card_bytes": (C.c_size_t, [C.c_int] * 4 + [_u8p]),
@@ -169,6 +175,23 @@ def k_decode(q, s):
     return int(lib().orc_k_decode(int(q), float(s)))
 
 
+def k_block_scale(k32_bits):
+    """q8_0 block: (fp16 scale bits, nonfinite, range) of 32 bf16 keys."""
+    k = _c(k32_bits, np.uint16)
+    assert k.size == 32
+    bad, rng = C.c_int(0), C.c_int(0)
+    sb = lib().orc_k_block_scale(_p(k, _u16p), C.byref(bad), C.byref(rng))
+    return int(sb), bool(bad.value), bool(rng.value)
+
+
+def k_block_code(k_bits, s_bits):
+    return int(lib().orc_k_block_code(int(k_bits), int(s_bits)))
+
+
+def k_block_decode(q, s_bits):
+    return int(lib().orc_k_block_decode(int(q), int(s_bits)))
+
+
 def v_encode_vec(v_bits):
     v = _c(v_bits, np.uint16).ravel()
     d = v.size
@@ -220,8 +243,9 @@ def _ptr_table(arrays, t):
     return arr
 
 
-def pool_encode(k_layers, v_layers, want_u=False):
+def pool_encode(k_layers, v_layers, want_u=False, k_mode=0):
     """k_layers/v_layers: lists of uint16 arrays shaped [H, T, d] (bf16 bits).
+    k_mode: 0 one key scale per layer tensor, 1 q8_0 key blocks.
 
     Returns (pool image uint8, error flags, u or None) where u is the fp64
     rotated coordinate behind every V code, shaped [L, H, T, d]."""
@@ -229,11 +253,27 @@ def pool_encode(k_layers, v_layers, want_u=False):
     v_layers = [_c(v, np.uint16) for v in v_layers]
     L = len(k_layers)
     H, T, d = k_layers[0].shape
-    pool = np.zeros(pool_bytes(L, H, d, T), np.uint8)
+    pool = np.zeros(pool_bytes_mode(L, H, d, T, k_mode), np.uint8)
     u = np.zeros((L, H, T, d), np.float64) if want_u else None
-    flags = lib().orc_pool_encode(L, H, d, T, _ptr_table(k_layers, _u16p), _ptr_table(v_layers, _u16p),
-                                  _p(pool, _u8p), _p(u, _dp) if want_u else None)
+    if k_mode == 0:
+        flags = lib().orc_pool_encode(L, H, d, T, _ptr_table(k_layers, _u16p), _ptr_table(v_layers, _u16p),
+                                      _p(pool, _u8p), _p(u, _dp) if want_u else None)
+    else:
+        flags = lib().orc_pool_encode_mode(L, H, d, T, k_mode, _ptr_table(k_layers, _u16p),
+                                           _ptr_table(v_layers, _u16p), _p(pool, _u8p),
+                                           _p(u, _dp) if want_u else None)
     return pool, int(flags), u
+
+
+def pool_bytes_mode(L, H, d, T, k_mode):
+    return int(lib().orc_pool_bytes_mode(L, H, d, T, int(k_mode)))
+
+
+def pool_geometry_q8(L, H, d, T):
+    """(off_kscales, total bytes) of a q8_0-key pool."""
+    g = np.zeros(2, np.uint64)
+    lib().orc_pool_geometry_q8(L, H, d, T, _p(g, _u64p))
+    return int(g[0]), int(g[1])
 
 
 def pool_decode_into(pool, layer_begin, layer_end, n_agents):

@@ -283,6 +283,40 @@ uint16_t orc_k_decode(int q, float s)
     return orc_f64_to_bf16((double)q * (double)s);
 }
 
+/* Keys in q8_0 blocks, the format [PolyKV] 2.B.1 names by its label "q8_0":
+ * every 32 consecutive elements of a key vector (along d) share one fp16
+ * scale s_b = fp16(max|k| / 127) (round to nearest even), and each element
+ * is the int8 code nearest to k / s_b (ties to even) clamped to [-127, 127]
+ * -- the clamp only bites when s_b is an fp16 subnormal, rounded down by
+ * more than a half code.  s_b = 0 (every |k| below 127 * 2^-25) gives codes
+ * 0.  Sets *nonfinite for Inf/NaN elements (skipped, code 0) and *range when
+ * finite input overflows the fp16 scale. */
+uint16_t orc_k_block_scale(const uint16_t *k32, int *nonfinite, int *range)
+{
+    double m = orc_k_absmax(k32, 32, nonfinite);
+    uint16_t sb = orc_f64_to_f16(m / 127.0);
+    if (range) *range = (sb & 0x7C00u) == 0x7C00u;
+    return sb;
+}
+
+int orc_k_block_code(uint16_t kbits, uint16_t sbits)
+{
+    double s = orc_f16_to_f64(sbits);
+    if (s == 0.0 || !isfinite(s)) return 0;
+    double k = orc_bf16_to_f64(kbits);
+    if (!isfinite(k)) return 0;
+    double q = nearbyint(k / s);
+    if (q > 127.0) q = 127.0;
+    if (q < -127.0) q = -127.0;
+    return (int)q;
+}
+
+/* Block key reconstruction: q * s_b (exact in fp64) rounded to bf16. */
+uint16_t orc_k_block_decode(int q, uint16_t sbits)
+{
+    return orc_f64_to_bf16((double)q * orc_f16_to_f64(sbits));
+}
+
 /* ------------------------------------------------------------------------- */
 /* Values: FWHT rotation + Lloyd-Max 3-bit codes.  [PolyKV] 2.B.2             */
 /* ------------------------------------------------------------------------- */
@@ -368,19 +402,21 @@ void orc_v_decode_vec(const uint8_t *codes, uint16_t sigma_h, int d, uint16_t *o
 /*
  * Layout (all integers little-endian, every section 256-byte aligned):
  *   [0,256)        header: u32 magic 'KVPL', u32 version 1, i32 L, H, d, T,
- *                  u32 error bits, u32 0, u64 off_scales, off_layers,
+ *                  u32 error bits, u32 key format (0: one scale per layer
+ *                  tensor, 1: q8_0 blocks), u64 off_scales, off_layers,
  *                  layer_stride, sec_v, sec_sigma, total_bytes, zero pad
- *   off_scales     fp32 s[L]
+ *   off_scales     fp32 s[L]          (format 1: zero)
  *   off_layers + l*layer_stride:
  *                  +0         int8 K codes  [H][T][d]
  *                  +sec_v     u8 V codes    [H][T][3d/8]
  *                  +sec_sigma fp16 sigma    [H][T]
+ *   off_kscales    format 1 only: fp16 block scales [L][H][T][d/32]
  */
 
 static uint64_t al256(uint64_t x) { return (x + 255u) & ~(uint64_t)255u; }
 
 typedef struct {
-    uint64_t off_scales, off_layers, layer_stride, sec_v, sec_sigma, total;
+    uint64_t off_scales, off_layers, layer_stride, sec_v, sec_sigma, total, off_kscales, total_q8;
 } orc_pool_geom;
 
 static orc_pool_geom pool_geom(int L, int H, int d, int T)
@@ -393,6 +429,8 @@ static orc_pool_geom pool_geom(int L, int H, int d, int T)
     g.sec_sigma = al256(g.sec_v + nv * (uint64_t)(3 * d / 8));
     g.layer_stride = al256(g.sec_sigma + 2ull * nv);
     g.total = g.off_layers + (uint64_t)L * g.layer_stride;
+    g.off_kscales = g.total;
+    g.total_q8 = g.off_kscales + al256((uint64_t)L * nv * (uint64_t)(d / 32) * 2u);
     return g;
 }
 
@@ -401,11 +439,25 @@ size_t orc_pool_bytes(int L, int H, int d, int T)
     return (size_t)pool_geom(L, H, d, T).total;
 }
 
+/* Pool bytes for key format k_mode (0: per-tensor scale, 1: q8_0 blocks). */
+size_t orc_pool_bytes_mode(int L, int H, int d, int T, int k_mode)
+{
+    orc_pool_geom g = pool_geom(L, H, d, T);
+    return (size_t)(k_mode == 1 ? g.total_q8 : g.total);
+}
+
 void orc_pool_geometry(int L, int H, int d, int T, uint64_t *out6)
 {
     orc_pool_geom g = pool_geom(L, H, d, T);
     out6[0] = g.off_scales; out6[1] = g.off_layers; out6[2] = g.layer_stride;
     out6[3] = g.sec_v; out6[4] = g.sec_sigma; out6[5] = g.total;
+}
+
+/* off_kscales and the format-1 total. */
+void orc_pool_geometry_q8(int L, int H, int d, int T, uint64_t *out2)
+{
+    orc_pool_geom g = pool_geom(L, H, d, T);
+    out2[0] = g.off_kscales; out2[1] = g.total_q8;
 }
 
 static void put32(uint8_t *p, uint32_t v) { memcpy(p, &v, 4); }
@@ -417,8 +469,20 @@ static uint64_t get64(const uint8_t *p) { uint64_t v; memcpy(&v, p, 8); return v
  * bytes.  k[l], v[l] point at layer l's bf16 [H][T][d] tensors.  If u_out is
  * given it receives the fp64 rotated coordinates u (layer-major, [L][H][T][d])
  * used to decide each V code.  Returns the error bits (also in the header). */
+uint32_t orc_pool_encode_mode(int L, int H, int d, int T, int k_mode, const uint16_t *const *k,
+                              const uint16_t *const *v, uint8_t *pool, double *u_out);
+
 uint32_t orc_pool_encode(int L, int H, int d, int T, const uint16_t *const *k,
                          const uint16_t *const *v, uint8_t *pool, double *u_out)
+{
+    return orc_pool_encode_mode(L, H, d, T, 0, k, v, pool, u_out);
+}
+
+/* As orc_pool_encode, with the key format chosen by k_mode: 0 one scale per
+ * layer tensor, 1 q8_0 blocks (scales in the off_kscales region, s[L] left
+ * zero).  The image is orc_pool_bytes_mode() bytes. */
+uint32_t orc_pool_encode_mode(int L, int H, int d, int T, int k_mode, const uint16_t *const *k,
+                              const uint16_t *const *v, uint8_t *pool, double *u_out)
 {
     orc_pool_geom g = pool_geom(L, H, d, T);
     uint64_t nv = (uint64_t)H * (uint64_t)T;
@@ -436,20 +500,37 @@ uint32_t orc_pool_encode(int L, int H, int d, int T, const uint16_t *const *k,
     put64(pool + 48, g.layer_stride);
     put64(pool + 56, g.sec_v);
     put64(pool + 64, g.sec_sigma);
-    put64(pool + 72, g.total);
+    put32(pool + 28, (uint32_t)k_mode);
+    put64(pool + 72, k_mode == 1 ? g.total_q8 : g.total);
 
     for (int l = 0; l < L; l++) {
         uint8_t *lay = pool + g.off_layers + (uint64_t)l * g.layer_stride;
-        int bad = 0;
-        double m = orc_k_absmax(k[l], (size_t)ne, &bad);
-        if (bad) flags |= ORC_FLAG_NONFINITE;
-        float s = orc_k_scale(m);
-        memcpy(pool + g.off_scales + 4u * (uint64_t)l, &s, 4);
-
         int8_t *kc = (int8_t *)lay;
         const uint16_t *kl = k[l];
+        if (k_mode == 1) {
+            const uint64_t nb = ne / 32u;
+            uint8_t *ks = pool + g.off_kscales + (uint64_t)l * nb * 2u;
+            uint32_t kflags = 0;
+#pragma omp parallel for schedule(static) reduction(| : kflags)
+            for (int64_t b = 0; b < (int64_t)nb; b++) {
+                int bad = 0, range = 0;
+                uint16_t sb = orc_k_block_scale(kl + (uint64_t)b * 32u, &bad, &range);
+                if (bad) kflags |= ORC_FLAG_NONFINITE;
+                else if (range) kflags |= ORC_FLAG_RANGE;
+                memcpy(ks + 2u * (uint64_t)b, &sb, 2);
+                for (int i = 0; i < 32; i++)
+                    kc[(uint64_t)b * 32u + (uint64_t)i] = (int8_t)orc_k_block_code(kl[(uint64_t)b * 32u + (uint64_t)i], sb);
+            }
+            flags |= kflags;
+        } else {
+            int bad = 0;
+            double m = orc_k_absmax(kl, (size_t)ne, &bad);
+            if (bad) flags |= ORC_FLAG_NONFINITE;
+            float s = orc_k_scale(m);
+            memcpy(pool + g.off_scales + 4u * (uint64_t)l, &s, 4);
 #pragma omp parallel for schedule(static)
-        for (int64_t i = 0; i < (int64_t)ne; i++) kc[i] = (int8_t)orc_k_code(kl[i], s);
+            for (int64_t i = 0; i < (int64_t)ne; i++) kc[i] = (int8_t)orc_k_code(kl[i], s);
+        }
 
         uint8_t *vc = lay + g.sec_v;
         uint8_t *sg = lay + g.sec_sigma;
@@ -480,6 +561,8 @@ int orc_pool_decode_into(const uint8_t *pool, int lb, int le, int n_agents,
     if (get32(pool) != 0x4C50564Bu || get32(pool + 4) != 1u) return -1;
     int L = (int)get32(pool + 8), H = (int)get32(pool + 12);
     int d = (int)get32(pool + 16), T = (int)get32(pool + 20);
+    const int k_mode = (int)get32(pool + 28);
+    if (k_mode != 0 && k_mode != 1) return -1;
     orc_pool_geom g = pool_geom(L, H, d, T);
     uint64_t nv = (uint64_t)H * (uint64_t)T;
     for (int l = lb; l < le; l++) {
@@ -489,12 +572,22 @@ int orc_pool_decode_into(const uint8_t *pool, int lb, int le, int n_agents,
         const int8_t *kc = (const int8_t *)lay;
         const uint8_t *vc = lay + g.sec_v;
         const uint8_t *sg = lay + g.sec_sigma;
+        const uint8_t *ks = pool + g.off_kscales + (uint64_t)l * nv * (uint64_t)(d / 32) * 2u;
 #pragma omp parallel for schedule(static)
         for (int64_t n = 0; n < (int64_t)nv; n++) {
             uint16_t kk[128], vv[128];
             uint8_t codes[128];
             uint16_t sh;
-            for (int i = 0; i < d; i++) kk[i] = orc_k_decode(kc[(uint64_t)n * d + i], s);
+            for (int i = 0; i < d; i++) {
+                const int q = kc[(uint64_t)n * d + i];
+                if (k_mode == 1) {
+                    uint16_t sb;
+                    memcpy(&sb, ks + 2u * ((uint64_t)n * (uint64_t)(d / 32) + (uint64_t)(i / 32)), 2);
+                    kk[i] = orc_k_block_decode(q, sb);
+                } else {
+                    kk[i] = orc_k_decode(q, s);
+                }
+            }
             orc_unpack3(vc + (uint64_t)n * (uint64_t)(3 * d / 8), d, codes);
             memcpy(&sh, sg + 2u * (uint64_t)n, 2);
             orc_v_decode_vec(codes, sh, d, vv);
@@ -842,7 +935,8 @@ int orc_card_unpack_at(const uint8_t *card, int64_t pos_dst, const float *w, uin
 /* One decode step of attention for n_agents agents against layer `layer` of
  * the pool: for agent a and query head j (GQA: query head j reads KV head
  * j / (n_q_heads / H)),
- *   s_t   = scale * (q . k_t),        k_t = q_t * s_l          (exact, fp64)
+ *   s_t   = scale * (q . k_t),        k_t = q_t * s_l  (q8_0 pools: q_t * s_b
+ *                                     per 32-element block; exact, fp64)
  *   p_t   = exp(s_t - max s) / sum,   v_t = sigma_h * (H_d c_t) / sqrt(d)
  *   out   = sum_t p_t v_t,            lse = log(sum_t exp(s_t))
  * over the T pooled tokens.  q: bf16 [n_agents][n_q_heads][d]; out:
@@ -856,8 +950,11 @@ int orc_pool_attend(const uint8_t *pool, int layer, int n_agents, int n_q_heads,
     int L = (int)get32(pool + 8), H = (int)get32(pool + 12);
     int d = (int)get32(pool + 16), T = (int)get32(pool + 20);
     if (layer < 0 || layer >= L || n_q_heads % H != 0) return -1;
+    const int k_mode = (int)get32(pool + 28);
+    if (k_mode != 0 && k_mode != 1) return -1;
     orc_pool_geom g = pool_geom(L, H, d, T);
     const uint8_t *lay = pool + g.off_layers + (uint64_t)layer * g.layer_stride;
+    const uint8_t *ks = pool + g.off_kscales + (uint64_t)layer * (uint64_t)H * T * (uint64_t)(d / 32) * 2u;
     float s;
     memcpy(&s, pool + g.off_scales + 4u * (uint64_t)layer, 4);
     const int8_t *kc = (const int8_t *)lay;
@@ -871,7 +968,15 @@ int orc_pool_attend(const uint8_t *pool, int layer, int n_agents, int n_q_heads,
         uint8_t codes[128];
         uint16_t sh;
         double z[128];
-        for (int i = 0; i < d; i++) kf[n * d + i] = (double)kc[n * d + i] * (double)s;
+        for (int i = 0; i < d; i++) {
+            double sk = (double)s;
+            if (k_mode == 1) {
+                uint16_t sb;
+                memcpy(&sb, ks + 2u * ((uint64_t)n * (uint64_t)(d / 32) + (uint64_t)(i / 32)), 2);
+                sk = orc_f16_to_f64(sb);
+            }
+            kf[n * d + i] = (double)kc[n * d + i] * sk;
+        }
         orc_unpack3(vc + (uint64_t)n * (uint64_t)(3 * d / 8), d, codes);
         memcpy(&sh, sg + 2u * (uint64_t)n, 2);
         for (int i = 0; i < d; i++) z[i] = CENTROID[codes[i]];

@@ -48,6 +48,13 @@ MUTANTS = [
     ("realign adjacent pairs", "double a = x[i], c = x[i + half];", "double a = x[i], c = x[i ^ 1];"),
     ("realign frequency order", "double phi = delta * (double)w[i];", "double phi = delta * (double)w[half - 1 - i];"),
     ("realign drops zero point", "x[32 * gi + i] = (double)q[i] * sc + z;", "x[32 * gi + i] = (double)q[i] * sc;"),
+    ("q8 scale divisor 128", "uint16_t sb = orc_f64_to_f16(m / 127.0);", "uint16_t sb = orc_f64_to_f16(m / 128.0);"),
+    ("q8 ties away from zero", "double q = nearbyint(k / s);", "double q = round(k / s);"),
+    ("q8 scales per layer offset", "uint8_t *ks = pool + g.off_kscales + (uint64_t)l * nb * 2u;",
+     "uint8_t *ks = pool + g.off_kscales + (uint64_t)l * nb;"),
+    ("q8 attend uses tensor scale", "sk = orc_f16_to_f64(sb);", "sk = (double)s;"),
+    ("q8 decode reads next block", "kk[i] = orc_k_block_decode(q, sb);",
+     "memcpy(&sb, ks + 2u * ((uint64_t)n * (uint64_t)(d / 32) + (uint64_t)((i / 32 + 1) % (d / 32))), 2);\n                    kk[i] = orc_k_block_decode(q, sb);"),
 ]
 
 

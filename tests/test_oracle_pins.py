@@ -740,3 +740,160 @@ def test_card_unpack_at_quantized_tokens_and_round_trip():
     for l in range(L):
         ref = _f(k0[l])
         assert np.all(np.abs(_f(k2[l]) - ref) <= 2.0 ** -7 * _pair_norm(ref) + 1e-12)
+
+
+# --------------------------------------------------------------------------
+# q8_0 key blocks (next row: block-wise int8 keys with fp16 scales)
+# --------------------------------------------------------------------------
+
+def _fp16_nearest(fr):
+    """Correctly rounded fp16 of a non-negative Fraction (ties to even), by
+    bracketing with numpy's fp16 neighbours."""
+    f = np.float16(float(fr))
+    cands = [np.nextafter(f, np.float16(0)), f, np.nextafter(f, np.float16(np.inf))]
+    cands = [c for c in cands if np.isfinite(c)]
+    return min(cands, key=lambda c: (abs(Fraction(float(c)) - fr), int(np.float16(c).view(np.uint16)) & 1))
+
+
+def _q8_block(x):
+    kb = _bf16(x)
+    sb, bad, rng = O.k_block_scale(kb)
+    return kb, sb, bad, rng
+
+
+def test_k_block_scale_is_correctly_rounded_fp16():
+    rng = np.random.default_rng(31)
+    mags = [1.0, 127.0, 3.5, 127 * 2.0 ** -25, 127 * 2.0 ** -14, 127 * 2.0 ** -24 * 3, 5.0e4, 8.0e6, 1e-7]
+    mags += list(10.0 ** rng.uniform(-7, 6.5, 300))
+    for m in mags:
+        x = rng.normal(size=32) * 0.3 * m
+        x[rng.integers(0, 32)] = m * (1 if rng.random() < 0.5 else -1)
+        kb, sb, bad, rng_flag = _q8_block(x)
+        mm = max(abs(O.bf16_to_f64(int(b))) for b in kb)
+        want = _fp16_nearest(Fraction(mm) / 127)
+        s = np.float16(O.f16_to_f64(sb))
+        if np.isinf(np.float16(float(Fraction(mm) / 127))) or float(Fraction(mm) / 127) >= 65520:
+            assert rng_flag and (sb & 0x7C00) == 0x7C00
+            continue
+        assert not bad and not rng_flag
+        assert s == want, (m, s, want)
+
+
+def test_k_block_codes_bruteforce_exact():
+    rng = np.random.default_rng(32)
+    for trial in range(40):
+        x = rng.normal(size=32) * (10.0 ** rng.uniform(-6, 3))
+        x[rng.integers(0, 32)] *= 20
+        kb, sb, _, _ = _q8_block(x)
+        S = Fraction(O.f16_to_f64(sb))
+        assert S > 0
+        clamped = 0
+        for b in kb:
+            K = Fraction(O.bf16_to_f64(int(b)))
+            best = min(range(-127, 128), key=lambda q: (abs(K - q * S), q & 1))
+            q = O.k_block_code(int(b), sb)
+            assert q == best
+            if abs(K - q * S) > S / 2:
+                clamped += 1
+                assert abs(q) == 127
+            assert O.k_block_decode(q, sb) == int(_bf16_rne(float(q * S)))
+        if O.f16_to_f64(sb) >= 2.0 ** -14:  # normal scale: nothing clamps, the absmax maps to +-127
+            assert clamped == 0
+            j = int(np.argmax(np.abs(_f(kb))))
+            assert abs(O.k_block_code(int(kb[j]), sb)) == 127
+
+
+def test_k_block_on_grid_zero_and_flags():
+    for e in (-10, -3, 0, 5):
+        qs = np.arange(-127, 128, 8)[:32].astype(np.float64)
+        qs[0] = -127
+        x = qs * 2.0 ** e
+        kb, sb, bad, rng_flag = _q8_block(x)
+        assert O.f16_to_f64(sb) == 2.0 ** e and not bad and not rng_flag
+        assert [O.k_block_code(int(b), sb) for b in kb] == [int(q) for q in qs]
+        assert [O.k_block_decode(int(q), sb) for q in qs] == list(kb)
+    kb, sb, bad, rng_flag = _q8_block(np.zeros(32))
+    assert sb == 0 and O.k_block_code(int(kb[0]), sb) == 0 and O.k_block_decode(0, sb) == 0
+    kb, sb, bad, rng_flag = _q8_block(np.full(32, 127 * 2.0 ** -26))  # below half the least scale
+    assert sb == 0 and all(O.k_block_code(int(b), sb) == 0 for b in kb)
+    x = np.ones(32)
+    x[3] = np.nan
+    assert _q8_block(x)[2]
+    x = np.ones(32)
+    x[5] = 1.0e7  # 1e7 / 127 overflows fp16
+    kb, sb, bad, rng_flag = _q8_block(x)
+    assert rng_flag and not bad
+
+
+def test_pool_q8_layout_and_consistency():
+    L, H, T, d = 2, 3, 11, 64
+    ks, vs = _tiny_kv(L, H, T, d, 33)
+    p0, f0, _ = O.pool_encode(ks, vs)
+    p1, f1, _ = O.pool_encode(ks, vs, k_mode=1)
+    assert f0 == 0 and f1 == 0
+    g = O.pool_geometry(L, H, d, T)
+    off_ks, total = O.pool_geometry_q8(L, H, d, T)
+    nb = H * T * d // 32
+    assert off_ks == g["total"] and total == g["total"] + ((L * nb * 2 + 255) // 256) * 256 == p1.size
+    hdr = p1[:80]
+    assert hdr[28:32].view(np.uint32)[0] == 1 and p0[28:32].view(np.uint32)[0] == 0
+    assert hdr[72:80].view(np.uint64)[0] == total
+    assert not p1[g["off_scales"]: g["off_scales"] + 4 * L].any()       # no per-tensor scales
+    for l in range(L):
+        base = g["off_layers"] + l * g["layer_stride"]
+        # values and sigma do not depend on the key format
+        np.testing.assert_array_equal(p1[base + g["sec_v"]: base + g["layer_stride"]],
+                                      p0[base + g["sec_v"]: base + g["layer_stride"]])
+        kc = p1[base: base + H * T * d].view(np.int8)
+        sc = p1[off_ks + l * nb * 2: off_ks + (l + 1) * nb * 2].view(np.uint16)
+        kflat = ks[l].reshape(-1)
+        for b in range(nb):
+            sb, _, _ = O.k_block_scale(kflat[32 * b: 32 * b + 32])
+            assert sc[b] == sb
+            assert [O.k_block_code(int(x), sb) for x in kflat[32 * b: 32 * b + 32]] == list(kc[32 * b: 32 * b + 32])
+    kd, vd = O.pool_decode_into(p1, 0, L, 1)
+    k0, v0 = O.pool_decode_into(p0, 0, L, 1)
+    for l in range(L):
+        base = g["off_layers"] + l * g["layer_stride"]
+        kc = p1[base: base + H * T * d].view(np.int8)
+        sc = p1[off_ks + l * nb * 2: off_ks + (l + 1) * nb * 2].view(np.uint16)
+        want = [O.k_block_decode(int(kc[i]), int(sc[i // 32])) for i in range(H * T * d)]
+        np.testing.assert_array_equal(kd[0][l].reshape(-1), np.array(want, np.uint16))
+        np.testing.assert_array_equal(vd[0][l], v0[0][l])
+
+
+def test_q8_blocks_beat_one_scale_on_outlier_channels():
+    """Keys with a few 20x channels per head (the synthetic recipe): per-block
+    scales confine the outliers' range to their own blocks, so the mean
+    reconstruction error is several times below the per-tensor scale's."""
+    L, H, T, d = 1, 2, 64, 128
+    ks, vs = _tiny_kv(L, H, T, d, 34)
+    x = _f(ks[0])
+    errs = []
+    for mode in (0, 1):
+        p, _, _ = O.pool_encode(ks, vs, k_mode=mode)
+        kd, _ = O.pool_decode_into(p, 0, 1, 1)
+        errs.append(np.mean(np.abs(_f(kd[0][0]) - x)))
+    assert errs[1] < errs[0] / 3, errs
+
+
+def test_pool_attend_q8_against_library_softmax():
+    import scipy.special
+    L, H, T, d = 1, 2, 45, 128
+    ks, vs = _tiny_kv(L, H, T, d, 35)
+    pool, _, _ = O.pool_encode(ks, vs, k_mode=1)
+    g = O.pool_geometry(L, H, d, T)
+    off_ks, _ = O.pool_geometry_q8(L, H, d, T)
+    kc = pool[g["off_layers"]: g["off_layers"] + H * T * d].view(np.int8).astype(np.float64)
+    sc = np.array([O.f16_to_f64(int(s)) for s in pool[off_ks: off_ks + H * T * d // 32 * 2].view(np.uint16)])
+    kf = (kc.reshape(-1, 32) * sc[:, None]).reshape(H, T, d)
+    _, vf = _decoded_fp64(pool, L, H, d, T, 0)
+    rng = np.random.default_rng(36)
+    q = _bf16(rng.normal(size=(2, 4, d)))
+    out, lse = O.pool_attend(pool, 0, q, 0.1)
+    for a in range(2):
+        for j in range(4):
+            h = j // 2
+            s = 0.1 * (kf[h] @ _f(q)[a, j])
+            np.testing.assert_allclose(out[a, j], scipy.special.softmax(s) @ vf[h], rtol=1e-10, atol=1e-12)
+            assert abs(lse[a, j] - scipy.special.logsumexp(s)) < 1e-10
