@@ -31,6 +31,8 @@ KVP_ERR_BITS = -8
 KVP_ERR_HEADER = -9
 KVP_ERR_TIMEOUT = -10
 KVP_MAX_LAYERS = 512
+KVP_K_PER_TENSOR = 0
+KVP_K_Q8_0 = 1
 KVP_NOALLOC_SCRATCH_BYTES = 262144
 
 
@@ -61,6 +63,9 @@ _SIGS = {
     "kvpool_workspace_bytes": (C.c_size_t, [C.POINTER(Shape)]),
     "kvpool_encode": (C.c_int, [C.POINTER(Shape), C.POINTER(_vp), C.POINTER(_vp), _vp, C.c_size_t,
                                 _vp, C.c_size_t, _vp]),
+    "kvpool_pool_bytes_ex": (C.c_size_t, [C.POINTER(Shape), C.c_int]),
+    "kvpool_encode_ex": (C.c_int, [C.POINTER(Shape), C.c_int, C.POINTER(_vp), C.POINTER(_vp), _vp, C.c_size_t,
+                                   _vp, C.c_size_t, _vp]),
     "kvpool_decode_into": (C.c_int, [_vp, C.POINTER(Shape), C.c_int, C.c_int, C.c_int,
                                      C.POINTER(_vp), C.POINTER(_vp), _vp]),
     "kvpool_status": (C.c_int, [_vp, _vp]),
@@ -157,6 +162,16 @@ def kvpool_workspace_bytes(shape):
 def kvpool_encode(shape, k_layers, v_layers, pool, pool_bytes, ws, ws_bytes, stream=None):
     return load().kvpool_encode(C.byref(_shape(shape)), _ptrs(k_layers), _ptrs(v_layers), _addr(pool),
                                 int(pool_bytes), _addr(ws), int(ws_bytes), _stream(stream))
+
+
+def kvpool_pool_bytes_ex(shape, k_mode):
+    return int(load().kvpool_pool_bytes_ex(C.byref(_shape(shape)), int(k_mode)))
+
+
+def kvpool_encode_ex(shape, k_mode, k_layers, v_layers, pool, pool_bytes, ws, ws_bytes, stream=None):
+    """k_mode: KVP_K_PER_TENSOR or KVP_K_Q8_0."""
+    return load().kvpool_encode_ex(C.byref(_shape(shape)), int(k_mode), _ptrs(k_layers), _ptrs(v_layers),
+                                   _addr(pool), int(pool_bytes), _addr(ws), int(ws_bytes), _stream(stream))
 
 
 def kvpool_encode_noalloc(shape, k_layers, v_layers, pool, pool_bytes, stream=None):

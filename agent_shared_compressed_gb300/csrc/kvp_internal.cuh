@@ -33,12 +33,14 @@ constexpr uint32_t POOL_MAGIC = 0x4C50564Bu;
 constexpr uint32_t POOL_VERSION = 1u;
 constexpr uint64_t POOL_HEADER_BYTES = 256;
 constexpr int POOL_ERR_WORD = 6;  // u32 index of the error word
+constexpr int POOL_KMODE_WORD = 7;  // u32 index of the key format word (KVP_K_PER_TENSOR / KVP_K_Q8_0)
 
 __host__ __device__ inline uint64_t align256(uint64_t x) { return (x + 255u) & ~uint64_t(255); }
 __host__ __device__ inline uint64_t align16(uint64_t x) { return (x + 15u) & ~uint64_t(15); }
 
 struct PoolGeom {
     uint64_t off_scales, off_layers, layer_stride, sec_v, sec_sigma, total;
+    uint64_t off_kscales, total_q8;  // q8_0 keys: fp16 block scales [L][H][T][d/32] after the last layer
 };
 
 __host__ __device__ inline PoolGeom pool_geom(int L, int H, int d, int T) {
@@ -50,6 +52,8 @@ __host__ __device__ inline PoolGeom pool_geom(int L, int H, int d, int T) {
     g.sec_sigma = align256(g.sec_v + nv * uint64_t(3 * d / 8));
     g.layer_stride = align256(g.sec_sigma + 2ull * nv);
     g.total = g.off_layers + uint64_t(L) * g.layer_stride;
+    g.off_kscales = g.total;
+    g.total_q8 = g.off_kscales + align256(uint64_t(L) * nv * uint64_t(d / 32) * 2ull);
     return g;
 }
 

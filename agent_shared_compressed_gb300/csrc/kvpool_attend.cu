@@ -81,7 +81,9 @@ struct AttendSmem {
     static constexpr int MS = D + 8;      // floats per row of a warp's merge slot (conflict-free float2 stores)
     static constexpr size_t q_words = size_t(ATT_MT) * RW;
     static constexpr size_t tile_words = size_t(ATT_TC) * RW;  // one K or C buffer
-    static constexpr size_t stage_words = q_words + 4 * tile_words + 2 * ATT_TC + 64;  // Q, K[2], C[2], sig[2], lut
+    static constexpr size_t ksb_words = size_t(ATT_TC) * (D / 32);  // one buffer of q8_0 key block scales
+    static constexpr size_t stage_words =
+        q_words + 4 * tile_words + 2 * ATT_TC + 64 + 2 * ksb_words;  // Q, K[2], C[2], sig[2], lut, ksb[2]
     static constexpr size_t merge_words = size_t(ATT_WARPS) * (16 * MS + 32);
     static constexpr size_t bytes = 4 * (stage_words > merge_words ? stage_words : merge_words);
 };
@@ -97,11 +99,12 @@ struct RawChunk {
     uint4 k[D / 64];
     uint32_t v[3];
     uint32_t sig;  // fp16 bits of token tid's sigma (tid < 64)
+    uint32_t ksc;  // q8_0 keys: fp16 bits of block tid % (D/32) of token tid / (D/32)
 };
 
-template <int D>
+template <int D, bool Q8>
 __device__ __forceinline__ void load_chunk(RawChunk<D> &r, const uint8_t *lay, const PoolGeom &geo, uint64_t vbase,
-                                           int t0, int T, int tid) {
+                                           int t0, int T, int tid, const uint16_t *kscales) {
     constexpr int VPT = D / 32;  // 32-code value items per token
     const int q = tid >> 3, l8 = tid & 7;
     const int tk = t0 + l8 + 8 * (q >> 2);
@@ -124,14 +127,18 @@ __device__ __forceinline__ void load_chunk(RawChunk<D> &r, const uint8_t *lay, c
     r.sig = 0u;
     if (tid < ATT_TC && t0 + tid < T)
         r.sig = reinterpret_cast<const uint16_t *>(lay + geo.sec_sigma)[vbase + t0 + tid];
+    if constexpr (Q8) {
+        r.ksc = 0u;
+        if (tid < ATT_TC * (D / 32) && t0 + tid / (D / 32) < T) r.ksc = kscales[(vbase + t0) * (D / 32) + tid];
+    }
 }
 
 // Registers -> shared tiles: keys int8 -> exact bf16 (|q| <= 127 has at most
 // 7 significant bits); value codes -> fp16 centroids, two dims per word via
 // the pair table.
-template <int D>
+template <int D, bool Q8>
 __device__ __forceinline__ void stage_chunk(const RawChunk<D> &r, uint32_t *Kb, uint32_t *Cs, float *sig,
-                                            const uint32_t *lut, int tid) {
+                                            const uint32_t *lut, float *ksb, int tid) {
     constexpr int RW = AttendSmem<D>::RW, VPT = D / 32;
     const int q = tid >> 3, l8 = tid & 7;
     {
@@ -167,24 +174,26 @@ __device__ __forceinline__ void stage_chunk(const RawChunk<D> &r, uint32_t *Kb, 
         for (int k = 0; k < 16; k += 4) *reinterpret_cast<uint4 *>(row + k) = make_uint4(o[k], o[k + 1], o[k + 2], o[k + 3]);
     }
     if (tid < ATT_TC) sig[tid] = __half2float(__ushort_as_half(static_cast<uint16_t>(r.sig)));
+    if constexpr (Q8)
+        if (tid < ATT_TC * (D / 32)) ksb[tid] = __half2float(__ushort_as_half(static_cast<uint16_t>(r.ksc)));
 }
 
 // TPW: tokens of a sub-chunk per warp (32: four 16-row tiles per pass; 16:
 // two 16-row tiles per pass, for blocks with at most 32 query rows).
-template <int D, int TPW>
-__global__ void __launch_bounds__(ATT_THREADS, 2) attend_split(const __grid_constant__ AttendArgs a) {
+template <int D, int TPW, bool Q8>
+__device__ __forceinline__ void attend_passes(const AttendArgs &a, uint32_t *smem, const uint16_t *kscales) {
     using SM = AttendSmem<D>;
     constexpr int RW = SM::RW, MSW = SM::MS;
     constexpr int MS = TPW / 8;       // 16-row tiles per pass
     constexpr int RP = 16 * MS;       // query rows per pass
     constexpr int NS = TPW / 8;       // S n-tiles per warp
     constexpr int NV = D / 8;         // PV n-tiles per warp (all dims)
-    extern __shared__ __align__(16) uint32_t smem[];
     uint32_t *Qs = smem;                       // [ATT_MT][RW] bf16 pairs
     uint32_t *Kb = Qs + SM::q_words;           // [2][ATT_TC][RW] bf16 pairs
     uint32_t *Cs = Kb + 2 * SM::tile_words;    // [2][ATT_TC][RW] fp16 pairs
     float *sig = reinterpret_cast<float *>(Cs + 2 * SM::tile_words);  // [2][ATT_TC]
     uint32_t *lut = reinterpret_cast<uint32_t *>(sig + 2 * ATT_TC);   // [64] (c[lo], c[hi]) fp16 pairs
+    float *ksb = reinterpret_cast<float *>(lut + 64);                  // [2][ATT_TC][D/32] q8_0 key block scales
     float *mrg = reinterpret_cast<float *>(smem);  // after the loop: [warps][16][MSW] acc, then [warps][32] m, l
 
     const int h = blockIdx.x, split = blockIdx.y;
@@ -192,15 +201,16 @@ __global__ void __launch_bounds__(ATT_THREADS, 2) attend_split(const __grid_cons
     const int g = lane >> 2, tig = lane & 3;
     const int mi = warp % MS, th = warp / MS;
     const uint8_t *lay = a.pool + a.geo.off_layers + uint64_t(a.layer) * a.geo.layer_stride;
+    // base-2 score scale; q8_0 block scales enter the scores themselves
     const float qk2 = a.scale * 1.4426950408889634f *
-                      reinterpret_cast<const float *>(a.pool + a.geo.off_scales)[a.layer];  // base-2 score scale
+                      (Q8 ? 1.0f : reinterpret_cast<const float *>(a.pool + a.geo.off_scales)[a.layer]);
     const uint64_t vbase = uint64_t(h) * uint64_t(a.T);
     const int sub0 = split * a.per_split, sub1 = min(a.nsub, sub0 + a.per_split);
 
     for (int m0 = 0; m0 < a.QH; m0 += RP) {
         __syncthreads();  // the previous pass's merge slots are read
         RawChunk<D> raw;  // the first sub-chunk's bytes are requested before the query tile
-        load_chunk<D>(raw, lay, a.geo, vbase, sub0 * ATT_TC, a.T, tid);
+        load_chunk<D, Q8>(raw, lay, a.geo, vbase, sub0 * ATT_TC, a.T, tid, kscales);
         if (tid < 64) {
             const float c0 = centroid_e4(uint32_t(tid & 7)) * 1e-4f, c1 = centroid_e4(uint32_t(tid >> 3)) * 1e-4f;
             lut[tid] = pack_half2(c0, c1);
@@ -225,8 +235,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 2) attend_split(const __grid_cons
             const int buf = (sub - sub0) & 1;
             uint32_t *Kt = Kb + buf * SM::tile_words, *Ct = Cs + buf * SM::tile_words;
             float *st = sig + buf * ATT_TC;
-            stage_chunk<D>(raw, Kt, Ct, st, lut, tid);
-            if (sub + 1 < sub1) load_chunk<D>(raw, lay, a.geo, vbase, (sub + 1) * ATT_TC, a.T, tid);
+            float *kst = ksb + buf * SM::ksb_words;
+            stage_chunk<D, Q8>(raw, Kt, Ct, st, lut, kst, tid);
+            if (sub + 1 < sub1) load_chunk<D, Q8>(raw, lay, a.geo, vbase, (sub + 1) * ATT_TC, a.T, tid, kscales);
             __syncthreads();  // this buffer is staged; every warp is done with the other one
             if (!active) continue;
 
@@ -234,17 +245,44 @@ __global__ void __launch_bounds__(ATT_THREADS, 2) attend_split(const __grid_cons
             float s[NS][4];
 #pragma unroll
             for (int nt = 0; nt < NS; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.0f;
+            if constexpr (!Q8) {
 #pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-                uint32_t qa[4];
-                ldsm_x4(qa, Qs + (mi * 16 + (lane & 15)) * RW + ks * 8 + (lane >> 4) * 4);
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    uint32_t qa[4];
+                    ldsm_x4(qa, Qs + (mi * 16 + (lane & 15)) * RW + ks * 8 + (lane >> 4) * 4);
 #pragma unroll
-                for (int np = 0; np < NS; np += 2) {
-                    uint32_t kb[4];
-                    const int tok = th * TPW + np * 8 + (lane & 7) + ((lane >> 4) << 3);
-                    ldsm_x4(kb, Kt + tok * RW + ks * 8 + ((lane >> 3) & 1) * 4);
-                    mma_bf16(s[np], qa, kb[0], kb[1]);
-                    mma_bf16(s[np + 1], qa, kb[2], kb[3]);
+                    for (int np = 0; np < NS; np += 2) {
+                        uint32_t kb[4];
+                        const int tok = th * TPW + np * 8 + (lane & 7) + ((lane >> 4) << 3);
+                        ldsm_x4(kb, Kt + tok * RW + ks * 8 + ((lane >> 3) & 1) * 4);
+                        mma_bf16(s[np], qa, kb[0], kb[1]);
+                        mma_bf16(s[np + 1], qa, kb[2], kb[3]);
+                    }
+                }
+            } else {
+                // q8_0: each 32-key block's exact partial products, one n-tile
+                // at a time, added in scaled by that token's block scale
+#pragma unroll
+                for (int nt = 0; nt < NS; ++nt) {
+                    const int tok = th * TPW + nt * 8 + (lane & 7);
+                    const int tl = th * TPW + nt * 8 + 2 * tig;
+#pragma unroll 1
+                    for (int blk = 0; blk < D / 32; ++blk) {
+                        float t1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                        uint32_t kb[4];  // k-steps 2 blk and 2 blk + 1 of this n-tile
+                        ldsm_x4(kb, Kt + tok * RW + blk * 16 + (lane >> 3) * 4);
+#pragma unroll
+                        for (int kk = 0; kk < 2; ++kk) {
+                            uint32_t qa[4];
+                            ldsm_x4(qa, Qs + (mi * 16 + (lane & 15)) * RW + (2 * blk + kk) * 8 + (lane >> 4) * 4);
+                            mma_bf16(t1, qa, kb[2 * kk], kb[2 * kk + 1]);
+                        }
+                        const float c0 = kst[tl * (D / 32) + blk], c1 = kst[(tl + 1) * (D / 32) + blk];
+                        s[nt][0] = fmaf(t1[0], c0, s[nt][0]);
+                        s[nt][1] = fmaf(t1[1], c1, s[nt][1]);
+                        s[nt][2] = fmaf(t1[2], c0, s[nt][2]);
+                        s[nt][3] = fmaf(t1[3], c1, s[nt][3]);
+                    }
                 }
             }
             // online softmax over this warp's slice (rows g and g+8 of the tile)
@@ -355,6 +393,25 @@ __global__ void __launch_bounds__(ATT_THREADS, 2) attend_split(const __grid_cons
             if (c4 == 0) a.stats[pbase + m0 + r] = make_float2(M, l);
         }
     }
+}
+
+template <int D, int TPW>
+__global__ void __launch_bounds__(ATT_THREADS, 2) attend_split(const __grid_constant__ AttendArgs a) {
+    extern __shared__ __align__(16) uint32_t smem[];
+    const uint32_t *hdr = reinterpret_cast<const uint32_t *>(a.pool);
+    const uint32_t kmode = hdr[POOL_KMODE_WORD];
+    if (hdr[0] != POOL_MAGIC || hdr[1] != POOL_VERSION || hdr[2] != uint32_t(a.L) || hdr[3] != uint32_t(a.H) ||
+        hdr[4] != uint32_t(D) || hdr[5] != uint32_t(a.T) || (kmode != KVP_K_PER_TENSOR && kmode != KVP_K_Q8_0)) {
+        if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0 && hdr[0] == POOL_MAGIC)
+            atomicOr(const_cast<uint32_t *>(hdr) + POOL_ERR_WORD, FLAG_HEADER);
+        return;
+    }
+    if (kmode == KVP_K_Q8_0)
+        attend_passes<D, TPW, true>(
+            a, smem,
+            reinterpret_cast<const uint16_t *>(a.pool + a.geo.off_kscales) + uint64_t(a.layer) * a.H * a.T * (D / 32));
+    else
+        attend_passes<D, TPW, false>(a, smem, nullptr);
 }
 
 // One 128-thread block per (agent, query head): merge the splits, inverse

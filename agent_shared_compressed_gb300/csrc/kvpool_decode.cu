@@ -48,8 +48,9 @@ __device__ __forceinline__ uint4 k_decode8(uint2 raw, float s) {
 // then values.  Value codes are staged in shared memory and each pair of
 // codes (a, b) is looked up in a 64-entry table of (c_a + c_b, c_a - c_b),
 // which is also the transform's first butterfly stage.
-template <int D>
-__global__ void __launch_bounds__(DEC_THREADS, 4) decode_fanout(const __grid_constant__ DecodeArgs a) {
+// The grid-stride walk over units; Q8: keys carry q8_0 block scales.
+template <int D, bool Q8>
+__device__ __forceinline__ void decode_units(const DecodeArgs &a, uint8_t (*stage)[384 + 16], const float2 *pair_lut) {
     constexpr int LPV = D / 32;
     constexpr int VPW = 32 / LPV;
     constexpr int CPV = D / 8;
@@ -57,29 +58,13 @@ __global__ void __launch_bounds__(DEC_THREADS, 4) decode_fanout(const __grid_con
     constexpr int KCH = VPW * D / 8 / 32;  // 8-byte key chunks per lane per step (4)
     // 1 / (sqrt(d) * 10^4): the orthonormal 1/sqrt(d) and the codebook's 10^4.
     constexpr float KS = D == 128 ? 8.838834764831845e-6f : 1.25e-5f;
-    __shared__ __align__(16) uint8_t stage[DEC_WARPS][384 + 16];
-    __shared__ float2 pair_lut[64];
-
-    if (threadIdx.x < 64) {
-        const float ca = centroid_e4(threadIdx.x & 7u), cb = centroid_e4(threadIdx.x >> 3);
-        pair_lut[threadIdx.x] = make_float2(ca + cb, ca - cb);  // exact: integers < 2^16
-    }
-    __syncthreads();
-
-    const uint32_t *hdr = reinterpret_cast<const uint32_t *>(a.pool);
-    if (hdr[0] != POOL_MAGIC || hdr[1] != POOL_VERSION) return;
-    if (hdr[2] != uint32_t(a.L) || hdr[3] != uint32_t(a.H) || hdr[4] != uint32_t(a.d) || hdr[5] != uint32_t(a.T)) {
-        if (blockIdx.x == 0 && threadIdx.x == 0)
-            atomicOr(const_cast<uint32_t *>(hdr) + POOL_ERR_WORD, FLAG_HEADER);
-        return;
-    }
-
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane / LPV, l = lane % LPV;
     const uint64_t nvec = uint64_t(a.H) * uint64_t(a.T);
     const uint64_t upl = (nvec + VPW - 1) / VPW;
     const uint64_t total = upl * uint64_t(a.nl);
     const float *scales = reinterpret_cast<const float *>(a.pool + a.geo.off_scales);
+    const uint16_t *kscales = reinterpret_cast<const uint16_t *>(a.pool + a.geo.off_kscales);
 
     for (uint64_t u = uint64_t(blockIdx.x) * DEC_WARPS + warp; u < total; u += uint64_t(gridDim.x) * DEC_WARPS) {
         const int r = int(u / upl);
@@ -111,13 +96,26 @@ __global__ void __launch_bounds__(DEC_THREADS, 4) decode_fanout(const __grid_con
         const uint64_t n = n0 + g;
         const bool valid = n < nvec;
         const uint16_t sh = valid ? reinterpret_cast<const uint16_t *>(lay + a.geo.sec_sigma)[n] : uint16_t(0);
-        const float s = scales[layer];
+        float ks[KCH];  // each 8-key chunk's scale: the layer's, or its q8_0 block's
+        if constexpr (Q8) {
+            // chunk k of the unit holds keys 8k .. 8k+7 from vector n0: block (n0 * D + 8k) / 32
+            const uint16_t *bs = kscales + (uint64_t(layer) * nvec + n0) * (D / 32);
+#pragma unroll
+            for (int it = 0; it < KCH; ++it) {
+                const uint32_t k = uint32_t(it) * 32u + uint32_t(lane);
+                ks[it] = k < kvalid ? __half2float(__ushort_as_half(bs[k >> 2])) : 0.0f;
+            }
+        } else {
+            const float s = scales[layer];
+#pragma unroll
+            for (int it = 0; it < KCH; ++it) ks[it] = s;
+        }
 
         // --- keys: decode, fan out
         {
             uint4 kout[KCH];
 #pragma unroll
-            for (int it = 0; it < KCH; ++it) kout[it] = k_decode8(kraw[it], s);
+            for (int it = 0; it < KCH; ++it) kout[it] = k_decode8(kraw[it], ks[it]);
             for (int ag = 0; ag < a.na; ++ag) {
                 uint4 *kd = a.kd[ag * a.nl + r] + n0 * (D / 8);
 #pragma unroll
@@ -161,6 +159,33 @@ __global__ void __launch_bounds__(DEC_THREADS, 4) decode_fanout(const __grid_con
         }
     }
 }
+
+template <int D>
+__global__ void __launch_bounds__(DEC_THREADS, 4) decode_fanout(const __grid_constant__ DecodeArgs a) {
+    __shared__ __align__(16) uint8_t stage[DEC_WARPS][384 + 16];
+    __shared__ float2 pair_lut[64];
+
+    if (threadIdx.x < 64) {
+        const float ca = centroid_e4(threadIdx.x & 7u), cb = centroid_e4(threadIdx.x >> 3);
+        pair_lut[threadIdx.x] = make_float2(ca + cb, ca - cb);  // exact: integers < 2^16
+    }
+    __syncthreads();
+
+    const uint32_t *hdr = reinterpret_cast<const uint32_t *>(a.pool);
+    if (hdr[0] != POOL_MAGIC || hdr[1] != POOL_VERSION) return;
+    const uint32_t kmode = hdr[POOL_KMODE_WORD];
+    if (hdr[2] != uint32_t(a.L) || hdr[3] != uint32_t(a.H) || hdr[4] != uint32_t(a.d) || hdr[5] != uint32_t(a.T) ||
+        (kmode != KVP_K_PER_TENSOR && kmode != KVP_K_Q8_0)) {
+        if (blockIdx.x == 0 && threadIdx.x == 0)
+            atomicOr(const_cast<uint32_t *>(hdr) + POOL_ERR_WORD, FLAG_HEADER);
+        return;
+    }
+    if (kmode == KVP_K_Q8_0)
+        decode_units<D, true>(a, stage, pair_lut);
+    else
+        decode_units<D, false>(a, stage, pair_lut);
+}
+
 
 template <int D>
 static int decode_grid(uint64_t total_units) {

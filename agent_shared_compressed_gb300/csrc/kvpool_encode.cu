@@ -65,6 +65,7 @@ struct EncodeArgs {
     uint32_t spin_limit;
     int L, H, T, d, P;
     int fail_layer;             // failure-path testing: this layer's flag is never released
+    uint32_t kmode;             // KVP_K_PER_TENSOR or KVP_K_Q8_0
 };
 
 struct WsLayout {
@@ -181,6 +182,16 @@ __device__ void absmax_slice(const EncodeArgs &a, int l, uint32_t p, uint64_t po
 
 // Layer l's absmax slices are all done: its scale, quantizer parameters and
 // alignment gaps; then release ready[l].  Whole block.
+// Zero a layer's alignment gaps so the pool image is deterministic (block-wide).
+__device__ void zero_layer_gaps(const EncodeArgs &a, int l) {
+    uint8_t *lay = a.pool + a.geo.off_layers + uint64_t(l) * a.geo.layer_stride;
+    const uint64_t gaps[3][2] = {{a.nvec * uint64_t(a.d), a.geo.sec_v},
+                                 {a.geo.sec_v + a.nvec * uint64_t(3 * a.d / 8), a.geo.sec_sigma},
+                                 {a.geo.sec_sigma + 2 * a.nvec, a.geo.layer_stride}};
+    for (int gi = 0; gi < 3; ++gi)
+        for (uint64_t i = gaps[gi][0] + threadIdx.x; i < gaps[gi][1]; i += ENC_THREADS) lay[i] = 0;
+}
+
 __device__ void finalize_layer(const EncodeArgs &a, int l, uint32_t *red) {
     __threadfence();  // the other blocks' partials (written before their counter increments)
     uint32_t m = 0;
@@ -217,14 +228,7 @@ __device__ void finalize_layer(const EncodeArgs &a, int l, uint32_t *red) {
         a.kparams[l] = kp;
         reinterpret_cast<float *>(a.pool + a.geo.off_scales)[l] = s;
     }
-    {   // zero the layer's alignment gaps so the pool image is deterministic
-        uint8_t *lay = a.pool + a.geo.off_layers + uint64_t(l) * a.geo.layer_stride;
-        const uint64_t gaps[3][2] = {{a.nvec * uint64_t(a.d), a.geo.sec_v},
-                                     {a.geo.sec_v + a.nvec * uint64_t(3 * a.d / 8), a.geo.sec_sigma},
-                                     {a.geo.sec_sigma + 2 * a.nvec, a.geo.layer_stride}};
-        for (int gi = 0; gi < 3; ++gi)
-            for (uint64_t i = gaps[gi][0] + threadIdx.x; i < gaps[gi][1]; i += ENC_THREADS) lay[i] = 0;
-    }
+    zero_layer_gaps(a, l);
     __syncthreads();
     if (threadIdx.x == 0) {
         __threadfence();
@@ -240,7 +244,7 @@ __device__ void finalize_layer(const EncodeArgs &a, int l, uint32_t *red) {
 // of a half-integer is the decision taken exactly: the sign of
 // k - (q0 +- 1/2) s is exact under one fma rounding.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t k_code_exact(float k, float s, float q0) {
+__device__ __forceinline__ int k_code_exact_int(float k, float s, float q0) {
     const float hi = fmaf(-(q0 + 0.5f), s, k);
     const float lo = fmaf(-(q0 - 0.5f), s, k);
     int q = int(q0);
@@ -252,7 +256,11 @@ __device__ __forceinline__ uint32_t k_code_exact(float k, float s, float q0) {
         q -= 1;
     else if (lo == 0.0f)
         q -= (q & 1);
-    return uint32_t(q) & 0xFFu;
+    return q;
+}
+
+__device__ __forceinline__ uint32_t k_code_exact(float k, float s, float q0) {
+    return uint32_t(k_code_exact_int(k, s, q0)) & 0xFFu;
 }
 
 template <bool PRESCALE>
@@ -474,14 +482,14 @@ __device__ void write_header(const EncodeArgs &a) {
         h[4] = uint32_t(a.d);
         h[5] = uint32_t(a.T);
         h[POOL_ERR_WORD] = *reinterpret_cast<volatile uint32_t *>(&a.ctl->flags);
-        h[7] = 0;
+        h[POOL_KMODE_WORD] = a.kmode;
         uint64_t *h64 = reinterpret_cast<uint64_t *>(a.pool);
         h64[4] = a.geo.off_scales;
         h64[5] = a.geo.off_layers;
         h64[6] = a.geo.layer_stride;
         h64[7] = a.geo.sec_v;
         h64[8] = a.geo.sec_sigma;
-        h64[9] = a.geo.total;
+        h64[9] = a.kmode == KVP_K_Q8_0 ? a.geo.total_q8 : a.geo.total;
     }
 }
 
@@ -564,6 +572,128 @@ __global__ void __launch_bounds__(ENC_THREADS, 3) encode_pool(const __grid_const
     if (s_flag) write_header(a);
 }
 
+// ---------------------------------------------------------------------------
+// q8_0 keys (KVP_K_Q8_0): every 32 consecutive keys of a vector share an fp16
+// scale s_b = fp16(max|k| / 127); codes as above against s_b, clamped to
+// [-127, 127].  No layer-wide maximum, so one sweep encodes keys and values:
+// warp tasks are, per layer, Q8_TASK_CHUNKS 16-byte key chunks (4 lanes per
+// 32-key block: two shuffles give the block's maximum) and single value
+// steps.  The fp16 scale is the fp32 quotient rounded to fp16: the real
+// quotient max|k|/127 never lies within fp32 rounding of an fp16 midpoint
+// (a bf16 over 127 is at least 2^-20 relative from any 12-bit fraction), so
+// the two roundings give the correctly rounded fp16.
+// ---------------------------------------------------------------------------
+constexpr int Q8_ITERS = 4;
+constexpr uint64_t Q8_TASK_CHUNKS = 32ull * Q8_ITERS;
+
+__device__ __forceinline__ uint2 k_quant8_block(uint4 w, float s, float rcp) {
+    const float k[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
+                        bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
+    uint32_t t[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float q0 = fmaf(k[i], rcp, RNE_MAGIC) - RNE_MAGIC;
+        const float e = fmaf(k[i], rcp, -q0);
+        int q = fabsf(e) > 0.4999f ? k_code_exact_int(k[i], s, q0) : int(q0);
+        q = max(-127, min(127, q));
+        if (!(fabsf(k[i]) <= 3.0e38f)) q = 0;  // Inf / NaN: code 0 (reported)
+        t[i] = uint32_t(q) & 0xFFu;
+    }
+    uint2 r;
+    r.x = __byte_perm(__byte_perm(t[0], t[1], 0x0040), __byte_perm(t[2], t[3], 0x0040), 0x5410);
+    r.y = __byte_perm(__byte_perm(t[4], t[5], 0x0040), __byte_perm(t[6], t[7], 0x0040), 0x5410);
+    return r;
+}
+
+// One warp's key task: chunks c0 .. c0 + Q8_TASK_CHUNKS - 1 of layer l.
+__device__ uint32_t q8_key_task(const EncodeArgs &a, int l, uint64_t c0, uint64_t pol) {
+    const int lane = threadIdx.x & 31;
+    const uint4 *src = a.k[l];
+    uint2 *dst = reinterpret_cast<uint2 *>(a.pool + a.geo.off_layers + uint64_t(l) * a.geo.layer_stride);
+    uint16_t *ksc = reinterpret_cast<uint16_t *>(a.pool + a.geo.off_kscales) + uint64_t(l) * (a.chunks / 4);
+    uint4 w[Q8_ITERS];
+#pragma unroll
+    for (int it = 0; it < Q8_ITERS; ++it) {
+        const uint64_t c = c0 + uint64_t(it) * 32u + uint64_t(lane);
+        w[it] = c < a.chunks ? ld_v4_policy(src + c, pol) : make_uint4(0, 0, 0, 0);
+    }
+    uint32_t flags = 0;
+#pragma unroll
+    for (int it = 0; it < Q8_ITERS; ++it) {
+        const uint64_t c = c0 + uint64_t(it) * 32u + uint64_t(lane);
+        const uint32_t ws[4] = {w[it].x, w[it].y, w[it].z, w[it].w};
+        uint32_t m = 0, bad = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t lo = ws[i] & 0x7FFFu, hi = (ws[i] >> 16) & 0x7FFFu;
+            bad |= uint32_t(lo >= 0x7F80u) | uint32_t(hi >= 0x7F80u);
+            m = max(m, lo < 0x7F80u ? lo : 0u);
+            m = max(m, hi < 0x7F80u ? hi : 0u);
+        }
+        m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
+        bad |= __shfl_xor_sync(0xffffffffu, bad, 1);
+        bad |= __shfl_xor_sync(0xffffffffu, bad, 2);
+        const __half sh = __float2half_rn(__fdiv_rn(__uint_as_float(m << 16), 127.0f));
+        const uint16_t sb = __half_as_ushort(sh);
+        const float s = __half2float(sh);
+        if (c < a.chunks) {
+            if (bad)
+                flags |= FLAG_NONFINITE;
+            else if ((sb & 0x7C00u) == 0x7C00u)
+                flags |= FLAG_RANGE;
+            const uint2 codes =
+                (s > 0.0f && s <= 65504.0f) ? k_quant8_block(w[it], s, __frcp_rn(s)) : make_uint2(0, 0);
+            dst[c] = codes;
+            if ((lane & 3) == 0) ksc[c >> 2] = sb;
+        }
+    }
+    return flags;
+}
+
+template <int D>
+__global__ void __launch_bounds__(ENC_THREADS, 3) encode_pool_q8(const __grid_constant__ EncodeArgs a) {
+    __shared__ __align__(16) uint8_t stage[ENC_WARPS][384];
+    __shared__ __align__(16) uint4 vbuf[ENC_WARPS][4][32];
+    __shared__ uint32_t s_last;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint64_t drop = l2_evict_first_policy();
+    uint32_t flags = 0;
+    const uint64_t ktasks = (a.chunks + Q8_TASK_CHUNKS - 1) / Q8_TASK_CHUNKS;
+    const uint64_t per_layer = ktasks + a.steps_per_layer;
+    const uint64_t total = per_layer * uint64_t(a.L);
+    for (uint64_t t = uint64_t(blockIdx.x) * ENC_WARPS + warp; t < total; t += uint64_t(gridDim.x) * ENC_WARPS) {
+        const int l = int(t / per_layer);
+        const uint64_t r = t % per_layer;
+        if (r < ktasks) {
+            flags |= q8_key_task(a, l, r * Q8_TASK_CHUNKS, drop);
+        } else {
+            const uint64_t step = r - ktasks;
+            v_prefetch<D>(a, l, step, vbuf[warp], drop);
+            cp_async_wait<0>();
+            flags |= v_encode_step<D>(a, l, step, stage[warp], vbuf[warp]);
+        }
+    }
+    // deterministic image: layer gaps, the unused per-tensor scales, the
+    // tail of the block-scale region
+    for (int l = blockIdx.x; l < a.L; l += gridDim.x) zero_layer_gaps(a, l);
+    if (blockIdx.x == gridDim.x - 1) {
+        for (uint64_t i = threadIdx.x; i < 4ull * uint64_t(a.L); i += ENC_THREADS) a.pool[a.geo.off_scales + i] = 0;
+        for (uint64_t i = a.geo.off_kscales + 2ull * uint64_t(a.L) * (a.chunks / 4) + threadIdx.x;
+             i < a.geo.total_q8; i += ENC_THREADS)
+            a.pool[i] = 0;
+    }
+    flags = __reduce_or_sync(0xffffffffu, flags);
+    if (lane == 0 && flags) atomicOr(&a.ctl->flags, flags);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        s_last = atomicAdd(&a.ctl->blocks_done, 1u) == gridDim.x - 1u;
+    }
+    __syncthreads();
+    if (s_last) write_header(a);
+}
+
 template <int D>
 static int encode_occupancy() {
     static int occ = 0;
@@ -596,10 +726,34 @@ extern "C" size_t kvpool_workspace_bytes(const kvp_shape *s) {
     return size_t(ws_layout(s->n_layers, chunks).total);
 }
 
+extern "C" size_t kvpool_pool_bytes_ex(const kvp_shape *s, int k_mode) {
+    if (shape_ok(s) != KVP_OK || (k_mode != KVP_K_PER_TENSOR && k_mode != KVP_K_Q8_0)) return 0;
+    const PoolGeom g = pool_geom(s->n_layers, s->n_kv_heads, s->head_dim, s->n_tokens);
+    return size_t(k_mode == KVP_K_Q8_0 ? g.total_q8 : g.total);
+}
+
+template <int D>
+static int encode_q8_occupancy() {
+    static int occ = 0;
+    if (occ == 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, encode_pool_q8<D>, ENC_THREADS, 0) != cudaSuccess ||
+            occ < 1)
+            occ = 1;
+    }
+    return occ;
+}
+
 extern "C" int kvpool_encode(const kvp_shape *s, const void *const *k_layers, const void *const *v_layers,
                              void *pool, size_t pool_bytes, void *ws, size_t ws_bytes, void *stream) {
+    return kvpool_encode_ex(s, KVP_K_PER_TENSOR, k_layers, v_layers, pool, pool_bytes, ws, ws_bytes, stream);
+}
+
+extern "C" int kvpool_encode_ex(const kvp_shape *s, int k_mode, const void *const *k_layers,
+                                const void *const *v_layers, void *pool, size_t pool_bytes, void *ws,
+                                size_t ws_bytes, void *stream) {
     int rc = shape_ok(s);
     if (rc != KVP_OK) return rc;
+    if (k_mode != KVP_K_PER_TENSOR && k_mode != KVP_K_Q8_0) return KVP_ERR_ARG;
     if (!k_layers || !v_layers || !pool || !ws) return KVP_ERR_ARG;
     const int L = s->n_layers;
     for (int l = 0; l < L; ++l) {
@@ -608,7 +762,7 @@ extern "C" int kvpool_encode(const kvp_shape *s, const void *const *k_layers, co
     }
     if (!aligned(pool, 256) || !aligned(ws, 16)) return KVP_ERR_ALIGN;
     const PoolGeom geo = pool_geom(L, s->n_kv_heads, s->head_dim, s->n_tokens);
-    if (pool_bytes < geo.total) return KVP_ERR_SIZE;
+    if (pool_bytes < (k_mode == KVP_K_Q8_0 ? geo.total_q8 : geo.total)) return KVP_ERR_SIZE;
     const uint64_t chunks = uint64_t(s->n_kv_heads) * uint64_t(s->n_tokens) * uint64_t(s->head_dim) / 8;
     const WsLayout wl = ws_layout(L, chunks);
     if (ws_bytes < wl.total) return KVP_ERR_SIZE;
@@ -630,6 +784,7 @@ extern "C" int kvpool_encode(const kvp_shape *s, const void *const *k_layers, co
     a.H = s->n_kv_heads;
     a.T = s->n_tokens;
     a.d = s->head_dim;
+    a.kmode = uint32_t(k_mode);
     a.P = slices_per_layer(chunks);
     a.chunks_per_slice = (chunks + a.P - 1) / a.P;
     a.nvec = uint64_t(a.H) * uint64_t(a.T);
@@ -667,10 +822,23 @@ extern "C" int kvpool_encode(const kvp_shape *s, const void *const *k_layers, co
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(a.ctl, 0, sizeof(EncodeCtl), st) != cudaSuccess) return KVP_ERR_CUDA;
-    if (a.d == 128)
+    if (k_mode == KVP_K_Q8_0) {
+        // one sweep, no waits: a grid of resident blocks, no more than there are warp tasks
+        const uint64_t tasks =
+            ((chunks + Q8_TASK_CHUNKS - 1) / Q8_TASK_CHUNKS + a.steps_per_layer) * uint64_t(L);
+        const uint64_t res_q8 =
+            uint64_t(sm_count()) * uint64_t(a.d == 128 ? encode_q8_occupancy<128>() : encode_q8_occupancy<64>());
+        const uint64_t blocks = (tasks + ENC_WARPS - 1) / ENC_WARPS;
+        const unsigned g8 = unsigned(blocks < res_q8 ? blocks : res_q8);
+        if (a.d == 128)
+            encode_pool_q8<128><<<g8, ENC_THREADS, 0, st>>>(a);
+        else
+            encode_pool_q8<64><<<g8, ENC_THREADS, 0, st>>>(a);
+    } else if (a.d == 128) {
         encode_pool<128><<<grid, ENC_THREADS, 0, st>>>(a);
-    else
+    } else {
         encode_pool<64><<<grid, ENC_THREADS, 0, st>>>(a);
+    }
     count_launch(1);
     return launch_status();
 }

@@ -1,6 +1,7 @@
 """Benchmark of the GB300 KV codec: one step = the whole hot path on one
 batch of synthetic KV cache --
-  1. kvpool_encode      (int8 K per-tensor scale; V FWHT + Lloyd-Max 3 bit)
+  1. kvpool_encode_ex   (int8 K, per-tensor scale or --k-format q8_0 blocks;
+                         V FWHT + Lloyd-Max 3 bit)
   2. kvpool_decode_into (fan-out of every layer into N agent caches)
   3. cachecard_pack     (per-token {2,4,8,16}-bit groups + metadata)
   4. cachecard_unpack   (back to bf16 past_key_values)
@@ -10,6 +11,7 @@ fraction of the GB300 HBM roofline.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                        [--workload NAME] [--agents N] [--tokens T] [--layers L]
+                       [--k-format per_tensor|q8_0] [--mode step|attend|realign]
 Under torchrun (N > 1) every rank runs its own replica (independent pools:
 weak scaling, no collective on the data path); rank 0 prints one JSON line.
 """
@@ -156,6 +158,9 @@ def workload(args):
     return w
 
 
+K_FORMATS = {"per_tensor": 0, "q8_0": 1}  # KVP_K_PER_TENSOR, KVP_K_Q8_0
+
+
 def step_bytes(w, pool_bytes, card_bytes):
     raw = 2 * w["L"] * w["H"] * w["T"] * w["d"] * 2
     return {
@@ -171,14 +176,15 @@ def step_bytes(w, pool_bytes, card_bytes):
 class Codec:
     """Device buffers for one replica of the step and the calls that run it."""
 
-    def __init__(self, w, device, seed=0, outputs=True):
+    def __init__(self, w, device, seed=0, outputs=True, k_mode=0):
         L, H, d, T, N = w["L"], w["H"], w["d"], w["T"], w["N"]
         self.w = w
+        self.k_mode = k_mode
         self.shape = kv.Shape(L, H, d, T)
         self.k, self.v = synth.kv_layers(L, H, T, d, seed=seed, device=device)
         self.bits_host = synth.card_bits(T, seed=seed).numpy()
         self.bits = torch.from_numpy(self.bits_host).to(device)
-        self.pool_bytes = kv.kvpool_pool_bytes(self.shape)
+        self.pool_bytes = kv.kvpool_pool_bytes_ex(self.shape, k_mode)
         self.ws_bytes = kv.kvpool_workspace_bytes(self.shape)
         self.card_bytes = kv.cachecard_bytes(self.shape, self.bits_host)
         self.pool = torch.empty(self.pool_bytes, dtype=torch.uint8, device=device)
@@ -193,8 +199,8 @@ class Codec:
         self.hdr = None
 
     def encode(self, st):
-        kv.check(kv.kvpool_encode(self.shape, self.k, self.v, self.pool, self.pool_bytes, self.ws,
-                                  self.ws_bytes, st), "encode")
+        kv.check(kv.kvpool_encode_ex(self.shape, self.k_mode, self.k, self.v, self.pool, self.pool_bytes,
+                                     self.ws, self.ws_bytes, st), "encode")
 
     def decode(self, st):
         kv.check(kv.kvpool_decode_into(self.pool, self.shape, 0, self.w["L"], self.w["N"], self.caches_k,
@@ -233,7 +239,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(device)
     kv.load()
     w = workload(args)
-    c = Codec(w, device, seed=rank)
+    c = Codec(w, device, seed=rank, k_mode=K_FORMATS[args.k_format])
     st = torch.cuda.current_stream(device)
     sb = step_bytes(w, c.pool_bytes, c.card_bytes)
     flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=device) if sb["raw"] < 4 * L2_BYTES else None
@@ -281,7 +287,7 @@ def run_ours(args, rank, world, local_rank):
     peak, peak_kind = hbm_peak()
     dec_ms = float(phase[:, 1].mean())
     achieved = sb["decode_alg"] / (dec_ms * 1e-3) / 1e9
-    traffic = recorded_traffic(args.workload, w["N"], w["T"], w["L"])
+    traffic = recorded_traffic(args.workload, w["N"], w["T"], w["L"]) if args.k_format == "per_tensor" else None
     names = ("encode", "decode", "pack", "unpack")
     algs = (sb["encode_alg"], sb["decode_alg"], sb["pack_alg"], sb["unpack_alg"])
     breakdown = {}
@@ -290,14 +296,15 @@ def run_ours(args, rank, world, local_rank):
         breakdown[n] = {"ms": round(ms, 4), "alg_bytes": int(b), "alg_GBps": round(b / (ms * 1e-3) / 1e9, 1),
                         "frac_of_measured_peak": round(b / (ms * 1e-3) / 1e9 / peak, 4),
                         "frac_of_8TBps": round(b / (ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 4)}
-    breakdown["encode"]["implemented_bytes"] = int(sb["encode_alg"] + sb["raw"] // 2)  # K is read twice
+    if args.k_format == "per_tensor":
+        breakdown["encode"]["implemented_bytes"] = int(sb["encode_alg"] + sb["raw"] // 2)  # K is read twice
 
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "io_dtype": "bf16", "data": "synthetic",
         "config": {"workload": args.workload, "layers": w["L"], "kv_heads": w["H"], "head_dim": w["d"],
-                   "tokens": w["T"], "agents": w["N"],
+                   "tokens": w["T"], "agents": w["N"], "k_format": args.k_format,
                    "card_bits": "iid {2,4,8,16} p={.25,.40,.25,.10}",
                    "l2": ("flushed between steps (2x L2 write)" if flush is not None
                           else "inputs larger than L2 (%d MB K/V per step)" % (sb["raw"] // 10 ** 6)),
@@ -353,7 +360,8 @@ def run_e2e(c, st, device, args, sb):
         st.wait_event(ev_in[b])
         st.wait_event(ev_out[b])                  # buffer b's previous results have been read
         kl, vl = list(dK[b].unbind(0)), list(dV[b].unbind(0))
-        kv.check(kv.kvpool_encode(c.shape, kl, vl, pools[b], c.pool_bytes, c.ws, c.ws_bytes, st), "encode")
+        kv.check(kv.kvpool_encode_ex(c.shape, c.k_mode, kl, vl, pools[b], c.pool_bytes, c.ws, c.ws_bytes, st),
+                 "encode")
         kv.check(kv.kvpool_decode_into(pools[b], c.shape, 0, L, c.w["N"], c.caches_k, c.caches_v, st), "decode")
         kv.check(kv.cachecard_pack(c.shape, 0x8B, 0, dbits[b], kl, vl, cards[b], c.card_bytes, st), "pack")
         kv.check(kv.cachecard_unpack(cards[b], c.hdr, c.out_k, c.out_v, st), "unpack")
@@ -483,7 +491,7 @@ def run_attend(args):
     w = workload(args)
     L, H, d, T, N = w["L"], w["H"], w["d"], w["T"], w["N"]
     nq = 32
-    c = Codec(w, torch.device("cuda", 0), seed=0, outputs=False)
+    c = Codec(w, torch.device("cuda", 0), seed=0, outputs=False, k_mode=K_FORMATS[args.k_format])
     st = torch.cuda.current_stream()
     c.encode(st)
     kv.check(kv.kvpool_status(c.pool, st), "encode")
@@ -536,7 +544,8 @@ def run_attend(args):
         "value": round(ms * 1e3 / L, 2), "unit": "us per layer", "higher_is_better": False,
         "ms_per_step": round(ms, 4), "steps": args.steps, "warmup": args.warmup, "n_gpus": 1,
         "dtype": "bf16 q / int8 k / 3-bit v", "data": "synthetic",
-        "config": {"workload": args.workload, "layers": L, "kv_heads": H, "q_heads": nq, "head_dim": d,
+        "config": {"workload": args.workload, "k_format": args.k_format, "layers": L, "kv_heads": H,
+                   "q_heads": nq, "head_dim": d,
                    "tokens": T, "agents": N},
         "pool_GBps": round(gbs, 1), "frac_of_measured_peak": round(gbs / peak, 4), "peak_kind": kind,
         "tensor_TFLOPs": round(flops / (ms * 1e-3) / 1e12, 2),
@@ -622,6 +631,8 @@ def main():
     ap.add_argument("--layers", type=int, default=0)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--k-format", choices=sorted(K_FORMATS), default="per_tensor",
+                    help="pool key format: one scale per layer tensor (default) or q8_0 blocks")
     ap.add_argument("--mode", choices=["step", "attend", "realign"], default="step",
                     help="step: the whole codec path (default); attend: attention over the pool; "
                          "realign: card unpack with keys moved to new positions")

@@ -68,6 +68,11 @@ extern "C" {
 /* Largest layer count one call accepts. */
 #define KVP_MAX_LAYERS 512
 
+/* Key formats of a pool (the pool header records which one it holds). */
+#define KVP_K_PER_TENSOR 0  /* one fp32 scale per layer's key tensor ("PolyKV" 2.B.1 text) */
+#define KVP_K_Q8_0 1        /* q8_0 blocks: 32 keys along d share an fp16 scale (the label
+                               "q8_0" that "PolyKV" 2.B.1 gives the same step)            */
+
 /* Shape of one KV cache: n_layers tensors of [n_kv_heads][n_tokens][head_dim]. */
 typedef struct kvp_shape {
     int32_t n_layers;
@@ -134,11 +139,34 @@ int kvpool_encode(const kvp_shape *shape, const void *const *k_layers,
                   const void *const *v_layers, void *pool, size_t pool_bytes,
                   void *ws, size_t ws_bytes, void *stream);
 
+/* Pool bytes for key format k_mode (KVP_K_PER_TENSOR: as kvpool_pool_bytes;
+ * KVP_K_Q8_0: that plus the block scales, 2 * n_layers * H * T * d/32 bytes
+ * rounded up to 256).  0 for an invalid shape or format. */
+size_t kvpool_pool_bytes_ex(const kvp_shape *shape, int k_mode);
+
+/* kvpool_encode with the key format chosen by k_mode.  KVP_K_PER_TENSOR is
+ * kvpool_encode.  KVP_K_Q8_0 ("PolyKV" 2.B.1 labels the key step "q8_0"):
+ * every 32 consecutive keys of a vector share the scale
+ * s_b = fp16(max|k| / 127) (round to nearest even); code = the integer
+ * nearest to the exact k / s_b (ties to even) clamped to [-127, 127] (the
+ * clamp only acts when s_b is an fp16 subnormal); s_b = 0 gives codes 0.  No
+ * layer-wide maximum is needed, so keys and values are encoded in one pass.
+ * Values as kvpool_encode.  pool_bytes >= kvpool_pool_bytes_ex(shape,
+ * k_mode); ws as kvpool_encode.  A block whose scale overflows fp16 is
+ * reported as KVP_ERR_RANGE by kvpool_status, non-finite keys as
+ * KVP_ERR_NONFINITE (they code as 0).  Returns KVP_ERR_ARG for an unknown
+ * k_mode. */
+int kvpool_encode_ex(const kvp_shape *shape, int k_mode, const void *const *k_layers,
+                     const void *const *v_layers, void *pool, size_t pool_bytes,
+                     void *ws, size_t ws_bytes, void *stream);
+
 /* Fan-out decode ("PolyKV" 2.A PooledAgent, 2.B.2 dequantization): read
  * layers [layer_begin, layer_end) of the pool once and write the decoded
  * bf16 K and V into each of n_agents caches.
- *  K: bf16(q * s_l).  V: bf16(sigma_h * (H_d c) / sqrt(d)) with c the
- *    centroids of the codes (the orthonormal transform is its own inverse).
+ *  K: bf16(q * s_l), or bf16(q * s_b) with the key's block scale in a
+ *    q8_0 pool (the format is read from the pool header on the device).
+ *    V: bf16(sigma_h * (H_d c) / sqrt(d)) with c the centroids of the codes
+ *    (the orthonormal transform is its own inverse).
  *  shape must equal the shape the pool was encoded with.
  *  k_dst, v_dst: host arrays of n_agents * n_layers device pointers,
  *    agent-major (entry a * n_layers + l is agent a's layer l, a bf16
@@ -199,14 +227,18 @@ size_t kvpool_attend_workspace_bytes(const kvp_shape *shape, int n_agents, int n
  *    j reads KV head j / (n_q_heads / n_kv_heads) (n_q_heads a multiple of
  *    n_kv_heads: grouped-query attention).
  *  For each (agent, head): s_t = scale * (q . k_t) over the T pooled tokens
- *    with k_t = code_t * s_layer; out = sum_t softmax(s)_t v_t with v_t the
+ *    with k_t = code_t * s_layer (q8_0 pools: code * s_b per 32-key block;
+ *    the format is read from the pool header); out = sum_t softmax(s)_t v_t with v_t the
  *    decoded value (sigma_t * H_d c_t / sqrt(d), accumulated in the rotated
  *    domain and transformed once); lse = log sum_t exp(s_t) (natural log), so a
  *    caller can merge with attention over its own further tokens.
  *  out: device fp32 [n_agents][n_q_heads][head_dim] (16-byte aligned); lse:
  *    device fp32 [n_agents][n_q_heads].  ws: kvpool_attend_workspace_bytes.
- *  Precision: scores are exact products accumulated in fp32; probabilities
- *  times sigma enter the value product as fp16. */
+ *  Precision: scores are exact products accumulated in fp32 (q8_0: exact
+ *  per-block partial sums, each scaled by its block scale in fp32);
+ *  probabilities times sigma enter the value product as fp16, centroids as
+ *  fp16.  A pool whose header does not match `shape` is not read and
+ *  kvpool_status reports KVP_ERR_HEADER. */
 int kvpool_attend(const void *pool, const kvp_shape *shape, int layer, int n_agents, int n_q_heads,
                   const void *q, float scale, float *out, float *lse, void *ws, size_t ws_bytes,
                   void *stream);

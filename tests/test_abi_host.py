@@ -38,6 +38,9 @@ SHAPES = [(1, 8, 128, 512), (24, 32, 64, 1851), (32, 8, 128, 4096), (32, 8, 128,
 def test_pool_bytes_match_oracle_format(shape):
     L, H, d, T = shape
     assert kv.kvpool_pool_bytes((L, H, d, T)) == O.pool_bytes(L, H, d, T)
+    assert kv.kvpool_pool_bytes_ex((L, H, d, T), kv.KVP_K_PER_TENSOR) == O.pool_bytes(L, H, d, T)
+    assert kv.kvpool_pool_bytes_ex((L, H, d, T), kv.KVP_K_Q8_0) == O.pool_bytes_mode(L, H, d, T, 1)
+    assert kv.kvpool_pool_bytes_ex((L, H, d, T), 2) == 0
     assert kv.kvpool_workspace_bytes((L, H, d, T)) > 0
 
 
@@ -99,6 +102,21 @@ def test_decode_argument_errors():
     # layers outside the range are not read: a NULL there is fine up to validation
     # (range [1,2) with an unaligned pool still fails on the pool, before launch)
     assert kv.kvpool_decode_into(ok + 64, s, 1, 2, 2, [None, ok, None] * 2, [None, ok, None] * 2) == kv.KVP_ERR_ALIGN
+
+
+def test_encode_ex_argument_errors():
+    """Host-side checks of the key-format encode, all before any launch."""
+    s = (2, 4, 128, 64)
+    ok = 0x10000
+    pb, wb = kv.kvpool_pool_bytes_ex(s, kv.KVP_K_Q8_0), kv.kvpool_workspace_bytes(s)
+    assert pb > kv.kvpool_pool_bytes(s)
+    assert kv.kvpool_encode_ex(s, 7, [ok] * 2, [ok] * 2, ok, pb, ok, wb) == kv.KVP_ERR_ARG
+    assert kv.kvpool_encode_ex(s, -1, [ok] * 2, [ok] * 2, ok, pb, ok, wb) == kv.KVP_ERR_ARG
+    # a per-tensor-sized buffer is too small for q8_0 keys
+    assert kv.kvpool_encode_ex(s, kv.KVP_K_Q8_0, [ok] * 2, [ok] * 2, ok, kv.kvpool_pool_bytes(s), ok,
+                               wb) == kv.KVP_ERR_SIZE
+    assert kv.kvpool_encode_ex(s, kv.KVP_K_Q8_0, [ok] * 2, [ok] * 2, ok + 16, pb, ok, wb) == kv.KVP_ERR_ALIGN
+    assert kv.kvpool_encode_ex(s, kv.KVP_K_Q8_0, [ok, None], [ok] * 2, ok, pb, ok, wb) == kv.KVP_ERR_ARG
 
 
 def test_card_argument_errors():
