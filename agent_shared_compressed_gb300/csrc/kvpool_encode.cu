@@ -577,27 +577,40 @@ __global__ void __launch_bounds__(ENC_THREADS, 3) encode_pool(const __grid_const
 // scale s_b = fp16(max|k| / 127); codes as above against s_b, clamped to
 // [-127, 127].  No layer-wide maximum, so one sweep encodes keys and values:
 // warp tasks are, per layer, Q8_TASK_CHUNKS 16-byte key chunks (4 lanes per
-// 32-key block: two shuffles give the block's maximum) and single value
-// steps.  The fp16 scale is the fp32 quotient rounded to fp16: the real
-// quotient max|k|/127 never lies within fp32 rounding of an fp16 midpoint
-// (a bf16 over 127 is at least 2^-20 relative from any 12-bit fraction), so
-// the two roundings give the correctly rounded fp16.
+// 32-key block: two shuffles give the block's maximum) and batches of
+// Q8_VSTEPS value steps.  The fp16 scale is the fp32 quotient rounded to
+// fp16: the real quotient max|k|/127 never lies within fp32 rounding of an
+// fp16 midpoint (a bf16 over 127 is at least 2^-20 relative from any 12-bit
+// fraction), so the two roundings give the correctly rounded fp16.
 // ---------------------------------------------------------------------------
 constexpr int Q8_ITERS = 4;
 constexpr uint64_t Q8_TASK_CHUNKS = 32ull * Q8_ITERS;
+constexpr int Q8_VSTEPS = 8;  // value steps per warp task, each prefetched while the previous is encoded
 
-__device__ __forceinline__ uint2 k_quant8_block(uint4 w, float s, float rcp) {
+// Fast path as k_quant8: the code is the low byte of fma(k, 1/s, 1.5*2^23).
+// The chunk is redone exactly when an estimate is within 1e-4 of a
+// half-integer or not finite, and when s is an fp16 subnormal (then |k/s|
+// may exceed 127.5 and the code is clamped); non-finite keys code as 0.
+__device__ __forceinline__ uint2 k_quant8_block(uint4 w, float s, float rcp, bool subnormal_scale) {
     const float k[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
                         bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
     uint32_t t[8];
+    bool slow = subnormal_scale;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        const float q0 = fmaf(k[i], rcp, RNE_MAGIC) - RNE_MAGIC;
-        const float e = fmaf(k[i], rcp, -q0);
-        int q = fabsf(e) > 0.4999f ? k_code_exact_int(k[i], s, q0) : int(q0);
-        q = max(-127, min(127, q));
-        if (!(fabsf(k[i]) <= 3.0e38f)) q = 0;  // Inf / NaN: code 0 (reported)
-        t[i] = uint32_t(q) & 0xFFu;
+        const float tf = fmaf(k[i], rcp, RNE_MAGIC);
+        const float e = fmaf(k[i], rcp, -(tf - RNE_MAGIC));
+        slow |= !(fabsf(e) <= 0.4999f);
+        t[i] = __float_as_uint(tf);
+    }
+    if (slow) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            int q = k_code_exact_int(k[i], s, __uint_as_float(t[i]) - RNE_MAGIC);
+            q = max(-127, min(127, q));
+            if (!(fabsf(k[i]) <= 3.0e38f)) q = 0;  // Inf / NaN: code 0 (reported)
+            t[i] = uint32_t(q) & 0xFFu;
+        }
     }
     uint2 r;
     r.x = __byte_perm(__byte_perm(t[0], t[1], 0x0040), __byte_perm(t[2], t[3], 0x0040), 0x5410);
@@ -642,8 +655,9 @@ __device__ uint32_t q8_key_task(const EncodeArgs &a, int l, uint64_t c0, uint64_
                 flags |= FLAG_NONFINITE;
             else if ((sb & 0x7C00u) == 0x7C00u)
                 flags |= FLAG_RANGE;
-            const uint2 codes =
-                (s > 0.0f && s <= 65504.0f) ? k_quant8_block(w[it], s, __frcp_rn(s)) : make_uint2(0, 0);
+            const uint2 codes = (s > 0.0f && s <= 65504.0f)
+                                    ? k_quant8_block(w[it], s, __frcp_rn(s), s < 0x1p-14f)
+                                    : make_uint2(0, 0);
             dst[c] = codes;
             if ((lane & 3) == 0) ksc[c >> 2] = sb;
         }
@@ -654,13 +668,14 @@ __device__ uint32_t q8_key_task(const EncodeArgs &a, int l, uint64_t c0, uint64_
 template <int D>
 __global__ void __launch_bounds__(ENC_THREADS, 3) encode_pool_q8(const __grid_constant__ EncodeArgs a) {
     __shared__ __align__(16) uint8_t stage[ENC_WARPS][384];
-    __shared__ __align__(16) uint4 vbuf[ENC_WARPS][4][32];
+    __shared__ __align__(16) uint4 vbuf[ENC_WARPS][2][4][32];  // per warp: two steps of value data
     __shared__ uint32_t s_last;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint64_t drop = l2_evict_first_policy();
     uint32_t flags = 0;
     const uint64_t ktasks = (a.chunks + Q8_TASK_CHUNKS - 1) / Q8_TASK_CHUNKS;
-    const uint64_t per_layer = ktasks + a.steps_per_layer;
+    const uint64_t vtasks = (a.steps_per_layer + Q8_VSTEPS - 1) / Q8_VSTEPS;
+    const uint64_t per_layer = ktasks + vtasks;
     const uint64_t total = per_layer * uint64_t(a.L);
     for (uint64_t t = uint64_t(blockIdx.x) * ENC_WARPS + warp; t < total; t += uint64_t(gridDim.x) * ENC_WARPS) {
         const int l = int(t / per_layer);
@@ -668,10 +683,20 @@ __global__ void __launch_bounds__(ENC_THREADS, 3) encode_pool_q8(const __grid_co
         if (r < ktasks) {
             flags |= q8_key_task(a, l, r * Q8_TASK_CHUNKS, drop);
         } else {
-            const uint64_t step = r - ktasks;
-            v_prefetch<D>(a, l, step, vbuf[warp], drop);
+            const uint64_t s0 = (r - ktasks) * Q8_VSTEPS;
+            v_prefetch<D>(a, l, s0, vbuf[warp][0], drop);
+#pragma unroll 1
+            for (int j = 0; j < Q8_VSTEPS; ++j) {
+                const uint64_t step = s0 + uint64_t(j);
+                if (j + 1 < Q8_VSTEPS)
+                    v_prefetch<D>(a, l, step + 1, vbuf[warp][(j + 1) & 1], drop);
+                else
+                    cp_async_commit();  // keep one group per iteration
+                cp_async_wait<1>();     // this step's group has landed
+                if (step < a.steps_per_layer)
+                    flags |= v_encode_step<D>(a, l, step, stage[warp], vbuf[warp][j & 1]);
+            }
             cp_async_wait<0>();
-            flags |= v_encode_step<D>(a, l, step, stage[warp], vbuf[warp]);
         }
     }
     // deterministic image: layer gaps, the unused per-tensor scales, the
@@ -824,8 +849,9 @@ extern "C" int kvpool_encode_ex(const kvp_shape *s, int k_mode, const void *cons
     if (cudaMemsetAsync(a.ctl, 0, sizeof(EncodeCtl), st) != cudaSuccess) return KVP_ERR_CUDA;
     if (k_mode == KVP_K_Q8_0) {
         // one sweep, no waits: a grid of resident blocks, no more than there are warp tasks
-        const uint64_t tasks =
-            ((chunks + Q8_TASK_CHUNKS - 1) / Q8_TASK_CHUNKS + a.steps_per_layer) * uint64_t(L);
+        const uint64_t tasks = ((chunks + Q8_TASK_CHUNKS - 1) / Q8_TASK_CHUNKS +
+                                (a.steps_per_layer + Q8_VSTEPS - 1) / Q8_VSTEPS) *
+                               uint64_t(L);
         const uint64_t res_q8 =
             uint64_t(sm_count()) * uint64_t(a.d == 128 ? encode_q8_occupancy<128>() : encode_q8_occupancy<64>());
         const uint64_t blocks = (tasks + ENC_WARPS - 1) / ENC_WARPS;
