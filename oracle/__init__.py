@@ -77,6 +77,8 @@ def lib():
         "orc_card_pack": (C.c_uint32, [C.c_int] * 4 + [C.c_uint64, C.c_int64, _u8p,
                                                       C.POINTER(_u16p), C.POINTER(_u16p), _u8p, _dp]),
         "orc_card_unpack": (C.c_int, [_u8p, C.POINTER(_u16p), C.POINTER(_u16p)]),
+        "orc_pool_attend_lora": (C.c_int, [_u8p, C.c_int, C.c_int, C.c_int, _u16p, C.c_double, C.c_int, _u16p, _u16p,
+                                          _dp, _dp]),
         "orc_card_unpack_at": (C.c_int, [_u8p, C.c_int64, C.POINTER(C.c_float), C.POINTER(_u16p),
                                          C.POINTER(_u16p)]),
         "orc_pool_attend": (C.c_int, [_u8p, C.c_int, C.c_int, C.c_int, _u16p, C.c_double, _dp, _dp]),
@@ -391,4 +393,25 @@ def pool_attend(pool, layer, q_bits, scale):
                                _p(out, _dp), _p(lse, _dp))
     if rc != 0:
         raise ValueError("oracle: bad pool header, layer or head count")
+    return out, lse
+
+
+def pool_attend_lora(pool, layer, q_bits, scale, vlr_bits, lora_b_bits):
+    """Attention of agents' queries over one pool layer with each agent's
+    values v_base + vlr @ B_a.  q_bits: bf16 [n_agents][n_q_heads][d];
+    vlr_bits: bf16 [T][rank]; lora_b_bits: bf16 [n_agents][rank][H*d].
+    Returns (out [n_agents][n_q_heads][d] fp64, lse [n_agents][n_q_heads])."""
+    pool = _c(pool, np.uint8)
+    q = _c(q_bits, np.uint16)
+    vlr = _c(vlr_bits, np.uint16)
+    b = _c(lora_b_bits, np.uint16)
+    na, nq, d = q.shape
+    rank = vlr.shape[1]
+    assert b.shape[0] == na and b.shape[1] == rank
+    out = np.zeros((na, nq, d), np.float64)
+    lse = np.zeros((na, nq), np.float64)
+    rc = lib().orc_pool_attend_lora(_p(pool, _u8p), int(layer), na, nq, _p(q, _u16p), float(scale), int(rank),
+                                    _p(vlr, _u16p), _p(b, _u16p), _p(out, _dp), _p(lse, _dp))
+    if rc != 0:
+        raise ValueError("oracle: bad pool header or head count")
     return out, lse

@@ -1014,3 +1014,97 @@ int orc_pool_attend(const uint8_t *pool, int layer, int n_agents, int n_q_heads,
     free(vf);
     return 0;
 }
+
+/* Attention over the pool with a shared low-rank value cache, "LRAgent"
+ * (2. Sharing Schemes, BaseLRShared; 3. Flash-LoRA-Attention): every agent's
+ * values are the shared base values plus its own LoRA term,
+ *   v_{a,h,t} = vbase_{h,t} + sum_k vlr_{t,k} * B_a[k][h*d + i],
+ * with vbase the pool's decoded values (exact dequantization), vlr the
+ * layer's shared low-rank cache (X A, bf16 [T][rank]) and B_a agent a's
+ * up-projection (bf16 [rank][H*d]).  This is the definition written out:
+ * each agent's values are formed first and attended over as in
+ * orc_pool_attend (the kernel's reordering P vbase + (P vlr) B is what it
+ * is checked against).  Returns 0, or -1 on a bad header or head count. */
+int orc_pool_attend_lora(const uint8_t *pool, int layer, int n_agents, int n_q_heads, const uint16_t *q,
+                         double scale, int rank, const uint16_t *vlr, const uint16_t *lora_b, double *out,
+                         double *lse)
+{
+    if (get32(pool) != 0x4C50564Bu || get32(pool + 4) != 1u) return -1;
+    int H = (int)get32(pool + 12), d = (int)get32(pool + 16), T = (int)get32(pool + 20);
+    if (n_q_heads % H != 0 || rank < 1) return -1;
+    const int grp = n_q_heads / H;
+    /* keys and base values, dequantized exactly as in orc_pool_attend */
+    int L = (int)get32(pool + 8);
+    if (layer < 0 || layer >= L) return -1;
+    const int k_mode = (int)get32(pool + 28);
+    if (k_mode != 0 && k_mode != 1) return -1;
+    orc_pool_geom g = pool_geom(L, H, d, T);
+    const uint8_t *lay = pool + g.off_layers + (uint64_t)layer * g.layer_stride;
+    const uint8_t *ks = pool + g.off_kscales + (uint64_t)layer * (uint64_t)H * T * (uint64_t)(d / 32) * 2u;
+    float s;
+    memcpy(&s, pool + g.off_scales + 4u * (uint64_t)layer, 4);
+    const int8_t *kc = (const int8_t *)lay;
+    const uint8_t *vc = lay + g.sec_v;
+    const uint8_t *sg = lay + g.sec_sigma;
+    double *kf = (double *)malloc(sizeof(double) * (size_t)H * T * d);
+    double *vb = (double *)malloc(sizeof(double) * (size_t)H * T * d);
+    for (int64_t n = 0; n < (int64_t)H * T; n++) {
+        uint8_t codes[128];
+        uint16_t sh;
+        double z[128];
+        for (int i = 0; i < d; i++) {
+            double sk = (double)s;
+            if (k_mode == 1) {
+                uint16_t sb;
+                memcpy(&sb, ks + 2u * ((uint64_t)n * (uint64_t)(d / 32) + (uint64_t)(i / 32)), 2);
+                sk = orc_f16_to_f64(sb);
+            }
+            kf[n * d + i] = (double)kc[n * d + i] * sk;
+        }
+        orc_unpack3(vc + (uint64_t)n * (uint64_t)(3 * d / 8), d, codes);
+        memcpy(&sh, sg + 2u * (uint64_t)n, 2);
+        for (int i = 0; i < d; i++) z[i] = CENTROID[codes[i]];
+        orc_fwht(z, d);
+        double sig = orc_f16_to_f64(sh);
+        for (int i = 0; i < d; i++) vb[n * d + i] = sig * z[i] / sqrt((double)d);
+    }
+#pragma omp parallel for schedule(static)
+    for (int aj = 0; aj < n_agents * n_q_heads; aj++) {
+        const int a = aj / n_q_heads, j = aj % n_q_heads;
+        const int h = j / grp;
+        const uint16_t *qv = q + (uint64_t)aj * d;
+        const uint16_t *ba = lora_b + (uint64_t)a * (uint64_t)rank * (uint64_t)H * d;
+        double *sc = (double *)malloc(sizeof(double) * (size_t)T);
+        double *vt = (double *)malloc(sizeof(double) * (size_t)d);
+        double mx = -INFINITY;
+        for (int t = 0; t < T; t++) {
+            const double *kt = kf + ((uint64_t)h * T + t) * d;
+            double dot = 0.0;
+            for (int i = 0; i < d; i++) dot += orc_bf16_to_f64(qv[i]) * kt[i];
+            sc[t] = scale * dot;
+            if (sc[t] > mx) mx = sc[t];
+        }
+        double sum = 0.0;
+        for (int t = 0; t < T; t++) { sc[t] = exp(sc[t] - mx); sum += sc[t]; }
+        double *o = out + (uint64_t)aj * d;
+        for (int i = 0; i < d; i++) o[i] = 0.0;
+        for (int t = 0; t < T; t++) {
+            /* agent a's value of token t at head h */
+            for (int i = 0; i < d; i++) {
+                double v = vb[((uint64_t)h * T + t) * d + i];
+                for (int k = 0; k < rank; k++)
+                    v += orc_bf16_to_f64(vlr[(uint64_t)t * rank + k]) *
+                         orc_bf16_to_f64(ba[(uint64_t)k * H * d + (uint64_t)h * d + i]);
+                vt[i] = v;
+            }
+            const double p = sc[t] / sum;
+            for (int i = 0; i < d; i++) o[i] += p * vt[i];
+        }
+        lse[aj] = mx + log(sum);
+        free(sc);
+        free(vt);
+    }
+    free(kf);
+    free(vb);
+    return 0;
+}

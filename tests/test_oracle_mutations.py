@@ -53,6 +53,14 @@ MUTANTS = [
     ("q8 scales per layer offset", "uint8_t *ks = pool + g.off_kscales + (uint64_t)l * nb * 2u;",
      "uint8_t *ks = pool + g.off_kscales + (uint64_t)l * nb;"),
     ("q8 attend uses tensor scale", "sk = orc_f16_to_f64(sb);", "sk = (double)s;"),
+    ("lora head slice by query head", "orc_bf16_to_f64(ba[(uint64_t)k * H * d + (uint64_t)h * d + i]);",
+     "orc_bf16_to_f64(ba[(uint64_t)k * H * d + (uint64_t)(j % H) * d + i]);"),
+    ("lora up-projection transposed", "orc_bf16_to_f64(ba[(uint64_t)k * H * d + (uint64_t)h * d + i]);",
+     "orc_bf16_to_f64(ba[((uint64_t)h * d + i) * (uint64_t)rank + k]);"),
+    ("lora first agent's B for all", "const uint16_t *ba = lora_b + (uint64_t)a * (uint64_t)rank * (uint64_t)H * d;",
+     "const uint16_t *ba = lora_b;"),
+    ("lora low-rank cache transposed", "v += orc_bf16_to_f64(vlr[(uint64_t)t * rank + k]) *",
+     "v += orc_bf16_to_f64(vlr[(uint64_t)k * T + t]) *"),
     ("q8 decode reads next block", "kk[i] = orc_k_block_decode(q, sb);",
      "memcpy(&sb, ks + 2u * ((uint64_t)n * (uint64_t)(d / 32) + (uint64_t)((i / 32 + 1) % (d / 32))), 2);\n                    kk[i] = orc_k_block_decode(q, sb);"),
 ]

@@ -897,3 +897,75 @@ def test_pool_attend_q8_against_library_softmax():
             s = 0.1 * (kf[h] @ _f(q)[a, j])
             np.testing.assert_allclose(out[a, j], scipy.special.softmax(s) @ vf[h], rtol=1e-10, atol=1e-12)
             assert abs(lse[a, j] - scipy.special.logsumexp(s)) < 1e-10
+
+
+# --------------------------------------------------------------------------
+# attention with a shared low-rank value cache (next row: Flash-LoRA reorder)
+# --------------------------------------------------------------------------
+
+def _lora_inputs(T, d, H, na, rank, seed):
+    rng = np.random.default_rng(seed)
+    vlr = _bf16(rng.normal(size=(T, rank)))
+    b = _bf16(rng.normal(size=(na, rank, H * d)) * 0.05)
+    return vlr, b
+
+
+def test_pool_attend_lora_zero_b_is_plain_attention():
+    L, H, T, d = 1, 2, 37, 64
+    ks, vs = _tiny_kv(L, H, T, d, 41)
+    pool, _, _ = O.pool_encode(ks, vs)
+    q = _bf16(np.random.default_rng(42).normal(size=(3, 8, d)))
+    vlr, _ = _lora_inputs(T, d, H, 3, 16, 43)
+    out0, lse0 = O.pool_attend(pool, 0, q, 0.125)
+    out1, lse1 = O.pool_attend_lora(pool, 0, q, 0.125, vlr, np.zeros((3, 16, H * d), np.uint16))
+    np.testing.assert_array_equal(out1, out0)
+    np.testing.assert_array_equal(lse1, lse0)
+
+
+@pytest.mark.parametrize("k_mode", [0, 1])
+def test_pool_attend_lora_against_reordered_library_form(k_mode):
+    """The oracle forms every agent's values first; numpy's softmax with the
+    reordered product P V_base + (P V_lr) B_a must agree."""
+    import scipy.special
+    L, H, T, d, na, nq, rank = 1, 2, 45, 128, 3, 8, 32
+    ks, vs = _tiny_kv(L, H, T, d, 44)
+    pool, _, _ = O.pool_encode(ks, vs, k_mode=k_mode)
+    vlr, b = _lora_inputs(T, d, H, na, rank, 45)
+    q = _bf16(np.random.default_rng(46).normal(size=(na, nq, d)))
+    out, lse = O.pool_attend_lora(pool, 0, q, 0.09, vlr, b)
+    kf, _ = _decoded_fp64(pool, L, H, d, T, 0) if k_mode == 0 else (None, None)
+    if k_mode == 1:
+        g = O.pool_geometry(L, H, d, T)
+        off_ks, _ = O.pool_geometry_q8(L, H, d, T)
+        kc = pool[g["off_layers"]: g["off_layers"] + H * T * d].view(np.int8).astype(np.float64)
+        sc = np.array([O.f16_to_f64(int(s)) for s in pool[off_ks: off_ks + H * T * d // 32 * 2].view(np.uint16)])
+        kf = (kc.reshape(-1, 32) * sc[:, None]).reshape(H, T, d)
+    _, vf = _decoded_fp64(pool, L, H, d, T, 0)
+    vl, bf = _f(vlr), _f(b)
+    for a in range(na):
+        for j in range(nq):
+            h = j // (nq // H)
+            p = scipy.special.softmax(0.09 * (kf[h] @ _f(q)[a, j]))
+            want = p @ vf[h] + (p @ vl) @ bf[a][:, h * d:(h + 1) * d]
+            np.testing.assert_allclose(out[a, j], want, rtol=1e-10, atol=1e-12)
+            assert abs(lse[a, j] - scipy.special.logsumexp(0.09 * (kf[h] @ _f(q)[a, j]))) < 1e-10
+
+
+def test_pool_attend_lora_one_hot_low_rank_cache():
+    """Every token's low-rank activation is e_k: the attention-weighted sum is
+    e_k whatever the weights, so the output shifts by row k of the agent's
+    up-projection, restricted to the query's KV head."""
+    L, H, T, d, na, nq, rank = 1, 4, 21, 64, 2, 8, 16
+    ks, vs = _tiny_kv(L, H, T, d, 47)
+    pool, _, _ = O.pool_encode(ks, vs)
+    _, b = _lora_inputs(T, d, H, na, rank, 48)
+    q = _bf16(np.random.default_rng(49).normal(size=(na, nq, d)))
+    out0, _ = O.pool_attend(pool, 0, q, 0.2)
+    for k in (0, 5, rank - 1):
+        vlr = np.zeros((T, rank), np.uint16)
+        vlr[:, k] = _bf16(1.0)
+        out, _ = O.pool_attend_lora(pool, 0, q, 0.2, vlr, b)
+        for a in range(na):
+            for j in range(nq):
+                h = j // (nq // H)
+                np.testing.assert_allclose(out[a, j] - out0[a, j], _f(b)[a, k, h * d:(h + 1) * d], atol=1e-12)
