@@ -72,6 +72,9 @@ _SIGS = {
     "kvpool_attend_workspace_bytes": (C.c_size_t, [C.POINTER(Shape), C.c_int, C.c_int]),
     "kvpool_attend": (C.c_int, [_vp, C.POINTER(Shape), C.c_int, C.c_int, C.c_int, _vp, C.c_float, _vp, _vp, _vp,
                                 C.c_size_t, _vp]),
+    "kvpool_attend_lora_workspace_bytes": (C.c_size_t, [C.POINTER(Shape), C.c_int, C.c_int, C.c_int]),
+    "kvpool_attend_lora": (C.c_int, [_vp, C.POINTER(Shape), C.c_int, C.c_int, C.c_int, _vp, C.c_float, C.c_int, _vp,
+                                     _vp, _vp, _vp, _vp, C.c_size_t, _vp]),
     "kvpool_encode_noalloc": (C.c_int, [C.POINTER(Shape), C.POINTER(_vp), C.POINTER(_vp), _vp, C.c_size_t, _vp]),
     "cachecard_bytes": (C.c_size_t, [C.POINTER(Shape), C.POINTER(C.c_uint8)]),
     "cachecard_pack": (C.c_int, [C.POINTER(Shape), C.c_uint64, C.c_int64, _vp, C.POINTER(_vp),
@@ -195,6 +198,19 @@ def kvpool_attend(pool, shape, layer, n_agents, n_q_heads, q, scale, out, lse, w
     return load().kvpool_attend(_addr(pool), C.byref(_shape(shape)), int(layer), int(n_agents), int(n_q_heads),
                                 _addr(q), C.c_float(scale), _addr(out), _addr(lse), _addr(ws), int(ws_bytes),
                                 _stream(stream))
+
+
+def kvpool_attend_lora_workspace_bytes(shape, n_agents, n_q_heads, rank):
+    return int(load().kvpool_attend_lora_workspace_bytes(C.byref(_shape(shape)), int(n_agents), int(n_q_heads),
+                                                         int(rank)))
+
+
+def kvpool_attend_lora(pool, shape, layer, n_agents, n_q_heads, q, scale, rank, v_lr, lora_b, out, lse, ws,
+                       ws_bytes, stream=None):
+    return load().kvpool_attend_lora(_addr(pool), C.byref(_shape(shape)), int(layer), int(n_agents),
+                                     int(n_q_heads), _addr(q), C.c_float(scale), int(rank), _addr(v_lr),
+                                     _addr(lora_b), _addr(out), _addr(lse), _addr(ws), int(ws_bytes),
+                                     _stream(stream))
 
 
 def kvpool_status(pool, stream=None):

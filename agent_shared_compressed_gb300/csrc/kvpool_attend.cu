@@ -37,11 +37,13 @@ struct AttendArgs {
     const uint16_t *q;  // bf16 [NA][NQ][d]
     float *out;         // [NA][NQ][d]
     float *lse;         // [NA][NQ]
-    float *part;        // [H][nsplit][QHP][d] rotated-domain partial sums
+    float *part;        // [H][nsplit][QHP][d + R] rotated-domain partial sums (+ P V_lr columns)
     float2 *stats;      // [H][nsplit][QHP]: (running max, running sum), base 2
     PoolGeom geo;
     float scale;
     int L, H, T, layer, NA, NQ, G, QH, QHP, nsub, per_split, nsplit;
+    const uint16_t *vlr;     // LoRA attention: bf16 [T][R] shared low-rank value cache
+    const uint16_t *lora_b;  // LoRA attention: bf16 [NA][R][H*d] per-agent up-projections
 };
 
 __device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -75,15 +77,17 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
-template <int D>
+template <int D, int R = 0>
 struct AttendSmem {
     static constexpr int RW = D / 2 + 4;  // 32-bit words per Q / K / C row (16-B multiple, conflict-free ldmatrix)
-    static constexpr int MS = D + 8;      // floats per row of a warp's merge slot (conflict-free float2 stores)
+    static constexpr int LW = R / 2 + 4;  // words per low-rank row (LoRA attention)
+    static constexpr int MS = D + R + 8;  // floats per row of a warp's merge slot (conflict-free float2 stores)
     static constexpr size_t q_words = size_t(ATT_MT) * RW;
     static constexpr size_t tile_words = size_t(ATT_TC) * RW;  // one K or C buffer
     static constexpr size_t ksb_words = size_t(ATT_TC) * (D / 32);  // one buffer of q8_0 key block scales
-    static constexpr size_t stage_words =
-        q_words + 4 * tile_words + 2 * ATT_TC + 64 + 2 * ksb_words;  // Q, K[2], C[2], sig[2], lut, ksb[2]
+    static constexpr size_t lr_words = R > 0 ? size_t(ATT_TC) * LW : 0;  // one buffer of the low-rank tile
+    static constexpr size_t stage_words = q_words + 4 * tile_words + 2 * ATT_TC + 64 + 2 * ksb_words +
+                                          2 * lr_words;  // Q, K[2], C[2], sig[2], lut, ksb[2], lr[2]
     static constexpr size_t merge_words = size_t(ATT_WARPS) * (16 * MS + 32);
     static constexpr size_t bytes = 4 * (stage_words > merge_words ? stage_words : merge_words);
 };
@@ -100,11 +104,12 @@ struct RawChunk {
     uint32_t v[3];
     uint32_t sig;  // fp16 bits of token tid's sigma (tid < 64)
     uint32_t ksc;  // q8_0 keys: fp16 bits of block tid % (D/32) of token tid / (D/32)
+    uint4 lr;      // LoRA attention: 8 low-rank values (bf16) of token tid / (R/8), part tid % (R/8)
 };
 
-template <int D, bool Q8>
+template <int D, bool Q8, int R>
 __device__ __forceinline__ void load_chunk(RawChunk<D> &r, const uint8_t *lay, const PoolGeom &geo, uint64_t vbase,
-                                           int t0, int T, int tid, const uint16_t *kscales) {
+                                           int t0, int T, int tid, const uint16_t *kscales, const uint16_t *vlr) {
     constexpr int VPT = D / 32;  // 32-code value items per token
     const int q = tid >> 3, l8 = tid & 7;
     const int tk = t0 + l8 + 8 * (q >> 2);
@@ -131,14 +136,19 @@ __device__ __forceinline__ void load_chunk(RawChunk<D> &r, const uint8_t *lay, c
         r.ksc = 0u;
         if (tid < ATT_TC * (D / 32) && t0 + tid / (D / 32) < T) r.ksc = kscales[(vbase + t0) * (D / 32) + tid];
     }
+    if constexpr (R > 0) {
+        r.lr = make_uint4(0, 0, 0, 0);
+        if (tid < ATT_TC * (R / 8) && t0 + tid / (R / 8) < T)
+            r.lr = ld_stream_v4(vlr + uint64_t(t0) * R + uint64_t(tid) * 8);
+    }
 }
 
 // Registers -> shared tiles: keys int8 -> exact bf16 (|q| <= 127 has at most
 // 7 significant bits); value codes -> fp16 centroids, two dims per word via
 // the pair table.
-template <int D, bool Q8>
+template <int D, bool Q8, int R>
 __device__ __forceinline__ void stage_chunk(const RawChunk<D> &r, uint32_t *Kb, uint32_t *Cs, float *sig,
-                                            const uint32_t *lut, float *ksb, int tid) {
+                                            const uint32_t *lut, float *ksb, uint32_t *Ls, int tid) {
     constexpr int RW = AttendSmem<D>::RW, VPT = D / 32;
     const int q = tid >> 3, l8 = tid & 7;
     {
@@ -176,24 +186,37 @@ __device__ __forceinline__ void stage_chunk(const RawChunk<D> &r, uint32_t *Kb, 
     if (tid < ATT_TC) sig[tid] = __half2float(__ushort_as_half(static_cast<uint16_t>(r.sig)));
     if constexpr (Q8)
         if (tid < ATT_TC * (D / 32)) ksb[tid] = __half2float(__ushort_as_half(static_cast<uint16_t>(r.ksc)));
+    if constexpr (R > 0)
+        if (tid < ATT_TC * (R / 8)) {  // bf16 -> fp16, exact within fp16's normal range
+            const uint32_t w[4] = {r.lr.x, r.lr.y, r.lr.z, r.lr.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) o[i] = pack_half2(bf16_lo(w[i]), bf16_hi(w[i]));
+            *reinterpret_cast<uint4 *>(Ls + (tid / (R / 8)) * AttendSmem<D, R>::LW + (tid % (R / 8)) * 4) =
+                make_uint4(o[0], o[1], o[2], o[3]);
+        }
 }
 
 // TPW: tokens of a sub-chunk per warp (32: four 16-row tiles per pass; 16:
 // two 16-row tiles per pass, for blocks with at most 32 query rows).
-template <int D, int TPW, bool Q8>
+template <int D, int TPW, bool Q8, int R>
 __device__ __forceinline__ void attend_passes(const AttendArgs &a, uint32_t *smem, const uint16_t *kscales) {
-    using SM = AttendSmem<D>;
+    using SM = AttendSmem<D, R>;
     constexpr int RW = SM::RW, MSW = SM::MS;
     constexpr int MS = TPW / 8;       // 16-row tiles per pass
     constexpr int RP = 16 * MS;       // query rows per pass
     constexpr int NS = TPW / 8;       // S n-tiles per warp
     constexpr int NV = D / 8;         // PV n-tiles per warp (all dims)
+    constexpr int NL = R / 8;         // P V_lr n-tiles per warp (LoRA attention)
+    constexpr int LW = SM::LW;
+    constexpr int PW = D + R;         // floats per partial row
     uint32_t *Qs = smem;                       // [ATT_MT][RW] bf16 pairs
     uint32_t *Kb = Qs + SM::q_words;           // [2][ATT_TC][RW] bf16 pairs
     uint32_t *Cs = Kb + 2 * SM::tile_words;    // [2][ATT_TC][RW] fp16 pairs
     float *sig = reinterpret_cast<float *>(Cs + 2 * SM::tile_words);  // [2][ATT_TC]
     uint32_t *lut = reinterpret_cast<uint32_t *>(sig + 2 * ATT_TC);   // [64] (c[lo], c[hi]) fp16 pairs
     float *ksb = reinterpret_cast<float *>(lut + 64);                  // [2][ATT_TC][D/32] q8_0 key block scales
+    uint32_t *Ls = reinterpret_cast<uint32_t *>(ksb + 2 * SM::ksb_words);  // [2][ATT_TC][LW] low-rank fp16 pairs
     float *mrg = reinterpret_cast<float *>(smem);  // after the loop: [warps][16][MSW] acc, then [warps][32] m, l
 
     const int h = blockIdx.x, split = blockIdx.y;
@@ -210,7 +233,7 @@ __device__ __forceinline__ void attend_passes(const AttendArgs &a, uint32_t *sme
     for (int m0 = 0; m0 < a.QH; m0 += RP) {
         __syncthreads();  // the previous pass's merge slots are read
         RawChunk<D> raw;  // the first sub-chunk's bytes are requested before the query tile
-        load_chunk<D, Q8>(raw, lay, a.geo, vbase, sub0 * ATT_TC, a.T, tid, kscales);
+        load_chunk<D, Q8, R>(raw, lay, a.geo, vbase, sub0 * ATT_TC, a.T, tid, kscales, a.vlr);
         if (tid < 64) {
             const float c0 = centroid_e4(uint32_t(tid & 7)) * 1e-4f, c1 = centroid_e4(uint32_t(tid >> 3)) * 1e-4f;
             lut[tid] = pack_half2(c0, c1);
@@ -229,6 +252,9 @@ __device__ __forceinline__ void attend_passes(const AttendArgs &a, uint32_t *sme
 #pragma unroll
         for (int nt = 0; nt < NV; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.0f;
         float mx[2] = {-INFINITY, -INFINITY}, ls[2] = {0.0f, 0.0f};
+        float lracc[NL > 0 ? NL : 1][4];  // P V_lr (LoRA attention)
+#pragma unroll
+        for (int nt = 0; nt < (NL > 0 ? NL : 1); ++nt) lracc[nt][0] = lracc[nt][1] = lracc[nt][2] = lracc[nt][3] = 0.0f;
 
         __syncthreads();  // the pair table and the query tile are in
         for (int sub = sub0; sub < sub1; ++sub) {
@@ -236,8 +262,10 @@ __device__ __forceinline__ void attend_passes(const AttendArgs &a, uint32_t *sme
             uint32_t *Kt = Kb + buf * SM::tile_words, *Ct = Cs + buf * SM::tile_words;
             float *st = sig + buf * ATT_TC;
             float *kst = ksb + buf * SM::ksb_words;
-            stage_chunk<D, Q8>(raw, Kt, Ct, st, lut, kst, tid);
-            if (sub + 1 < sub1) load_chunk<D, Q8>(raw, lay, a.geo, vbase, (sub + 1) * ATT_TC, a.T, tid, kscales);
+            uint32_t *Lt = Ls + buf * SM::lr_words;
+            stage_chunk<D, Q8, R>(raw, Kt, Ct, st, lut, kst, Lt, tid);
+            if (sub + 1 < sub1)
+                load_chunk<D, Q8, R>(raw, lay, a.geo, vbase, (sub + 1) * ATT_TC, a.T, tid, kscales, a.vlr);
             __syncthreads();  // this buffer is staged; every warp is done with the other one
             if (!active) continue;
 
@@ -316,11 +344,20 @@ __device__ __forceinline__ void attend_passes(const AttendArgs &a, uint32_t *sme
                 acc[nt][2] *= al[1];
                 acc[nt][3] *= al[1];
             }
+            if constexpr (R > 0) {
+#pragma unroll
+                for (int nt = 0; nt < NL; ++nt) {
+                    lracc[nt][0] *= al[0];
+                    lracc[nt][1] *= al[0];
+                    lracc[nt][2] *= al[1];
+                    lracc[nt][3] *= al[1];
+                }
+            }
             // P' = p * sigma as fp16 A fragments: the S accumulator of n-tiles
             // 2kk, 2kk+1 is the A operand of k-step kk
 #pragma unroll
             for (int kk = 0; kk < NS / 2; ++kk) {
-                uint32_t pa[4];
+                uint32_t pa[4], pl[4];  // p * sigma for the pool's values; p for the low-rank cache
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
                     const int nt = 2 * kk + hf;
@@ -332,6 +369,10 @@ __device__ __forceinline__ void attend_passes(const AttendArgs &a, uint32_t *sme
                     ls[1] += p2 + p3;
                     pa[2 * hf] = pack_half2(p0 * s0, p1 * s1);
                     pa[2 * hf + 1] = pack_half2(p2 * s0, p3 * s1);
+                    if constexpr (R > 0) {
+                        pl[2 * hf] = pack_half2(p0, p1);
+                        pl[2 * hf + 1] = pack_half2(p2, p3);
+                    }
                 }
                 // A += P' C over tokens th*TPW + kk*16 .. +15, every dim
 #pragma unroll
@@ -341,6 +382,17 @@ __device__ __forceinline__ void attend_passes(const AttendArgs &a, uint32_t *sme
                     ldsm_x4_t(cb, Ct + tok * RW + np * 4 + (lane >> 4) * 4);
                     mma_f16(acc[np], pa, cb[0], cb[1]);
                     mma_f16(acc[np + 1], pa, cb[2], cb[3]);
+                }
+                if constexpr (R > 0) {
+                    // Flash-LoRA reorder: P V_lr over the same tokens, r columns
+#pragma unroll
+                    for (int np = 0; np < NL; np += 2) {
+                        uint32_t lb[4];
+                        const int tok = th * TPW + kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+                        ldsm_x4_t(lb, Lt + tok * LW + np * 4 + (lane >> 4) * 4);
+                        mma_f16(lracc[np], pl, lb[0], lb[1]);
+                        mma_f16(lracc[np + 1], pl, lb[2], lb[3]);
+                    }
                 }
             }
         }
@@ -359,6 +411,15 @@ __device__ __forceinline__ void attend_passes(const AttendArgs &a, uint32_t *sme
                 *reinterpret_cast<float2 *>(slot + (g + 8) * MSW + nt * 8 + 2 * tig) =
                     make_float2(acc[nt][2], acc[nt][3]);
             }
+            if constexpr (R > 0) {
+#pragma unroll
+                for (int nt = 0; nt < NL; ++nt) {
+                    *reinterpret_cast<float2 *>(slot + g * MSW + D + nt * 8 + 2 * tig) =
+                        make_float2(lracc[nt][0], lracc[nt][1]);
+                    *reinterpret_cast<float2 *>(slot + (g + 8) * MSW + D + nt * 8 + 2 * tig) =
+                        make_float2(lracc[nt][2], lracc[nt][3]);
+                }
+            }
             float *ms = mrg + ATT_WARPS * 16 * MSW + warp * 32;
             if (tig == 0) {
                 ms[g] = mx[0];
@@ -369,8 +430,8 @@ __device__ __forceinline__ void attend_passes(const AttendArgs &a, uint32_t *sme
         }
         __syncthreads();
         const uint64_t pbase = (uint64_t(h) * a.nsplit + split) * uint64_t(a.QHP);
-        for (int e = tid; e < RP * (D / 4); e += ATT_THREADS) {
-            const int r = e / (D / 4), c4 = e % (D / 4);
+        for (int e = tid; e < RP * (PW / 4); e += ATT_THREADS) {
+            const int r = e / (PW / 4), c4 = e % (PW / 4);
             if (m0 + r >= a.QH) continue;
             const int ti = r >> 4, rr = r & 15;
             const float *ms = mrg + ATT_WARPS * 16 * MSW;
@@ -389,13 +450,13 @@ __device__ __forceinline__ void attend_passes(const AttendArgs &a, uint32_t *sme
                 o.w = fmaf(f, x.w, o.w);
                 l = fmaf(f, ms[w * 32 + 16 + rr], l);
             }
-            *reinterpret_cast<float4 *>(a.part + (pbase + m0 + r) * D + c4 * 4) = o;
+            *reinterpret_cast<float4 *>(a.part + (pbase + m0 + r) * PW + c4 * 4) = o;
             if (c4 == 0) a.stats[pbase + m0 + r] = make_float2(M, l);
         }
     }
 }
 
-template <int D, int TPW>
+template <int D, int TPW, int R>
 __global__ void __launch_bounds__(ATT_THREADS, 2) attend_split(const __grid_constant__ AttendArgs a) {
     extern __shared__ __align__(16) uint32_t smem[];
     const uint32_t *hdr = reinterpret_cast<const uint32_t *>(a.pool);
@@ -407,46 +468,53 @@ __global__ void __launch_bounds__(ATT_THREADS, 2) attend_split(const __grid_cons
         return;
     }
     if (kmode == KVP_K_Q8_0)
-        attend_passes<D, TPW, true>(
+        attend_passes<D, TPW, true, R>(
             a, smem,
             reinterpret_cast<const uint16_t *>(a.pool + a.geo.off_kscales) + uint64_t(a.layer) * a.H * a.T * (D / 32));
     else
-        attend_passes<D, TPW, false>(a, smem, nullptr);
+        attend_passes<D, TPW, false, R>(a, smem, nullptr);
 }
 
 // One 128-thread block per (agent, query head): merge the splits, inverse
 // transform.  Warp w merges splits w, w+4, ... online, with the statistics
 // and partial rows of up to eight splits in flight at once; the four warps'
 // states are then merged in shared memory and warp 0 applies the transform.
+// LoRA attention (R > 0): lane k < R also merges column k of P V_lr, and the
+// agent's up-projection is applied once, after the transform:
+// out += (P V_lr / l) B_a[:, h*d .. h*d + d).
 constexpr int CMB_THREADS = 128;
 constexpr int CMB_WARPS = CMB_THREADS / 32;
 
-template <int D>
+template <int D, int R>
 __global__ void __launch_bounds__(CMB_THREADS) attend_combine(const __grid_constant__ AttendArgs a) {
     constexpr int PL = D / 32;  // dims per lane, indices lane*PL + e
     constexpr int UN = 8;       // splits in flight per warp
-    __shared__ float wacc[CMB_WARPS][D];
+    constexpr int PW = D + R;   // floats per partial row
+    __shared__ float wacc[CMB_WARPS][D + (R > 0 ? 32 : 0)];
     __shared__ float wml[CMB_WARPS][2];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ag = blockIdx.x / a.NQ, j = blockIdx.x % a.NQ;
     const int h = j / a.G, r = ag * a.G + j % a.G;
     const uint64_t row0 = uint64_t(h) * a.nsplit * uint64_t(a.QHP) + r;  // split sp: row0 + sp * QHP
-    float m = -INFINITY, l = 0.0f, acc[PL];
+    float m = -INFINITY, l = 0.0f, acc[PL], lrv = 0.0f;
 #pragma unroll
     for (int e = 0; e < PL; ++e) acc[e] = 0.0f;
     for (int sp0 = warp; sp0 < a.nsplit; sp0 += CMB_WARPS * UN) {
         float2 st[UN];
-        float v[UN][PL];
+        float v[UN][PL], vl[UN];
 #pragma unroll
         for (int u = 0; u < UN; ++u) {
             const int sp = sp0 + u * CMB_WARPS;
             st[u] = make_float2(-INFINITY, 0.0f);
+            vl[u] = 0.0f;
 #pragma unroll
             for (int e = 0; e < PL; ++e) v[u][e] = 0.0f;
             if (sp < a.nsplit) {
                 const uint64_t row = row0 + uint64_t(sp) * a.QHP;
                 st[u] = a.stats[row];
-                const float *pp = a.part + row * D + lane * PL;
+                const float *pp = a.part + row * PW + lane * PL;
+                if constexpr (R > 0)
+                    if (lane < R) vl[u] = a.part[row * PW + D + lane];
                 if constexpr (PL == 4) {
                     const float4 x = *reinterpret_cast<const float4 *>(pp);
                     v[u][0] = x.x, v[u][1] = x.y, v[u][2] = x.z, v[u][3] = x.w;
@@ -464,11 +532,13 @@ __global__ void __launch_bounds__(CMB_THREADS) attend_combine(const __grid_const
             l = l * f0 + st[u].y * f1;
 #pragma unroll
             for (int e = 0; e < PL; ++e) acc[e] = acc[e] * f0 + v[u][e] * f1;
+            if constexpr (R > 0) lrv = lrv * f0 + vl[u] * f1;
             m = nm;
         }
     }
 #pragma unroll
     for (int e = 0; e < PL; ++e) wacc[warp][lane * PL + e] = acc[e];
+    if constexpr (R > 0) wacc[warp][D + lane] = lrv;
     if (lane == 0) {
         wml[warp][0] = m;
         wml[warp][1] = l;
@@ -479,6 +549,7 @@ __global__ void __launch_bounds__(CMB_THREADS) attend_combine(const __grid_const
 #pragma unroll
     for (int w = 0; w < CMB_WARPS; ++w) M = fmaxf(M, wml[w][0]);
     l = 0.0f;
+    lrv = 0.0f;
 #pragma unroll
     for (int e = 0; e < PL; ++e) acc[e] = 0.0f;
 #pragma unroll
@@ -487,6 +558,7 @@ __global__ void __launch_bounds__(CMB_THREADS) attend_combine(const __grid_const
         l = fmaf(f, wml[w][1], l);
 #pragma unroll
         for (int e = 0; e < PL; ++e) acc[e] = fmaf(f, wacc[w][lane * PL + e], acc[e]);
+        if constexpr (R > 0) lrv = fmaf(f, wacc[w][D + lane], lrv);
     }
     // unnormalised Walsh-Hadamard transform over d: register bits, then lane bits
 #pragma unroll
@@ -507,32 +579,63 @@ __global__ void __launch_bounds__(CMB_THREADS) attend_combine(const __grid_const
     const float f = (D == 128 ? 0.08838834764831845f : 0.125f) / l;  // 1/sqrt(d) / l
     float *o = a.out + (uint64_t(ag) * a.NQ + j) * D + lane * PL;
 #pragma unroll
-    for (int e = 0; e < PL; ++e) o[e] = acc[e] * f;
+    for (int e = 0; e < PL; ++e) acc[e] *= f;
+    if constexpr (R > 0) {
+        // (P V_lr / l) B_a, restricted to this KV head's d columns
+        const float il = 1.0f / l;
+        const uint16_t *bh = a.lora_b + uint64_t(ag) * R * uint64_t(a.H) * D + uint64_t(h) * D + lane * PL;
+#pragma unroll 4
+        for (int k = 0; k < R; ++k) {
+            const float c = __shfl_sync(0xffffffffu, lrv, k) * il;
+            const uint16_t *bk = bh + uint64_t(k) * a.H * D;
+            if constexpr (PL == 4) {
+                const uint2 w = *reinterpret_cast<const uint2 *>(bk);
+                acc[0] = fmaf(c, bf16_lo(w.x), acc[0]);
+                acc[1] = fmaf(c, bf16_hi(w.x), acc[1]);
+                acc[2] = fmaf(c, bf16_lo(w.y), acc[2]);
+                acc[3] = fmaf(c, bf16_hi(w.y), acc[3]);
+            } else {
+                const uint32_t w = *reinterpret_cast<const uint32_t *>(bk);
+                acc[0] = fmaf(c, bf16_lo(w), acc[0]);
+                acc[1] = fmaf(c, bf16_hi(w), acc[1]);
+            }
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < PL; ++e) o[e] = acc[e];
     if (lane == 0) a.lse[uint64_t(ag) * a.NQ + j] = (M + __log2f(l)) * 0.6931471805599453f;
 }
 
 // The split kernel's dynamic shared memory exceeds the default 48 KB: raise
 // the limit once per device (the first call on a device does it).
-template <int D, int TPW>
+template <int D, int TPW, int R>
 static bool attend_smem_ready() {
     static bool done[64] = {false};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
     if (!done[dev]) {
-        if (cudaFuncSetAttribute(attend_split<D, TPW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 int(AttendSmem<D>::bytes)) != cudaSuccess)
+        if (cudaFuncSetAttribute(attend_split<D, TPW, R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(AttendSmem<D, R>::bytes)) != cudaSuccess)
             return false;
         done[dev] = true;
     }
     return true;
 }
 
-template <int D, int TPW>
+template <int D, int TPW, int R>
 static int attend_launch(const AttendArgs &a, dim3 grid, unsigned cgrid, cudaStream_t st) {
-    if (!attend_smem_ready<D, TPW>()) return KVP_ERR_CUDA;
-    attend_split<D, TPW><<<grid, ATT_THREADS, AttendSmem<D>::bytes, st>>>(a);
-    attend_combine<D><<<cgrid, CMB_THREADS, 0, st>>>(a);
+    if (!attend_smem_ready<D, TPW, R>()) return KVP_ERR_CUDA;
+    attend_split<D, TPW, R><<<grid, ATT_THREADS, AttendSmem<D, R>::bytes, st>>>(a);
+    attend_combine<D, R><<<cgrid, CMB_THREADS, 0, st>>>(a);
     return KVP_OK;
+}
+
+// head_dim, token-slice width (at most 32 query rows per KV head: 16) and rank
+template <int R>
+static int attend_dispatch(const AttendArgs &a, int d, bool narrow, dim3 grid, unsigned cgrid, cudaStream_t st) {
+    if (d == 128)
+        return narrow ? attend_launch<128, 16, R>(a, grid, cgrid, st) : attend_launch<128, 32, R>(a, grid, cgrid, st);
+    return narrow ? attend_launch<64, 16, R>(a, grid, cgrid, st) : attend_launch<64, 32, R>(a, grid, cgrid, st);
 }
 
 struct AttendPlan {
@@ -540,7 +643,7 @@ struct AttendPlan {
     uint64_t part_off, stats_off, total;
 };
 
-static inline AttendPlan attend_plan(const kvp_shape *s, int na, int nq) {
+static inline AttendPlan attend_plan(const kvp_shape *s, int na, int nq, int rank = 0) {
     AttendPlan p;
     p.G = nq / s->n_kv_heads;
     p.QH = na * p.G;
@@ -553,32 +656,26 @@ static inline AttendPlan attend_plan(const kvp_shape *s, int na, int nq) {
     p.nsplit = (p.nsub + p.per_split - 1) / p.per_split;
     const uint64_t rows = uint64_t(s->n_kv_heads) * uint64_t(p.nsplit) * uint64_t(p.QHP);
     p.part_off = 0;
-    p.stats_off = align256(rows * uint64_t(s->head_dim) * 4u);
+    p.stats_off = align256(rows * uint64_t(s->head_dim + rank) * 4u);
     p.total = align256(p.stats_off + rows * 8u);
     return p;
 }
 
-}  // namespace kvp
-
-using namespace kvp;
-
-extern "C" size_t kvpool_attend_workspace_bytes(const kvp_shape *s, int n_agents, int n_q_heads) {
-    if (shape_ok(s) != KVP_OK || n_agents < 1 || n_q_heads < 1 || n_q_heads % s->n_kv_heads != 0) return 0;
-    return size_t(attend_plan(s, n_agents, n_q_heads).total);
-}
-
-extern "C" int kvpool_attend(const void *pool, const kvp_shape *s, int layer, int n_agents, int n_q_heads,
-                             const void *q, float scale, float *out, float *lse, void *ws, size_t ws_bytes,
-                             void *stream) {
+// Checks, arguments and launches shared by plain (rank 0) and LoRA attention.
+static int attend_common(const void *pool, const kvp_shape *s, int layer, int n_agents, int n_q_heads,
+                         const void *q, float scale, int rank, const void *v_lr, const void *lora_b, float *out,
+                         float *lse, void *ws, size_t ws_bytes, void *stream) {
     int rc = shape_ok(s);
     if (rc != KVP_OK) return rc;
     if (!pool || !q || !out || !lse || !ws) return KVP_ERR_ARG;
     if (layer < 0 || layer >= s->n_layers || n_agents < 1 || n_q_heads < 1 || n_q_heads % s->n_kv_heads != 0)
         return KVP_ERR_ARG;
+    if (rank != 0 && (!v_lr || !lora_b)) return KVP_ERR_ARG;
     if (uint64_t(n_agents) * uint64_t(n_q_heads) >= (1ull << 24)) return KVP_ERR_SIZE;
     if (!aligned(pool, 256) || !aligned(q, 16) || !aligned(out, 16) || !aligned(lse, 4) || !aligned(ws, 16))
         return KVP_ERR_ALIGN;
-    const AttendPlan p = attend_plan(s, n_agents, n_q_heads);
+    if (rank != 0 && (!aligned(v_lr, 16) || !aligned(lora_b, 16))) return KVP_ERR_ALIGN;
+    const AttendPlan p = attend_plan(s, n_agents, n_q_heads, rank);
     if (ws_bytes < p.total) return KVP_ERR_SIZE;
     AttendArgs a;
     a.pool = static_cast<const uint8_t *>(pool);
@@ -601,16 +698,51 @@ extern "C" int kvpool_attend(const void *pool, const kvp_shape *s, int layer, in
     a.nsub = p.nsub;
     a.per_split = p.per_split;
     a.nsplit = p.nsplit;
+    a.vlr = static_cast<const uint16_t *>(v_lr);
+    a.lora_b = static_cast<const uint16_t *>(lora_b);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const dim3 grid(unsigned(a.H), unsigned(a.nsplit));
     const unsigned cgrid = unsigned(n_agents) * unsigned(n_q_heads);  // one block per query
-    // at most 32 query rows per KV head: two 16-row tiles, four 16-token slices
     const bool narrow = p.QH <= 32;
-    if (s->head_dim == 128)
-        rc = narrow ? attend_launch<128, 16>(a, grid, cgrid, st) : attend_launch<128, 32>(a, grid, cgrid, st);
+    if (rank == 0)
+        rc = attend_dispatch<0>(a, s->head_dim, narrow, grid, cgrid, st);
+    else if (rank == 16)
+        rc = attend_dispatch<16>(a, s->head_dim, narrow, grid, cgrid, st);
     else
-        rc = narrow ? attend_launch<64, 16>(a, grid, cgrid, st) : attend_launch<64, 32>(a, grid, cgrid, st);
+        rc = attend_dispatch<32>(a, s->head_dim, narrow, grid, cgrid, st);
     if (rc != KVP_OK) return rc;
     count_launch(2);
     return launch_status();
+}
+
+static inline bool rank_ok(int rank) { return rank == 16 || rank == 32; }
+
+}  // namespace kvp
+
+using namespace kvp;
+
+extern "C" size_t kvpool_attend_workspace_bytes(const kvp_shape *s, int n_agents, int n_q_heads) {
+    if (shape_ok(s) != KVP_OK || n_agents < 1 || n_q_heads < 1 || n_q_heads % s->n_kv_heads != 0) return 0;
+    return size_t(attend_plan(s, n_agents, n_q_heads).total);
+}
+
+extern "C" int kvpool_attend(const void *pool, const kvp_shape *s, int layer, int n_agents, int n_q_heads,
+                             const void *q, float scale, float *out, float *lse, void *ws, size_t ws_bytes,
+                             void *stream) {
+    return attend_common(pool, s, layer, n_agents, n_q_heads, q, scale, 0, nullptr, nullptr, out, lse, ws, ws_bytes,
+                         stream);
+}
+
+extern "C" size_t kvpool_attend_lora_workspace_bytes(const kvp_shape *s, int n_agents, int n_q_heads, int rank) {
+    if (shape_ok(s) != KVP_OK || n_agents < 1 || n_q_heads < 1 || n_q_heads % s->n_kv_heads != 0 || !rank_ok(rank))
+        return 0;
+    return size_t(attend_plan(s, n_agents, n_q_heads, rank).total);
+}
+
+extern "C" int kvpool_attend_lora(const void *pool, const kvp_shape *s, int layer, int n_agents, int n_q_heads,
+                                  const void *q, float scale, int rank, const void *v_lr, const void *lora_b,
+                                  float *out, float *lse, void *ws, size_t ws_bytes, void *stream) {
+    if (!rank_ok(rank)) return KVP_ERR_ARG;
+    return attend_common(pool, s, layer, n_agents, n_q_heads, q, scale, rank, v_lr, lora_b, out, lse, ws, ws_bytes,
+                         stream);
 }

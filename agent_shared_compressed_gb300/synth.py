@@ -16,7 +16,10 @@ those caches are known for:
   ("PolyKV", 2.B.2); drawn as Z / sqrt(W/5) with W a sum of 5 squared
   standard normals, the textbook construction of the t distribution;
 * CacheCard bitwidths: i.i.d. per token from {2,4,8,16} with probabilities
-  {0.25, 0.40, 0.25, 0.10} ("QKVShare", Methodology 1 names the set).
+  {0.25, 0.40, 0.25, 0.10} ("QKVShare", Methodology 1 names the set);
+* LoRA value adapters ("LRAgent"): the shared low-rank cache X A ~ N(0,1)
+  per entry, each agent's up-projection B ~ N(0, 0.02^2), so the adapter term
+  is a small perturbation of the base values, as that page describes it.
 
 Both are rounded to bf16 (round-to-nearest-even), laid out per layer as
 [H][T][d], the Hugging Face past_key_values layout at batch 1.
@@ -81,6 +84,15 @@ def card_bits(T, seed=0, device="cpu"):
     for b, e in zip(reversed(CARD_BITS[:-1]), reversed(edges)):
         out[u < float(e)] = b
     return out
+
+
+def lora_inputs(T, H, d, n_agents, rank, seed=0, device="cpu"):
+    """Shared low-rank value cache (bf16 [T, rank]) and per-agent value
+    up-projections (bf16 [n_agents, rank, H*d], rank-major rows)."""
+    g = _gen(seed + 0x10AA, device)
+    vlr = torch.randn(T, rank, generator=g, device=device)
+    b = torch.randn(n_agents, rank, H * d, generator=g, device=device) * 0.02
+    return vlr.to(torch.bfloat16), b.to(torch.bfloat16)
 
 
 def bits16(t):

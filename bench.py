@@ -499,14 +499,22 @@ def run_attend(args):
     q = torch.randn(N, nq, d, generator=g, device="cuda").to(torch.bfloat16)
     out = torch.empty(N, nq, d, dtype=torch.float32, device="cuda")
     lse = torch.empty(N, nq, dtype=torch.float32, device="cuda")
-    wsb = kv.kvpool_attend_workspace_bytes(c.shape, N, nq)
+    R = args.lora_rank
+    wsb = (kv.kvpool_attend_lora_workspace_bytes(c.shape, N, nq, R) if R
+           else kv.kvpool_attend_workspace_bytes(c.shape, N, nq))
     ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
     scale = 1.0 / math.sqrt(d)
+    if R:  # one shared low-rank cache and per-agent up-projections per layer
+        lora = [synth.lora_inputs(T, H, d, N, R, seed=100 + l, device="cuda") for l in range(L)]
 
     def step():
         cur = torch.cuda.current_stream()
         for l in range(L):
-            kv.check(kv.kvpool_attend(c.pool, c.shape, l, N, nq, q, scale, out, lse, ws, wsb, cur), "attend")
+            if R:
+                kv.check(kv.kvpool_attend_lora(c.pool, c.shape, l, N, nq, q, scale, R, lora[l][0], lora[l][1], out,
+                                               lse, ws, wsb, cur), "attend_lora")
+            else:
+                kv.check(kv.kvpool_attend(c.pool, c.shape, l, N, nq, q, scale, out, lse, ws, wsb, cur), "attend")
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -534,7 +542,7 @@ def run_attend(args):
     launches = 2 * L * args.steps  # replayed graph nodes (the counter sees only direct launches)
     pool_bytes = c.pool_bytes
     io = N * nq * d * 2 + N * nq * (d + 1) * 4
-    flops = 2.0 * 2.0 * N * nq * T * d * L
+    flops = 2.0 * N * nq * T * (2 * d + R) * L + (2.0 * N * nq * R * d * L if R else 0.0)
     peak, kind = hbm_peak()
     gbs = (pool_bytes + L * io) / (ms * 1e-3) / 1e9
     # what the agents would otherwise read: N bf16 caches of every layer
@@ -544,7 +552,7 @@ def run_attend(args):
         "value": round(ms * 1e3 / L, 2), "unit": "us per layer", "higher_is_better": False,
         "ms_per_step": round(ms, 4), "steps": args.steps, "warmup": args.warmup, "n_gpus": 1,
         "dtype": "bf16 q / int8 k / 3-bit v", "data": "synthetic",
-        "config": {"workload": args.workload, "k_format": args.k_format, "layers": L, "kv_heads": H,
+        "config": {"workload": args.workload, "k_format": args.k_format, "lora_rank": R, "layers": L, "kv_heads": H,
                    "q_heads": nq, "head_dim": d,
                    "tokens": T, "agents": N},
         "pool_GBps": round(gbs, 1), "frac_of_measured_peak": round(gbs / peak, 4), "peak_kind": kind,
@@ -631,6 +639,8 @@ def main():
     ap.add_argument("--layers", type=int, default=0)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--lora-rank", type=int, default=0, choices=[0, 16, 32],
+                    help="attend mode: agents' values carry a LoRA term from a shared low-rank cache of this rank")
     ap.add_argument("--k-format", choices=sorted(K_FORMATS), default="per_tensor",
                     help="pool key format: one scale per layer tensor (default) or q8_0 blocks")
     ap.add_argument("--mode", choices=["step", "attend", "realign"], default="step",

@@ -243,6 +243,31 @@ int kvpool_attend(const void *pool, const kvp_shape *shape, int layer, int n_age
                   const void *q, float scale, float *out, float *lse, void *ws, size_t ws_bytes,
                   void *stream);
 
+/* Bytes of device workspace kvpool_attend_lora needs (0 for an invalid shape,
+ * head count or rank). */
+size_t kvpool_attend_lora_workspace_bytes(const kvp_shape *shape, int n_agents, int n_q_heads, int rank);
+
+/* Pool attention for agents that differ by a LoRA adapter on the value
+ * projection, with one shared low-rank cache ("LRAgent": BaseLRShared shares
+ * the base cache and the low-rank cache X A between agents, each agent keeping
+ * its own up-projection B; Flash-LoRA-Attention computes
+ * P (V_base + V_lr B) as P V_base + (P V_lr) B, so the up-projection is
+ * applied once per query instead of expanding the cache).  Agent a's value of
+ * token t at KV head h is
+ *   v = (the pool's decoded value) + sum_k v_lr[t][k] * lora_b[a][k][h*d + i];
+ * otherwise as kvpool_attend (same out, lse, GQA map and key formats).
+ *  rank: 16 or 32 (KVP_ERR_ARG otherwise).
+ *  v_lr: device bf16 [n_tokens][rank], the layer's shared low-rank cache
+ *    (16-byte aligned).  It enters the product as fp16: exact for values in
+ *    fp16's normal range, |x| in [2^-14, 65504].
+ *  lora_b: device bf16 [n_agents][rank][n_kv_heads * head_dim], each agent's
+ *    up-projection with rank-major rows (the transpose of a PyTorch LoRA
+ *    B weight), 16-byte aligned.
+ *  ws: kvpool_attend_lora_workspace_bytes. */
+int kvpool_attend_lora(const void *pool, const kvp_shape *shape, int layer, int n_agents, int n_q_heads,
+                       const void *q, float scale, int rank, const void *v_lr, const void *lora_b, float *out,
+                       float *lse, void *ws, size_t ws_bytes, void *stream);
+
 /* ---------------------------------------------------------------------- */
 /* CacheCard                                                               */
 /* ---------------------------------------------------------------------- */
