@@ -316,15 +316,26 @@ __device__ __forceinline__ void attend_passes(const AttendArgs &a, uint32_t *sme
             // online softmax over this warp's slice (rows g and g+8 of the tile)
             const int tbase = sub * ATT_TC + th * TPW;
             float cm[2] = {-INFINITY, -INFINITY};
+            if (tbase + TPW <= a.T) {  // warp-uniform: every token of the slice is real
 #pragma unroll
-            for (int nt = 0; nt < NS; ++nt) {
-                const int tk = tbase + nt * 8 + 2 * tig;
-                s[nt][0] = tk < a.T ? s[nt][0] * qk2 : -INFINITY;
-                s[nt][1] = tk + 1 < a.T ? s[nt][1] * qk2 : -INFINITY;
-                s[nt][2] = tk < a.T ? s[nt][2] * qk2 : -INFINITY;
-                s[nt][3] = tk + 1 < a.T ? s[nt][3] * qk2 : -INFINITY;
-                cm[0] = fmaxf(cm[0], fmaxf(s[nt][0], s[nt][1]));
-                cm[1] = fmaxf(cm[1], fmaxf(s[nt][2], s[nt][3]));
+                for (int nt = 0; nt < NS; ++nt) {
+                    const float2 lo = __fmul2_rn(make_float2(s[nt][0], s[nt][1]), make_float2(qk2, qk2));
+                    const float2 hi = __fmul2_rn(make_float2(s[nt][2], s[nt][3]), make_float2(qk2, qk2));
+                    s[nt][0] = lo.x, s[nt][1] = lo.y, s[nt][2] = hi.x, s[nt][3] = hi.y;
+                    cm[0] = fmaxf(cm[0], fmaxf(s[nt][0], s[nt][1]));
+                    cm[1] = fmaxf(cm[1], fmaxf(s[nt][2], s[nt][3]));
+                }
+            } else {
+#pragma unroll
+                for (int nt = 0; nt < NS; ++nt) {
+                    const int tk = tbase + nt * 8 + 2 * tig;
+                    s[nt][0] = tk < a.T ? s[nt][0] * qk2 : -INFINITY;
+                    s[nt][1] = tk + 1 < a.T ? s[nt][1] * qk2 : -INFINITY;
+                    s[nt][2] = tk < a.T ? s[nt][2] * qk2 : -INFINITY;
+                    s[nt][3] = tk + 1 < a.T ? s[nt][3] * qk2 : -INFINITY;
+                    cm[0] = fmaxf(cm[0], fmaxf(s[nt][0], s[nt][1]));
+                    cm[1] = fmaxf(cm[1], fmaxf(s[nt][2], s[nt][3]));
+                }
             }
             float ref[2], al[2];
 #pragma unroll
@@ -337,12 +348,14 @@ __device__ __forceinline__ void attend_passes(const AttendArgs &a, uint32_t *sme
                 mx[i] = nm;
                 ls[i] *= al[i];
             }
+            {
+                const float2 a0 = make_float2(al[0], al[0]), a1 = make_float2(al[1], al[1]);
 #pragma unroll
-            for (int nt = 0; nt < NV; ++nt) {
-                acc[nt][0] *= al[0];
-                acc[nt][1] *= al[0];
-                acc[nt][2] *= al[1];
-                acc[nt][3] *= al[1];
+                for (int nt = 0; nt < NV; ++nt) {
+                    const float2 lo = __fmul2_rn(make_float2(acc[nt][0], acc[nt][1]), a0);
+                    const float2 hi = __fmul2_rn(make_float2(acc[nt][2], acc[nt][3]), a1);
+                    acc[nt][0] = lo.x, acc[nt][1] = lo.y, acc[nt][2] = hi.x, acc[nt][3] = hi.y;
+                }
             }
             if constexpr (R > 0) {
 #pragma unroll
