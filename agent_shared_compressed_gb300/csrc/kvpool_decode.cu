@@ -2,8 +2,8 @@
 // PooledAgent receives the decompressed KV layer by layer in its own cache;
 // 2.B.2 dequantization: centroid lookup, inverse Walsh-Hadamard transform,
 // rescale).  The pool is read once per launch; every decoded tile is stored
-// to all agents' caches from registers, so HBM traffic is the pool plus
-// N x the bf16 cache -- the write side is the roofline.
+// to all agents' caches by bulk copies from shared memory, so HBM traffic is
+// the pool plus N x the bf16 cache -- the write side is the roofline.
 #include "kvp_vec.cuh"
 
 namespace kvp {
@@ -11,6 +11,25 @@ namespace kvp {
 constexpr int DEC_THREADS = 256;
 constexpr int DEC_WARPS = DEC_THREADS / 32;
 constexpr int DEC_MAX_PTRS = 1024;  // (agent, layer) destinations per launch
+// Fan-out by bulk copies: each warp decodes a unit into shared memory once and
+// its lanes hand the agents' copies to the bulk-copy (TMA) engine, so the
+// stores take no issue slots or registers of the SM.  Used from this many
+// agents per launch; fewer are written with direct stores.
+constexpr int DEC_BULK_MIN_AGENTS = 2;
+
+// Asynchronous bulk copy shared -> global (16-byte aligned addresses, size a
+// multiple of 16), tracked per thread in bulk async-groups.
+__device__ __forceinline__ void bulk_store(void *gdst, const void *ssrc, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                 :: "l"(gdst), "r"(static_cast<uint32_t>(__cvta_generic_to_shared(ssrc))), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// every committed group of this thread has finished reading shared memory
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// every committed group of this thread is complete
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// generic-proxy shared-memory writes become visible to the bulk-copy engine
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 struct DecodeArgs {
     uint4 *kd[DEC_MAX_PTRS];  // index a * nl + r: agent a, layer lb + r
@@ -44,13 +63,16 @@ __device__ __forceinline__ uint4 k_decode8(uint2 raw, float s) {
 
 // One warp step ("unit"): VPW consecutive vectors of one layer.  The pool
 // bytes of the unit are loaded up front (keys 4 x 8 B per lane, value codes
-// 16 B on 24 lanes, sigma 2 B); keys are decoded and stored to every agent,
-// then values.  Value codes are staged in shared memory and each pair of
-// codes (a, b) is looked up in a 64-entry table of (c_a + c_b, c_a - c_b),
-// which is also the transform's first butterfly stage.
+// 16 B on 24 lanes, sigma 2 B).  Value codes are staged in shared memory and
+// each pair of codes (a, b) is looked up in a 64-entry table of
+// (c_a + c_b, c_a - c_b), which is also the transform's first butterfly
+// stage.  The decoded keys and values (2 KB each: VPW contiguous vectors)
+// are written to the warp's staging area, and lane a hands agent a's two
+// copies to the bulk-copy engine.
 // The grid-stride walk over units; Q8: keys carry q8_0 block scales.
-template <int D, bool Q8>
-__device__ __forceinline__ void decode_units(const DecodeArgs &a, uint8_t (*stage)[384 + 16], const float2 *pair_lut) {
+template <int D, bool Q8, bool BULK>
+__device__ __forceinline__ void decode_units(const DecodeArgs &a, uint8_t (*stage)[384 + 16], const float2 *pair_lut,
+                                             uint4 *ostage) {
     constexpr int LPV = D / 32;
     constexpr int VPW = 32 / LPV;
     constexpr int CPV = D / 8;
@@ -65,6 +87,8 @@ __device__ __forceinline__ void decode_units(const DecodeArgs &a, uint8_t (*stag
     const uint64_t total = upl * uint64_t(a.nl);
     const float *scales = reinterpret_cast<const float *>(a.pool + a.geo.off_scales);
     const uint16_t *kscales = reinterpret_cast<const uint16_t *>(a.pool + a.geo.off_kscales);
+    uint4 *osk = ostage + warp * (2 * VPW * CPV);  // this warp's decoded unit: keys, then values
+    uint4 *osv = osk + VPW * CPV;
 
     for (uint64_t u = uint64_t(blockIdx.x) * DEC_WARPS + warp; u < total; u += uint64_t(gridDim.x) * DEC_WARPS) {
         const int r = int(u / upl);
@@ -96,6 +120,11 @@ __device__ __forceinline__ void decode_units(const DecodeArgs &a, uint8_t (*stag
         const uint64_t n = n0 + g;
         const bool valid = n < nvec;
         const uint16_t sh = valid ? reinterpret_cast<const uint16_t *>(lay + a.geo.sec_sigma)[n] : uint16_t(0);
+        if constexpr (BULK) {
+            // the previous unit's copies have read this warp's staging area
+            bulk_wait_read_all();
+            __syncwarp();
+        }
         float ks[KCH];  // each 8-key chunk's scale: the layer's, or its q8_0 block's
         if constexpr (Q8) {
             // chunk k of the unit holds keys 8k .. 8k+7 from vector n0: block (n0 * D + 8k) / 32
@@ -116,12 +145,20 @@ __device__ __forceinline__ void decode_units(const DecodeArgs &a, uint8_t (*stag
             uint4 kout[KCH];
 #pragma unroll
             for (int it = 0; it < KCH; ++it) kout[it] = k_decode8(kraw[it], ks[it]);
-            for (int ag = 0; ag < a.na; ++ag) {
-                uint4 *kd = a.kd[ag * a.nl + r] + n0 * (D / 8);
+            if constexpr (BULK) {
 #pragma unroll
                 for (int it = 0; it < KCH; ++it) {
                     const uint32_t k = uint32_t(it) * 32u + uint32_t(lane);
-                    if (k < kvalid) st_stream_v4(kd + k, kout[it]);
+                    if (k < kvalid) osk[k] = kout[it];
+                }
+            } else {
+                for (int ag = 0; ag < a.na; ++ag) {
+                    uint4 *kd = a.kd[ag * a.nl + r] + n0 * (D / 8);
+#pragma unroll
+                    for (int it = 0; it < KCH; ++it) {
+                        const uint32_t k = uint32_t(it) * 32u + uint32_t(lane);
+                        if (k < kvalid) st_stream_v4(kd + k, kout[it]);
+                    }
                 }
             }
         }
@@ -150,7 +187,21 @@ __device__ __forceinline__ void decode_units(const DecodeArgs &a, uint8_t (*stag
             vout[j] = make_uint4(pack_bf16x2(y0.x, y0.y), pack_bf16x2(y1.x, y1.y), pack_bf16x2(y2.x, y2.y),
                                  pack_bf16x2(y3.x, y3.y));
         }
-        if (valid) {
+        if constexpr (BULK) {
+            if (valid) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) osv[g * CPV + j * LPV + l] = vout[j];
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            // lane a sends the unit (cnt contiguous vectors of keys and of values) to agent a
+            const uint32_t nbytes = cnt * uint32_t(D) * 2u;
+            for (int ag = lane; ag < a.na; ag += 32) {
+                bulk_store(a.kd[ag * a.nl + r] + n0 * (D / 8), osk, nbytes);
+                bulk_store(a.vd[ag * a.nl + r] + n0 * CPV, osv, nbytes);
+            }
+            if (lane < a.na) bulk_commit();
+        } else if (valid) {
             for (int ag = 0; ag < a.na; ++ag) {
                 uint4 *vd = a.vd[ag * a.nl + r] + n * CPV;
 #pragma unroll
@@ -158,12 +209,17 @@ __device__ __forceinline__ void decode_units(const DecodeArgs &a, uint8_t (*stag
             }
         }
     }
+    if constexpr (BULK) bulk_wait_all();
 }
 
-template <int D>
+// BULK: fan-out by bulk copies (several agents); otherwise direct streaming
+// stores from registers (one agent: the copies would be too few to pay).
+template <int D, bool BULK>
 __global__ void __launch_bounds__(DEC_THREADS, 4) decode_fanout(const __grid_constant__ DecodeArgs a) {
     __shared__ __align__(16) uint8_t stage[DEC_WARPS][384 + 16];
     __shared__ float2 pair_lut[64];
+    // per warp: one decoded unit (keys, then values) for the bulk copies
+    __shared__ __align__(128) uint4 ostage[BULK ? DEC_WARPS * 2 * (32 / (D / 32)) * (D / 8) : 1];
 
     if (threadIdx.x < 64) {
         const float ca = centroid_e4(threadIdx.x & 7u), cb = centroid_e4(threadIdx.x >> 3);
@@ -181,25 +237,33 @@ __global__ void __launch_bounds__(DEC_THREADS, 4) decode_fanout(const __grid_con
         return;
     }
     if (kmode == KVP_K_Q8_0)
-        decode_units<D, true>(a, stage, pair_lut);
+        decode_units<D, true, BULK>(a, stage, pair_lut, ostage);
     else
-        decode_units<D, false>(a, stage, pair_lut);
+        decode_units<D, false, BULK>(a, stage, pair_lut, ostage);
 }
 
 
-template <int D>
+template <int D, bool BULK>
 static int decode_grid(uint64_t total_units) {
+    const uint64_t want = (total_units + DEC_WARPS - 1) / DEC_WARPS;
+    if (BULK) {
+        // One unit per warp: every warp decodes one tile, hands its copies to
+        // the bulk-copy engine and retires, so as many units as the SMs can
+        // hold are being written at any time (measured on the 4K/15-agent
+        // pool: 1.242 ms with three resident grids' worth of blocks, 1.183 ms
+        // with one unit per warp; 2.88 -> 2.69 ms on the 32K/4-agent pool).
+        return int(want < 1 ? 1 : (want < 0x7FFFFFFFull ? want : 0x7FFFFFFFull));
+    }
     static int occ[2] = {0, 0};
     int &o = occ[D == 128 ? 1 : 0];
     if (o == 0) {
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, decode_fanout<D>, DEC_THREADS, 0) != cudaSuccess || o < 1)
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, decode_fanout<D, false>, DEC_THREADS, 0) != cudaSuccess ||
+            o < 1)
             o = 1;
     }
-    // Three resident grids' worth of blocks: each resident block's grid-stride
-    // walk then strides over units the later blocks will write, spreading the
-    // concurrent stores over more of every destination (measured 7-9 % faster
-    // than a single resident grid on the 4K/15-agent and 32K/4-agent pools).
-    const uint64_t want = (total_units + DEC_WARPS - 1) / DEC_WARPS;
+    // Direct stores: three resident grids' worth of blocks, each block's
+    // grid-stride walk spreading the concurrent stores over more of the
+    // destination (measured 7-9 % faster than a single resident grid).
     const uint64_t cap = uint64_t(sm_count()) * uint64_t(o) * 3u;
     return int(want < cap ? (want < 1 ? 1 : want) : cap);
 }
@@ -253,10 +317,17 @@ extern "C" int kvpool_decode_into(const void *pool, const kvp_shape *s, int lb, 
                     a.vd[ag * nl + r] = static_cast<uint4 *>(v_dst[size_t(a0 + ag) * L + l0 + r]);
                 }
             const uint64_t units = upl * uint64_t(nl);
-            if (a.d == 128)
-                decode_fanout<128><<<decode_grid<128>(units), DEC_THREADS, 0, st>>>(a);
-            else
-                decode_fanout<64><<<decode_grid<64>(units), DEC_THREADS, 0, st>>>(a);
+            // bulk copies pay from DEC_BULK_MIN_AGENTS destinations per unit up
+            if (nag >= DEC_BULK_MIN_AGENTS) {
+                if (a.d == 128)
+                    decode_fanout<128, true><<<decode_grid<128, true>(units), DEC_THREADS, 0, st>>>(a);
+                else
+                    decode_fanout<64, true><<<decode_grid<64, true>(units), DEC_THREADS, 0, st>>>(a);
+            } else if (a.d == 128) {
+                decode_fanout<128, false><<<decode_grid<128, false>(units), DEC_THREADS, 0, st>>>(a);
+            } else {
+                decode_fanout<64, false><<<decode_grid<64, false>(units), DEC_THREADS, 0, st>>>(a);
+            }
             ++launches;
         }
     }
