@@ -932,27 +932,12 @@ int orc_card_unpack_at(const uint8_t *card, int64_t pos_dst, const float *w, uin
 /* shared pool.                                                                */
 /* ------------------------------------------------------------------------- */
 
-/* One decode step of attention for n_agents agents against layer `layer` of
- * the pool: for agent a and query head j (GQA: query head j reads KV head
- * j / (n_q_heads / H)),
- *   s_t   = scale * (q . k_t),        k_t = q_t * s_l  (q8_0 pools: q_t * s_b
- *                                     per 32-element block; exact, fp64)
- *   p_t   = exp(s_t - max s) / sum,   v_t = sigma_h * (H_d c_t) / sqrt(d)
- *   out   = sum_t p_t v_t,            lse = log(sum_t exp(s_t))
- * over the T pooled tokens.  q: bf16 [n_agents][n_q_heads][d]; out:
- * [n_agents][n_q_heads][d]; lse: [n_agents][n_q_heads].  Keys and values are
- * dequantized exactly (no bf16 rounding).  Returns 0, or -1 on a bad header
- * or head count. */
-int orc_pool_attend(const uint8_t *pool, int layer, int n_agents, int n_q_heads, const uint16_t *q,
-                    double scale, double *out, double *lse)
+/* Keys and values of every KV head of one pool layer, dequantized exactly:
+ * k = q * s_l (format 1: q * s_b of the key's 32-key block) and
+ * v = sigma_h * (H_d c) / sqrt(d), as fp64 [H][T][d] arrays (caller frees). */
+static void attend_dequant(const uint8_t *pool, orc_pool_geom g, int layer, int H, int d, int T, int k_mode,
+                           double **kf_out, double **vf_out)
 {
-    if (get32(pool) != 0x4C50564Bu || get32(pool + 4) != 1u) return -1;
-    int L = (int)get32(pool + 8), H = (int)get32(pool + 12);
-    int d = (int)get32(pool + 16), T = (int)get32(pool + 20);
-    if (layer < 0 || layer >= L || n_q_heads % H != 0) return -1;
-    const int k_mode = (int)get32(pool + 28);
-    if (k_mode != 0 && k_mode != 1) return -1;
-    orc_pool_geom g = pool_geom(L, H, d, T);
     const uint8_t *lay = pool + g.off_layers + (uint64_t)layer * g.layer_stride;
     const uint8_t *ks = pool + g.off_kscales + (uint64_t)layer * (uint64_t)H * T * (uint64_t)(d / 32) * 2u;
     float s;
@@ -960,8 +945,6 @@ int orc_pool_attend(const uint8_t *pool, int layer, int n_agents, int n_q_heads,
     const int8_t *kc = (const int8_t *)lay;
     const uint8_t *vc = lay + g.sec_v;
     const uint8_t *sg = lay + g.sec_sigma;
-    const int grp = n_q_heads / H;
-    /* dequantized values of every KV head, exact */
     double *kf = (double *)malloc(sizeof(double) * (size_t)H * T * d);
     double *vf = (double *)malloc(sizeof(double) * (size_t)H * T * d);
     for (int64_t n = 0; n < (int64_t)H * T; n++) {
@@ -984,6 +967,35 @@ int orc_pool_attend(const uint8_t *pool, int layer, int n_agents, int n_q_heads,
         double sig = orc_f16_to_f64(sh);
         for (int i = 0; i < d; i++) vf[n * d + i] = sig * z[i] / sqrt((double)d);
     }
+    *kf_out = kf;
+    *vf_out = vf;
+}
+
+/* One decode step of attention for n_agents agents against layer `layer` of
+ * the pool: for agent a and query head j (GQA: query head j reads KV head
+ * j / (n_q_heads / H)),
+ *   s_t   = scale * (q . k_t),        k_t = q_t * s_l  (q8_0 pools: q_t * s_b
+ *                                     per 32-element block; exact, fp64)
+ *   p_t   = exp(s_t - max s) / sum,   v_t = sigma_h * (H_d c_t) / sqrt(d)
+ *   out   = sum_t p_t v_t,            lse = log(sum_t exp(s_t))
+ * over the T pooled tokens.  q: bf16 [n_agents][n_q_heads][d]; out:
+ * [n_agents][n_q_heads][d]; lse: [n_agents][n_q_heads].  Keys and values are
+ * dequantized exactly (no bf16 rounding).  Returns 0, or -1 on a bad header
+ * or head count. */
+int orc_pool_attend(const uint8_t *pool, int layer, int n_agents, int n_q_heads, const uint16_t *q,
+                    double scale, double *out, double *lse)
+{
+    if (get32(pool) != 0x4C50564Bu || get32(pool + 4) != 1u) return -1;
+    int L = (int)get32(pool + 8), H = (int)get32(pool + 12);
+    int d = (int)get32(pool + 16), T = (int)get32(pool + 20);
+    if (layer < 0 || layer >= L || n_q_heads % H != 0) return -1;
+    const int k_mode = (int)get32(pool + 28);
+    if (k_mode != 0 && k_mode != 1) return -1;
+    orc_pool_geom g = pool_geom(L, H, d, T);
+    const int grp = n_q_heads / H;
+    /* dequantized keys and values of every KV head, exact */
+    double *kf, *vf;
+    attend_dequant(pool, g, layer, H, d, T, k_mode, &kf, &vf);
 #pragma omp parallel for schedule(static)
     for (int aj = 0; aj < n_agents * n_q_heads; aj++) {
         const int j = aj % n_q_heads;
@@ -1033,41 +1045,13 @@ int orc_pool_attend_lora(const uint8_t *pool, int layer, int n_agents, int n_q_h
     int H = (int)get32(pool + 12), d = (int)get32(pool + 16), T = (int)get32(pool + 20);
     if (n_q_heads % H != 0 || rank < 1) return -1;
     const int grp = n_q_heads / H;
-    /* keys and base values, dequantized exactly as in orc_pool_attend */
     int L = (int)get32(pool + 8);
     if (layer < 0 || layer >= L) return -1;
     const int k_mode = (int)get32(pool + 28);
     if (k_mode != 0 && k_mode != 1) return -1;
     orc_pool_geom g = pool_geom(L, H, d, T);
-    const uint8_t *lay = pool + g.off_layers + (uint64_t)layer * g.layer_stride;
-    const uint8_t *ks = pool + g.off_kscales + (uint64_t)layer * (uint64_t)H * T * (uint64_t)(d / 32) * 2u;
-    float s;
-    memcpy(&s, pool + g.off_scales + 4u * (uint64_t)layer, 4);
-    const int8_t *kc = (const int8_t *)lay;
-    const uint8_t *vc = lay + g.sec_v;
-    const uint8_t *sg = lay + g.sec_sigma;
-    double *kf = (double *)malloc(sizeof(double) * (size_t)H * T * d);
-    double *vb = (double *)malloc(sizeof(double) * (size_t)H * T * d);
-    for (int64_t n = 0; n < (int64_t)H * T; n++) {
-        uint8_t codes[128];
-        uint16_t sh;
-        double z[128];
-        for (int i = 0; i < d; i++) {
-            double sk = (double)s;
-            if (k_mode == 1) {
-                uint16_t sb;
-                memcpy(&sb, ks + 2u * ((uint64_t)n * (uint64_t)(d / 32) + (uint64_t)(i / 32)), 2);
-                sk = orc_f16_to_f64(sb);
-            }
-            kf[n * d + i] = (double)kc[n * d + i] * sk;
-        }
-        orc_unpack3(vc + (uint64_t)n * (uint64_t)(3 * d / 8), d, codes);
-        memcpy(&sh, sg + 2u * (uint64_t)n, 2);
-        for (int i = 0; i < d; i++) z[i] = CENTROID[codes[i]];
-        orc_fwht(z, d);
-        double sig = orc_f16_to_f64(sh);
-        for (int i = 0; i < d; i++) vb[n * d + i] = sig * z[i] / sqrt((double)d);
-    }
+    double *kf, *vb;  /* keys and base values, dequantized exactly */
+    attend_dequant(pool, g, layer, H, d, T, k_mode, &kf, &vb);
 #pragma omp parallel for schedule(static)
     for (int aj = 0; aj < n_agents * n_q_heads; aj++) {
         const int a = aj / n_q_heads, j = aj % n_q_heads;

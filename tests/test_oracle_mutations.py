@@ -39,8 +39,10 @@ MUTANTS = [
     ("card params per group", "+ (uint64_t)H * (uint64_t)(d / 32) * 4ull);", "+ (uint64_t)H * (uint64_t)(d / 32) * 2ull);"),
     ("pool sigma offset", "g.sec_sigma = al256(g.sec_v + nv * (uint64_t)(3 * d / 8));", "g.sec_sigma = al256(g.sec_v + nv * (uint64_t)(d / 2));"),
     ("k absmax skips sign", "double a = fabs(orc_bf16_to_f64(k[i]));", "double a = orc_bf16_to_f64(k[i]);"),
-    ("attend GQA head map", "const int h = j / grp;", "const int h = j % H;"),
-    ("attend lse drops max", "lse[aj] = mx + log(sum);", "lse[aj] = log(sum);"),
+    ("attend GQA head map", "const int j = aj % n_q_heads;\n        const int h = j / grp;",
+     "const int j = aj % n_q_heads;\n        const int h = j % H;"),
+    ("attend lse drops max", "lse[aj] = mx + log(sum);\n        free(sc);\n    }",
+     "lse[aj] = log(sum);\n        free(sc);\n    }"),
     ("realign shift reversed", "const double delta = (double)(pos_dst - pos_src);",
      "const double delta = (double)(pos_src - pos_dst);"),
     ("realign sine sign", "row[i] = orc_f64_to_bf16(a * cs[i] - c * sn[i]);",
@@ -78,15 +80,34 @@ def _build(text, out):
     assert r.returncode == 0, r.stderr
 
 
-@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
-def test_pins_catch_mutant(name, old, new):
+def _run_mutant(old, new):
+    """Build the oracle with one mistake planted and run the pin suite against
+    it in a child process; returns (site count, return code, output tail)."""
     text = open(SRC).read()
-    assert text.count(old) == 1, "mutation site not found exactly once: %r" % old
+    count = text.count(old)
+    if count != 1:
+        return count, None, ""
     with tempfile.TemporaryDirectory() as tmp:
         lib = os.path.join(tmp, "mutant.so")
         _build(text.replace(old, new), lib)
-        env = dict(os.environ, KV_ORACLE_LIB=lib, PYTHONPATH=ROOT)
+        env = dict(os.environ, KV_ORACLE_LIB=lib, PYTHONPATH=ROOT, OMP_NUM_THREADS="2")
         r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                             os.path.join(ROOT, "tests", "test_oracle_pins.py")],
                            capture_output=True, text=True, env=env, cwd=ROOT, timeout=600)
-    assert r.returncode != 0, "mutant '%s' passed every pin:\n%s" % (name, r.stdout[-2000:])
+    return count, r.returncode, r.stdout[-2000:]
+
+
+@pytest.fixture(scope="module")
+def mutant_results():
+    """Every mutant's run, eight child processes at a time."""
+    import concurrent.futures as cf
+    with cf.ThreadPoolExecutor(max_workers=8) as ex:
+        futs = {name: ex.submit(_run_mutant, old, new) for name, old, new in MUTANTS}
+        return {name: f.result() for name, f in futs.items()}
+
+
+@pytest.mark.parametrize("name", [m[0] for m in MUTANTS])
+def test_pins_catch_mutant(name, mutant_results):
+    count, rc, out = mutant_results[name]
+    assert count == 1, "mutation site found %d times, not once" % count
+    assert rc != 0, "mutant '%s' passed every pin:\n%s" % (name, out)
