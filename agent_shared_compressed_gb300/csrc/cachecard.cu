@@ -214,18 +214,19 @@ __global__ void __launch_bounds__(CARD_THREADS, 4) card_pack(const __grid_consta
                 w[4 * q + 3] = v.w;
             }
             float2 x[16];
-            float mn0 = bf16_lo(w[0]), mx0 = mn0, mn1 = bf16_hi(w[0]), mx1 = mn1;
+            // min / max on the packed bf16 pairs (exact; NaN is ignored as by fminf / fmaxf)
+            __nv_bfloat162 mnp = *reinterpret_cast<const __nv_bfloat162 *>(&w[0]), mxp = mnp;
             float2 nfacc = make_float2(0.0f, 0.0f);
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
+                const __nv_bfloat162 pr = *reinterpret_cast<const __nv_bfloat162 *>(&w[i]);
+                mnp = __hmin2(mnp, pr);
+                mxp = __hmax2(mxp, pr);
                 x[i] = make_float2(bf16_lo(w[i]), bf16_hi(w[i]));
-                mn0 = fminf(mn0, x[i].x);
-                mx0 = fmaxf(mx0, x[i].x);
-                mn1 = fminf(mn1, x[i].y);
-                mx1 = fmaxf(mx1, x[i].y);
                 nfacc = __ffma2_rn(x[i], make_float2(0.0f, 0.0f), nfacc);  // NaN iff Inf/NaN seen
             }
-            const float mn = fminf(mn0, mn1), mx = fmaxf(mx0, mx1);
+            const float mn = fminf(__low2float(mnp), __high2float(mnp));
+            const float mx = fmaxf(__low2float(mxp), __high2float(mxp));
             const bool nf = (nfacc.x != nfacc.x) || (nfacc.y != nfacc.y);
             const uint32_t sb = group_scale_f16(mx, mn, qmax, rcp_qmax);
             const uint32_t zb = __half_as_ushort(__float2half_rn(mn));
@@ -244,6 +245,8 @@ __global__ void __launch_bounds__(CARD_THREADS, 4) card_pack(const __grid_consta
             const bool clamp = !(tmn >= lo_c && tmx <= hi_c);
             const float2 negz = make_float2(-zf, -zf), inv2 = make_float2(inv, inv);
             const float2 mg = make_float2(RNE_MAGIC_C, RNE_MAGIC_C);
+            // q[i]: the code in the low byte, higher bits not cleared (the packing below
+            // selects or masks the low bits)
             uint32_t q[32];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
@@ -252,8 +255,8 @@ __global__ void __launch_bounds__(CARD_THREADS, 4) card_pack(const __grid_consta
                     tf.x = fminf(fmaxf(tf.x, lo_c), hi_c);
                     tf.y = fminf(fmaxf(tf.y, lo_c), hi_c);
                 }
-                q[2 * i] = __float_as_uint(tf.x) & 0xFFu;
-                q[2 * i + 1] = __float_as_uint(tf.y) & 0xFFu;
+                q[2 * i] = __float_as_uint(tf.x);
+                q[2 * i + 1] = __float_as_uint(tf.y);
             }
             if (b == 8) {
                 uint4 *o = reinterpret_cast<uint4 *>(codes) + 2 * gi;
@@ -264,7 +267,7 @@ __global__ void __launch_bounds__(CARD_THREADS, 4) card_pack(const __grid_consta
             } else if (b == 4) {
                 uint32_t by[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) by[i] = q[2 * i] | (q[2 * i + 1] << 4);
+                for (int i = 0; i < 16; ++i) by[i] = (q[2 * i] & 0xFu) | ((q[2 * i + 1] & 0xFu) << 4);
                 reinterpret_cast<uint4 *>(codes)[gi] =
                     make_uint4(pack_bytes4(by[0], by[1], by[2], by[3]), pack_bytes4(by[4], by[5], by[6], by[7]),
                                pack_bytes4(by[8], by[9], by[10], by[11]), pack_bytes4(by[12], by[13], by[14], by[15]));
@@ -272,7 +275,8 @@ __global__ void __launch_bounds__(CARD_THREADS, 4) card_pack(const __grid_consta
                 uint32_t by[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
-                    by[i] = q[4 * i] | (q[4 * i + 1] << 2) | (q[4 * i + 2] << 4) | (q[4 * i + 3] << 6);
+                    by[i] = (q[4 * i] & 3u) | ((q[4 * i + 1] & 3u) << 2) | ((q[4 * i + 2] & 3u) << 4) |
+                            ((q[4 * i + 3] & 3u) << 6);
                 reinterpret_cast<uint2 *>(codes)[gi] =
                     make_uint2(pack_bytes4(by[0], by[1], by[2], by[3]), pack_bytes4(by[4], by[5], by[6], by[7]));
             }
