@@ -149,7 +149,9 @@ __device__ void absmax_slice(const EncodeArgs &a, int l, uint32_t p, uint64_t po
     const uint64_t c0 = uint64_t(p) * a.chunks_per_slice;
     const uint64_t c1 = min(c0 + a.chunks_per_slice, a.chunks);
     const uint4 *src = a.k[l];
-    uint32_t mlo = 0, mhi = 0;
+    // per-halfword unsigned max of the bf16 patterns with the sign cleared
+    // (Inf / NaN patterns sort above every finite value)
+    uint32_t m2 = 0;
     uint64_t c = c0 + threadIdx.x;
     for (; c + 7 * ENC_THREADS < c1; c += 8 * ENC_THREADS) {
         uint4 w[8];
@@ -157,17 +159,16 @@ __device__ void absmax_slice(const EncodeArgs &a, int l, uint32_t p, uint64_t po
         for (int u = 0; u < 8; ++u) w[u] = ld_v4_policy(src + c + u * ENC_THREADS, pol);
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-            mlo = max(mlo, max(max(w[u].x & 0x7FFFu, w[u].y & 0x7FFFu), max(w[u].z & 0x7FFFu, w[u].w & 0x7FFFu)));
-            mhi = max(mhi, max(max(w[u].x & 0x7FFF0000u, w[u].y & 0x7FFF0000u),
-                               max(w[u].z & 0x7FFF0000u, w[u].w & 0x7FFF0000u)));
+            m2 = __vmaxu2(m2, __vmaxu2(w[u].x & 0x7FFF7FFFu, w[u].y & 0x7FFF7FFFu));
+            m2 = __vmaxu2(m2, __vmaxu2(w[u].z & 0x7FFF7FFFu, w[u].w & 0x7FFF7FFFu));
         }
     }
     for (; c < c1; c += ENC_THREADS) {
         const uint4 w = ld_v4_policy(src + c, pol);
-        mlo = max(mlo, max(max(w.x & 0x7FFFu, w.y & 0x7FFFu), max(w.z & 0x7FFFu, w.w & 0x7FFFu)));
-        mhi = max(mhi, max(max(w.x & 0x7FFF0000u, w.y & 0x7FFF0000u), max(w.z & 0x7FFF0000u, w.w & 0x7FFF0000u)));
+        m2 = __vmaxu2(m2, __vmaxu2(w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu));
+        m2 = __vmaxu2(m2, __vmaxu2(w.z & 0x7FFF7FFFu, w.w & 0x7FFF7FFFu));
     }
-    uint32_t m = max(mlo, mhi >> 16);
+    uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
     m = __reduce_max_sync(0xffffffffu, m);
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
     __syncthreads();
