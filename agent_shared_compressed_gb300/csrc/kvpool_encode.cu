@@ -636,14 +636,17 @@ __device__ uint32_t q8_key_task(const EncodeArgs &a, int l, uint64_t c0, uint64_
     for (int it = 0; it < Q8_ITERS; ++it) {
         const uint64_t c = c0 + uint64_t(it) * 32u + uint64_t(lane);
         const uint32_t ws[4] = {w[it].x, w[it].y, w[it].z, w[it].w};
-        uint32_t m = 0, bad = 0;
+        // per-halfword max of the finite keys' sign-cleared patterns
+        uint32_t m2 = 0, bad = 0;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const uint32_t lo = ws[i] & 0x7FFFu, hi = (ws[i] >> 16) & 0x7FFFu;
-            bad |= uint32_t(lo >= 0x7F80u) | uint32_t(hi >= 0x7F80u);
-            m = max(m, lo < 0x7F80u ? lo : 0u);
-            m = max(m, hi < 0x7F80u ? hi : 0u);
+            const uint32_t ab = ws[i] & 0x7FFF7FFFu;
+            const uint32_t nf = __vcmpgeu2(ab, 0x7F807F80u);  // 0xFFFF in each Inf / NaN half
+            bad |= nf;
+            m2 = __vmaxu2(m2, ab & ~nf);
         }
+        uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+        bad = bad != 0u;
         m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
         m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
         bad |= __shfl_xor_sync(0xffffffffu, bad, 1);
