@@ -579,19 +579,23 @@ __global__ void __launch_bounds__(ENC_THREADS, 3) encode_pool(const __grid_const
 // [-127, 127].  No layer-wide maximum, so one sweep encodes keys and values:
 // warp tasks are, per layer, Q8_TASK_CHUNKS 16-byte key chunks (4 lanes per
 // 32-key block: two shuffles give the block's maximum) and batches of
-// Q8_VSTEPS value steps.  The fp16 scale is the fp32 quotient rounded to
-// fp16: the real quotient max|k|/127 never lies within fp32 rounding of an
-// fp16 midpoint (a bf16 over 127 is at least 2^-20 relative from any 12-bit
-// fraction), so the two roundings give the correctly rounded fp16.
+// Q8_VSTEPS value steps.  The fp16 scale is fp16(max|k| * fl(1/127)): that
+// fp32 product is within 2^-23 relative of the real quotient max|k|/127,
+// which never lies closer than 2^-20 relative to an fp16 midpoint (a bf16
+// over 127 is at least that far from any 12-bit fraction), so the fp16
+// rounding is the correct one.
 // ---------------------------------------------------------------------------
 constexpr int Q8_ITERS = 4;
 constexpr uint64_t Q8_TASK_CHUNKS = 32ull * Q8_ITERS;
 constexpr int Q8_VSTEPS = 8;  // value steps per warp task, each prefetched while the previous is encoded
+constexpr float Q8_INV127 = 1.0f / 127.0f;
 
-// Fast path as k_quant8: the code is the low byte of fma(k, 1/s, 1.5*2^23).
-// The chunk is redone exactly when an estimate is within 1e-4 of a
-// half-integer or not finite, and when s is an fp16 subnormal (then |k/s|
-// may exceed 127.5 and the code is clamped); non-finite keys code as 0.
+// Fast path as k_quant8: the code is the low byte of fma(k, r, 1.5*2^23),
+// with r an approximate 1/s (relative error below 2^-21, so k*r is within
+// 4e-5 of k/s for |k/s| <= 127.1).  The chunk is redone exactly when an
+// estimate is within 1e-4 of a half-integer or not finite, and when s is an
+// fp16 subnormal (then |k/s| may exceed 127.5 and the code is clamped);
+// non-finite keys code as 0.
 __device__ __forceinline__ uint2 k_quant8_block(uint4 w, float s, float rcp, bool subnormal_scale) {
     const float k[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
                         bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
@@ -636,22 +640,31 @@ __device__ uint32_t q8_key_task(const EncodeArgs &a, int l, uint64_t c0, uint64_
     for (int it = 0; it < Q8_ITERS; ++it) {
         const uint64_t c = c0 + uint64_t(it) * 32u + uint64_t(lane);
         const uint32_t ws[4] = {w[it].x, w[it].y, w[it].z, w[it].w};
-        // per-halfword max of the finite keys' sign-cleared patterns
-        uint32_t m2 = 0, bad = 0;
+        // block maximum: per-halfword max of the sign-cleared patterns; Inf /
+        // NaN patterns sort above every finite one, so a block holding one is
+        // redone with those halves masked out (its maximum over finite keys)
+        uint32_t m2 = 0;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t ab = ws[i] & 0x7FFF7FFFu;
-            const uint32_t nf = __vcmpgeu2(ab, 0x7F807F80u);  // 0xFFFF in each Inf / NaN half
-            bad |= nf;
-            m2 = __vmaxu2(m2, ab & ~nf);
-        }
+        for (int i = 0; i < 4; ++i) m2 = __vmaxu2(m2, ws[i] & 0x7FFF7FFFu);
         uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
-        bad = bad != 0u;
         m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
         m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
-        bad |= __shfl_xor_sync(0xffffffffu, bad, 1);
-        bad |= __shfl_xor_sync(0xffffffffu, bad, 2);
-        const __half sh = __float2half_rn(__fdiv_rn(__uint_as_float(m << 16), 127.0f));
+        const bool bad = m >= 0x7F80u;
+        if (__any_sync(0xffffffffu, bad)) {
+            uint32_t f2 = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t ab = ws[i] & 0x7FFF7FFFu;
+                f2 = __vmaxu2(f2, ab & ~__vcmpgeu2(ab, 0x7F807F80u));  // 0xFFFF in each Inf / NaN half
+            }
+            uint32_t f = max(f2 & 0xFFFFu, f2 >> 16);
+            f = max(f, __shfl_xor_sync(0xffffffffu, f, 1));
+            f = max(f, __shfl_xor_sync(0xffffffffu, f, 2));
+            if (bad) m = f;
+        }
+        // fp16(max|k| * fl(1/127)): for every finite bf16 maximum this is the
+        // fp16 nearest to the real max|k|/127 (checked over all of them)
+        const __half sh = __float2half_rn(__fmul_rn(__uint_as_float(m << 16), Q8_INV127));
         const uint16_t sb = __half_as_ushort(sh);
         const float s = __half2float(sh);
         if (c < a.chunks) {
@@ -660,7 +673,7 @@ __device__ uint32_t q8_key_task(const EncodeArgs &a, int l, uint64_t c0, uint64_
             else if ((sb & 0x7C00u) == 0x7C00u)
                 flags |= FLAG_RANGE;
             const uint2 codes = (s > 0.0f && s <= 65504.0f)
-                                    ? k_quant8_block(w[it], s, __frcp_rn(s), s < 0x1p-14f)
+                                    ? k_quant8_block(w[it], s, __fdividef(1.0f, s), s < 0x1p-14f)
                                     : make_uint2(0, 0);
             dst[c] = codes;
             if ((lane & 3) == 0) ksc[c >> 2] = sb;
