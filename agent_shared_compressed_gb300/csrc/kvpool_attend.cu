@@ -12,9 +12,10 @@
 // query at the end.
 //
 // attend_split: one block per (KV head, token split).  The split's 64-token
-// sub-chunks are staged in shared memory, double-buffered (keys as exact bf16
-// integers, centroids as fp16, both [token][dim]), with the next sub-chunk's
-// raw bytes already in registers while the current one is multiplied.  Warp
+// sub-chunks arrive as raw pool bytes in a shared-memory ring that bulk
+// copies (the TMA engine) keep up to four sub-chunks ahead; the current one
+// is staged from there into tiles (keys as exact bf16 integers, centroids as
+// fp16, both [token][dim]) and multiplied.  Warp
 // (mi, th) owns query rows mi*16.. and a token slice th of every sub-chunk; it
 // runs its own online softmax over that slice with warp-level tensor-core
 // products: S = Q K^T (bf16 in, fp32 accumulate: exact products) and
@@ -77,85 +78,138 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
+// Bulk copies (the TMA engine's 1-D form) from global into shared memory,
+// each completing on an mbarrier that counts the bytes still to land.
+__device__ __forceinline__ uint32_t att_smem(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void att_mbar_init(uint32_t bar) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void att_mbar_expect(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool att_mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0u;
+}
+// Waits for the completion of the barrier's phase of the given parity; gives
+// up (false) after about half a second.
+constexpr uint32_t ATT_WAIT_LIMIT = 1u << 22;
+__device__ __forceinline__ bool att_mbar_wait(uint32_t bar, uint32_t parity) {
+    for (uint32_t i = 0; i < ATT_WAIT_LIMIT; ++i) {
+        if (att_mbar_try(bar, parity)) return true;
+        if (i >= 16) __nanosleep(128);
+    }
+    return false;
+}
+__device__ __forceinline__ void att_bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+// Orders this thread's earlier generic-proxy accesses of shared memory before
+// its later bulk copies into it.
+__device__ __forceinline__ void att_fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// Shared memory of the split kernel (bytes).  A ring of NST raw sub-chunks
+// (the pool's bytes as they are, filled by bulk copies), then the staged
+// tiles of the current sub-chunk: Q, K as exact bf16 integers, values as fp16
+// centroids (rows of RW words: 16-byte multiples, conflict-free ldmatrix),
+// sigma, the centroid pair table, q8_0 block scales and the low-rank tile.
+// After the loop the warps' states are merged from offset BAR_BYTES on.
 template <int D, int R = 0>
 struct AttendSmem {
-    static constexpr int RW = D / 2 + 4;  // 32-bit words per Q / K / C row (16-B multiple, conflict-free ldmatrix)
-    static constexpr int LW = R / 2 + 4;  // words per low-rank row (LoRA attention)
-    static constexpr int MS = D + R + 8;  // floats per row of a warp's merge slot (conflict-free float2 stores)
-    static constexpr size_t q_words = size_t(ATT_MT) * RW;
-    static constexpr size_t tile_words = size_t(ATT_TC) * RW;  // one K or C buffer
-    static constexpr size_t ksb_words = size_t(ATT_TC) * (D / 32);  // one buffer of q8_0 key block scales
-    static constexpr size_t lr_words = R > 0 ? size_t(ATT_TC) * LW : 0;  // one buffer of the low-rank tile
-    static constexpr size_t stage_words = q_words + 4 * tile_words + 2 * ATT_TC + 64 + 2 * ksb_words +
-                                          2 * lr_words;  // Q, K[2], C[2], sig[2], lut, ksb[2], lr[2]
-    static constexpr size_t merge_words = size_t(ATT_WARPS) * (16 * MS + 32);
-    static constexpr size_t bytes = 4 * (stage_words > merge_words ? stage_words : merge_words);
+    static constexpr int NST = R > 0 ? 3 : 4;  // ring depth
+    static constexpr int RW = D / 2 + 4;       // 32-bit words per Q / K / C row
+    static constexpr int LW = R / 2 + 4;       // words per low-rank row (LoRA attention)
+    static constexpr int MS = D + R + 8;       // floats per row of a warp's merge slot (conflict-free float2 stores)
+    // one raw slot; the V, sigma and block-scale windows start at the 16-byte
+    // boundary below their first byte, hence 16 bytes of slack each
+    static constexpr uint32_t RAW_K = 0;                                   // [64][D] int8 codes
+    static constexpr uint32_t RAW_V = RAW_K + ATT_TC * D;                  // [64][3D/8] code bytes
+    static constexpr uint32_t RAW_SG = RAW_V + ATT_TC * 3 * D / 8 + 16;    // [64] fp16 sigma
+    static constexpr uint32_t RAW_KS = RAW_SG + ATT_TC * 2 + 16;           // [64][D/32] fp16 block scales
+    static constexpr uint32_t RAW_LR = RAW_KS + ATT_TC * (D / 32) * 2 + 16;  // [64][R] bf16 low-rank values
+    static constexpr uint32_t SLOT = RAW_LR + ATT_TC * R * 2;
+    static constexpr uint32_t BAR_BYTES = 64;
+    static constexpr uint32_t OFF_RING = BAR_BYTES;
+    static constexpr uint32_t OFF_Q = OFF_RING + NST * SLOT;
+    static constexpr uint32_t OFF_K = OFF_Q + ATT_MT * RW * 4;
+    static constexpr uint32_t OFF_C = OFF_K + ATT_TC * RW * 4;
+    static constexpr uint32_t OFF_SIG = OFF_C + ATT_TC * RW * 4;
+    static constexpr uint32_t OFF_LUT = OFF_SIG + ATT_TC * 4;
+    static constexpr uint32_t OFF_KSB = OFF_LUT + 64 * 4;
+    static constexpr uint32_t OFF_LS = OFF_KSB + ATT_TC * (D / 32) * 4;
+    static constexpr uint32_t STAGE_END = OFF_LS + (R > 0 ? ATT_TC * LW * 4 : 0);
+    static constexpr uint32_t MERGE_END = BAR_BYTES + ATT_WARPS * (16 * MS + 32) * 4;
+    static constexpr size_t bytes = STAGE_END > MERGE_END ? STAGE_END : MERGE_END;
+    static_assert(SLOT % 16 == 0 && RAW_V % 16 == 0 && RAW_SG % 16 == 0 && RAW_KS % 16 == 0 && RAW_LR % 16 == 0,
+                  "bulk-copy destinations are 16-byte aligned");
+    static_assert(NST * 8 <= BAR_BYTES, "one mbarrier per slot");
 };
 
-// Raw bytes of one sub-chunk held by one thread between load and staging.
-// Thread mapping: the eight lanes of a quarter-warp take eight consecutive
-// tokens of the same part of the row, so their 16-byte shared stores fall on
-// eight distinct bank groups (row strides are 4 words mod 32).
-//   keys:   token (tid & 7) + 8 * (tid >> 5), part (tid >> 3) & 3 of 4 (D/4 codes)
-//   values: token (tid & 7) + 8 * ((tid >> 3) / VPT), item (tid >> 3) % VPT (32 codes)
-template <int D>
-struct RawChunk {
-    uint4 k[D / 64];
-    uint32_t v[3];
-    uint32_t sig;  // fp16 bits of token tid's sigma (tid < 64)
-    uint32_t ksc;  // q8_0 keys: fp16 bits of block tid % (D/32) of token tid / (D/32)
-    uint4 lr;      // LoRA attention: 8 low-rank values (bf16) of token tid / (R/8), part tid % (R/8)
-};
-
+// Thread 0: the bulk copies of sub-chunk tokens t0 .. t0 + nt - 1 of KV head
+// (vbase / T) into one raw slot, completing on its barrier.  Every source is
+// a 16-byte aligned run inside its section (sections are 256-byte aligned):
+// keys exactly; value codes, sigma and block scales as the 16-byte aligned
+// window around their bytes.
 template <int D, bool Q8, int R>
-__device__ __forceinline__ void load_chunk(RawChunk<D> &r, const uint8_t *lay, const PoolGeom &geo, uint64_t vbase,
-                                           int t0, int T, int tid, const uint16_t *kscales, const uint16_t *vlr) {
-    constexpr int VPT = D / 32;  // 32-code value items per token
-    const int q = tid >> 3, l8 = tid & 7;
-    const int tk = t0 + l8 + 8 * (q >> 2);
-    if (tk < T) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(lay + (vbase + tk) * D + (q & 3) * (D / 4));
-#pragma unroll
-        for (int u = 0; u < D / 64; ++u) r.k[u] = ld_stream_v4(src + u);
-    } else {
-#pragma unroll
-        for (int u = 0; u < D / 64; ++u) r.k[u] = make_uint4(0, 0, 0, 0);
-    }
-    const int tv = t0 + l8 + 8 * (q / VPT);
-    if (q < 8 * VPT && tv < T) {
-        const uint8_t *src = lay + geo.sec_v + (vbase + tv) * (3 * D / 8) + (q % VPT) * 12;
-#pragma unroll
-        for (int u = 0; u < 3; ++u) r.v[u] = ld_stream_u32(src + 4 * u);
-    } else {
-        r.v[0] = r.v[1] = r.v[2] = 0u;
-    }
-    r.sig = 0u;
-    if (tid < ATT_TC && t0 + tid < T)
-        r.sig = reinterpret_cast<const uint16_t *>(lay + geo.sec_sigma)[vbase + t0 + tid];
+__device__ __forceinline__ void issue_chunk(uint8_t *raw, uint32_t bar, const uint8_t *lay, const PoolGeom &geo,
+                                            uint64_t vbase, int t0, int T, const uint16_t *kscales,
+                                            const uint16_t *vlr) {
+    using SM = AttendSmem<D, R>;
+    const uint32_t nt = uint32_t(min(ATT_TC, T - t0));
+    const uint64_t n0 = vbase + uint64_t(t0);
+    const uint8_t *ksrc = lay + n0 * D;
+    const uintptr_t v = reinterpret_cast<uintptr_t>(lay + geo.sec_v + n0 * (3 * D / 8));
+    const uintptr_t sg = reinterpret_cast<uintptr_t>(lay + geo.sec_sigma + n0 * 2);
+    const uint32_t kb = nt * D;
+    const uint32_t vb = uint32_t(align16(v + nt * (3 * D / 8)) - (v & ~uintptr_t(15)));
+    const uint32_t sb = uint32_t(align16(sg + nt * 2) - (sg & ~uintptr_t(15)));
+    uint32_t qb = 0, lb = 0;
+    uintptr_t qs = 0;
     if constexpr (Q8) {
-        r.ksc = 0u;
-        if (tid < ATT_TC * (D / 32) && t0 + tid / (D / 32) < T) r.ksc = kscales[(vbase + t0) * (D / 32) + tid];
+        qs = reinterpret_cast<uintptr_t>(kscales + n0 * (D / 32));
+        qb = uint32_t(align16(qs + nt * (D / 32) * 2) - (qs & ~uintptr_t(15)));
     }
-    if constexpr (R > 0) {
-        r.lr = make_uint4(0, 0, 0, 0);
-        if (tid < ATT_TC * (R / 8) && t0 + tid / (R / 8) < T)
-            r.lr = ld_stream_v4(vlr + uint64_t(t0) * R + uint64_t(tid) * 8);
-    }
+    if constexpr (R > 0) lb = nt * R * 2;
+    att_mbar_expect(bar, kb + vb + sb + qb + lb);
+    att_bulk_load(att_smem(raw + SM::RAW_K), ksrc, kb, bar);
+    att_bulk_load(att_smem(raw + SM::RAW_V), reinterpret_cast<const void *>(v & ~uintptr_t(15)), vb, bar);
+    att_bulk_load(att_smem(raw + SM::RAW_SG), reinterpret_cast<const void *>(sg & ~uintptr_t(15)), sb, bar);
+    if constexpr (Q8)
+        att_bulk_load(att_smem(raw + SM::RAW_KS), reinterpret_cast<const void *>(qs & ~uintptr_t(15)), qb, bar);
+    if constexpr (R > 0) att_bulk_load(att_smem(raw + SM::RAW_LR), vlr + uint64_t(t0) * R, lb, bar);
 }
 
-// Registers -> shared tiles: keys int8 -> exact bf16 (|q| <= 127 has at most
-// 7 significant bits); value codes -> fp16 centroids, two dims per word via
-// the pair table.
+// Raw slot -> staged tiles (whole block): keys int8 -> exact bf16 (|q| <= 127
+// has at most 7 significant bits); value codes -> fp16 centroids, two dims
+// per word via the pair table.  Tokens at or past T stage as zeros.  Thread
+// mapping: the eight lanes of a quarter-warp take eight consecutive tokens;
+// for keys each lane starts at a different 16-byte chunk of its token, so
+// the raw reads and the tile stores of a quarter-warp both fall on eight
+// distinct bank groups (d = 128).  voff / soff / qoff: where the value,
+// sigma and block-scale bytes start within their 16-byte aligned windows.
 template <int D, bool Q8, int R>
-__device__ __forceinline__ void stage_chunk(const RawChunk<D> &r, uint32_t *Kb, uint32_t *Cs, float *sig,
-                                            const uint32_t *lut, float *ksb, uint32_t *Ls, int tid) {
-    constexpr int RW = AttendSmem<D>::RW, VPT = D / 32;
+__device__ __forceinline__ void stage_raw(const uint8_t *raw, int t0, int T, int tid, uint32_t voff, uint32_t soff,
+                                          uint32_t qoff, uint32_t *Kb, uint32_t *Cs, float *sig, const uint32_t *lut,
+                                          float *ksb, uint32_t *Ls) {
+    using SM = AttendSmem<D, R>;
+    constexpr int RW = SM::RW, VPT = D / 32, CPT = D / 16;
     const int q = tid >> 3, l8 = tid & 7;
     {
-        uint32_t *row = Kb + (l8 + 8 * (q >> 2)) * RW + (q & 3) * (D / 8);
+        const int tl = l8 + 8 * (q >> 2);
+        const bool real = t0 + tl < T;
+        uint32_t *row = Kb + tl * RW;
 #pragma unroll
         for (int u = 0; u < D / 64; ++u) {
-            const uint32_t w4[4] = {r.k[u].x, r.k[u].y, r.k[u].z, r.k[u].w};
+            const int c = ((q & 3) * (D / 64) + u + l8) % CPT;  // 16-byte chunk of the token
+            const uint4 w = real ? *reinterpret_cast<const uint4 *>(raw + SM::RAW_K + tl * D + c * 16)
+                                 : make_uint4(0, 0, 0, 0);
+            const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
             uint32_t o[8];
 #pragma unroll
             for (int b = 0; b < 4; ++b) {
@@ -167,13 +221,21 @@ __device__ __forceinline__ void stage_chunk(const RawChunk<D> &r, uint32_t *Kb, 
                 o[2 * b] = __byte_perm(__float_as_uint(f[0]), __float_as_uint(f[1]), 0x7632u);
                 o[2 * b + 1] = __byte_perm(__float_as_uint(f[2]), __float_as_uint(f[3]), 0x7632u);
             }
-            *reinterpret_cast<uint4 *>(row + 8 * u) = make_uint4(o[0], o[1], o[2], o[3]);
-            *reinterpret_cast<uint4 *>(row + 8 * u + 4) = make_uint4(o[4], o[5], o[6], o[7]);
+            *reinterpret_cast<uint4 *>(row + 8 * c) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4 *>(row + 8 * c + 4) = make_uint4(o[4], o[5], o[6], o[7]);
         }
     }
     if (q < 8 * VPT) {
-        uint32_t *row = Cs + (l8 + 8 * (q / VPT)) * RW + (q % VPT) * 16;
-        const uint32_t w[4] = {r.v[0], r.v[1], r.v[2], 0u};
+        const int tl = l8 + 8 * (q / VPT);
+        uint32_t *row = Cs + tl * RW + (q % VPT) * 16;
+        uint32_t w[4] = {0u, 0u, 0u, 0u};
+        if (t0 + tl < T) {
+            const uint32_t *src =
+                reinterpret_cast<const uint32_t *>(raw + SM::RAW_V + voff + tl * (3 * D / 8) + (q % VPT) * 12);
+            w[0] = src[0];
+            w[1] = src[1];
+            w[2] = src[2];
+        }
         uint32_t o[16];
 #pragma unroll
         for (int k = 0; k < 16; ++k) {  // codes 2k, 2k+1: bits 6k .. 6k+5
@@ -183,16 +245,24 @@ __device__ __forceinline__ void stage_chunk(const RawChunk<D> &r, uint32_t *Kb, 
 #pragma unroll
         for (int k = 0; k < 16; k += 4) *reinterpret_cast<uint4 *>(row + k) = make_uint4(o[k], o[k + 1], o[k + 2], o[k + 3]);
     }
-    if (tid < ATT_TC) sig[tid] = __half2float(__ushort_as_half(static_cast<uint16_t>(r.sig)));
+    if (tid < ATT_TC)
+        sig[tid] = t0 + tid < T ? __half2float(*reinterpret_cast<const __half *>(raw + SM::RAW_SG + soff + 2 * tid))
+                                : 0.0f;
     if constexpr (Q8)
-        if (tid < ATT_TC * (D / 32)) ksb[tid] = __half2float(__ushort_as_half(static_cast<uint16_t>(r.ksc)));
+        if (tid < ATT_TC * (D / 32))
+            ksb[tid] = t0 + tid / (D / 32) < T
+                           ? __half2float(*reinterpret_cast<const __half *>(raw + SM::RAW_KS + qoff + 2 * tid))
+                           : 0.0f;
     if constexpr (R > 0)
         if (tid < ATT_TC * (R / 8)) {  // bf16 -> fp16, exact within fp16's normal range
-            const uint32_t w[4] = {r.lr.x, r.lr.y, r.lr.z, r.lr.w};
-            uint32_t o[4];
+            uint32_t o[4] = {0u, 0u, 0u, 0u};
+            if (t0 + tid / (R / 8) < T) {
+                const uint4 x = *reinterpret_cast<const uint4 *>(raw + SM::RAW_LR + 16 * tid);
+                const uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) o[i] = pack_half2(bf16_lo(w[i]), bf16_hi(w[i]));
-            *reinterpret_cast<uint4 *>(Ls + (tid / (R / 8)) * AttendSmem<D, R>::LW + (tid % (R / 8)) * 4) =
+                for (int i = 0; i < 4; ++i) o[i] = pack_half2(bf16_lo(w[i]), bf16_hi(w[i]));
+            }
+            *reinterpret_cast<uint4 *>(Ls + (tid / (R / 8)) * SM::LW + (tid % (R / 8)) * 4) =
                 make_uint4(o[0], o[1], o[2], o[3]);
         }
 }
@@ -210,14 +280,18 @@ __device__ __forceinline__ void attend_passes(const AttendArgs &a, uint32_t *sme
     constexpr int NL = R / 8;         // P V_lr n-tiles per warp (LoRA attention)
     constexpr int LW = SM::LW;
     constexpr int PW = D + R;         // floats per partial row
-    uint32_t *Qs = smem;                       // [ATT_MT][RW] bf16 pairs
-    uint32_t *Kb = Qs + SM::q_words;           // [2][ATT_TC][RW] bf16 pairs
-    uint32_t *Cs = Kb + 2 * SM::tile_words;    // [2][ATT_TC][RW] fp16 pairs
-    float *sig = reinterpret_cast<float *>(Cs + 2 * SM::tile_words);  // [2][ATT_TC]
-    uint32_t *lut = reinterpret_cast<uint32_t *>(sig + 2 * ATT_TC);   // [64] (c[lo], c[hi]) fp16 pairs
-    float *ksb = reinterpret_cast<float *>(lut + 64);                  // [2][ATT_TC][D/32] q8_0 key block scales
-    uint32_t *Ls = reinterpret_cast<uint32_t *>(ksb + 2 * SM::ksb_words);  // [2][ATT_TC][LW] low-rank fp16 pairs
-    float *mrg = reinterpret_cast<float *>(smem);  // after the loop: [warps][16][MSW] acc, then [warps][32] m, l
+    constexpr int NST = SM::NST;
+    uint8_t *sm8 = reinterpret_cast<uint8_t *>(smem);
+    const uint32_t bar0 = att_smem(sm8);                                   // [NST] mbarriers, 8 bytes each
+    uint8_t *ring = sm8 + SM::OFF_RING;                                    // [NST] raw sub-chunks
+    uint32_t *Qs = reinterpret_cast<uint32_t *>(sm8 + SM::OFF_Q);          // [ATT_MT][RW] bf16 pairs
+    uint32_t *Kt = reinterpret_cast<uint32_t *>(sm8 + SM::OFF_K);          // [ATT_TC][RW] bf16 pairs
+    uint32_t *Ct = reinterpret_cast<uint32_t *>(sm8 + SM::OFF_C);          // [ATT_TC][RW] fp16 pairs
+    float *st = reinterpret_cast<float *>(sm8 + SM::OFF_SIG);              // [ATT_TC] sigma
+    uint32_t *lut = reinterpret_cast<uint32_t *>(sm8 + SM::OFF_LUT);       // [64] (c[lo], c[hi]) fp16 pairs
+    float *kst = reinterpret_cast<float *>(sm8 + SM::OFF_KSB);             // [ATT_TC][D/32] q8_0 key block scales
+    uint32_t *Lt = reinterpret_cast<uint32_t *>(sm8 + SM::OFF_LS);         // [ATT_TC][LW] low-rank fp16 pairs
+    float *mrg = reinterpret_cast<float *>(sm8 + SM::BAR_BYTES);  // after the loop: [warps][16][MSW] acc, [warps][32] m, l
 
     const int h = blockIdx.x, split = blockIdx.y;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -229,23 +303,42 @@ __device__ __forceinline__ void attend_passes(const AttendArgs &a, uint32_t *sme
                       (Q8 ? 1.0f : reinterpret_cast<const float *>(a.pool + a.geo.off_scales)[a.layer]);
     const uint64_t vbase = uint64_t(h) * uint64_t(a.T);
     const int sub0 = split * a.per_split, sub1 = min(a.nsub, sub0 + a.per_split);
+    const int nsubs = sub1 - sub0;
+    if (tid == 0) {
+        for (int sl = 0; sl < NST; ++sl) att_mbar_init(bar0 + 8 * sl);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    uint32_t phases = 0;  // bit sl: parity of slot sl's next completion (the same in every thread)
 
     for (int m0 = 0; m0 < a.QH; m0 += RP) {
-        __syncthreads();  // the previous pass's merge slots are read
-        RawChunk<D> raw;  // the first sub-chunk's bytes are requested before the query tile
-        load_chunk<D, Q8, R>(raw, lay, a.geo, vbase, sub0 * ATT_TC, a.T, tid, kscales, a.vlr);
+        __syncthreads();  // the barriers are set up; the previous pass's merge slots are read
+        if (tid == 0) {   // the ring's first sub-chunks are requested before the query tile
+            att_fence_proxy_async();
+            for (int sl = 0; sl < NST && sl < nsubs; ++sl)
+                issue_chunk<D, Q8, R>(ring + sl * SM::SLOT, bar0 + 8 * sl, lay, a.geo, vbase, (sub0 + sl) * ATT_TC,
+                                      a.T, kscales, a.vlr);
+        }
         if (tid < 64) {
             const float c0 = centroid_e4(uint32_t(tid & 7)) * 1e-4f, c1 = centroid_e4(uint32_t(tid >> 3)) * 1e-4f;
             lut[tid] = pack_half2(c0, c1);
         }
-        for (int e = tid; e < RP * (D / 8); e += ATT_THREADS) {
-            const int r = e / (D / 8), c8 = e % (D / 8);
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (m0 + r < a.QH) {
-                const int ag = (m0 + r) / a.G, j = h * a.G + (m0 + r) % a.G;
-                v = *reinterpret_cast<const uint4 *>(a.q + (uint64_t(ag) * a.NQ + j) * D + c8 * 8);
+        {   // the query tile: every load of a thread issued before its stores
+            constexpr int QPT = (RP * (D / 8) + ATT_THREADS - 1) / ATT_THREADS;
+            uint4 v[QPT];
+#pragma unroll
+            for (int u = 0; u < QPT; ++u) {
+                const int e = tid + u * ATT_THREADS, r = e / (D / 8), c8 = e % (D / 8);
+                v[u] = make_uint4(0, 0, 0, 0);
+                if (e < RP * (D / 8) && m0 + r < a.QH) {
+                    const int ag = (m0 + r) / a.G, j = h * a.G + (m0 + r) % a.G;
+                    v[u] = *reinterpret_cast<const uint4 *>(a.q + (uint64_t(ag) * a.NQ + j) * D + c8 * 8);
+                }
             }
-            *reinterpret_cast<uint4 *>(Qs + r * RW + c8 * 4) = v;
+#pragma unroll
+            for (int u = 0; u < QPT; ++u) {
+                const int e = tid + u * ATT_THREADS, r = e / (D / 8), c8 = e % (D / 8);
+                if (e < RP * (D / 8)) *reinterpret_cast<uint4 *>(Qs + r * RW + c8 * 4) = v[u];
+            }
         }
         const bool active = m0 + mi * 16 < a.QH;  // warp-uniform: this tile has real rows
         float acc[NV][4];
@@ -257,16 +350,29 @@ __device__ __forceinline__ void attend_passes(const AttendArgs &a, uint32_t *sme
         for (int nt = 0; nt < (NL > 0 ? NL : 1); ++nt) lracc[nt][0] = lracc[nt][1] = lracc[nt][2] = lracc[nt][3] = 0.0f;
 
         __syncthreads();  // the pair table and the query tile are in
-        for (int sub = sub0; sub < sub1; ++sub) {
-            const int buf = (sub - sub0) & 1;
-            uint32_t *Kt = Kb + buf * SM::tile_words, *Ct = Cs + buf * SM::tile_words;
-            float *st = sig + buf * ATT_TC;
-            float *kst = ksb + buf * SM::ksb_words;
-            uint32_t *Lt = Ls + buf * SM::lr_words;
-            stage_chunk<D, Q8, R>(raw, Kt, Ct, st, lut, kst, Lt, tid);
-            if (sub + 1 < sub1)
-                load_chunk<D, Q8, R>(raw, lay, a.geo, vbase, (sub + 1) * ATT_TC, a.T, tid, kscales, a.vlr);
-            __syncthreads();  // this buffer is staged; every warp is done with the other one
+        int failed_at = -1;
+        for (int i = 0; i < nsubs; ++i) {
+            const int sub = sub0 + i, sl = i % NST;
+            const int t0 = sub * ATT_TC;
+            uint8_t *raw = ring + sl * SM::SLOT;
+            if (i > 0) __syncthreads();  // every warp is done with the staged tiles
+            const bool ok = att_mbar_wait(bar0 + 8 * sl, (phases >> sl) & 1u);
+            phases ^= 1u << sl;
+            {
+                const uint64_t n0 = vbase + uint64_t(t0);
+                const uint32_t voff = uint32_t(reinterpret_cast<uintptr_t>(lay + a.geo.sec_v + n0 * (3 * D / 8)) & 15u);
+                const uint32_t soff = uint32_t(reinterpret_cast<uintptr_t>(lay + a.geo.sec_sigma + n0 * 2) & 15u);
+                const uint32_t qoff = Q8 ? uint32_t(reinterpret_cast<uintptr_t>(kscales + n0 * (D / 32)) & 15u) : 0u;
+                stage_raw<D, Q8, R>(raw, t0, a.T, tid, voff, soff, qoff, Kt, Ct, st, lut, kst, Lt);
+            }
+            if (__syncthreads_or(!ok)) {  // the tiles are staged and the slot is free, unless a wait ran out
+                failed_at = i;
+                break;
+            }
+            if (tid == 0 && i + NST < nsubs) {  // refill the slot with the sub-chunk NST ahead
+                att_fence_proxy_async();
+                issue_chunk<D, Q8, R>(raw, bar0 + 8 * sl, lay, a.geo, vbase, t0 + NST * ATT_TC, a.T, kscales, a.vlr);
+            }
             if (!active) continue;
 
             // S = Q K^T for rows mi*16.., tokens th*TPW..
@@ -408,6 +514,20 @@ __device__ __forceinline__ void attend_passes(const AttendArgs &a, uint32_t *sme
                     }
                 }
             }
+        }
+        if (failed_at >= 0) {
+            // a bulk copy did not complete in time: report it, let the copies
+            // still outstanding (sub-chunks failed_at .. failed_at + NST - 1)
+            // land (bounded), and give up on this block
+            if (tid == 0) {
+                atomicOr(const_cast<uint32_t *>(reinterpret_cast<const uint32_t *>(a.pool)) + POOL_ERR_WORD,
+                         FLAG_TIMEOUT);
+                for (int k = failed_at; k < nsubs && k < failed_at + NST; ++k) {
+                    const int sl = k % NST;
+                    att_mbar_wait(bar0 + 8 * sl, ((phases >> sl) & 1u) ^ (k == failed_at ? 1u : 0u));
+                }
+            }
+            return;
         }
         // merge the token slices of each row tile
 #pragma unroll
@@ -662,7 +782,7 @@ static inline AttendPlan attend_plan(const kvp_shape *s, int na, int nq, int ran
     p.QH = na * p.G;
     p.QHP = (p.QH + ATT_MT - 1) / ATT_MT * ATT_MT;
     p.nsub = (s->n_tokens + ATT_TC - 1) / ATT_TC;
-    int want = (ATT_TARGET_BLOCKS + s->n_kv_heads - 1) / s->n_kv_heads;
+    int want = ATT_TARGET_BLOCKS / s->n_kv_heads;  // splits per KV head: the grid stays within one wave
     if (want < 1) want = 1;
     if (want > p.nsub) want = p.nsub;
     p.per_split = (p.nsub + want - 1) / want;
