@@ -213,13 +213,15 @@ __device__ __forceinline__ void stage_raw(const uint8_t *raw, int t0, int T, int
             uint32_t o[8];
 #pragma unroll
             for (int b = 0; b < 4; ++b) {
-                const uint32_t x = w4[b] ^ 0x80808080u;
-                float f[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    f[i] = __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7650u | i)) - 8388736.0f;
-                o[2 * b] = __byte_perm(__float_as_uint(f[0]), __float_as_uint(f[1]), 0x7632u);
-                o[2 * b + 1] = __byte_perm(__float_as_uint(f[2]), __float_as_uint(f[3]), 0x7632u);
+                const uint32_t x = w4[b] ^ 0x80808080u;  // byte i: q + 128
+                // 2^23 + q + 128 as fp32, minus 2^23 + 128 (exact), two at a time
+                const float2 off = make_float2(-8388736.0f, -8388736.0f);
+                const float2 f01 = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(x, 0x4B000000u, 0x7650u)),
+                                                          __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7651u))), off);
+                const float2 f23 = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(x, 0x4B000000u, 0x7652u)),
+                                                          __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7653u))), off);
+                o[2 * b] = __byte_perm(__float_as_uint(f01.x), __float_as_uint(f01.y), 0x7632u);
+                o[2 * b + 1] = __byte_perm(__float_as_uint(f23.x), __float_as_uint(f23.y), 0x7632u);
             }
             *reinterpret_cast<uint4 *>(row + 8 * c) = make_uint4(o[0], o[1], o[2], o[3]);
             *reinterpret_cast<uint4 *>(row + 8 * c + 4) = make_uint4(o[4], o[5], o[6], o[7]);
@@ -529,6 +531,10 @@ __device__ __forceinline__ void attend_passes(const AttendArgs &a, uint32_t *sme
             }
             return;
         }
+        // the combine kernel (launched as this kernel's programmatic
+        // dependent) may be placed once every block is this far; it waits for
+        // this grid's completion before it reads
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
         // merge the token slices of each row tile
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
@@ -625,6 +631,9 @@ __global__ void __launch_bounds__(CMB_THREADS) attend_combine(const __grid_const
     constexpr int PW = D + R;   // floats per partial row
     __shared__ float wacc[CMB_WARPS][D + (R > 0 ? 32 : 0)];
     __shared__ float wml[CMB_WARPS][2];
+    // launched as a programmatic dependent of the split kernel: its partial
+    // rows and statistics are complete and visible after this wait
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ag = blockIdx.x / a.NQ, j = blockIdx.x % a.NQ;
     const int h = j / a.G, r = ag * a.G + j % a.G;
@@ -759,7 +768,19 @@ template <int D, int TPW, int R>
 static int attend_launch(const AttendArgs &a, dim3 grid, unsigned cgrid, cudaStream_t st) {
     if (!attend_smem_ready<D, TPW, R>()) return KVP_ERR_CUDA;
     attend_split<D, TPW, R><<<grid, ATT_THREADS, AttendSmem<D, R>::bytes, st>>>(a);
-    attend_combine<D, R><<<cgrid, CMB_THREADS, 0, st>>>(a);
+    // programmatic dependent launch: the combine's blocks are placed while the
+    // split runs and wait (griddepcontrol.wait) for its results
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cgrid);
+    cfg.blockDim = dim3(CMB_THREADS);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, attend_combine<D, R>, a) != cudaSuccess) return KVP_ERR_CUDA;
     return KVP_OK;
 }
 
