@@ -214,20 +214,20 @@ __global__ void __launch_bounds__(CARD_THREADS, 4) card_pack(const __grid_consta
                 w[4 * q + 3] = v.w;
             }
             float2 x[16];
-            // min / max on the packed bf16 pairs (exact; NaN is ignored as by fminf / fmaxf)
+            // min / max on the packed bf16 pairs (exact).  The maximum propagates
+            // NaN, so a group holding Inf or NaN has a non-finite min or max.
             __nv_bfloat162 mnp = *reinterpret_cast<const __nv_bfloat162 *>(&w[0]), mxp = mnp;
-            float2 nfacc = make_float2(0.0f, 0.0f);
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const __nv_bfloat162 pr = *reinterpret_cast<const __nv_bfloat162 *>(&w[i]);
                 mnp = __hmin2(mnp, pr);
-                mxp = __hmax2(mxp, pr);
+                mxp = __hmax2_nan(mxp, pr);
                 x[i] = make_float2(bf16_lo(w[i]), bf16_hi(w[i]));
-                nfacc = __ffma2_rn(x[i], make_float2(0.0f, 0.0f), nfacc);  // NaN iff Inf/NaN seen
             }
             const float mn = fminf(__low2float(mnp), __high2float(mnp));
-            const float mx = fmaxf(__low2float(mxp), __high2float(mxp));
-            const bool nf = (nfacc.x != nfacc.x) || (nfacc.y != nfacc.y);
+            const float mx0 = __low2float(mxp), mx1 = __high2float(mxp);
+            const float mx = fmaxf(mx0, mx1);
+            const bool nf = !(fabsf(mn) <= 3.0e38f) || !(fabsf(mx0) <= 3.0e38f) || !(fabsf(mx1) <= 3.0e38f);
             const uint32_t sb = group_scale_f16(mx, mn, qmax, rcp_qmax);
             const uint32_t zb = __half_as_ushort(__float2half_rn(mn));
             if (nf)
@@ -236,9 +236,12 @@ __global__ void __launch_bounds__(CARD_THREADS, 4) card_pack(const __grid_consta
                 flags |= FLAG_RANGE;
             const float sf = __half2float(__ushort_as_half(uint16_t(sb)));
             const float zf = __half2float(__ushort_as_half(uint16_t(zb)));
-            const float inv = (sf > 0.0f && sf <= 65504.0f) ? __frcp_rn(sf) : 0.0f;
+            const float inv = (sf > 0.0f && sf <= 65504.0f) ? __fdividef(1.0f, sf) : 0.0f;
             // code = clamp(round((x - z_h) / s_h), 0, 2^b - 1): the low mantissa bits
-            // of (x - z_h) * (1/s_h) + 1.5*2^23.  The map is monotone, so the clamp is
+            // of (x - z_h) * r + 1.5*2^23, r the fast reciprocal of s_h (within 2
+            // ulp): for codes up to 255 the estimate is within 8e-5 of the exact
+            // quotient, so it rounds the same way unless that quotient lies
+            // within 8e-5 of a half-integer.  The map is monotone, so the clamp is
             // needed only if the group's extremes fall outside the code range.
             const float lo_c = RNE_MAGIC_C, hi_c = RNE_MAGIC_C + qmax;
             const float tmn = fmaf(mn - zf, inv, RNE_MAGIC_C), tmx = fmaf(mx - zf, inv, RNE_MAGIC_C);
