@@ -87,6 +87,7 @@ _SIGS = {
     "kvp_strerror": (C.c_char_p, [C.c_int]),
     "kvp_launch_count": (C.c_uint64, []),
     "kvp_test_fail_next_encode": (C.c_int, [C.c_int, C.c_uint32]),
+    "kvp_test_limit_next_attend": (C.c_int, [C.c_uint32]),
 }
 
 _lib = None
@@ -263,6 +264,10 @@ def kvp_launch_count():
 
 def kvp_test_fail_next_encode(layer, spin_iters):
     return load().kvp_test_fail_next_encode(int(layer), int(spin_iters))
+
+
+def kvp_test_limit_next_attend(polls):
+    return load().kvp_test_limit_next_attend(int(polls))
 
 
 class KVPError(RuntimeError):

@@ -45,6 +45,7 @@ struct AttendArgs {
     int L, H, T, layer, NA, NQ, G, QH, QHP, nsub, per_split, nsplit;
     const uint16_t *vlr;     // LoRA attention: bf16 [T][R] shared low-rank value cache
     const uint16_t *lora_b;  // LoRA attention: bf16 [NA][R][H*d] per-agent up-projections
+    uint32_t wait_polls;     // polls of a sub-chunk's barrier before giving up
 };
 
 __device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -97,10 +98,10 @@ __device__ __forceinline__ bool att_mbar_try(uint32_t bar, uint32_t parity) {
     return ok != 0u;
 }
 // Waits for the completion of the barrier's phase of the given parity; gives
-// up (false) after about half a second.
+// up (false) after `limit` polls (ATT_WAIT_LIMIT: about half a second).
 constexpr uint32_t ATT_WAIT_LIMIT = 1u << 22;
-__device__ __forceinline__ bool att_mbar_wait(uint32_t bar, uint32_t parity) {
-    for (uint32_t i = 0; i < ATT_WAIT_LIMIT; ++i) {
+__device__ __forceinline__ bool att_mbar_wait(uint32_t bar, uint32_t parity, uint32_t limit) {
+    for (uint32_t i = 0; i < limit; ++i) {
         if (att_mbar_try(bar, parity)) return true;
         if (i >= 16) __nanosleep(128);
     }
@@ -358,7 +359,7 @@ __device__ __forceinline__ void attend_passes(const AttendArgs &a, uint32_t *sme
             const int t0 = sub * ATT_TC;
             uint8_t *raw = ring + sl * SM::SLOT;
             if (i > 0) __syncthreads();  // every warp is done with the staged tiles
-            const bool ok = att_mbar_wait(bar0 + 8 * sl, (phases >> sl) & 1u);
+            const bool ok = att_mbar_wait(bar0 + 8 * sl, (phases >> sl) & 1u, a.wait_polls);
             phases ^= 1u << sl;
             {
                 const uint64_t n0 = vbase + uint64_t(t0);
@@ -526,7 +527,7 @@ __device__ __forceinline__ void attend_passes(const AttendArgs &a, uint32_t *sme
                          FLAG_TIMEOUT);
                 for (int k = failed_at; k < nsubs && k < failed_at + NST; ++k) {
                     const int sl = k % NST;
-                    att_mbar_wait(bar0 + 8 * sl, ((phases >> sl) & 1u) ^ (k == failed_at ? 1u : 0u));
+                    att_mbar_wait(bar0 + 8 * sl, ((phases >> sl) & 1u) ^ (k == failed_at ? 1u : 0u), ATT_WAIT_LIMIT);
                 }
             }
             return;
@@ -815,6 +816,10 @@ static inline AttendPlan attend_plan(const kvp_shape *s, int na, int nq, int ran
     return p;
 }
 
+// Failure-path testing (kvp_test_limit_next_attend): consumed by the next
+// attention call on the calling thread.
+static thread_local uint32_t t_att_polls = ATT_WAIT_LIMIT;
+
 // Checks, arguments and launches shared by plain (rank 0) and LoRA attention.
 static int attend_common(const void *pool, const kvp_shape *s, int layer, int n_agents, int n_q_heads,
                          const void *q, float scale, int rank, const void *v_lr, const void *lora_b, float *out,
@@ -854,6 +859,8 @@ static int attend_common(const void *pool, const kvp_shape *s, int layer, int n_
     a.nsplit = p.nsplit;
     a.vlr = static_cast<const uint16_t *>(v_lr);
     a.lora_b = static_cast<const uint16_t *>(lora_b);
+    a.wait_polls = t_att_polls;
+    t_att_polls = ATT_WAIT_LIMIT;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const dim3 grid(unsigned(a.H), unsigned(a.nsplit));
     const unsigned cgrid = unsigned(n_agents) * unsigned(n_q_heads);  // one block per query
@@ -871,9 +878,15 @@ static int attend_common(const void *pool, const kvp_shape *s, int layer, int n_
 
 static inline bool rank_ok(int rank) { return rank == 16 || rank == 32; }
 
+
 }  // namespace kvp
 
 using namespace kvp;
+
+extern "C" int kvp_test_limit_next_attend(uint32_t polls) {
+    t_att_polls = polls;
+    return KVP_OK;
+}
 
 extern "C" size_t kvpool_attend_workspace_bytes(const kvp_shape *s, int n_agents, int n_q_heads) {
     if (shape_ok(s) != KVP_OK || n_agents < 1 || n_q_heads < 1 || n_q_heads % s->n_kv_heads != 0) return 0;

@@ -238,7 +238,11 @@ size_t kvpool_attend_workspace_bytes(const kvp_shape *shape, int n_agents, int n
  *  per-block partial sums, each scaled by its block scale in fp32);
  *  probabilities times sigma enter the value product as fp16, centroids as
  *  fp16.  A pool whose header does not match `shape` is not read and
- *  kvpool_status reports KVP_ERR_HEADER. */
+ *  kvpool_status reports KVP_ERR_HEADER.  The kernel streams the pool's bytes
+ *  into shared memory with bulk copies and waits on them for at most about
+ *  half a second; should a wait run out, out / lse are unspecified and
+ *  kvpool_status reports KVP_ERR_TIMEOUT.  Errors are recorded in the pool's
+ *  error word (the only bytes of the pool a call may write). */
 int kvpool_attend(const void *pool, const kvp_shape *shape, int layer, int n_agents, int n_q_heads,
                   const void *q, float scale, float *out, float *lse, void *ws, size_t ws_bytes,
                   void *stream);
@@ -354,6 +358,15 @@ uint64_t kvp_launch_count(void);
  * a test can exercise that path; layer < 0 restores normal operation.
  * Returns KVP_OK. */
 int kvp_test_fail_next_encode(int layer, uint32_t spin_iters);
+
+/* Failure-path testing of pool attention.  Its split kernel waits, with a
+ * bounded number of polls, for the bulk copies of each sub-chunk; a wait that
+ * runs out is reported by kvpool_status as KVP_ERR_TIMEOUT (the block first
+ * lets its copies in flight land, with the normal limit) and leaves the CUDA
+ * context usable.  Makes the NEXT kvpool_attend / kvpool_attend_lora on this
+ * thread poll each sub-chunk's copies at most `polls` times (0: not at all, so
+ * every block gives up on its first sub-chunk).  Returns KVP_OK. */
+int kvp_test_limit_next_attend(uint32_t polls);
 
 #ifdef __cplusplus
 }

@@ -138,3 +138,31 @@ def test_attend_full_size_layers(name, n_q):
     for layer in (0, L - 1):
         out, lse = _attend(pool, shape, layer, q.cuda(), 1.0 / math.sqrt(d))
         _check(img, shape, layer, qb, 1.0 / math.sqrt(d), out, lse)
+
+
+def test_attend_wait_timeout_is_reported_and_context_survives():
+    """The split kernel waits (bounded) for each sub-chunk's bulk copies.  With
+    the next call limited to zero polls every block gives up on its first
+    sub-chunk: it lets the copies it issued land, records the timeout in the
+    pool's error word (kvpool_status: KVP_ERR_TIMEOUT) and returns.  The
+    context stays usable and the next call, on a fresh pool, is correct.
+    Four sub-chunks per block here, so each block drains a full ring."""
+    shape = (1, 8, 128, 8192)
+    L, H, d, T = shape
+    ks_t, vs_t = synth.kv_layers(L, H, T, d, seed=41, device="cuda")
+    pool = _pool(ks_t, vs_t, shape)
+    g = torch.Generator(device="cpu").manual_seed(3)
+    q = torch.randn(2, 32, d, generator=g).to(torch.bfloat16)
+    na, nq = q.shape[0], q.shape[1]
+    out = torch.empty(na, nq, d, dtype=torch.float32, device="cuda")
+    lse = torch.empty(na, nq, dtype=torch.float32, device="cuda")
+    wsb = kv.kvpool_attend_workspace_bytes(shape, na, nq)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    assert kv.kvp_test_limit_next_attend(0) == kv.KVP_OK
+    assert kv.kvpool_attend(pool, shape, 0, na, nq, q.cuda(), 0.1, out, lse, ws, wsb) == kv.KVP_OK
+    assert kv.kvpool_status(pool) == kv.KVP_ERR_TIMEOUT
+    torch.cuda.synchronize()
+    pool2 = _pool(ks_t, vs_t, shape)                   # the hook applies to one call only
+    res, res_lse = _attend(pool2, shape, 0, q.cuda(), 0.1)
+    assert kv.kvpool_status(pool2) == kv.KVP_OK
+    _check(pool2.cpu().numpy(), shape, 0, synth.bits16(q), 0.1, res, res_lse)
