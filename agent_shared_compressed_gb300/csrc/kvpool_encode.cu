@@ -311,15 +311,15 @@ __device__ void quant_slice(const EncodeArgs &a, int l, uint32_t p, uint64_t pol
         for (int u = 0; u < 4; ++u) w[u] = ld_v4_policy(src + c + u * ENC_THREADS, pol);
         if (pre) {
 #pragma unroll
-            for (int u = 0; u < 4; ++u) dst[c + u * ENC_THREADS] = k_quant8<true>(w[u], kp);
+            for (int u = 0; u < 4; ++u) __stcs(dst + c + u * ENC_THREADS, k_quant8<true>(w[u], kp));
         } else {
 #pragma unroll
-            for (int u = 0; u < 4; ++u) dst[c + u * ENC_THREADS] = k_quant8<false>(w[u], kp);
+            for (int u = 0; u < 4; ++u) __stcs(dst + c + u * ENC_THREADS, k_quant8<false>(w[u], kp));
         }
     }
     for (; c < c1; c += ENC_THREADS) {
         const uint4 w0 = ld_v4_policy(src + c, pol);
-        dst[c] = pre ? k_quant8<true>(w0, kp) : k_quant8<false>(w0, kp);
+        __stcs(dst + c, pre ? k_quant8<true>(w0, kp) : k_quant8<false>(w0, kp));
     }
 }
 
@@ -459,11 +459,11 @@ __device__ uint32_t v_encode_step(const EncodeArgs &a, int layer, uint64_t step,
     uint8_t *vdst = lay + a.geo.sec_v + n0 * CB;
     const uint32_t off = uint32_t(lane) * 16u;
     if (off + 16u <= bytes) {
-        *reinterpret_cast<uint4 *>(vdst + off) = *reinterpret_cast<const uint4 *>(stage + off);
+        __stcs(reinterpret_cast<uint4 *>(vdst + off), *reinterpret_cast<const uint4 *>(stage + off));
     } else if (off < bytes) {  // bytes is a multiple of 8
-        *reinterpret_cast<uint2 *>(vdst + off) = *reinterpret_cast<const uint2 *>(stage + off);
+        __stcs(reinterpret_cast<uint2 *>(vdst + off), *reinterpret_cast<const uint2 *>(stage + off));
     }
-    if (valid && l == 0) reinterpret_cast<uint16_t *>(lay + a.geo.sec_sigma)[n] = sig_bits;
+    if (valid && l == 0) __stcs(reinterpret_cast<unsigned short *>(lay + a.geo.sec_sigma) + n, (unsigned short)sig_bits);
     __syncwarp();
     return flags;
 }
@@ -675,8 +675,8 @@ __device__ uint32_t q8_key_task(const EncodeArgs &a, int l, uint64_t c0, uint64_
             const uint2 codes = (s > 0.0f && s <= 65504.0f)
                                     ? k_quant8_block(w[it], s, __fdividef(1.0f, s), s < 0x1p-14f)
                                     : make_uint2(0, 0);
-            dst[c] = codes;
-            if ((lane & 3) == 0) ksc[c >> 2] = sb;
+            __stcs(dst + c, codes);
+            if ((lane & 3) == 0) __stcs(reinterpret_cast<unsigned short *>(ksc) + (c >> 2), (unsigned short)sb);
         }
     }
     return flags;
