@@ -318,24 +318,31 @@ __global__ void card_zero_tails(const __grid_constant__ CardArgs a) {
 // codes cw (2, 4 or 8 bits each, low bits first), group parameters pw
 // (fp16 scale | fp16 zero point << 16).
 __device__ __forceinline__ void card_chunk_values(int b, uint2 cw, uint32_t pw, float (&y)[8]) {
-    uint32_t q[8];
+    uint32_t q[8];  // the fp32 bit patterns of 2^23 + code
     if (b == 2) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) q[e] = (cw.x >> (2 * e)) & 3u;
+        for (int e = 0; e < 8; ++e) q[e] = ((cw.x >> (2 * e)) & 3u) | 0x4B000000u;
     } else if (b == 4) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) q[e] = (cw.x >> (4 * e)) & 15u;
+        for (int e = 0; e < 8; ++e) q[e] = ((cw.x >> (4 * e)) & 15u) | 0x4B000000u;
     } else {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            q[e] = (cw.x >> (8 * e)) & 255u;
-            q[4 + e] = (cw.y >> (8 * e)) & 255u;
+            q[e] = __byte_perm(cw.x, 0x4B000000u, 0x7650u | e);
+            q[4 + e] = __byte_perm(cw.y, 0x4B000000u, 0x7650u | e);
         }
     }
     const float sf = __half2float(__ushort_as_half(uint16_t(pw & 0xFFFFu)));
     const float zf = __half2float(__ushort_as_half(uint16_t(pw >> 16)));
+    // (2^23 + code) - 2^23 (exact), then code * s + z rounded once: two lanes at a time
+    const float2 off = make_float2(-8388608.0f, -8388608.0f), s2 = make_float2(sf, sf), z2 = make_float2(zf, zf);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) y[e] = fmaf(__uint_as_float(0x4B000000u | q[e]) - 8388608.0f, sf, zf);
+    for (int e = 0; e < 8; e += 2) {
+        const float2 c = __fadd2_rn(make_float2(__uint_as_float(q[e]), __uint_as_float(q[e + 1])), off);
+        const float2 v = __ffma2_rn(c, s2, z2);
+        y[e] = v.x;
+        y[e + 1] = v.y;
+    }
 }
 
 // Codes of chunk c of a b-bit record part.
