@@ -210,3 +210,36 @@ def test_card_full_size():
     for l in range(L):
         assert_bf16_close(ku[l], ok_[l], "K layer %d" % l)
         assert_bf16_close(vu[l], ov[l], "V layer %d" % l)
+
+
+def test_card_group_scales_across_fp16_range():
+    """Groups whose scale (max - min) / (2^b - 1) falls in fp16's subnormal
+    range, at zero (constant groups), in the normal range and near its top, and
+    zero points up to 3e4, on every bitwidth: the exactly rounded fp16 scale
+    and zero point, the codes (outside the half-integer band) and the unpacked
+    values match the oracle."""
+    L, H, d, T = 1, 2, 64, 16
+    rng = np.random.default_rng(8)
+    spans = [0.0, 1e-8, 2e-7, 3e-6, 4e-5, 1e-3, 0.5, 20.0, 900.0, 3e4]
+    bases = [0.0, -1e-6, 5e-5, 1.0, -30.0, 3e4]
+    x = np.zeros((2, H, T, d), np.float64)
+    for part in range(2):
+        for h in range(H):
+            for t in range(T):
+                for gi in range(d // 32):
+                    span = spans[(t + 3 * gi + part + h) % len(spans)]
+                    base = bases[(2 * t + gi + h) % len(bases)]
+                    x[part, h, t, 32 * gi: 32 * gi + 32] = base + span * rng.uniform(0, 1, 32)
+    bits16 = (x.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)   # bf16 by truncation
+    ks, vs = [bits16[0]], [bits16[1]]
+    bits = np.array([[2, 4, 8, 16][t % 4] for t in range(T)], np.uint8)
+    card, status = gpu_pack(bf16_dev_layers(ks), bf16_dev_layers(vs), bits, (L, H, d, T))
+    assert status == kv.KVP_OK
+    oimg, flags, r = O.card_pack(ks, vs, bits, want_r=True)
+    assert flags == 0
+    gimg = card.host()
+    assert_card_parity(gimg, oimg, r, L, H, d, T, bits)
+    _, gk, gv = gpu_unpack(card, L, H, T, d)
+    ok_, ov = O.card_unpack(gimg)
+    assert_bf16_close(gk[0], ok_[0], "K")
+    assert_bf16_close(gv[0], ov[0], "V")
