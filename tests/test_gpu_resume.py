@@ -3,7 +3,8 @@
 byte images (header plus offsets, no pointers), so saving one is a copy: the
 pool and the card go device -> host -> file -> host -> device, into buffers at
 other addresses, and decode, attention and unpack from the restored copies
-give exactly the bytes they give from the originals."""
+give exactly the bytes they give from the originals.  Also: calls on several
+streams at once give the bytes of a sequential run."""
 import numpy as np
 import pytest
 import torch
@@ -97,3 +98,45 @@ def test_pool_and_card_survive_a_file_round_trip(tmp_path, k_mode):
         torch.cuda.synchronize()
         outs.append((torch.stack(uk), torch.stack(uv)))
     assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+
+
+def test_concurrent_streams_match_sequential_results():
+    """Decode (into two agents), attention and a CacheCard pack of the same
+    source, issued on three streams with no ordering between them, give the
+    bytes a sequential run gives: the calls share no hidden state (the pool
+    is only read; each call has its own outputs and workspace)."""
+    shape = (2, 4, 128, 700)
+    L, H, d, T = shape
+    ks_t, vs_t = synth.kv_layers(L, H, T, d, seed=91, device="cuda")
+    pool = torch.empty(kv.kvpool_pool_bytes(shape), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(kv.kvpool_workspace_bytes(shape), dtype=torch.uint8, device="cuda")
+    assert kv.kvpool_encode(shape, ks_t, vs_t, pool, pool.numel(), ws, ws.numel()) == kv.KVP_OK
+    bits = synth.card_bits(T, seed=91).numpy()
+    bits_dev = torch.from_numpy(bits).cuda()
+    q = torch.randn(3, 16, d, generator=torch.Generator(device="cpu").manual_seed(9)).to(torch.bfloat16).cuda()
+    torch.cuda.synchronize()
+
+    def run(streams):
+        ck = [torch.empty(H * T * d * 2, dtype=torch.uint8, device="cuda") for _ in range(2 * L)]
+        cv = [torch.empty(H * T * d * 2, dtype=torch.uint8, device="cuda") for _ in range(2 * L)]
+        out = torch.empty(3, 16, d, dtype=torch.float32, device="cuda")
+        lse = torch.empty(3, 16, dtype=torch.float32, device="cuda")
+        wsb = kv.kvpool_attend_workspace_bytes(shape, 3, 16)
+        wsa = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+        card = torch.empty(kv.cachecard_bytes(shape, bits), dtype=torch.uint8, device="cuda")
+        s1, s2, s3 = streams
+        assert kv.kvpool_decode_into(pool, shape, 0, L, 2, ck, cv, s1) == kv.KVP_OK
+        assert kv.kvpool_attend(pool, shape, L - 1, 3, 16, q, 0.1, out, lse, wsa, wsb, s2) == kv.KVP_OK
+        assert kv.cachecard_pack(shape, 1, 0, bits_dev, ks_t, vs_t, card, card.numel(), s3) == kv.KVP_OK
+        torch.cuda.synchronize()
+        return torch.cat(ck + cv), out, lse, card
+
+    cur = torch.cuda.current_stream()
+    seq = run((cur, cur, cur))
+    side = [torch.cuda.Stream() for _ in range(3)]
+    for s in side:
+        s.wait_stream(cur)
+    par = run(side)
+    for a, b in zip(seq, par):
+        assert torch.equal(a, b)
+    assert kv.kvpool_status(pool) == kv.KVP_OK
