@@ -576,18 +576,15 @@ __global__ void __launch_bounds__(ENC_THREADS, 3) encode_pool(const __grid_const
 // ---------------------------------------------------------------------------
 // q8_0 keys (KVP_K_Q8_0): every 32 consecutive keys of a vector share an fp16
 // scale s_b = fp16(max|k| / 127); codes as above against s_b, clamped to
-// [-127, 127].  No layer-wide maximum, so one sweep encodes keys and values:
-// warp tasks are, per layer, Q8_TASK_CHUNKS 16-byte key chunks (4 lanes per
-// 32-key block: two shuffles give the block's maximum) and batches of
-// Q8_VSTEPS value steps.  The fp16 scale is fp16(max|k| * fl(1/127)): that
+// [-127, 127].  No layer-wide maximum, so one sweep encodes keys and values
+// on the block-level queue: per layer, key slices (4 lanes per 32-key block:
+// two shuffles give the block's maximum) spread among the value batches, and
+// nothing waits.  The fp16 scale is fp16(max|k| * fl(1/127)): that
 // fp32 product is within 2^-23 relative of the real quotient max|k|/127,
 // which never lies closer than 2^-20 relative to an fp16 midpoint (a bf16
 // over 127 is at least that far from any 12-bit fraction), so the fp16
 // rounding is the correct one.
 // ---------------------------------------------------------------------------
-constexpr int Q8_ITERS = 4;
-constexpr uint64_t Q8_TASK_CHUNKS = 32ull * Q8_ITERS;
-constexpr int Q8_VSTEPS = 8;  // value steps per warp task, each prefetched while the previous is encoded
 constexpr float Q8_INV127 = 1.0f / 127.0f;
 
 // Fast path as k_quant8: the code is the low byte of fma(k, r, 1.5*2^23),
@@ -623,95 +620,120 @@ __device__ __forceinline__ uint2 k_quant8_block(uint4 w, float s, float rcp, boo
     return r;
 }
 
-// One warp's key task: chunks c0 .. c0 + Q8_TASK_CHUNKS - 1 of layer l.
-__device__ uint32_t q8_key_task(const EncodeArgs &a, int l, uint64_t c0, uint64_t pol) {
+// One 16-byte key chunk c of layer l (w: its 8 keys; valid: c < chunks),
+// with the warp's lanes 4k .. 4k+3 holding the 4 chunks of one 32-key block
+// (every lane of the warp takes part: the block maximum is two shuffles).
+__device__ __forceinline__ uint32_t q8_chunk(const EncodeArgs &a, uint2 *dst, uint16_t *ksc, uint64_t c, uint4 w,
+                                             bool valid) {
     const int lane = threadIdx.x & 31;
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+    // block maximum: per-halfword max of the sign-cleared patterns; Inf /
+    // NaN patterns sort above every finite one, so a block holding one is
+    // redone with those halves masked out (its maximum over finite keys)
+    uint32_t m2 = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) m2 = __vmaxu2(m2, ws[i] & 0x7FFF7FFFu);
+    uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+    m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+    m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
+    const bool bad = m >= 0x7F80u;
+    if (__any_sync(0xffffffffu, bad)) {
+        uint32_t f2 = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t ab = ws[i] & 0x7FFF7FFFu;
+            f2 = __vmaxu2(f2, ab & ~__vcmpgeu2(ab, 0x7F807F80u));  // 0xFFFF in each Inf / NaN half
+        }
+        uint32_t f = max(f2 & 0xFFFFu, f2 >> 16);
+        f = max(f, __shfl_xor_sync(0xffffffffu, f, 1));
+        f = max(f, __shfl_xor_sync(0xffffffffu, f, 2));
+        if (bad) m = f;
+    }
+    // fp16(max|k| * fl(1/127)): for every finite bf16 maximum this is the
+    // fp16 nearest to the real max|k|/127 (checked over all of them)
+    const __half sh = __float2half_rn(__fmul_rn(__uint_as_float(m << 16), Q8_INV127));
+    const uint16_t sb = __half_as_ushort(sh);
+    const float s = __half2float(sh);
+    uint32_t flags = 0;
+    if (valid) {
+        if (bad)
+            flags |= FLAG_NONFINITE;
+        else if ((sb & 0x7C00u) == 0x7C00u)
+            flags |= FLAG_RANGE;
+        const uint2 codes =
+            (s > 0.0f && s <= 65504.0f) ? k_quant8_block(w, s, __fdividef(1.0f, s), s < 0x1p-14f) : make_uint2(0, 0);
+        __stcs(dst + c, codes);
+        if ((lane & 3) == 0) __stcs(reinterpret_cast<unsigned short *>(ksc) + (c >> 2), (unsigned short)sb);
+    }
+    return flags;
+}
+
+// One key slice of layer l on the block-level queue: chunks
+// [p * chunks_per_slice, ...) (slice bounds are multiples of 4 chunks, so
+// lanes 4k .. 4k+3 hold one 32-key block), 4 chunks per thread in flight.
+__device__ uint32_t q8_slice(const EncodeArgs &a, int l, uint32_t p, uint64_t pol) {
+    const uint64_t c0 = uint64_t(p) * a.chunks_per_slice;
+    const uint64_t c1 = min(c0 + a.chunks_per_slice, a.chunks);
     const uint4 *src = a.k[l];
     uint2 *dst = reinterpret_cast<uint2 *>(a.pool + a.geo.off_layers + uint64_t(l) * a.geo.layer_stride);
     uint16_t *ksc = reinterpret_cast<uint16_t *>(a.pool + a.geo.off_kscales) + uint64_t(l) * (a.chunks / 4);
-    uint4 w[Q8_ITERS];
-#pragma unroll
-    for (int it = 0; it < Q8_ITERS; ++it) {
-        const uint64_t c = c0 + uint64_t(it) * 32u + uint64_t(lane);
-        w[it] = c < a.chunks ? ld_v4_policy(src + c, pol) : make_uint4(0, 0, 0, 0);
-    }
     uint32_t flags = 0;
+    for (uint64_t cb = c0; cb < c1; cb += 4 * ENC_THREADS) {  // the same trip count in every thread
+        uint4 w[4];
 #pragma unroll
-    for (int it = 0; it < Q8_ITERS; ++it) {
-        const uint64_t c = c0 + uint64_t(it) * 32u + uint64_t(lane);
-        const uint32_t ws[4] = {w[it].x, w[it].y, w[it].z, w[it].w};
-        // block maximum: per-halfword max of the sign-cleared patterns; Inf /
-        // NaN patterns sort above every finite one, so a block holding one is
-        // redone with those halves masked out (its maximum over finite keys)
-        uint32_t m2 = 0;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) m2 = __vmaxu2(m2, ws[i] & 0x7FFF7FFFu);
-        uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
-        m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
-        m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
-        const bool bad = m >= 0x7F80u;
-        if (__any_sync(0xffffffffu, bad)) {
-            uint32_t f2 = 0;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t ab = ws[i] & 0x7FFF7FFFu;
-                f2 = __vmaxu2(f2, ab & ~__vcmpgeu2(ab, 0x7F807F80u));  // 0xFFFF in each Inf / NaN half
-            }
-            uint32_t f = max(f2 & 0xFFFFu, f2 >> 16);
-            f = max(f, __shfl_xor_sync(0xffffffffu, f, 1));
-            f = max(f, __shfl_xor_sync(0xffffffffu, f, 2));
-            if (bad) m = f;
+        for (int u = 0; u < 4; ++u) {
+            const uint64_t c = cb + threadIdx.x + uint64_t(u) * ENC_THREADS;
+            w[u] = c < c1 ? ld_v4_policy(src + c, pol) : make_uint4(0, 0, 0, 0);
         }
-        // fp16(max|k| * fl(1/127)): for every finite bf16 maximum this is the
-        // fp16 nearest to the real max|k|/127 (checked over all of them)
-        const __half sh = __float2half_rn(__fmul_rn(__uint_as_float(m << 16), Q8_INV127));
-        const uint16_t sb = __half_as_ushort(sh);
-        const float s = __half2float(sh);
-        if (c < a.chunks) {
-            if (bad)
-                flags |= FLAG_NONFINITE;
-            else if ((sb & 0x7C00u) == 0x7C00u)
-                flags |= FLAG_RANGE;
-            const uint2 codes = (s > 0.0f && s <= 65504.0f)
-                                    ? k_quant8_block(w[it], s, __fdividef(1.0f, s), s < 0x1p-14f)
-                                    : make_uint2(0, 0);
-            __stcs(dst + c, codes);
-            if ((lane & 3) == 0) __stcs(reinterpret_cast<unsigned short *>(ksc) + (c >> 2), (unsigned short)sb);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const uint64_t c = cb + threadIdx.x + uint64_t(u) * ENC_THREADS;
+            flags |= q8_chunk(a, dst, ksc, c, w[u], c < c1);
         }
     }
     return flags;
 }
 
+// The q8_0 encoder on the block-level queue: per layer, its P key slices
+// spread evenly among its value batches (there is no layer-wide maximum, so
+// nothing waits); item t belongs to layer t / (P + vitems).
 template <int D>
-__global__ void __launch_bounds__(ENC_THREADS, 3) encode_pool_q8(const __grid_constant__ EncodeArgs a) {
+__global__ void __launch_bounds__(ENC_THREADS, 3) encode_pool_q8q(const __grid_constant__ EncodeArgs a) {
     __shared__ __align__(16) uint8_t stage[ENC_WARPS][384];
     __shared__ __align__(16) uint4 vbuf[ENC_WARPS][2][4][32];  // per warp: two steps of value data
-    __shared__ uint32_t s_last;
+    __shared__ uint32_t s_item[2], s_last;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint64_t drop = l2_evict_first_policy();
+    const uint32_t M = uint32_t(a.P) + a.vitems;
     uint32_t flags = 0;
-    const uint64_t ktasks = (a.chunks + Q8_TASK_CHUNKS - 1) / Q8_TASK_CHUNKS;
-    const uint64_t vtasks = (a.steps_per_layer + Q8_VSTEPS - 1) / Q8_VSTEPS;
-    const uint64_t per_layer = ktasks + vtasks;
-    const uint64_t total = per_layer * uint64_t(a.L);
-    for (uint64_t t = uint64_t(blockIdx.x) * ENC_WARPS + warp; t < total; t += uint64_t(gridDim.x) * ENC_WARPS) {
-        const int l = int(t / per_layer);
-        const uint64_t r = t % per_layer;
-        if (r < ktasks) {
-            flags |= q8_key_task(a, l, r * Q8_TASK_CHUNKS, drop);
+    uint32_t next = 0;
+    if (threadIdx.x == 0) next = atomicAdd(&a.ctl->next_item, 1u);
+    for (uint32_t k = 0;; ++k) {
+        if (threadIdx.x == 0) s_item[k & 1u] = next;
+        __syncthreads();
+        const uint32_t t = s_item[k & 1u];
+        if (t >= a.total_items) break;
+        if (threadIdx.x == 0) next = atomicAdd(&a.ctl->next_item, 1u);
+        const int layer = int(t / M);
+        int kind;
+        uint32_t id;
+        mixed_item(a, t % M, kind, id);
+        if (kind == ITEM_KEYS) {
+            flags |= q8_slice(a, layer, id, drop);
         } else {
-            const uint64_t s0 = (r - ktasks) * Q8_VSTEPS;
-            v_prefetch<D>(a, l, s0, vbuf[warp][0], drop);
+            // the warp's VSTEPS steps, each prefetched while the previous one is encoded
+            const uint64_t step0 = uint64_t(id) * VSTEPS * ENC_WARPS + warp;
+            v_prefetch<D>(a, layer, step0, vbuf[warp][0], drop);
 #pragma unroll 1
-            for (int j = 0; j < Q8_VSTEPS; ++j) {
-                const uint64_t step = s0 + uint64_t(j);
-                if (j + 1 < Q8_VSTEPS)
-                    v_prefetch<D>(a, l, step + 1, vbuf[warp][(j + 1) & 1], drop);
+            for (int vs = 0; vs < VSTEPS; ++vs) {
+                const uint64_t step = step0 + uint64_t(vs) * ENC_WARPS;
+                if (vs + 1 < VSTEPS)
+                    v_prefetch<D>(a, layer, step + ENC_WARPS, vbuf[warp][(vs + 1) & 1], drop);
                 else
                     cp_async_commit();  // keep one group per iteration
                 cp_async_wait<1>();     // this step's group has landed
                 if (step < a.steps_per_layer)
-                    flags |= v_encode_step<D>(a, l, step, stage[warp], vbuf[warp][j & 1]);
+                    flags |= v_encode_step<D>(a, layer, step, stage[warp], vbuf[warp][vs & 1]);
             }
             cp_async_wait<0>();
         }
@@ -778,7 +800,7 @@ template <int D>
 static int encode_q8_occupancy() {
     static int occ = 0;
     if (occ == 0) {
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, encode_pool_q8<D>, ENC_THREADS, 0) != cudaSuccess ||
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, encode_pool_q8q<D>, ENC_THREADS, 0) != cudaSuccess ||
             occ < 1)
             occ = 1;
     }
@@ -865,18 +887,22 @@ extern "C" int kvpool_encode_ex(const kvp_shape *s, int k_mode, const void *cons
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(a.ctl, 0, sizeof(EncodeCtl), st) != cudaSuccess) return KVP_ERR_CUDA;
     if (k_mode == KVP_K_Q8_0) {
-        // one sweep, no waits: a grid of resident blocks, no more than there are warp tasks
-        const uint64_t tasks = ((chunks + Q8_TASK_CHUNKS - 1) / Q8_TASK_CHUNKS +
-                                (a.steps_per_layer + Q8_VSTEPS - 1) / Q8_VSTEPS) *
-                               uint64_t(L);
+        // the block-level queue without absmax items: per layer, key slices (a
+        // multiple of 4 chunks each: whole 32-key blocks) spread among the
+        // value batches; nothing waits
+        a.chunks_per_slice = (a.chunks_per_slice + 3) & ~uint64_t(3);
+        a.P = int((chunks + a.chunks_per_slice - 1) / a.chunks_per_slice);
+        a.vhead = 0;
+        const uint64_t items = (uint64_t(a.P) + vitems) * uint64_t(L);
+        if (items >= (1ull << 32)) return KVP_ERR_SIZE;
+        a.total_items = uint32_t(items);
         const uint64_t res_q8 =
             uint64_t(sm_count()) * uint64_t(a.d == 128 ? encode_q8_occupancy<128>() : encode_q8_occupancy<64>());
-        const uint64_t blocks = (tasks + ENC_WARPS - 1) / ENC_WARPS;
-        const unsigned g8 = unsigned(blocks < res_q8 ? blocks : res_q8);
+        const unsigned g8 = unsigned(items < res_q8 ? items : res_q8);
         if (a.d == 128)
-            encode_pool_q8<128><<<g8, ENC_THREADS, 0, st>>>(a);
+            encode_pool_q8q<128><<<g8, ENC_THREADS, 0, st>>>(a);
         else
-            encode_pool_q8<64><<<g8, ENC_THREADS, 0, st>>>(a);
+            encode_pool_q8q<64><<<g8, ENC_THREADS, 0, st>>>(a);
     } else if (a.d == 128) {
         encode_pool<128><<<grid, ENC_THREADS, 0, st>>>(a);
     } else {
