@@ -165,3 +165,29 @@ def test_strerror_and_counter():
         assert kv.kvp_strerror(code) and kv.kvp_strerror(code) != "unknown status"
     assert kv.kvp_strerror(-100) == "unknown status"
     assert kv.kvp_launch_count() >= 0
+
+
+def _attend_ws(H, d, T, na, nq, rank=0):
+    """The attention workspace the split plan implies: the splits of each KV
+    head (64-token sub-chunks) are as many as keep the grid of H x splits
+    blocks within 304 (two per SM on 152 SMs); one partial row of d + rank
+    floats and one (max, sum) pair per query row (padded to 64) per split."""
+    nsub = (T + 63) // 64
+    want = max(1, min(304 // H, nsub))
+    per = (nsub + want - 1) // want
+    nsplit = (nsub + per - 1) // per
+    qhp = (na * (nq // H) + 63) // 64 * 64
+    rows = H * nsplit * qhp
+    a256 = lambda x: (x + 255) // 256 * 256
+    return a256(a256(rows * (d + rank) * 4) + rows * 8), H * nsplit
+
+
+@pytest.mark.parametrize("H,d,T,na,nq", [(8, 128, 4096, 15, 32), (8, 128, 32768, 4, 32), (32, 64, 1851, 3, 32),
+                                          (1, 128, 1, 1, 1), (4, 128, 1000, 4, 32), (2, 64, 37, 3, 8)])
+def test_attention_plan_stays_within_one_wave(H, d, T, na, nq):
+    shape = (1, H, d, T)
+    ws, blocks = _attend_ws(H, d, T, na, nq)
+    assert blocks <= 304
+    assert kv.kvpool_attend_workspace_bytes(shape, na, nq) == ws
+    for rank in (16, 32):
+        assert kv.kvpool_attend_lora_workspace_bytes(shape, na, nq, rank) == _attend_ws(H, d, T, na, nq, rank)[0]
