@@ -34,6 +34,9 @@ KVP_MAX_LAYERS = 512
 KVP_K_PER_TENSOR = 0
 KVP_K_Q8_0 = 1
 KVP_NOALLOC_SCRATCH_BYTES = 262144
+KVP_PROBE_STORE = 0
+KVP_PROBE_BULK_STORE = 1
+KVP_PROBE_COPY = 2
 
 
 class Shape(C.Structure):
@@ -86,6 +89,7 @@ _SIGS = {
     "cachecard_status": (C.c_int, [_vp, _vp]),
     "kvp_strerror": (C.c_char_p, [C.c_int]),
     "kvp_launch_count": (C.c_uint64, []),
+    "kvp_bandwidth_probe": (C.c_int, [C.c_int, _vp, _vp, C.c_size_t, _vp]),
     "kvp_test_fail_next_encode": (C.c_int, [C.c_int, C.c_uint32]),
     "kvp_test_limit_next_attend": (C.c_int, [C.c_uint32]),
 }
@@ -260,6 +264,10 @@ def kvp_strerror(status):
 
 def kvp_launch_count():
     return int(load().kvp_launch_count())
+
+
+def kvp_bandwidth_probe(mode, dst, src, nbytes, stream=None):
+    return load().kvp_bandwidth_probe(int(mode), _addr(dst), _addr(src), int(nbytes), _stream(stream))
 
 
 def kvp_test_fail_next_encode(layer, spin_iters):

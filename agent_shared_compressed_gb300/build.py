@@ -18,7 +18,8 @@ INCLUDE = os.path.join(ROOT, "include")
 OBJ_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libkvcodec.so")
 
-SOURCES = ["kvp_host.cu", "kvpool_encode.cu", "kvpool_decode.cu", "cachecard.cu", "kvpool_noalloc.cu", "kvpool_attend.cu"]
+SOURCES = ["kvp_host.cu", "kvpool_encode.cu", "kvpool_decode.cu", "cachecard.cu", "kvpool_noalloc.cu", "kvpool_attend.cu",
+           "kvp_probe.cu"]
 HEADERS = ["kvp_internal.cuh", "kvp_vec.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -234,76 +234,106 @@ def aggregate_ranks(local_ms, steps, bytes_per_step, world, device):
     return ms_per_step, world * bytes_per_step / (ms_per_step * 1e-3) / 1e9
 
 
-def run_ours(args, rank, world, local_rank):
-    device = torch.device("cuda", local_rank)
-    torch.cuda.set_device(device)
-    kv.load()
-    w = workload(args)
-    c = Codec(w, device, seed=rank, k_mode=K_FORMATS[args.k_format])
+MIN_TIMED_S = 0.5          # the timed blocks together last at least this long
+MAX_BLOCKS = 60
+EXTRA_WORKLOADS = ["llama3-8b-32k-4agents"]  # timed beside the headline one in the default run
+
+
+def phase_stats(ms, alg_bytes, peak):
+    """Best / median / mean of one phase's per-step CUDA-event times (ms)."""
+    best, med = float(np.min(ms)), float(np.median(ms))
+    gbs = alg_bytes / (med * 1e-3) / 1e9
+    return {"ms": round(med, 4), "ms_best": round(best, 4), "ms_mean": round(float(np.mean(ms)), 4),
+            "alg_bytes": int(alg_bytes), "alg_GBps": round(gbs, 1),
+            "alg_GBps_best": round(alg_bytes / (best * 1e-3) / 1e9, 1),
+            "frac_of_measured_peak": round(gbs / peak, 4), "frac_of_8TBps": round(gbs / NOMINAL_HBM_GBS, 4)}
+
+
+def time_blocks(c, st, flush, steps, world, device, est_step_ms, local_rank):
+    """Time blocks of exactly `steps` steps, each bracketed by a barrier and a
+    device synchronisation on both sides, until the blocks together last at
+    least MIN_TIMED_S (so the clock sampler sees the GPU under load).
+    Returns (per-phase ms [blocks, steps, 4], launches, clocks summary)."""
+    blocks = int(min(MAX_BLOCKS, max(1, math.ceil(MIN_TIMED_S * 1e3 / max(1e-3, steps * est_step_ms)))))
+    if world > 1:  # every rank runs the same number of blocks
+        t = torch.tensor([blocks], dtype=torch.int64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        blocks = int(t.item())
+    phases = []
+    launches0 = kv.kvp_launch_count()
+    sampler = ClockSampler(local_rank)
+    with sampler:
+        for _ in range(blocks):
+            ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+            if world > 1:
+                torch.distributed.barrier()
+            torch.cuda.synchronize(device)
+            for i in range(steps):
+                if flush is not None:
+                    flush.zero_()
+                e = ev[i]
+                e[0].record(st)
+                c.encode(st)
+                e[1].record(st)
+                c.decode(st)
+                e[2].record(st)
+                c.pack(st)
+                e[3].record(st)
+                c.unpack(st)
+                e[4].record(st)
+            torch.cuda.synchronize(device)
+            if world > 1:
+                torch.distributed.barrier()
+            phases.append([[e[j].elapsed_time(e[j + 1]) for j in range(4)] for e in ev])
+    launches = kv.kvp_launch_count() - launches0
+    return np.array(phases), launches, sampler.summary()
+
+
+def measure_workload(name, w, args, rank, world, device, local_rank, k_mode, e2e=True):
+    """Set up one workload's replica, warm up, time it (median block) and
+    return (result dict, Codec, step bytes)."""
+    c = Codec(w, device, seed=rank, k_mode=k_mode)
     st = torch.cuda.current_stream(device)
     sb = step_bytes(w, c.pool_bytes, c.card_bytes)
     flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=device) if sb["raw"] < 4 * L2_BYTES else None
 
-    # warm-up (also reads the card header once: the unpack's host metadata)
-    for _ in range(args.warmup):
+    # warm-up (also reads the card header once: the unpack's host metadata);
+    # the last warm-up steps' times size the timed blocks
+    wev = [torch.cuda.Event(enable_timing=True) for _ in range(args.warmup + 1)]
+    wev[0].record(st)
+    for i in range(args.warmup):
         c.encode(st); c.decode(st); c.pack(st); c.unpack(st)
+        wev[i + 1].record(st)
     torch.cuda.synchronize(device)
     for rc, what in ((kv.kvpool_status(c.pool, st), "pool"), (kv.cachecard_status(c.card, st), "card")):
         if rc != kv.KVP_OK:
             raise RuntimeError("%s status after warm-up: %s" % (what, kv.kvp_strerror(rc)))
+    est_step_ms = min(wev[i].elapsed_time(wev[i + 1]) for i in range(1, args.warmup)) if args.warmup > 1 else 5.0
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize(device)
-    launches0 = kv.kvp_launch_count()
-    sampler = ClockSampler(local_rank)
-    with sampler:
-        for i in range(args.steps):
-            if flush is not None:
-                flush.zero_()
-            e = ev[i]
-            e[0].record(st)
-            c.encode(st)
-            e[1].record(st)
-            c.decode(st)
-            e[2].record(st)
-            c.pack(st)
-            e[3].record(st)
-            c.unpack(st)
-            e[4].record(st)
-        torch.cuda.synchronize(device)
-    launches = kv.kvp_launch_count() - launches0
-    if world > 1:
-        torch.distributed.barrier()
-    phase = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(4)] for e in ev])  # ms
-    ms_per_step, value = aggregate_ranks(float(phase.sum()), args.steps, sb["bf16_equiv"], world, device)
-
-    # end to end through the C ABI with host buffers: H2D of the step's K/V
-    # (and bitwidths) from pinned memory, the four calls, D2H of the pool and
-    # the card (the two shareable artefacts) and their status words.
-    e2e = run_e2e(c, st, device, args, sb)
+    phase, launches, clocks = time_blocks(c, st, flush, args.steps, world, device, est_step_ms, local_rank)
+    block_ms = phase.sum(axis=(1, 2))                 # [blocks]
+    med_block = float(np.median(block_ms))
+    ms_per_step, value = aggregate_ranks(med_block, args.steps, sb["bf16_equiv"], world, device)
 
     peak, peak_kind = hbm_peak()
-    dec_ms = float(phase[:, 1].mean())
-    achieved = sb["decode_alg"] / (dec_ms * 1e-3) / 1e9
-    traffic = recorded_traffic(args.workload, w["N"], w["T"], w["L"]) if args.k_format == "per_tensor" else None
+    flat = phase.reshape(-1, 4)
     names = ("encode", "decode", "pack", "unpack")
     algs = (sb["encode_alg"], sb["decode_alg"], sb["pack_alg"], sb["unpack_alg"])
-    breakdown = {}
-    for j, (n, b) in enumerate(zip(names, algs)):
-        ms = float(phase[:, j].mean())
-        breakdown[n] = {"ms": round(ms, 4), "alg_bytes": int(b), "alg_GBps": round(b / (ms * 1e-3) / 1e9, 1),
-                        "frac_of_measured_peak": round(b / (ms * 1e-3) / 1e9 / peak, 4),
-                        "frac_of_8TBps": round(b / (ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 4)}
-    if args.k_format == "per_tensor":
+    breakdown = {n: phase_stats(flat[:, j], b, peak) for j, (n, b) in enumerate(zip(names, algs))}
+    if k_mode == 0:
         breakdown["encode"]["implemented_bytes"] = int(sb["encode_alg"] + sb["raw"] // 2)  # K is read twice
-
+    dec_ms = breakdown["decode"]["ms"]
+    achieved = sb["decode_alg"] / (dec_ms * 1e-3) / 1e9
+    traffic = recorded_traffic(name, w["N"], w["T"], w["L"]) if k_mode == 0 else None
     out = {
-        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "io_dtype": "bf16", "data": "synthetic",
-        "config": {"workload": args.workload, "layers": w["L"], "kv_heads": w["H"], "head_dim": w["d"],
+        "value": round(value, 2), "unit": "GB/s", "ms_per_step": round(ms_per_step, 4),
+        "steps": args.steps, "blocks": int(phase.shape[0]),
+        "timed_s": round(float(block_ms.sum()) * 1e-3, 3),
+        "block_GBps": {"median": round(value, 2),
+                       "best": round(sb["bf16_equiv"] * args.steps / (float(block_ms.min()) * 1e-3) / 1e9 * world, 2),
+                       "worst": round(sb["bf16_equiv"] * args.steps / (float(block_ms.max()) * 1e-3) / 1e9 * world,
+                                      2)},
+        "config": {"workload": name, "layers": w["L"], "kv_heads": w["H"], "head_dim": w["d"],
                    "tokens": w["T"], "agents": w["N"], "k_format": args.k_format,
                    "card_bits": "iid {2,4,8,16} p={.25,.40,.25,.10}",
                    "l2": ("flushed between steps (2x L2 write)" if flush is not None
@@ -313,12 +343,83 @@ def run_ours(args, rank, world, local_rank):
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "frac_nominal_8000": round(achieved / NOMINAL_HBM_GBS, 4),
                      "alg_bytes_per_launch": int(sb["decode_alg"]), "traffic": traffic},
-        "e2e": e2e,
         "gpu_launches": int(launches),
-        "clocks": sampler.summary(),
+        "clocks": clocks,
         "breakdown": breakdown,
     }
+    if e2e:
+        # end to end through the C ABI with host buffers: H2D of the step's
+        # K/V (and bitwidths) from pinned memory, the four calls, D2H of the
+        # pool and the card (the two shareable artefacts) and their status
+        out["e2e"] = run_e2e(c, st, device, args, sb)
     return out, c, sb
+
+
+def store_ceilings(device, nbytes=8 << 30, reps=10):
+    """HBM ceilings of the codec's store patterns, measured by the library's
+    probe kernels over `nbytes` (far beyond L2): best and median GB/s of
+    `reps` launches each, CUDA events on the launching stream."""
+    st = torch.cuda.current_stream(device)
+    dst = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    src = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    out = {}
+    for name, mode, moved in (("store_v4", kv.KVP_PROBE_STORE, nbytes),
+                              ("bulk_store_4k", kv.KVP_PROBE_BULK_STORE, nbytes),
+                              ("copy_v4", kv.KVP_PROBE_COPY, 2 * nbytes)):
+        for _ in range(3):
+            kv.check(kv.kvp_bandwidth_probe(mode, dst, src, nbytes, st), name)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+        ev[0].record(st)
+        for i in range(reps):
+            kv.check(kv.kvp_bandwidth_probe(mode, dst, src, nbytes, st), name)
+            ev[i + 1].record(st)
+        torch.cuda.synchronize(device)
+        ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(reps)]
+        out[name] = {"GBps_best": round(moved / (min(ms) * 1e-3) / 1e9, 1),
+                     "GBps_median": round(moved / (float(np.median(ms)) * 1e-3) / 1e9, 1)}
+    del dst, src
+    torch.cuda.empty_cache()
+    out["bytes"] = int(nbytes)
+    return out
+
+
+def run_ours(args, rank, world, local_rank):
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    kv.load()
+    k_mode = K_FORMATS[args.k_format]
+    w = workload(args)
+    res, c, sb = measure_workload(args.workload, w, args, rank, world, device, local_rank, k_mode)
+    out = {
+        "metric": METRIC, "value": res["value"], "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": res["ms_per_step"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "io_dtype": "bf16", "data": "synthetic",
+        "config": res["config"], "roofline": res["roofline"], "e2e": res["e2e"],
+        "gpu_launches": res["gpu_launches"], "clocks": res["clocks"], "breakdown": res["breakdown"],
+        "timing": {"blocks": res["blocks"], "steps_per_block": args.steps, "timed_s": res["timed_s"],
+                   "value_from": "median block", "block_GBps": res["block_GBps"],
+                   "phase_ms": "median over every timed step (ms_best: best)"},
+    }
+    ks, vs = c.k, c.v  # the headline inputs stay for the CPU baseline; the rest is freed
+    host = {"oracle_inputs": (lambda i: (synth.bits16(ks[i]), synth.bits16(vs[i]))), "w": c.w}
+    del c
+    torch.cuda.empty_cache()
+    extra = EXTRA_WORKLOADS if (args.extra_workloads and args.workload == DEFAULT_WORKLOAD and
+                                not (args.agents or args.tokens or args.layers)) else []
+    if extra:
+        out["per_workload"] = {}
+        for name in extra:
+            r, c2, _ = measure_workload(name, dict(synth.WORKLOADS[name]), args, rank, world, device, local_rank,
+                                        k_mode)
+            out["per_workload"][name] = r
+            del c2
+            torch.cuda.empty_cache()
+    if args.ceilings and rank == 0:
+        out["store_ceilings"] = store_ceilings(device)
+        dec = out["breakdown"]["decode"]["alg_GBps"]
+        bulk = out["store_ceilings"]["bulk_store_4k"]["GBps_best"]
+        out["roofline"]["frac_of_bulk_store_ceiling"] = round(dec / bulk, 4)
+    return out, host, sb
 
 
 def run_e2e(c, st, device, args, sb):
@@ -448,6 +549,45 @@ def oracle_sample(w, seed, budget_s, layer_fn):
     desc = ("layers 0..%d of %d, all %d agents, whole step (encode, fan-out decode, card pack, unpack), "
             "%d repetitions" % (n - 1, L, N, reps))
     return gbs, O.get_threads(), desc, t
+
+
+def oracle_phases(w, seed, layer_fn, reps=3):
+    """Each phase of the step on the oracle (encode, fan-out decode into N,
+    card pack, card unpack) for layer 0 of the workload, on every host core
+    (OpenMP) and on one thread: best and median of `reps` runs, as seconds
+    and bf16-equivalent GB/s (encode and pack consume the layer's raw K/V,
+    decode produces N copies of it, unpack one)."""
+    import oracle as O
+    H, d, T, N = w["H"], w["d"], w["T"], w["N"]
+    raw1 = 2 * H * T * d * 2
+    bits = synth.card_bits(T, seed=seed).numpy()
+    k0, v0 = layer_fn(0)
+    pool, _, _ = O.pool_encode([k0], [v0])
+    card, _, _ = O.card_pack([k0], [v0], bits)
+    calls = {"encode": (lambda: O.pool_encode([k0], [v0]), raw1),
+             "decode": (lambda: O.pool_decode_into(pool, 0, 1, N), N * raw1),
+             "pack": (lambda: O.card_pack([k0], [v0], bits), raw1),
+             "unpack": (lambda: O.card_unpack(card), raw1)}
+    all_cores = O.get_threads()
+    out = {"sample": "layer 0 of %d (H=%d d=%d T=%d), %d agents; best and median of %d" % (w["L"], H, d, T, N, reps),
+           "threads_all": all_cores}
+    try:
+        for label, th in (("all_cores", all_cores), ("one_thread", 1)):
+            O.set_threads(th)
+            res = {}
+            for name, (fn, nbytes) in calls.items():
+                secs = []
+                for _ in range(reps):
+                    t0 = time.perf_counter()
+                    fn()
+                    secs.append(time.perf_counter() - t0)
+                best, med = min(secs), float(np.median(secs))
+                res[name] = {"s_best": round(best, 4), "s_median": round(med, 4),
+                             "GBps_best": round(nbytes / best / 1e9, 4), "GBps_median": round(nbytes / med / 1e9, 4)}
+            out[label] = res
+    finally:
+        O.set_threads(all_cores)
+    return out
 
 
 def run_reference(args, rank, world):
@@ -640,6 +780,10 @@ def main():
     ap.add_argument("--layers", type=int, default=0)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra-workloads", dest="extra_workloads", action="store_false",
+                    help="time only the selected workload (default: also the 32K-token / 4-agent pool)")
+    ap.add_argument("--no-ceilings", dest="ceilings", action="store_false",
+                    help="skip the store / copy ceiling probes")
     ap.add_argument("--lora-rank", type=int, default=0, choices=[0, 16, 32],
                     help="attend mode: agents' values carry a LoRA term from a shared low-rank cache of this rank")
     ap.add_argument("--k-format", choices=sorted(K_FORMATS), default="per_tensor",
@@ -668,15 +812,16 @@ def main():
     if world > 1:
         torch.cuda.set_device(local_rank)
         torch.distributed.init_process_group("nccl")
-    out, c, sb = run_ours(args, rank, world, local_rank)
+    out, host, sb = run_ours(args, rank, world, local_rank)
     if rank == 0:
         if args.no_cpu_baseline:
             out["cpu_baseline"] = None
         else:
-            gbs, cores, desc, secs = oracle_sample(
-                c.w, 0, args.cpu_budget, lambda i: (synth.bits16(c.k[i]), synth.bits16(c.v[i])))
+            gbs, cores, desc, secs = oracle_sample(host["w"], 0, args.cpu_budget, host["oracle_inputs"])
             out["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-                                   "sample": desc, "seconds": round(secs, 2)}
+                                   "sample": desc, "seconds": round(secs, 2),
+                                   "nproc": os.cpu_count(),
+                                   "per_phase": oracle_phases(host["w"], 0, host["oracle_inputs"])}
         print(json.dumps(out), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -39,8 +39,13 @@
  *    Conditions only the device can see (non-finite input, a value whose
  *    fp16 scale overflows, an invalid bitwidth in device memory) are
  *    recorded in an error word inside the pool / card header and returned
- *    by the *_status calls.  No kernel traps, asserts or waits on another
- *    block.
+ *    by the *_status calls.  No kernel traps or asserts.  Two kinds of
+ *    device-side wait exist, both bounded: the pool encoder's key-quantize
+ *    work waits for its layer's scale, released by another block of the same
+ *    kernel, and pool attention waits on mbarriers for its own bulk copies
+ *    into shared memory.  A wait that runs out is recorded in the error word
+ *    and reported as KVP_ERR_TIMEOUT by kvpool_status; the CUDA context stays
+ *    usable.
  */
 #ifndef KVPOOL_H
 #define KVPOOL_H
@@ -198,11 +203,13 @@ int kvpool_status(const void *pool, void *stream);
  * fixed array of KVP_NOALLOC_SCRATCH_BYTES in the library's device memory.
  *  Arguments and results are those of kvpool_encode minus ws / ws_bytes.
  *  Shapes whose kvpool_workspace_bytes() exceeds KVP_NOALLOC_SCRATCH_BYTES
- *    (about 240 layers at the largest per-layer partial count) are rejected
- *    with KVP_ERR_SIZE before anything is enqueued.
- *  The first call on a device looks up the array's device address (with
- *    that device current) and caches it; make that first call before any
- *    stream capture.
+ *    (more than 247 layers at the largest per-layer partial count, 256) are
+ *    rejected with KVP_ERR_SIZE before anything is enqueued.
+ *  The first call in each CUDA context looks up the array's device address
+ *    (with that context current) and caches it under the driver's context
+ *    id; make that first call before any stream capture.  A context created
+ *    later (after cudaDeviceReset, say) gets a fresh lookup on its first
+ *    call, so the library may outlive a context.
  *  Every call on a device shares the one array.  The encoder overwrites
  *    everything it reads from it, so nothing needs clearing between calls,
  *    but calls that overlap on the GPU (other streams, no ordering between
@@ -348,6 +355,26 @@ const char *kvp_strerror(int status);
 
 /* Number of kernels this library has launched in this process. */
 uint64_t kvp_launch_count(void);
+
+/* Bandwidth probes (the papers have no counterpart: measurement support).
+ * They give the HBM ceiling of the access pattern each codec kernel uses, so
+ * a benchmark can report a kernel against its own pattern's ceiling.
+ *  KVP_PROBE_STORE: write `bytes` to dst with 16-byte streaming stores, one
+ *    resident grid walking the buffer (the one-agent decode's and the card
+ *    unpack's store pattern).  bytes a multiple of 16.
+ *  KVP_PROBE_BULK_STORE: write `bytes` to dst as 4 KB bulk copies from
+ *    shared memory, one per warp (the fan-out decode's store pattern).
+ *    bytes a multiple of 4096.
+ *  KVP_PROBE_COPY: copy `bytes` from src to dst with 16-byte loads and
+ *    stores (read + write).  bytes a multiple of 16; src 256-byte aligned.
+ * dst: device buffer of at least `bytes`, 256-byte aligned; its contents are
+ * overwritten with an arbitrary pattern.  Enqueues one kernel on `stream`.
+ * Returns KVP_ERR_ARG (unknown mode, null pointer, zero bytes),
+ * KVP_ERR_ALIGN or KVP_ERR_SIZE before launching anything. */
+#define KVP_PROBE_STORE 0
+#define KVP_PROBE_BULK_STORE 1
+#define KVP_PROBE_COPY 2
+int kvp_bandwidth_probe(int mode, void *dst, const void *src, size_t bytes, void *stream);
 
 /* Failure-path testing.  The pool encoder's key-quantization work waits, with
  * an iteration limit, for a per-layer "scale ready" flag set by other blocks

@@ -191,3 +191,16 @@ def test_attention_plan_stays_within_one_wave(H, d, T, na, nq):
     assert kv.kvpool_attend_workspace_bytes(shape, na, nq) == ws
     for rank in (16, 32):
         assert kv.kvpool_attend_lora_workspace_bytes(shape, na, nq, rank) == _attend_ws(H, d, T, na, nq, rank)[0]
+
+
+def test_bandwidth_probe_argument_errors():
+    ok = 0x10000
+    assert kv.kvp_bandwidth_probe(7, ok, ok, 4096) == kv.KVP_ERR_ARG          # unknown mode
+    assert kv.kvp_bandwidth_probe(kv.KVP_PROBE_STORE, None, None, 4096) == kv.KVP_ERR_ARG
+    assert kv.kvp_bandwidth_probe(kv.KVP_PROBE_STORE, ok, None, 0) == kv.KVP_ERR_ARG
+    assert kv.kvp_bandwidth_probe(kv.KVP_PROBE_STORE, ok + 16, None, 4096) == kv.KVP_ERR_ALIGN
+    assert kv.kvp_bandwidth_probe(kv.KVP_PROBE_STORE, ok, None, 4100) == kv.KVP_ERR_SIZE
+    assert kv.kvp_bandwidth_probe(kv.KVP_PROBE_BULK_STORE, ok, None, 4096 + 16) == kv.KVP_ERR_SIZE
+    assert kv.kvp_bandwidth_probe(kv.KVP_PROBE_COPY, ok, None, 4096) == kv.KVP_ERR_ARG
+    assert kv.kvp_bandwidth_probe(kv.KVP_PROBE_COPY, ok, ok + 16, 4096) == kv.KVP_ERR_ALIGN
+    assert kv.kvp_bandwidth_probe(kv.KVP_PROBE_COPY, ok, ok, 4100) == kv.KVP_ERR_SIZE

@@ -61,7 +61,7 @@ def test_noalloc_encode_matches_workspace_encode_twice():
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
-    too_many_layers = (250, 8, 128, 32768)   # workspace 264,096 B > 262,144 B
+    too_many_layers = (250, 8, 128, 32768)   # workspace 264,352 B > 262,144 B
     assert kv.kvpool_workspace_bytes(too_many_layers) > kv.KVP_NOALLOC_SCRATCH_BYTES
     rc = kv.kvpool_encode_noalloc(too_many_layers, [0] * 250, [0] * 250, 0, 0)
     assert rc == kv.KVP_ERR_SIZE
