@@ -28,7 +28,7 @@ struct CardArgs {
     uint64_t off_offsets, off_layers, layer_stride;
     int L, H, T, d;
     int64_t shift;      // unpack_at: target offset - card offset
-    float inv_freq[64]; // unpack_at: rotary frequencies, d/2 of them
+    float2 rot[64];     // unpack_at: (cos, sin) of shift * w_i for the d/2 rotary frequencies w_i
 };
 
 // ---------------------------------------------------------------------------
@@ -438,30 +438,24 @@ __global__ void __launch_bounds__(CARD_THREADS) card_unpack(const __grid_constan
 // turn through shift * w_i, shift = pos_dst - card offset ("KVCMAS", How it
 // is used: the source cache's key positions are re-aligned to the target's;
 // "QKVShare", Methodology 2: the card carries the position offset).  The
-// angle is formed and its sine / cosine taken in fp64 once per block; each
-// key is dequantized and turned in fp32 and rounded to bf16 once.  Values
+// angle is formed and its sine / cosine taken in fp64 on the host, once per
+// call, and rounded to fp32; each key is dequantized and turned in fp32, two
+// coordinates per packed f32x2 instruction, and rounded to bf16 once.  Values
 // are unpacked as by card_unpack.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(CARD_THREADS, 4) card_unpack_rope(const __grid_constant__ CardArgs a) {
-    __shared__ float2 rot[64];  // (cos, sin) per frequency
-    for (int i = threadIdx.x; i < a.d / 2; i += CARD_THREADS) {
-        double sv, cv;
-        sincos(double(a.shift) * double(a.inv_freq[i]), &sv, &cv);
-        rot[i] = make_float2(float(cv), float(sv));
-    }
-    __syncthreads();
     const int lane = threadIdx.x & 31;
     const int cpr = a.d / 8, half = cpr / 2;  // chunks per row, per half row
     const int hshift = a.d == 128 ? 3 : 2;     // log2(half)
     const int npairs = a.H * half;
     // a lane's chunk within the half row is the same for every pair it takes
     const int chl = lane & (half - 1);
-    float rc[8], rs[8];
+    float2 rc[4], rs[4];  // (cos, sin) of the lane's 8 frequencies, two per packed register
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        const float2 r = rot[chl * 8 + e];
-        rc[e] = r.x;
-        rs[e] = r.y;
+    for (int e = 0; e < 4; ++e) {
+        const float2 r0 = a.rot[chl * 8 + 2 * e], r1 = a.rot[chl * 8 + 2 * e + 1];
+        rc[e] = make_float2(r0.x, r1.x);
+        rs[e] = make_float2(r0.y, r1.y);
     }
     const uint32_t T = uint32_t(a.T);
     const uint32_t tasks = uint32_t(a.L) * T * 2u;
@@ -525,11 +519,16 @@ __global__ void __launch_bounds__(CARD_THREADS, 4) card_unpack_rope(const __grid
                     card_chunk_values(b, make_uint2(ra[it].x, ra[it].y), pa[it], ya);
                     card_chunk_values(b, make_uint2(rb[it].x, rb[it].y), pb[it], yb);
                 }
+                // oa = ya cos - yb sin, ob = ya sin + yb cos: one product rounded, then one fma
                 float oa[8], ob[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    oa[e] = fmaf(ya[e], rc[e], -yb[e] * rs[e]);
-                    ob[e] = fmaf(ya[e], rs[e], yb[e] * rc[e]);
+                for (int e = 0; e < 4; ++e) {
+                    const float2 xa = make_float2(ya[2 * e], ya[2 * e + 1]), xb = make_float2(yb[2 * e], yb[2 * e + 1]);
+                    const float2 ta = __fmul2_rn(xb, rs[e]), tb = __fmul2_rn(xb, rc[e]);
+                    const float2 u = __ffma2_rn(xa, rc[e], make_float2(-ta.x, -ta.y));
+                    const float2 w = __ffma2_rn(xa, rs[e], tb);
+                    oa[2 * e] = u.x, oa[2 * e + 1] = u.y;
+                    ob[2 * e] = w.x, ob[2 * e + 1] = w.y;
                 }
                 st_stream_v4(dst + (uint64_t(h) * T + t) * cpr + (ca - h * cpr), pack_bf16x8(oa));
                 st_stream_v4(dst + (uint64_t(h) * T + t) * cpr + (cb - h * cpr), pack_bf16x8(ob));
@@ -661,7 +660,8 @@ extern "C" int cachecard_unpack_at(const void *card, const kvp_card_header *hdr,
     if (__builtin_sub_overflow(pos_dst, hdr->pos_offset, &a.shift)) return KVP_ERR_ARG;
     for (int i = 0; i < a.d / 2; ++i) {
         if (!std::isfinite(inv_freq[i])) return KVP_ERR_ARG;
-        a.inv_freq[i] = inv_freq[i];
+        const double ang = double(a.shift) * double(inv_freq[i]);
+        a.rot[i] = make_float2(float(std::cos(ang)), float(std::sin(ang)));
     }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const uint64_t tasks = uint64_t(a.L) * uint64_t(a.T) * 2u;
