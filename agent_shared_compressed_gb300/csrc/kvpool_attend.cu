@@ -31,7 +31,6 @@ constexpr int ATT_THREADS = 256;
 constexpr int ATT_WARPS = ATT_THREADS / 32;
 constexpr int ATT_TC = 64;  // tokens per sub-chunk
 constexpr int ATT_MT = 64;  // query rows per tile (the Q buffer)
-constexpr int ATT_TARGET_BLOCKS = 304;
 
 struct AttendArgs {
     const uint8_t *pool;
@@ -757,8 +756,12 @@ static bool attend_smem_ready() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
     if (!done[dev]) {
+        // two blocks per SM need the largest shared-memory carveout; without
+        // the preference the driver may configure the SM for one block
         if (cudaFuncSetAttribute(attend_split<D, TPW, R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 int(AttendSmem<D, R>::bytes)) != cudaSuccess)
+                                 int(AttendSmem<D, R>::bytes)) != cudaSuccess ||
+            cudaFuncSetAttribute(attend_split<D, TPW, R>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 int(cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
             return false;
         done[dev] = true;
     }
@@ -793,6 +796,32 @@ static int attend_dispatch(const AttendArgs &a, int d, bool narrow, dim3 grid, u
     return narrow ? attend_launch<64, 16, R>(a, grid, cgrid, st) : attend_launch<64, 32, R>(a, grid, cgrid, st);
 }
 
+// Blocks of the split kernel resident at once: SMs times blocks per SM (two:
+// about 100 KB of shared memory and 128 registers per thread each).  The
+// plan keeps the grid within that one wave.  Without a device (a size query
+// on a host without a GPU) it is made for the GB300's 152 SMs.
+static int attend_target_blocks() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
+        (void)cudaGetLastError();
+        return 2 * 152;
+    }
+    static int cached[64] = {0};
+    if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+    int occ = 0;
+    if (!attend_smem_ready<128, 32, 0>() ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, attend_split<128, 32, 0>, ATT_THREADS,
+                                                      AttendSmem<128, 0>::bytes) != cudaSuccess ||
+        occ < 1) {
+        (void)cudaGetLastError();
+        occ = 1;
+    }
+    const int n = sms * occ;
+    if (dev >= 0 && dev < 64) cached[dev] = n;
+    return n;
+}
+
 struct AttendPlan {
     int G, QH, QHP, nsub, per_split, nsplit;
     uint64_t part_off, stats_off, total;
@@ -804,7 +833,7 @@ static inline AttendPlan attend_plan(const kvp_shape *s, int na, int nq, int ran
     p.QH = na * p.G;
     p.QHP = (p.QH + ATT_MT - 1) / ATT_MT * ATT_MT;
     p.nsub = (s->n_tokens + ATT_TC - 1) / ATT_TC;
-    int want = ATT_TARGET_BLOCKS / s->n_kv_heads;  // splits per KV head: the grid stays within one wave
+    int want = attend_target_blocks() / s->n_kv_heads;  // splits per KV head: the grid stays within one wave
     if (want < 1) want = 1;
     if (want > p.nsub) want = p.nsub;
     p.per_split = (p.nsub + want - 1) / want;

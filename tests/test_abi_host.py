@@ -170,8 +170,10 @@ def test_strerror_and_counter():
 def _attend_ws(H, d, T, na, nq, rank=0):
     """The attention workspace the split plan implies: the splits of each KV
     head (64-token sub-chunks) are as many as keep the grid of H x splits
-    blocks within 304 (two per SM on 152 SMs); one partial row of d + rank
-    floats and one (max, sum) pair per query row (padded to 64) per split."""
+    blocks within one wave of resident blocks, which a host without a GPU
+    takes as 304 (two per SM on the GB300's 152 SMs); one partial row of
+    d + rank floats and one (max, sum) pair per query row (padded to 64) per
+    split."""
     nsub = (T + 63) // 64
     want = max(1, min(304 // H, nsub))
     per = (nsub + want - 1) // want
