@@ -152,14 +152,40 @@ __device__ uint16_t group_scale_f16(float mx, float mn, float qmax, float rcp_qm
 }
 
 // ---------------------------------------------------------------------------
-// Pack: one warp per (layer, token, K|V); one thread per group of 32
-// coordinates.  A thread loads its group's 64 contiguous bytes (L1-cached, so
-// the warp's 2 KB are fetched once), reduces min / max, takes the exactly
-// rounded fp16 scale, quantizes and packs its 32 codes (4b bytes) and stores
-// them with the group's (s_h, z_h).
+// Pack: one warp per (layer, token, K|V) task; one thread per group of 32
+// coordinates (a task with more than 32 groups takes several rounds).  A
+// thread loads its group's 64 contiguous bytes (L1-cached, so the warp's
+// 2 KB are fetched once), reduces min / max, takes the exactly rounded fp16
+// scale, quantizes and packs its 32 codes (4b bytes) and stores them with the
+// group's (s_h, z_h); a 16-bit token's group is copied as it is.  The warp's
+// rounds form one sequence, software-pipelined: the next round's group is
+// loaded before the current one is quantized, so a warp keeps two rounds'
+// loads in flight.  Codes are formed and packed eight at a time, which keeps
+// the live registers to the two groups and the packed output.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t pack_bytes4(uint32_t b0, uint32_t b1, uint32_t b2, uint32_t b3) {
     return __byte_perm(__byte_perm(b0, b1, 0x0040), __byte_perm(b2, b3, 0x0040), 0x5410);
+}
+
+// A pack task's coordinates: layer l, token t, kv (0 keys, 1 values).  A
+// warp's tasks advance by a fixed stride, so the coordinates are stepped
+// rather than divided out of the task index.
+struct PackPos {
+    uint32_t t;
+    int l, kv;
+};
+
+__device__ __forceinline__ void pack_load(const CardArgs &a, const PackPos &pos, int gi, int ngroups, int cpr,
+                                          int gshift, uint32_t T, uint4 (&w)[4]) {
+    if (gi < ngroups) {
+        const int h = gi >> gshift, gg = gi & ((1 << gshift) - 1);
+        const uint4 *p = a.src[pos.kv][pos.l] + (uint64_t(h) * T + pos.t) * cpr + gg * 4;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) w[q] = __ldg(p + q);
+    } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) w[q] = make_uint4(0, 0, 0, 0);
+    }
 }
 
 __global__ void __launch_bounds__(CARD_THREADS, 4) card_pack(const __grid_constant__ CardArgs a) {
@@ -168,129 +194,156 @@ __global__ void __launch_bounds__(CARD_THREADS, 4) card_pack(const __grid_consta
     const uint64_t stride = hdr->layer_stride;  // depends on the device-resident bitwidths
     const int lane = threadIdx.x & 31;
     const int cpr = a.d / 8;                     // 16-byte chunks per head row (8 or 16)
-    const int cshift = a.d == 128 ? 4 : 3;
-    const int gpr = a.d / 32;                    // groups per head row (2 or 4)
-    const int gshift = a.d == 128 ? 2 : 1;
-    const int nchunks = a.H * cpr;               // 16-byte chunks per (token, K|V)
-    const int ngroups = a.H * gpr;
+    const int gshift = a.d == 128 ? 2 : 1;       // log2(groups per head row)
+    const int ngroups = a.H * (a.d / 32);
+    const int rounds = (ngroups + 31) >> 5;
     const uint32_t T = uint32_t(a.T);
     const uint32_t tasks = uint32_t(a.L) * T * 2u;  // fits: checked on the host
     const uint8_t *bits = a.card + CARD_HEADER_BYTES;
     const uint32_t *offs = reinterpret_cast<const uint32_t *>(a.card + a.off_offsets);
+    const uint32_t tstep = gridDim.x * CARD_WARPS;
     uint32_t flags = 0;
 
-    for (uint32_t task = blockIdx.x * CARD_WARPS + (threadIdx.x >> 5); task < tasks;
-         task += gridDim.x * CARD_WARPS) {
-        const int kv = int(task & 1u);
-        const uint32_t lt = task >> 1;
-        const uint32_t t = lt % T;
-        const int l = int(lt / T);
+    uint32_t task = blockIdx.x * CARD_WARPS + (threadIdx.x >> 5);
+    // task = 2 (l T + t) + kv; the stride (a multiple of 2 CARD_WARPS) keeps kv
+    // and moves (l, t) by dl layers and dt tokens, with a carry
+    const uint32_t dlt = tstep >> 1, dt = dlt % T;
+    const int dl = int(dlt / T);
+    PackPos pos;
+    pos.kv = int(task & 1u);
+    pos.t = (task >> 1) % T;
+    pos.l = int((task >> 1) / T);
+    int round = 0;
+    uint4 w[4];
+    if (task < tasks) pack_load(a, pos, lane, ngroups, cpr, gshift, T, w);
+    while (task < tasks) {
+        // the next round of this warp's sequence, loaded now
+        uint32_t ntask = task;
+        PackPos npos = pos;
+        int nround = round + 1;
+        if (nround == rounds) {
+            nround = 0;
+            ntask += tstep;
+            npos.t += dt;
+            npos.l += dl;
+            if (npos.t >= T) {
+                npos.t -= T;
+                npos.l += 1;
+            }
+        }
+        uint4 wn[4];
+        if (ntask < tasks) pack_load(a, npos, nround * 32 + lane, ngroups, cpr, gshift, T, wn);
+
+        const int gi = round * 32 + lane;
+        const int kv = pos.kv;
+        const uint32_t t = pos.t;
+        const int l = pos.l;
         const int b = bits[t];
         uint8_t *rec = a.card + a.off_layers + uint64_t(l) * stride + offs[t];
-        const uint4 *src = a.src[kv][l];
         if (b == 16) {
-            uint4 *out = reinterpret_cast<uint4 *>(rec + uint64_t(kv) * a.H * a.d * 2);
-            for (int c = lane; c < nchunks; c += 32) {
-                const int h = c >> cshift, ch = c & (cpr - 1);
-                out[c] = ld_stream_v4(src + (uint64_t(h) * T + t) * cpr + ch);
-            }
-            continue;
-        }
-        const float qmax = float((1 << b) - 1);
-        const float rcp_qmax = 1.0f / qmax;
-        const uint64_t code_bytes = uint64_t(a.H) * a.d * b / 8;
-        uint8_t *codes = rec + uint64_t(kv) * code_bytes;
-        uint32_t *par = reinterpret_cast<uint32_t *>(rec + 2 * code_bytes + uint64_t(kv) * a.H * (a.d / 32) * 4);
-        for (int gi = lane; gi < ngroups; gi += 32) {
-            const int h = gi >> gshift, gg = gi & (gpr - 1);
-            const uint4 *p = src + (uint64_t(h) * T + t) * cpr + gg * 4;
-            uint32_t w[16];
+            if (gi < ngroups) {
+                uint4 *out = reinterpret_cast<uint4 *>(rec + uint64_t(kv) * a.H * a.d * 2) + 4 * gi;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const uint4 v = __ldg(p + q);
-                w[4 * q] = v.x;
-                w[4 * q + 1] = v.y;
-                w[4 * q + 2] = v.z;
-                w[4 * q + 3] = v.w;
+                for (int q = 0; q < 4; ++q) out[q] = w[q];
             }
-            float2 x[16];
-            // min / max on the packed bf16 pairs (exact).  The maximum propagates
-            // NaN, so a group holding Inf or NaN has a non-finite min or max.
-            __nv_bfloat162 mnp = *reinterpret_cast<const __nv_bfloat162 *>(&w[0]), mxp = mnp;
+        } else {
+            const uint64_t code_bytes = uint64_t(a.H) * a.d * b / 8;
+            if (gi < ngroups) {
+                const float qmax = float((1 << b) - 1);
+                const uint32_t ws[16] = {w[0].x, w[0].y, w[0].z, w[0].w, w[1].x, w[1].y, w[1].z, w[1].w,
+                                         w[2].x, w[2].y, w[2].z, w[2].w, w[3].x, w[3].y, w[3].z, w[3].w};
+                // min / max on the packed bf16 pairs (exact).  The maximum
+                // propagates NaN, so a group holding Inf or NaN has a non-finite
+                // min or max.
+                __nv_bfloat162 mnp = *reinterpret_cast<const __nv_bfloat162 *>(&ws[0]), mxp = mnp;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const __nv_bfloat162 pr = *reinterpret_cast<const __nv_bfloat162 *>(&w[i]);
-                mnp = __hmin2(mnp, pr);
-                mxp = __hmax2_nan(mxp, pr);
-                x[i] = make_float2(bf16_lo(w[i]), bf16_hi(w[i]));
-            }
-            const float mn = fminf(__low2float(mnp), __high2float(mnp));
-            const float mx0 = __low2float(mxp), mx1 = __high2float(mxp);
-            const float mx = fmaxf(mx0, mx1);
-            const bool nf = !(fabsf(mn) <= 3.0e38f) || !(fabsf(mx0) <= 3.0e38f) || !(fabsf(mx1) <= 3.0e38f);
-            const uint32_t sb = group_scale_f16(mx, mn, qmax, rcp_qmax);
-            const uint32_t zb = __half_as_ushort(__float2half_rn(mn));
-            if (nf)
-                flags |= FLAG_NONFINITE;
-            else if (((sb & 0x7C00u) == 0x7C00u) || ((zb & 0x7C00u) == 0x7C00u))
-                flags |= FLAG_RANGE;
-            const float sf = __half2float(__ushort_as_half(uint16_t(sb)));
-            const float zf = __half2float(__ushort_as_half(uint16_t(zb)));
-            const float inv = (sf > 0.0f && sf <= 65504.0f) ? __fdividef(1.0f, sf) : 0.0f;
-            // code = clamp(round((x - z_h) / s_h), 0, 2^b - 1): the low mantissa bits
-            // of (x - z_h) * r + 1.5*2^23, r the fast reciprocal of s_h (within 2
-            // ulp): for codes up to 255 the estimate is within 8e-5 of the exact
-            // quotient, so it rounds the same way unless that quotient lies
-            // within 8e-5 of a half-integer.  The map is monotone, so the clamp is
-            // needed only if the group's extremes fall outside the code range.
-            const float lo_c = RNE_MAGIC_C, hi_c = RNE_MAGIC_C + qmax;
-            const float tmn = fmaf(mn - zf, inv, RNE_MAGIC_C), tmx = fmaf(mx - zf, inv, RNE_MAGIC_C);
-            const bool clamp = !(tmn >= lo_c && tmx <= hi_c);
-            const float2 negz = make_float2(-zf, -zf), inv2 = make_float2(inv, inv);
-            const float2 mg = make_float2(RNE_MAGIC_C, RNE_MAGIC_C);
-            // q[i]: the code in the low byte, higher bits not cleared (the packing below
-            // selects or masks the low bits)
-            uint32_t q[32];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                float2 tf = __ffma2_rn(__fadd2_rn(x[i], negz), inv2, mg);
-                if (clamp) {
-                    tf.x = fminf(fmaxf(tf.x, lo_c), hi_c);
-                    tf.y = fminf(fmaxf(tf.y, lo_c), hi_c);
+                for (int i = 1; i < 16; ++i) {
+                    const __nv_bfloat162 pr = *reinterpret_cast<const __nv_bfloat162 *>(&ws[i]);
+                    mnp = __hmin2(mnp, pr);
+                    mxp = __hmax2_nan(mxp, pr);
                 }
-                q[2 * i] = __float_as_uint(tf.x);
-                q[2 * i + 1] = __float_as_uint(tf.y);
-            }
-            if (b == 8) {
-                uint4 *o = reinterpret_cast<uint4 *>(codes) + 2 * gi;
-                o[0] = make_uint4(pack_bytes4(q[0], q[1], q[2], q[3]), pack_bytes4(q[4], q[5], q[6], q[7]),
-                                  pack_bytes4(q[8], q[9], q[10], q[11]), pack_bytes4(q[12], q[13], q[14], q[15]));
-                o[1] = make_uint4(pack_bytes4(q[16], q[17], q[18], q[19]), pack_bytes4(q[20], q[21], q[22], q[23]),
-                                  pack_bytes4(q[24], q[25], q[26], q[27]), pack_bytes4(q[28], q[29], q[30], q[31]));
-            } else if (b == 4) {
-                uint32_t by[16];
+                const float mn = fminf(__low2float(mnp), __high2float(mnp));
+                const float mx0 = __low2float(mxp), mx1 = __high2float(mxp);
+                const float mx = fmaxf(mx0, mx1);
+                const bool nf = !(fabsf(mn) <= 3.0e38f) || !(fabsf(mx0) <= 3.0e38f) || !(fabsf(mx1) <= 3.0e38f);
+                const uint32_t sb = group_scale_f16(mx, mn, qmax, 1.0f / qmax);
+                const uint32_t zb = __half_as_ushort(__float2half_rn(mn));
+                if (nf)
+                    flags |= FLAG_NONFINITE;
+                else if (((sb & 0x7C00u) == 0x7C00u) || ((zb & 0x7C00u) == 0x7C00u))
+                    flags |= FLAG_RANGE;
+                const float sf = __half2float(__ushort_as_half(uint16_t(sb)));
+                const float zf = __half2float(__ushort_as_half(uint16_t(zb)));
+                const float inv = (sf > 0.0f && sf <= 65504.0f) ? __fdividef(1.0f, sf) : 0.0f;
+                // code = clamp(round((x - z_h) / s_h), 0, 2^b - 1): the low mantissa
+                // bits of (x - z_h) * r + 1.5*2^23, r the fast reciprocal of s_h
+                // (within 2 ulp): for codes up to 255 the estimate is within 8e-5
+                // of the exact quotient, so it rounds the same way unless that
+                // quotient lies within 8e-5 of a half-integer.  The map is
+                // monotone, so the clamp is needed only if the group's extremes
+                // fall outside the code range.
+                const float lo_c = RNE_MAGIC_C, hi_c = RNE_MAGIC_C + qmax;
+                const float tmn = fmaf(mn - zf, inv, RNE_MAGIC_C), tmx = fmaf(mx - zf, inv, RNE_MAGIC_C);
+                const bool clamp = !(tmn >= lo_c && tmx <= hi_c);
+                const float2 negz = make_float2(-zf, -zf), inv2 = make_float2(inv, inv);
+                const float2 mg = make_float2(RNE_MAGIC_C, RNE_MAGIC_C);
+                uint32_t out[8];  // packed codes: 4b bytes
 #pragma unroll
-                for (int i = 0; i < 16; ++i) by[i] = (q[2 * i] & 0xFu) | ((q[2 * i + 1] & 0xFu) << 4);
-                reinterpret_cast<uint4 *>(codes)[gi] =
-                    make_uint4(pack_bytes4(by[0], by[1], by[2], by[3]), pack_bytes4(by[4], by[5], by[6], by[7]),
-                               pack_bytes4(by[8], by[9], by[10], by[11]), pack_bytes4(by[12], by[13], by[14], by[15]));
-            } else {
-                uint32_t by[8];
+                for (int e = 0; e < 4; ++e) {  // 8 values (4 words) at a time
+                    uint32_t q[8];  // the code in the low bits, higher bits not cleared
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    by[i] = (q[4 * i] & 3u) | ((q[4 * i + 1] & 3u) << 2) | ((q[4 * i + 2] & 3u) << 4) |
-                            ((q[4 * i + 3] & 3u) << 6);
-                reinterpret_cast<uint2 *>(codes)[gi] =
-                    make_uint2(pack_bytes4(by[0], by[1], by[2], by[3]), pack_bytes4(by[4], by[5], by[6], by[7]));
+                    for (int i = 0; i < 4; ++i) {
+                        const uint32_t wv = ws[4 * e + i];
+                        float2 tf = __ffma2_rn(__fadd2_rn(make_float2(bf16_lo(wv), bf16_hi(wv)), negz), inv2, mg);
+                        if (clamp) {
+                            tf.x = fminf(fmaxf(tf.x, lo_c), hi_c);
+                            tf.y = fminf(fmaxf(tf.y, lo_c), hi_c);
+                        }
+                        q[2 * i] = __float_as_uint(tf.x);
+                        q[2 * i + 1] = __float_as_uint(tf.y);
+                    }
+                    if (b == 8) {
+                        out[2 * e] = pack_bytes4(q[0], q[1], q[2], q[3]);
+                        out[2 * e + 1] = pack_bytes4(q[4], q[5], q[6], q[7]);
+                    } else if (b == 4) {
+                        uint32_t by[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) by[i] = (q[2 * i] & 0xFu) | ((q[2 * i + 1] & 0xFu) << 4);
+                        out[e] = pack_bytes4(by[0], by[1], by[2], by[3]);
+                    } else {
+                        const uint32_t b0 = (q[0] & 3u) | ((q[1] & 3u) << 2) | ((q[2] & 3u) << 4) | ((q[3] & 3u) << 6);
+                        const uint32_t b1 = (q[4] & 3u) | ((q[5] & 3u) << 2) | ((q[6] & 3u) << 4) | ((q[7] & 3u) << 6);
+                        if (e & 1)
+                            out[e >> 1] |= (b0 << 16) | (b1 << 24);
+                        else
+                            out[e >> 1] = b0 | (b1 << 8);
+                    }
+                }
+                uint8_t *codes = rec + uint64_t(kv) * code_bytes;
+                if (b == 8) {
+                    uint4 *o = reinterpret_cast<uint4 *>(codes) + 2 * gi;
+                    o[0] = make_uint4(out[0], out[1], out[2], out[3]);
+                    o[1] = make_uint4(out[4], out[5], out[6], out[7]);
+                } else if (b == 4) {
+                    reinterpret_cast<uint4 *>(codes)[gi] = make_uint4(out[0], out[1], out[2], out[3]);
+                } else {
+                    reinterpret_cast<uint2 *>(codes)[gi] = make_uint2(out[0], out[1]);
+                }
+                uint32_t *par = reinterpret_cast<uint32_t *>(rec + 2 * code_bytes + uint64_t(kv) * a.H * (a.d / 32) * 4);
+                par[gi] = sb | (zb << 16);
             }
-            par[gi] = sb | (zb << 16);
+            // zero the record's padding (sizes are multiples of 8, records of 16)
+            if (kv == 1 && lane == 0 && round == rounds - 1) {
+                const uint64_t used = 2 * code_bytes + 2ull * a.H * (a.d / 32) * 4;
+                const uint64_t padded = card_record_bytes(b, a.H, a.d);
+                if (padded > used) *reinterpret_cast<uint2 *>(rec + used) = make_uint2(0, 0);
+            }
         }
-        // zero the record's padding (sizes are multiples of 8, records of 16)
-        if (kv == 1 && lane == 0) {
-            const uint64_t used = 2 * code_bytes + 2ull * a.H * (a.d / 32) * 4;
-            const uint64_t padded = card_record_bytes(b, a.H, a.d);
-            if (padded > used) *reinterpret_cast<uint2 *>(rec + used) = make_uint2(0, 0);
-        }
+        task = ntask;
+        pos = npos;
+        round = nround;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) w[q] = wn[q];
     }
     flags = __reduce_or_sync(0xffffffffu, flags);
     if (lane == 0 && flags) atomicOr(const_cast<uint32_t *>(&hdr->error), flags);
