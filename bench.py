@@ -69,9 +69,10 @@ def source_hash(paths):
 
 
 def recorded_traffic(workload, agents, tokens, layers):
-    """DRAM bytes (read + write) of one decode launch from the committed ncu
-    capture, if it was taken on this workload and on the current decode
-    kernel source; else None."""
+    """DRAM bytes (read + write) of one decode launch, from the committed ncu
+    capture of a small case scaled to this workload's launch, if the capture
+    is of the current decode kernel source and its scaling names this
+    workload; else None."""
     try:
         with open(TRAFFIC_FILE) as f:
             rec = json.load(f)
@@ -79,7 +80,8 @@ def recorded_traffic(workload, agents, tokens, layers):
         return None
     if rec.get("source_hash") != source_hash(DECODE_SOURCES):
         return None
-    if (rec.get("workload"), rec.get("agents"), rec.get("tokens"), rec.get("layers")) != (workload, agents, tokens, layers):
+    sc = rec.get("scale", {})
+    if (sc.get("workload"), sc.get("agents"), sc.get("tokens"), sc.get("layers")) != (workload, agents, tokens, layers):
         return None
     return rec.get("dram_bytes_per_launch")
 
