@@ -1,8 +1,9 @@
-// kvp_vec.cuh -- per-warp vector machinery shared by the pool encoder and
-// decoder: the register / warp-shuffle Walsh-Hadamard transform and the
-// 3-bit Lloyd-Max codebook.
+// kvp_vec.cuh -- per-warp vector machinery of the pool decoder (the
+// register / warp-shuffle Walsh-Hadamard transform), the packed f32x2
+// helpers, and the 3-bit Lloyd-Max codebook shared by the encoder, the
+// decoder and the attention kernels.
 //
-// Lane mapping.  A value vector of d = 64 or 128 coordinates is held by
+// Decoder lane mapping.  A value vector of d = 64 or 128 coordinates is held by
 // LPV = d/32 lanes, 32 coordinates per lane, as 4 chunks of 8 consecutive
 // coordinates: lane l of the vector holds chunks c = j*LPV + l (j = 0..3),
 // coordinate i = 8c + e (e = 0..7).  So coordinate bits 0-2 live in
@@ -16,63 +17,18 @@
 
 namespace kvp {
 
-// Unnormalised Sylvester-order Walsh-Hadamard transform of the vector held
-// in x by the LPV lanes of each vector ("PolyKV" 2.B.2 rotation):
-// y_i = sum_j (-1)^popcount(i & j) x_j, one butterfly stage per index bit.
-template <int LPV>
-__device__ __forceinline__ void fwht(float (&x)[4][8], int lane) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-#pragma unroll
-        for (int h = 1; h < 8; h <<= 1) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                if ((i & h) == 0) {
-                    const float p = x[j][i], q = x[j][i + h];
-                    x[j][i] = p + q;
-                    x[j][i + h] = p - q;
-                }
-            }
-        }
-    }
-#pragma unroll
-    for (int h = 1; h < 4; h <<= 1) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            if ((j & h) == 0) {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float p = x[j][i], q = x[j + h][i];
-                    x[j][i] = p + q;
-                    x[j + h][i] = p - q;
-                }
-            }
-        }
-    }
-    // Lane bits: the lane holding the lower index keeps p + q, the upper
-    // one p - q, i.e. new = partner + sgn * own with sgn = -1 on the upper.
-#pragma unroll
-    for (int m = 1; m < LPV; m <<= 1) {
-        const float sgn = (lane & m) ? -1.0f : 1.0f;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float o = __shfl_xor_sync(0xffffffffu, x[j][i], m);
-                x[j][i] = fmaf(sgn, x[j][i], o);
-            }
-        }
-    }
-}
-
-// The same transform on packed pairs: x[j][p] holds coordinates (8c + 2p,
-// 8c + 2p + 1) of chunk c = j*LPV + l, and the caller has already applied the
-// butterfly of coordinate bit 0 (x[j][p] = (a + b, a - b)).  The remaining
-// stages run as f32x2 operations; a - b is fma(b, -1, a), rounded once like
+// Packed f32x2 add and subtract; a - b is fma(b, -1, a), rounded once like
 // the subtraction.
 __device__ __forceinline__ float2 f2add(float2 a, float2 b) { return __fadd2_rn(a, b); }
 __device__ __forceinline__ float2 f2sub(float2 a, float2 b) { return __ffma2_rn(b, make_float2(-1.0f, -1.0f), a); }
 
+// Unnormalised Sylvester-order Walsh-Hadamard transform ("PolyKV" 2.B.2
+// rotation, y_i = sum_j (-1)^popcount(i & j) x_j, one butterfly stage per
+// index bit) of the vector held by the LPV lanes of each vector, on packed
+// pairs: x[j][p] holds coordinates (8c + 2p, 8c + 2p + 1) of chunk
+// c = j*LPV + l, and the caller has already applied the butterfly of
+// coordinate bit 0 (x[j][p] = (a + b, a - b)).  The remaining stages run as
+// f32x2 operations.
 template <int LPV>
 __device__ __forceinline__ void fwht_pairs(float2 (&x)[4][4], int lane) {
 #pragma unroll
@@ -126,17 +82,6 @@ __device__ __forceinline__ void fwht_pairs(float2 (&x)[4][4], int lane) {
 constexpr float THR1 = 0.50055f;  // (0.2451 + 0.7560) / 2
 constexpr float THR2 = 1.05f;     // (0.7560 + 1.3440) / 2
 constexpr float THR3 = 1.748f;    // (1.3440 + 2.1520) / 2
-
-// Code of a rotated coordinate y given the scaled thresholds T_k = t_k*||v||
-// (u = y/||v|| compared with t_k without a division): the number of
-// thresholds not above u.  For y >= 0 that is 4 + #{T_k <= |y|}; for y < 0
-// it is 3 - #{T_k < |y|}, taken here as 3 - #{T_k <= |y|} (the two differ
-// only when |y| equals a threshold exactly).
-__device__ __forceinline__ uint32_t v_code(float y, float T1, float T2, float T3) {
-    const float a = fabsf(y);
-    const uint32_t cnt = uint32_t(a >= T1) + uint32_t(a >= T2) + uint32_t(a >= T3);
-    return cnt ^ (y >= 0.0f ? 4u : 3u);
-}
 
 // Centroid of a code scaled by 10^4 -- the codebook's values are integers at
 // that scale (2451, 7560, 13440, 21520), so a Walsh-Hadamard transform of

@@ -21,6 +21,8 @@
 // whatever the number of resident blocks.  The last block to finish writes
 // the pool header with the OR of every error bit.  The workspace's control
 // block is zeroed on the stream before the kernel.
+#include <cfloat>
+
 #include "kvp_vec.cuh"
 
 namespace kvp {
@@ -266,33 +268,43 @@ __device__ __forceinline__ uint32_t k_code_exact(float k, float s, float q0) {
 
 template <bool PRESCALE>
 __device__ __forceinline__ uint2 k_quant8(uint4 w, float4 kp) {
-    float k[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
-                  bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
+    // pairs of keys (low and high bf16 half of each word), on f32x2 lanes
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+    float2 k[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) k[i] = make_float2(bf16_lo(ws[i]), bf16_hi(ws[i]));
     if (PRESCALE) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) k[i] = (k[i] * kp.z) * kp.w;
+        for (int i = 0; i < 4; ++i) k[i] = __fmul2_rn(__fmul2_rn(k[i], make_float2(kp.z, kp.z)), make_float2(kp.w, kp.w));
     }
-    uint32_t t[8];
+    const float2 r = make_float2(kp.y, kp.y), mg = make_float2(RNE_MAGIC, RNE_MAGIC);
+    float2 tf[4];
     bool near = false;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const float tf = fmaf(k[i], kp.y, RNE_MAGIC);
-        const float q0 = tf - RNE_MAGIC;
-        const float e = fmaf(k[i], kp.y, -q0);
-        near |= fabsf(e) > 0.4999f;
-        t[i] = __float_as_uint(tf);
+    for (int i = 0; i < 4; ++i) {
+        tf[i] = __ffma2_rn(k[i], r, mg);
+        const float2 nq0 = __ffma2_rn(tf[i], make_float2(-1.0f, -1.0f), mg);  // -q0, exact
+        const float2 e = __ffma2_rn(k[i], r, nq0);
+        near |= fabsf(e.x) > 0.4999f;
+        near |= fabsf(e.y) > 0.4999f;
+    }
+    uint32_t t[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        t[2 * i] = __float_as_uint(tf[i].x);
+        t[2 * i + 1] = __float_as_uint(tf[i].y);
     }
     if (near) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float q0 = __uint_as_float(t[i]) - RNE_MAGIC;
-            t[i] = k_code_exact(k[i], kp.x, q0);
+        for (int i = 0; i < 4; ++i) {
+            t[2 * i] = k_code_exact(k[i].x, kp.x, tf[i].x - RNE_MAGIC);
+            t[2 * i + 1] = k_code_exact(k[i].y, kp.x, tf[i].y - RNE_MAGIC);
         }
     }
-    uint2 r;
-    r.x = __byte_perm(__byte_perm(t[0], t[1], 0x0040), __byte_perm(t[2], t[3], 0x0040), 0x5410);
-    r.y = __byte_perm(__byte_perm(t[4], t[5], 0x0040), __byte_perm(t[6], t[7], 0x0040), 0x5410);
-    return r;
+    uint2 r8;
+    r8.x = __byte_perm(__byte_perm(t[0], t[1], 0x0040), __byte_perm(t[2], t[3], 0x0040), 0x5410);
+    r8.y = __byte_perm(__byte_perm(t[4], t[5], 0x0040), __byte_perm(t[6], t[7], 0x0040), 0x5410);
+    return r8;
 }
 
 __device__ void quant_slice(const EncodeArgs &a, int l, uint32_t p, uint64_t pol) {
@@ -324,12 +336,41 @@ __device__ void quant_slice(const EncodeArgs &a, int l, uint32_t p, uint64_t pol
 }
 
 // ---------------------------------------------------------------------------
-// Values ("PolyKV" 2.B.2): one warp step, VPW consecutive vectors of one layer
-// (see kvp_vec.cuh for the lane mapping).  Returns error bits.
+// Values ("PolyKV" 2.B.2): one warp step encodes 1024 coordinates, the 8
+// vectors of d = 128 or 16 of d = 64 that follow one another in the layer.
+//
+// Rotation.  The Sylvester-order Walsh-Hadamard matrix is the Kronecker
+// product of H_2 over the bits of the coordinate index, so any 4 of the
+// index bits can be transformed at once by H_16 and the others separately.
+// Four bits go through the tensor cores: mma.m16n8k16 with the vector's bf16
+// elements as A and H_16 (entries +-1, exact in bf16) as B, so every product
+// is exact and the sums are fp32.  The other 3 bits (d = 128) or 2 bits
+// (d = 64) are butterflies on fp32 pairs in registers.
+//
+// The MMA's k and n index bits (k0, k1, k2, k3) stand for the coordinate
+// bits (i0, i5, i6, i1) at d = 128 and (i0, i4, i5, i1) at d = 64: the same
+// relabelling on both sides, so B is H_16 in natural order.  A row is a
+// (vector, i2, i3 [, i4]) combination.  Then each 16-byte chunk of the input
+// is one A fragment as it stands (registers x, z, y, w), and lane (g, q) =
+// (lane / 4, lane % 4) ends up with the consecutive rotated coordinates
+// [q d/4, (q+1) d/4) of vector g (and of vector 8 + g at d = 64): the C
+// element c_{2h+e} of M-tile m, N-tile nt is local coordinate 8t + 4h + 2nt
+// + e, t = m (d = 128) or m % 2 (d = 64).
+//
+// Codes.  u = y / ||v|| (y = H_d v, unnormalised) falls in cell
+// cnt ^ (y >= 0 ? 4 : 3) with cnt = #{k : |y| >= t_k ||v||}.  With
+// S = ||y||^2 = d ||v||^2 (Parseval), |y| >= t_k ||v|| exactly when
+// y^2 - (t_k^2 / d) S >= 0, and one fma gives that difference with an exact
+// sign.  Let n_k be the sign bits of the three differences and s the sign
+// of y.  The cells are nested (n1 >= n2 >= n3), so
+//     code bit 2 = ~s,  bit 1 = ~(n2 ^ s),  bit 0 = ~(n1 ^ n2 ^ n3 ^ s):
+// the sign bits of y, of P = d2 * y (a product's sign is the xor of its
+// factors' signs) and of Q = d1 ^ d3 ^ P, inverted.  Each bit is funnel-
+// shifted into the little-endian code words, highest coordinate first.
 // ---------------------------------------------------------------------------
 
-// Slow path for the rare vector whose squared norm is not finite: Inf/NaN in
-// the input (NONFINITE) or finite values too large for sigma (RANGE).
+// Slow path for the rare vector whose S is not finite: Inf/NaN in the input
+// (NONFINITE) or finite values too large for sigma (RANGE).
 __device__ uint32_t classify_nonfinite(const uint4 *vec, int nchunks) {
     for (int c = 0; c < nchunks; ++c) {
         const uint4 w = vec[c];
@@ -340,131 +381,234 @@ __device__ uint32_t classify_nonfinite(const uint4 *vec, int nchunks) {
     return FLAG_RANGE;
 }
 
-// Issue the cp.async copies of one warp step's value data into a lane-private
-// buffer: lane l's 4 chunks at buf[j][lane] (chunk-major, so the later 16-byte
-// reads of a warp are conflict-free).  Lanes past the layer's last vector get
-// zeros.  Always commits one group.
+// Slot of chunk c of vector v (within the warp step) in the warp's 2 KB
+// staging buffer.  The XOR swizzle makes both the coalesced fill and the
+// fragment reads conflict-free: the 8 lanes of a quarter-warp always reach
+// 8 different 16-byte bank groups.
 template <int D>
-__device__ __forceinline__ void v_prefetch(const EncodeArgs &a, int layer, uint64_t step, uint4 (*buf)[32],
-                                           uint64_t pol) {
-    constexpr int LPV = D / 32;
-    constexpr int VPW = 32 / LPV;
+__device__ __forceinline__ int v_slot(int v, int c) {
     constexpr int CPV = D / 8;
+    return v * CPV + (D == 128 ? (c ^ (((c >> 3) & 1) << 1) ^ (v & 1)) : (c ^ (v & 1)));
+}
+
+// Issue the cp.async copies of one warp step's 2 KB of value data into the
+// staging buffer: instruction j, lane i copies the step's 16-byte chunk
+// 32j + i.  Vectors past the layer's end get zeros.  Always commits one group.
+template <int D>
+__device__ __forceinline__ void v_prefetch(const EncodeArgs &a, int layer, uint64_t step, uint4 *buf, uint64_t pol) {
+    constexpr int CPV = D / 8;
+    constexpr int VPW = 1024 / D;
     const int lane = threadIdx.x & 31;
-    const int g = lane / LPV, l = lane % LPV;
-    const uint64_t n = step * VPW + g;
-    const bool valid = step < a.steps_per_layer && n < a.nvec;
-    const uint4 *vec = a.v[layer] + (valid ? n * CPV : 0);
+    const uint64_t n0 = step * VPW;
+    const bool live = step < a.steps_per_layer;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) cp_async16(&buf[j][lane], vec + j * LPV + l, valid ? 16u : 0u, pol);
+    for (int j = 0; j < 4; ++j) {
+        const int C = 32 * j + lane;
+        const int v = C / CPV, c = C % CPV;
+        const bool valid = live && n0 + uint64_t(v) < a.nvec;
+        const uint4 *src = a.v[layer] + (valid ? (n0 + uint64_t(v)) * CPV + uint64_t(c) : 0);
+        cp_async16(buf + v_slot<D>(v, c), src, valid ? 16u : 0u, pol);
+    }
     cp_async_commit();
 }
 
+// The B fragments of H_16 for N-tiles 0 and 1: lane (g, q) holds the entries
+// (k, n) = (2q + {0, 1}, 8nt + g) and (2q + 8 + {0, 1}, 8nt + g), +-1 in bf16
+// with the lower k in the low half.
+__device__ __forceinline__ void h16_fragments(uint32_t (&hb)[2][2]) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int k = 2 * q + 8 * r, n = 8 * nt + g;
+            const uint32_t lo = (__popc(k & n) & 1) ? 0xBF80u : 0x3F80u;
+            const uint32_t hi = (__popc((k + 1) & n) & 1) ? 0xBF80u : 0x3F80u;
+            hb[nt][r] = lo | (hi << 16);
+        }
+}
+
+__device__ __forceinline__ void mma_h16(float2 &lo, float2 &hi, uint4 w, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%10,%10,%10,%10};"
+        : "=f"(lo.x), "=f"(lo.y), "=f"(hi.x), "=f"(hi.y)
+        : "r"(w.x), "r"(w.z), "r"(w.y), "r"(w.w), "r"(b0), "r"(b1), "f"(0.0f));
+}
+
+__device__ __forceinline__ void bfly2(float2 &a, float2 &b) {
+    const float2 s = f2add(a, b);
+    b = f2sub(a, b);
+    a = s;
+}
+
+// Appends bit 31 of src below the bits already in word.
+__device__ __forceinline__ void put_bit(uint32_t &word, float src) {
+    word = __funnelshift_l(__float_as_uint(src), word, 1);
+}
+__device__ __forceinline__ void put_bit(uint32_t &word, uint32_t src) { word = __funnelshift_l(src, word, 1); }
+
+// Codes of one lane's coordinates of one vector: pairs y[p] hold local
+// coordinates (2p, 2p + 1); nt_k = -(t_k^2 / d) S.  W gets the 3 NP * 2 bits,
+// code of local coordinate j at bits 3j .. 3j + 2 (inverted afterwards).
+template <int NP>
+__device__ __forceinline__ void v_codes(const float2 (&y)[NP], float nt1, float nt2, float nt3,
+                                        uint32_t (&W)[(6 * NP + 31) / 32]) {
+    const float2 n1 = make_float2(nt1, nt1), n2 = make_float2(nt2, nt2), n3 = make_float2(nt3, nt3);
+#pragma unroll
+    for (int p = NP - 1; p >= 0; --p) {
+        const float2 yy = y[p];
+        const float2 d1 = __ffma2_rn(yy, yy, n1), d2 = __ffma2_rn(yy, yy, n2), d3 = __ffma2_rn(yy, yy, n3);
+        const float2 P = __fmul2_rn(d2, yy);
+        const uint32_t qx = __float_as_uint(d1.x) ^ __float_as_uint(d3.x) ^ __float_as_uint(P.x);
+        const uint32_t qy = __float_as_uint(d1.y) ^ __float_as_uint(d3.y) ^ __float_as_uint(P.y);
+        const int j1 = 2 * p + 1, j0 = 2 * p;
+        put_bit(W[(3 * j1 + 2) >> 5], yy.y);
+        put_bit(W[(3 * j1 + 1) >> 5], P.y);
+        put_bit(W[(3 * j1) >> 5], qy);
+        put_bit(W[(3 * j0 + 2) >> 5], yy.x);
+        put_bit(W[(3 * j0 + 1) >> 5], P.x);
+        put_bit(W[(3 * j0) >> 5], qx);
+    }
+}
+
+// t_k^2 for the Lloyd-Max decision thresholds t_k (kvp_vec.cuh).
+constexpr float TSQ1 = float(double(THR1) * double(THR1));
+constexpr float TSQ2 = float(double(THR2) * double(THR2));
+constexpr float TSQ3 = float(double(THR3) * double(THR3));
+
 template <int D>
-__device__ uint32_t v_encode_step(const EncodeArgs &a, int layer, uint64_t step, uint8_t *stage,
-                                  const uint4 (*buf)[32]) {
-    constexpr int LPV = D / 32;      // lanes per vector
-    constexpr int VPW = 32 / LPV;    // vectors per warp step
-    constexpr int CPV = D / 8;       // 16-byte chunks per vector
-    constexpr int CB = 3 * D / 8;    // code bytes per vector
-    static_assert(VPW * CB == 384, "a warp step stages 384 code bytes");
-    const int lane = threadIdx.x & 31;
-    const int g = lane / LPV, l = lane % LPV;
-    const uint64_t nvec = a.nvec;
-    const float inv_d = 1.0f / float(D);
-    uint32_t flags = 0;
-
+__device__ uint32_t v_encode_step(const EncodeArgs &a, int layer, uint64_t step, const uint4 *buf,
+                                  const uint32_t (&hb)[2][2]) {
+    constexpr int VPW = 1024 / D;           // vectors per warp step
+    constexpr int NV = D == 128 ? 1 : 2;    // vectors per lane
+    constexpr int NP = D / 8;               // coordinate pairs per lane and vector
+    constexpr int CPV = D / 8;              // 16-byte chunks per vector
+    constexpr int CB = 3 * D / 8;           // code bytes per vector
+    constexpr float INV_D = 1.0f / float(D);
+    const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
     const uint64_t n0 = step * VPW;
-    const uint64_t n = n0 + g;
-    const bool valid = n < nvec;
-    const uint4 *vec = a.v[layer] + n * CPV;
 
-    // x[j][p] = (v_a + v_b, v_a - v_b) for the coordinate pair (a, b) = (2p, 2p+1)
-    // of chunk j: the first butterfly stage is applied while unpacking.
-    uint4 w[4];
+    // y[m][nt][h] = (c_{2h}, c_{2h+1}) of M-tile m, N-tile nt
+    float2 y[4][2][2];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) w[j] = buf[j][lane];
-    float2 x[4][4];
-    float2 n2v = make_float2(0.0f, 0.0f);
+    for (int m = 0; m < 4; ++m) {
+        const int v = D == 128 ? g : 8 * (m >> 1) + g;
+        const int c = D == 128 ? 4 * q + m : 2 * q + (m & 1);
+        const uint4 w = buf[v_slot<D>(v, c)];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const uint32_t ws[4] = {w[j].x, w[j].y, w[j].z, w[j].w};
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-            const float2 v = make_float2(bf16_lo(ws[p]), bf16_hi(ws[p]));
-            n2v = __ffma2_rn(v, v, n2v);
-            x[j][p] = make_float2(v.x + v.y, v.x - v.y);
-        }
+        for (int nt = 0; nt < 2; ++nt) mma_h16(y[m][nt][0], y[m][nt][1], w, hb[nt][0], hb[nt][1]);
     }
-    float n2 = n2v.x + n2v.y;
+    // the register-held index bits: i2 (h), i3 (bit 0 of m) and, at d = 128, i4 (bit 1 of m)
 #pragma unroll
-    for (int m = 1; m < LPV; m <<= 1) n2 += __shfl_xor_sync(0xffffffffu, n2, m);
+    for (int m = 0; m < 4; ++m)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) bfly2(y[m][nt][0], y[m][nt][1]);
+#pragma unroll
+    for (int m = 0; m < 4; m += 2)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) bfly2(y[m][nt][h], y[m + 1][nt][h]);
+    if (D == 128) {
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) bfly2(y[m][nt][h], y[m + 2][nt][h]);
+    }
 
-    fwht_pairs<LPV>(x, lane);
+    // the lane's pairs per vector, in local-coordinate order: pair p = 4t + 2h + nt
+    float2 yp[NV][NP];
+#pragma unroll
+    for (int vi = 0; vi < NV; ++vi)
+#pragma unroll
+        for (int p = 0; p < NP; ++p) {
+            const int t = p >> 2, h = (p >> 1) & 1, nt = p & 1;
+            yp[vi][p] = y[D == 128 ? t : 2 * vi + t][nt][h];
+        }
 
-    // Thresholds t_k * ||v|| in the unnormalised rotated domain.
-    float nrm = sqrtf(n2);
-    uint16_t sig_bits = __half_as_ushort(__float2half_rn(sqrtf(n2 * inv_d)));
-    // A norm below 2^-50 loses precision to underflow in n2: rescale the
-    // rotated vector by 2^60 (exact) and take the norm from it through
-    // Parseval (||y||^2 = d ||v||^2).  sigma is below 2^-53: fp16 zero.
-    const bool tiny = n2 < 0x1p-100f;
-    if (__any_sync(0xffffffffu, tiny)) {
-        float s2 = 0.0f;
-        const float2 sc = make_float2(0x1p60f, 0x1p60f);
+    float S[NV];
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
+    for (int vi = 0; vi < NV; ++vi) {
+        float2 acc = make_float2(0.0f, 0.0f);
 #pragma unroll
-            for (int p = 0; p < 4; ++p) {
-                const float2 ys = __fmul2_rn(x[j][p], sc);
-                if (tiny) x[j][p] = ys;
-                s2 = fmaf(ys.x, ys.x, fmaf(ys.y, ys.y, s2));
+        for (int p = 0; p < NP; ++p) acc = __ffma2_rn(yp[vi][p], yp[vi][p], acc);
+        S[vi] = acc.x + acc.y;
+        S[vi] += __shfl_xor_sync(0xffffffffu, S[vi], 1);
+        S[vi] += __shfl_xor_sync(0xffffffffu, S[vi], 2);
+    }
+    bool tiny[NV];
+    bool any_tiny = false;
+#pragma unroll
+    for (int vi = 0; vi < NV; ++vi) {
+        tiny[vi] = S[vi] < 0x1p-100f;
+        any_tiny |= tiny[vi];
+    }
+    // S below 2^-100 loses precision to underflow in the squares: rescale the
+    // rotated vector by 2^60 (exact) and take S again (codes are scale-free;
+    // sigma is below 2^-56, an fp16 zero).  A zero vector gets +0 everywhere
+    // and thresholds above every square: every code 4.
+    if (__any_sync(0xffffffffu, any_tiny)) {
+#pragma unroll
+        for (int vi = 0; vi < NV; ++vi) {
+            const float f = tiny[vi] ? 0x1p60f : 1.0f;
+            float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+            for (int p = 0; p < NP; ++p) {
+                yp[vi][p] = __fmul2_rn(yp[vi][p], make_float2(f, f));
+                acc = __ffma2_rn(yp[vi][p], yp[vi][p], acc);
             }
+            float s2 = acc.x + acc.y;
+            s2 += __shfl_xor_sync(0xffffffffu, s2, 1);
+            s2 += __shfl_xor_sync(0xffffffffu, s2, 2);
+            if (tiny[vi]) {
+                S[vi] = s2;
+                if (s2 == 0.0f) {
 #pragma unroll
-        for (int m = 1; m < LPV; m <<= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, m);
-        if (tiny) {
-            nrm = sqrtf(s2 * inv_d);
-            sig_bits = 0;
+                    for (int p = 0; p < NP; ++p) yp[vi][p] = make_float2(0.0f, 0.0f);
+                }
+            }
         }
     }
-    // RANGE: finite input whose sigma exceeds fp16; non-finite input is
-    // NONFINITE only.
-    if (valid && !(n2 <= 3.0e38f))
-        flags |= classify_nonfinite(vec, CPV);
-    else if (valid && (sig_bits & 0x7C00u) == 0x7C00u)
-        flags |= FLAG_RANGE;
 
-    float T1 = THR1 * nrm, T2 = THR2 * nrm, T3 = THR3 * nrm;
-    if (nrm == 0.0f) T1 = T2 = T3 = __int_as_float(0x7F800000);  // zero vector: all codes 4
-
-    uint8_t *st = stage + g * CB;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        uint32_t cw = 0;
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-            cw |= v_code(x[j][p].x, T1, T2, T3) << (6 * p);
-            cw |= v_code(x[j][p].y, T1, T2, T3) << (6 * p + 3);
-        }
-        const int c = j * LPV + l;
-        st[3 * c + 0] = uint8_t(cw);
-        st[3 * c + 1] = uint8_t(cw >> 8);
-        st[3 * c + 2] = uint8_t(cw >> 16);
-    }
-    __syncwarp();
-
+    uint32_t flags = 0;
     uint8_t *lay = a.pool + a.geo.off_layers + uint64_t(layer) * a.geo.layer_stride;
-    const uint64_t nv_here = min(uint64_t(VPW), nvec - n0);
-    const uint32_t bytes = uint32_t(nv_here) * CB;
-    uint8_t *vdst = lay + a.geo.sec_v + n0 * CB;
-    const uint32_t off = uint32_t(lane) * 16u;
-    if (off + 16u <= bytes) {
-        __stcs(reinterpret_cast<uint4 *>(vdst + off), *reinterpret_cast<const uint4 *>(stage + off));
-    } else if (off < bytes) {  // bytes is a multiple of 8
-        __stcs(reinterpret_cast<uint2 *>(vdst + off), *reinterpret_cast<const uint2 *>(stage + off));
+#pragma unroll
+    for (int vi = 0; vi < NV; ++vi) {
+        const uint64_t n = n0 + uint64_t(D == 128 ? g : 8 * vi + g);
+        const bool valid = n < a.nvec;
+        const float s = S[vi];
+        const uint16_t sig_bits = tiny[vi] ? 0 : __half_as_ushort(__float2half_rn(sqrtf(s) * INV_D));
+        // RANGE: finite input whose sigma exceeds fp16; non-finite input is NONFINITE only
+        if (valid && !(s <= 3.0e38f))
+            flags |= classify_nonfinite(a.v[layer] + n * CPV, CPV);
+        else if (valid && (sig_bits & 0x7C00u) == 0x7C00u)
+            flags |= FLAG_RANGE;
+        // a zero vector (y = +0): thresholds below every square, but finite,
+        // so that P = d2 * y is -0 and not inf * 0
+        const float nt1 = s == 0.0f ? -FLT_MAX : -(s * (TSQ1 * INV_D));
+        const float nt2 = s == 0.0f ? -FLT_MAX : -(s * (TSQ2 * INV_D));
+        const float nt3 = s == 0.0f ? -FLT_MAX : -(s * (TSQ3 * INV_D));
+        uint32_t W[(6 * NP + 31) / 32];
+#pragma unroll
+        for (int i = 0; i < (6 * NP + 31) / 32; ++i) W[i] = 0;
+        v_codes<NP>(yp[vi], nt1, nt2, nt3, W);
+        if (valid) {
+            uint8_t *dst = lay + a.geo.sec_v + n * CB + uint64_t(q) * (CB / 4);
+            if (D == 128) {
+#pragma unroll
+                for (int i = 0; i < 3; ++i) __stcs(reinterpret_cast<unsigned int *>(dst) + i, ~W[i]);
+            } else {
+                unsigned short *d16 = reinterpret_cast<unsigned short *>(dst);
+                __stcs(d16 + 0, (unsigned short)(~W[0]));
+                __stcs(d16 + 1, (unsigned short)(~W[0] >> 16));
+                __stcs(d16 + 2, (unsigned short)(~W[1]));
+            }
+            if (q == 0) __stcs(reinterpret_cast<unsigned short *>(lay + a.geo.sec_sigma) + n, (unsigned short)sig_bits);
+        }
     }
-    if (valid && l == 0) __stcs(reinterpret_cast<unsigned short *>(lay + a.geo.sec_sigma) + n, (unsigned short)sig_bits);
-    __syncwarp();
     return flags;
 }
 
@@ -496,12 +640,13 @@ __device__ void write_header(const EncodeArgs &a) {
 
 template <int D>
 __global__ void __launch_bounds__(ENC_THREADS, 3) encode_pool(const __grid_constant__ EncodeArgs a) {
-    __shared__ __align__(16) uint8_t stage[ENC_WARPS][384];
-    __shared__ __align__(16) uint4 vbuf[ENC_WARPS][2][4][32];  // per warp: two steps of value data
+    __shared__ __align__(16) uint4 vbuf[ENC_WARPS][2][128];  // per warp: two steps of value data
     __shared__ uint32_t red[ENC_WARPS];
     __shared__ uint32_t s_item[2], s_flag;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint64_t keep = l2_evict_last_policy(), drop = l2_evict_first_policy();
+    uint32_t hb[2][2];
+    h16_fragments(hb);
     uint32_t flags = 0;
     // The next queue index is fetched while the current item runs (thread 0
     // holds it in a register); the broadcast slot alternates between two
@@ -555,9 +700,11 @@ __global__ void __launch_bounds__(ENC_THREADS, 3) encode_pool(const __grid_const
                     v_prefetch<D>(a, layer, step + ENC_WARPS, vbuf[warp][(vs + 1) & 1], drop);
                 else
                     cp_async_commit();  // keep one group per iteration
-                cp_async_wait<1>();     // this step's group has landed
-                if (step < a.steps_per_layer)
-                    flags |= v_encode_step<D>(a, layer, step, stage[warp], vbuf[warp][vs & 1]);
+                cp_async_wait<1>();     // this lane's copies of this step have landed
+                __syncwarp();           // ... and every other lane's
+                if (step < a.steps_per_layer)  // warp-uniform
+                    flags |= v_encode_step<D>(a, layer, step, vbuf[warp][vs & 1], hb);
+                __syncwarp();           // the buffer is read before it is refilled
             }
             cp_async_wait<0>();
         }
@@ -699,11 +846,12 @@ __device__ uint32_t q8_slice(const EncodeArgs &a, int l, uint32_t p, uint64_t po
 // nothing waits); item t belongs to layer t / (P + vitems).
 template <int D>
 __global__ void __launch_bounds__(ENC_THREADS, 3) encode_pool_q8q(const __grid_constant__ EncodeArgs a) {
-    __shared__ __align__(16) uint8_t stage[ENC_WARPS][384];
-    __shared__ __align__(16) uint4 vbuf[ENC_WARPS][2][4][32];  // per warp: two steps of value data
+    __shared__ __align__(16) uint4 vbuf[ENC_WARPS][2][128];  // per warp: two steps of value data
     __shared__ uint32_t s_item[2], s_last;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint64_t drop = l2_evict_first_policy();
+    uint32_t hb[2][2];
+    h16_fragments(hb);
     const uint32_t M = uint32_t(a.P) + a.vitems;
     uint32_t flags = 0;
     uint32_t next = 0;
@@ -731,9 +879,11 @@ __global__ void __launch_bounds__(ENC_THREADS, 3) encode_pool_q8q(const __grid_c
                     v_prefetch<D>(a, layer, step + ENC_WARPS, vbuf[warp][(vs + 1) & 1], drop);
                 else
                     cp_async_commit();  // keep one group per iteration
-                cp_async_wait<1>();     // this step's group has landed
-                if (step < a.steps_per_layer)
-                    flags |= v_encode_step<D>(a, layer, step, stage[warp], vbuf[warp][vs & 1]);
+                cp_async_wait<1>();     // this lane's copies of this step have landed
+                __syncwarp();           // ... and every other lane's
+                if (step < a.steps_per_layer)  // warp-uniform
+                    flags |= v_encode_step<D>(a, layer, step, vbuf[warp][vs & 1], hb);
+                __syncwarp();           // the buffer is read before it is refilled
             }
             cp_async_wait<0>();
         }
