@@ -348,14 +348,15 @@ __device__ void quant_slice(const EncodeArgs &a, int l, uint32_t p, uint64_t pol
 // (d = 64) are butterflies on fp32 pairs in registers.
 //
 // The MMA's k and n index bits (k0, k1, k2, k3) stand for the coordinate
-// bits (i0, i5, i6, i1) at d = 128 and (i0, i4, i5, i1) at d = 64: the same
-// relabelling on both sides, so B is H_16 in natural order.  A row is a
-// (vector, i2, i3 [, i4]) combination.  Then each 16-byte chunk of the input
-// is one A fragment as it stands (registers x, z, y, w), and lane (g, q) =
-// (lane / 4, lane % 4) ends up with the consecutive rotated coordinates
-// [q d/4, (q+1) d/4) of vector g (and of vector 8 + g at d = 64): the C
-// element c_{2h+e} of M-tile m, N-tile nt is local coordinate 8t + 4h + 2nt
-// + e, t = m (d = 128) or m % 2 (d = 64).
+// bits (i0, i5, i6, i2) at d = 128 and (i0, i4, i5, i2) at d = 64: the same
+// relabelling on both sides, so B is H_16 in natural order.  An A row is a
+// (vector, i1, i3 [, i4]) combination, rows g and g + 8 differing in i1.
+// Then each 16-byte chunk of the input is one A fragment as it stands
+// (registers x, y, z, w), and lane (g, q) = (lane / 4, lane % 4) ends up
+// with the consecutive rotated coordinates [q d/4, (q+1) d/4) of vector g
+// (and of vector 8 + g at d = 64): the C element c_{2h+e} of M-tile m,
+// N-tile nt is local coordinate 8t + 4nt + 2h + e, t = m (d = 128) or m % 2
+// (d = 64).
 //
 // Codes.  u = y / ||v|| (y = H_d v, unnormalised) falls in cell
 // cnt ^ (y >= 0 ? 4 : 3) with cnt = #{k : |y| >= t_k ||v||}.  With
@@ -381,33 +382,37 @@ __device__ uint32_t classify_nonfinite(const uint4 *vec, int nchunks) {
     return FLAG_RANGE;
 }
 
-// Slot of chunk c of vector v (within the warp step) in the warp's 2 KB
-// staging buffer.  The XOR swizzle makes both the coalesced fill and the
-// fragment reads conflict-free: the 8 lanes of a quarter-warp always reach
-// 8 different 16-byte bank groups.
+// Staging layout.  Chunk c of vector v of a warp step sits at slot
+// v * d/8 + (c ^ ((c >> 3 & 1) << 1) ^ (v & 1)) (d = 128) or
+// v * d/8 + (c ^ (v & 1)) (d = 64) of the warp's 2 KB buffer.  The XOR
+// swizzle makes both the coalesced fill and the fragment reads
+// conflict-free: the 8 lanes of a quarter-warp always reach 8 different
+// 16-byte bank groups.  The fill copies chunk 32j + lane (j = 0..3) of the
+// step, which lands at slot 32j + v_fill_slot(lane).
 template <int D>
-__device__ __forceinline__ int v_slot(int v, int c) {
-    constexpr int CPV = D / 8;
-    return v * CPV + (D == 128 ? (c ^ (((c >> 3) & 1) << 1) ^ (v & 1)) : (c ^ (v & 1)));
+__device__ __forceinline__ int v_fill_slot(int lane) {
+    if (D == 128) {
+        const int c = lane & 15, v = lane >> 4;
+        return 16 * v + (c ^ (((c >> 3) & 1) << 1) ^ v);
+    }
+    const int c = lane & 7, v = lane >> 3;
+    return 8 * v + (c ^ (v & 1));
 }
 
-// Issue the cp.async copies of one warp step's 2 KB of value data into the
-// staging buffer: instruction j, lane i copies the step's 16-byte chunk
-// 32j + i.  Vectors past the layer's end get zeros.  Always commits one group.
-template <int D>
-__device__ __forceinline__ void v_prefetch(const EncodeArgs &a, int layer, uint64_t step, uint4 *buf, uint64_t pol) {
-    constexpr int CPV = D / 8;
-    constexpr int VPW = 1024 / D;
+// Issue the cp.async copies of one warp step's 2 KB of value data (chunks
+// [128 step, 128 step + 128) of the layer's values, which hold
+// layer_chunks) into the staging buffer.  Chunks past the layer's end get
+// zeros.  Always commits one group.
+__device__ __forceinline__ void v_prefetch(const uint4 *vlayer, uint64_t layer_chunks, uint64_t step, uint4 *buf,
+                                           int fill_slot, uint64_t pol) {
     const int lane = threadIdx.x & 31;
-    const uint64_t n0 = step * VPW;
-    const bool live = step < a.steps_per_layer;
+    const uint64_t c0 = step * 128u;
+    const uint32_t left = c0 < layer_chunks ? uint32_t(min(layer_chunks - c0, uint64_t(128))) : 0u;
+    const uint4 *src = vlayer + c0 + lane;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        const int C = 32 * j + lane;
-        const int v = C / CPV, c = C % CPV;
-        const bool valid = live && n0 + uint64_t(v) < a.nvec;
-        const uint4 *src = a.v[layer] + (valid ? (n0 + uint64_t(v)) * CPV + uint64_t(c) : 0);
-        cp_async16(buf + v_slot<D>(v, c), src, valid ? 16u : 0u, pol);
+        const bool valid = uint32_t(32 * j + lane) < left;
+        cp_async16(buf + 32 * j + fill_slot, valid ? src + 32 * j : vlayer, valid ? 16u : 0u, pol);
     }
     cp_async_commit();
 }
@@ -433,7 +438,7 @@ __device__ __forceinline__ void mma_h16(float2 &lo, float2 &hi, uint4 w, uint32_
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%10,%10,%10,%10};"
         : "=f"(lo.x), "=f"(lo.y), "=f"(hi.x), "=f"(hi.y)
-        : "r"(w.x), "r"(w.z), "r"(w.y), "r"(w.w), "r"(b0), "r"(b1), "f"(0.0f));
+        : "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w), "r"(b0), "r"(b1), "f"(0.0f));
 }
 
 __device__ __forceinline__ void bfly2(float2 &a, float2 &b) {
@@ -477,9 +482,19 @@ constexpr float TSQ1 = float(double(THR1) * double(THR1));
 constexpr float TSQ2 = float(double(THR2) * double(THR2));
 constexpr float TSQ3 = float(double(THR3) * double(THR3));
 
+// Square root for sigma: the approximate instruction is within 2^-22 of the
+// real root, well inside the fp16 rounding that follows.
+__device__ __forceinline__ float sqrt_approx(float x) {
+    float r;
+    asm("sqrt.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+// One warp step: vectors [step * VPW, step * VPW + VPW) of the layer whose
+// values start at vlayer and whose pool section starts at lay.
 template <int D>
-__device__ uint32_t v_encode_step(const EncodeArgs &a, int layer, uint64_t step, const uint4 *buf,
-                                  const uint32_t (&hb)[2][2]) {
+__device__ uint32_t v_encode_step(const EncodeArgs &a, const uint4 *vlayer, uint8_t *lay, uint64_t step,
+                                  const uint4 *buf, const uint32_t (&hb)[2][2]) {
     constexpr int VPW = 1024 / D;           // vectors per warp step
     constexpr int NV = D == 128 ? 1 : 2;    // vectors per lane
     constexpr int NP = D / 8;               // coordinate pairs per lane and vector
@@ -489,17 +504,19 @@ __device__ uint32_t v_encode_step(const EncodeArgs &a, int layer, uint64_t step,
     const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
     const uint64_t n0 = step * VPW;
 
-    // y[m][nt][h] = (c_{2h}, c_{2h+1}) of M-tile m, N-tile nt
+    // y[m][nt][h] = (c_{2h}, c_{2h+1}) of M-tile m, N-tile nt.  M-tile m
+    // reads chunk 4q + m of vector g (d = 128) or chunk 2q + m % 2 of vector
+    // 8 (m / 2) + g (d = 64); the staging layout puts it at rd + off(m).
+    const uint4 *rd = buf + (D == 128 ? 16 * g + 4 * q : 8 * g + 2 * q);
+    const int X = D == 128 ? 2 * (q >> 1) + (g & 1) : (g & 1);
     float2 y[4][2][2];
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
-        const int v = D == 128 ? g : 8 * (m >> 1) + g;
-        const int c = D == 128 ? 4 * q + m : 2 * q + (m & 1);
-        const uint4 w = buf[v_slot<D>(v, c)];
+        const uint4 w = rd[D == 128 ? (m ^ X) : 64 * (m >> 1) + ((m & 1) ^ X)];
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) mma_h16(y[m][nt][0], y[m][nt][1], w, hb[nt][0], hb[nt][1]);
     }
-    // the register-held index bits: i2 (h), i3 (bit 0 of m) and, at d = 128, i4 (bit 1 of m)
+    // the register-held index bits: i1 (h), i3 (bit 0 of m) and, at d = 128, i4 (bit 1 of m)
 #pragma unroll
     for (int m = 0; m < 4; ++m)
 #pragma unroll
@@ -519,13 +536,13 @@ __device__ uint32_t v_encode_step(const EncodeArgs &a, int layer, uint64_t step,
                 for (int h = 0; h < 2; ++h) bfly2(y[m][nt][h], y[m + 2][nt][h]);
     }
 
-    // the lane's pairs per vector, in local-coordinate order: pair p = 4t + 2h + nt
+    // the lane's pairs per vector, in local-coordinate order: pair p = 4t + 2nt + h
     float2 yp[NV][NP];
 #pragma unroll
     for (int vi = 0; vi < NV; ++vi)
 #pragma unroll
         for (int p = 0; p < NP; ++p) {
-            const int t = p >> 2, h = (p >> 1) & 1, nt = p & 1;
+            const int t = p >> 2, nt = (p >> 1) & 1, h = p & 1;
             yp[vi][p] = y[D == 128 ? t : 2 * vi + t][nt][h];
         }
 
@@ -574,16 +591,15 @@ __device__ uint32_t v_encode_step(const EncodeArgs &a, int layer, uint64_t step,
     }
 
     uint32_t flags = 0;
-    uint8_t *lay = a.pool + a.geo.off_layers + uint64_t(layer) * a.geo.layer_stride;
 #pragma unroll
     for (int vi = 0; vi < NV; ++vi) {
         const uint64_t n = n0 + uint64_t(D == 128 ? g : 8 * vi + g);
         const bool valid = n < a.nvec;
         const float s = S[vi];
-        const uint16_t sig_bits = tiny[vi] ? 0 : __half_as_ushort(__float2half_rn(sqrtf(s) * INV_D));
+        const uint16_t sig_bits = tiny[vi] ? 0 : __half_as_ushort(__float2half_rn(sqrt_approx(s) * INV_D));
         // RANGE: finite input whose sigma exceeds fp16; non-finite input is NONFINITE only
         if (valid && !(s <= 3.0e38f))
-            flags |= classify_nonfinite(a.v[layer] + n * CPV, CPV);
+            flags |= classify_nonfinite(vlayer + n * CPV, CPV);
         else if (valid && (sig_bits & 0x7C00u) == 0x7C00u)
             flags |= FLAG_RANGE;
         // a zero vector (y = +0): thresholds below every square, but finite,
@@ -647,6 +663,7 @@ __global__ void __launch_bounds__(ENC_THREADS, 3) encode_pool(const __grid_const
     const uint64_t keep = l2_evict_last_policy(), drop = l2_evict_first_policy();
     uint32_t hb[2][2];
     h16_fragments(hb);
+    const int fill_slot = v_fill_slot<D>(lane);
     uint32_t flags = 0;
     // The next queue index is fetched while the current item runs (thread 0
     // holds it in a register); the broadcast slot alternates between two
@@ -692,18 +709,20 @@ __global__ void __launch_bounds__(ENC_THREADS, 3) encode_pool(const __grid_const
         } else {
             // the warp's VSTEPS steps, each prefetched while the previous one is encoded
             const uint64_t step0 = uint64_t(id) * VSTEPS * ENC_WARPS + warp;
-            v_prefetch<D>(a, layer, step0, vbuf[warp][0], drop);
+            const uint4 *vlayer = a.v[layer];
+            uint8_t *lay = a.pool + a.geo.off_layers + uint64_t(layer) * a.geo.layer_stride;
+            v_prefetch(vlayer, a.chunks, step0, vbuf[warp][0], fill_slot, drop);
 #pragma unroll 1
             for (int vs = 0; vs < VSTEPS; ++vs) {
                 const uint64_t step = step0 + uint64_t(vs) * ENC_WARPS;
                 if (vs + 1 < VSTEPS)
-                    v_prefetch<D>(a, layer, step + ENC_WARPS, vbuf[warp][(vs + 1) & 1], drop);
+                    v_prefetch(vlayer, a.chunks, step + ENC_WARPS, vbuf[warp][(vs + 1) & 1], fill_slot, drop);
                 else
                     cp_async_commit();  // keep one group per iteration
                 cp_async_wait<1>();     // this lane's copies of this step have landed
                 __syncwarp();           // ... and every other lane's
                 if (step < a.steps_per_layer)  // warp-uniform
-                    flags |= v_encode_step<D>(a, layer, step, vbuf[warp][vs & 1], hb);
+                    flags |= v_encode_step<D>(a, vlayer, lay, step, vbuf[warp][vs & 1], hb);
                 __syncwarp();           // the buffer is read before it is refilled
             }
             cp_async_wait<0>();
@@ -852,6 +871,7 @@ __global__ void __launch_bounds__(ENC_THREADS, 3) encode_pool_q8q(const __grid_c
     const uint64_t drop = l2_evict_first_policy();
     uint32_t hb[2][2];
     h16_fragments(hb);
+    const int fill_slot = v_fill_slot<D>(lane);
     const uint32_t M = uint32_t(a.P) + a.vitems;
     uint32_t flags = 0;
     uint32_t next = 0;
@@ -871,18 +891,20 @@ __global__ void __launch_bounds__(ENC_THREADS, 3) encode_pool_q8q(const __grid_c
         } else {
             // the warp's VSTEPS steps, each prefetched while the previous one is encoded
             const uint64_t step0 = uint64_t(id) * VSTEPS * ENC_WARPS + warp;
-            v_prefetch<D>(a, layer, step0, vbuf[warp][0], drop);
+            const uint4 *vlayer = a.v[layer];
+            uint8_t *lay = a.pool + a.geo.off_layers + uint64_t(layer) * a.geo.layer_stride;
+            v_prefetch(vlayer, a.chunks, step0, vbuf[warp][0], fill_slot, drop);
 #pragma unroll 1
             for (int vs = 0; vs < VSTEPS; ++vs) {
                 const uint64_t step = step0 + uint64_t(vs) * ENC_WARPS;
                 if (vs + 1 < VSTEPS)
-                    v_prefetch<D>(a, layer, step + ENC_WARPS, vbuf[warp][(vs + 1) & 1], drop);
+                    v_prefetch(vlayer, a.chunks, step + ENC_WARPS, vbuf[warp][(vs + 1) & 1], fill_slot, drop);
                 else
                     cp_async_commit();  // keep one group per iteration
                 cp_async_wait<1>();     // this lane's copies of this step have landed
                 __syncwarp();           // ... and every other lane's
                 if (step < a.steps_per_layer)  // warp-uniform
-                    flags |= v_encode_step<D>(a, layer, step, vbuf[warp][vs & 1], hb);
+                    flags |= v_encode_step<D>(a, vlayer, lay, step, vbuf[warp][vs & 1], hb);
                 __syncwarp();           // the buffer is read before it is refilled
             }
             cp_async_wait<0>();
