@@ -400,15 +400,17 @@ __device__ __forceinline__ int v_fill_slot(int lane) {
 }
 
 // Issue the cp.async copies of one warp step's 2 KB of value data (chunks
-// [128 step, 128 step + 128) of the layer's values, which hold
-// layer_chunks) into the staging buffer.  Chunks past the layer's end get
-// zeros.  Always commits one group.
-__device__ __forceinline__ void v_prefetch(const uint4 *vlayer, uint64_t layer_chunks, uint64_t step, uint4 *buf,
+// [128 step, 128 step + 128) of the layer's values, which hold nvec vectors)
+// into the staging buffer.  Chunks past the layer's end get zeros.  Always
+// commits one group.
+template <int D>
+__device__ __forceinline__ void v_prefetch(const uint4 *vlayer, uint32_t nvec, uint32_t step, uint4 *buf,
                                            int fill_slot, uint64_t pol) {
+    constexpr uint32_t VPW = 1024 / D;
     const int lane = threadIdx.x & 31;
-    const uint64_t c0 = step * 128u;
-    const uint32_t left = c0 < layer_chunks ? uint32_t(min(layer_chunks - c0, uint64_t(128))) : 0u;
-    const uint4 *src = vlayer + c0 + lane;
+    const uint32_t n0 = step * VPW;
+    const uint32_t left = n0 < nvec ? min(nvec - n0, VPW) * (D / 8) : 0u;
+    const uint4 *src = vlayer + uint64_t(step) * 128u + lane;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const bool valid = uint32_t(32 * j + lane) < left;
@@ -490,10 +492,11 @@ __device__ __forceinline__ float sqrt_approx(float x) {
     return r;
 }
 
-// One warp step: vectors [step * VPW, step * VPW + VPW) of the layer whose
-// values start at vlayer and whose pool section starts at lay.
+// One warp step: vectors [step * VPW, step * VPW + VPW) of a layer of nvec
+// vectors whose values start at vlayer, whose packed codes go to vsec and
+// whose sigmas go to ssec.
 template <int D>
-__device__ uint32_t v_encode_step(const EncodeArgs &a, const uint4 *vlayer, uint8_t *lay, uint64_t step,
+__device__ uint32_t v_encode_step(const uint4 *vlayer, uint8_t *vsec, uint16_t *ssec, uint32_t nvec, uint32_t step,
                                   const uint4 *buf, const uint32_t (&hb)[2][2]) {
     constexpr int VPW = 1024 / D;           // vectors per warp step
     constexpr int NV = D == 128 ? 1 : 2;    // vectors per lane
@@ -502,7 +505,7 @@ __device__ uint32_t v_encode_step(const EncodeArgs &a, const uint4 *vlayer, uint
     constexpr int CB = 3 * D / 8;           // code bytes per vector
     constexpr float INV_D = 1.0f / float(D);
     const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
-    const uint64_t n0 = step * VPW;
+    const uint32_t n0 = step * VPW;
 
     // y[m][nt][h] = (c_{2h}, c_{2h+1}) of M-tile m, N-tile nt.  M-tile m
     // reads chunk 4q + m of vector g (d = 128) or chunk 2q + m % 2 of vector
@@ -590,18 +593,33 @@ __device__ uint32_t v_encode_step(const EncodeArgs &a, const uint4 *vlayer, uint
         }
     }
 
+    // sigma; the rare non-finite or out-of-range vector is classified off the
+    // common path (RANGE: finite input whose sigma exceeds fp16; non-finite
+    // input is NONFINITE only)
     uint32_t flags = 0;
+    uint32_t n[NV];
+    bool valid[NV];
+    uint16_t sig[NV];
+    bool bad = false;
 #pragma unroll
     for (int vi = 0; vi < NV; ++vi) {
-        const uint64_t n = n0 + uint64_t(D == 128 ? g : 8 * vi + g);
-        const bool valid = n < a.nvec;
+        n[vi] = n0 + uint32_t(D == 128 ? g : 8 * vi + g);
+        valid[vi] = n[vi] < nvec;
+        sig[vi] = tiny[vi] ? 0 : __half_as_ushort(__float2half_rn(sqrt_approx(S[vi]) * INV_D));
+        bad |= valid[vi] && (!(S[vi] <= 3.0e38f) || (sig[vi] & 0x7C00u) == 0x7C00u);
+    }
+    if (__any_sync(0xffffffffu, bad)) {
+#pragma unroll
+        for (int vi = 0; vi < NV; ++vi) {
+            if (valid[vi] && !(S[vi] <= 3.0e38f))
+                flags |= classify_nonfinite(vlayer + uint64_t(n[vi]) * CPV, CPV);
+            else if (valid[vi] && (sig[vi] & 0x7C00u) == 0x7C00u)
+                flags |= FLAG_RANGE;
+        }
+    }
+#pragma unroll
+    for (int vi = 0; vi < NV; ++vi) {
         const float s = S[vi];
-        const uint16_t sig_bits = tiny[vi] ? 0 : __half_as_ushort(__float2half_rn(sqrt_approx(s) * INV_D));
-        // RANGE: finite input whose sigma exceeds fp16; non-finite input is NONFINITE only
-        if (valid && !(s <= 3.0e38f))
-            flags |= classify_nonfinite(vlayer + n * CPV, CPV);
-        else if (valid && (sig_bits & 0x7C00u) == 0x7C00u)
-            flags |= FLAG_RANGE;
         // a zero vector (y = +0): thresholds below every square, but finite,
         // so that P = d2 * y is -0 and not inf * 0
         const float nt1 = s == 0.0f ? -FLT_MAX : -(s * (TSQ1 * INV_D));
@@ -611,8 +629,8 @@ __device__ uint32_t v_encode_step(const EncodeArgs &a, const uint4 *vlayer, uint
 #pragma unroll
         for (int i = 0; i < (6 * NP + 31) / 32; ++i) W[i] = 0;
         v_codes<NP>(yp[vi], nt1, nt2, nt3, W);
-        if (valid) {
-            uint8_t *dst = lay + a.geo.sec_v + n * CB + uint64_t(q) * (CB / 4);
+        uint8_t *dst = vsec + uint64_t(n[vi]) * CB + uint32_t(q) * (CB / 4);
+        if (valid[vi]) {
             if (D == 128) {
 #pragma unroll
                 for (int i = 0; i < 3; ++i) __stcs(reinterpret_cast<unsigned int *>(dst) + i, ~W[i]);
@@ -622,8 +640,8 @@ __device__ uint32_t v_encode_step(const EncodeArgs &a, const uint4 *vlayer, uint
                 __stcs(d16 + 1, (unsigned short)(~W[0] >> 16));
                 __stcs(d16 + 2, (unsigned short)(~W[1]));
             }
-            if (q == 0) __stcs(reinterpret_cast<unsigned short *>(lay + a.geo.sec_sigma) + n, (unsigned short)sig_bits);
         }
+        if (valid[vi] && q == 0) __stcs(reinterpret_cast<unsigned short *>(ssec) + n[vi], (unsigned short)sig[vi]);
     }
     return flags;
 }
@@ -708,21 +726,24 @@ __global__ void __launch_bounds__(ENC_THREADS, 3) encode_pool(const __grid_const
                 flags |= FLAG_TIMEOUT;
         } else {
             // the warp's VSTEPS steps, each prefetched while the previous one is encoded
-            const uint64_t step0 = uint64_t(id) * VSTEPS * ENC_WARPS + warp;
+            const uint32_t step0 = id * uint32_t(VSTEPS * ENC_WARPS) + uint32_t(warp);
+            const uint32_t nvec = uint32_t(a.nvec), nsteps = uint32_t(a.steps_per_layer);
             const uint4 *vlayer = a.v[layer];
             uint8_t *lay = a.pool + a.geo.off_layers + uint64_t(layer) * a.geo.layer_stride;
-            v_prefetch(vlayer, a.chunks, step0, vbuf[warp][0], fill_slot, drop);
+            uint8_t *vsec = lay + a.geo.sec_v;
+            uint16_t *ssec = reinterpret_cast<uint16_t *>(lay + a.geo.sec_sigma);
+            v_prefetch<D>(vlayer, nvec, step0, vbuf[warp][0], fill_slot, drop);
 #pragma unroll 1
             for (int vs = 0; vs < VSTEPS; ++vs) {
-                const uint64_t step = step0 + uint64_t(vs) * ENC_WARPS;
+                const uint32_t step = step0 + uint32_t(vs * ENC_WARPS);
                 if (vs + 1 < VSTEPS)
-                    v_prefetch(vlayer, a.chunks, step + ENC_WARPS, vbuf[warp][(vs + 1) & 1], fill_slot, drop);
+                    v_prefetch<D>(vlayer, nvec, step + ENC_WARPS, vbuf[warp][(vs + 1) & 1], fill_slot, drop);
                 else
                     cp_async_commit();  // keep one group per iteration
                 cp_async_wait<1>();     // this lane's copies of this step have landed
                 __syncwarp();           // ... and every other lane's
-                if (step < a.steps_per_layer)  // warp-uniform
-                    flags |= v_encode_step<D>(a, vlayer, lay, step, vbuf[warp][vs & 1], hb);
+                if (step < nsteps)  // warp-uniform
+                    flags |= v_encode_step<D>(vlayer, vsec, ssec, nvec, step, vbuf[warp][vs & 1], hb);
                 __syncwarp();           // the buffer is read before it is refilled
             }
             cp_async_wait<0>();
@@ -890,21 +911,24 @@ __global__ void __launch_bounds__(ENC_THREADS, 3) encode_pool_q8q(const __grid_c
             flags |= q8_slice(a, layer, id, drop);
         } else {
             // the warp's VSTEPS steps, each prefetched while the previous one is encoded
-            const uint64_t step0 = uint64_t(id) * VSTEPS * ENC_WARPS + warp;
+            const uint32_t step0 = id * uint32_t(VSTEPS * ENC_WARPS) + uint32_t(warp);
+            const uint32_t nvec = uint32_t(a.nvec), nsteps = uint32_t(a.steps_per_layer);
             const uint4 *vlayer = a.v[layer];
             uint8_t *lay = a.pool + a.geo.off_layers + uint64_t(layer) * a.geo.layer_stride;
-            v_prefetch(vlayer, a.chunks, step0, vbuf[warp][0], fill_slot, drop);
+            uint8_t *vsec = lay + a.geo.sec_v;
+            uint16_t *ssec = reinterpret_cast<uint16_t *>(lay + a.geo.sec_sigma);
+            v_prefetch<D>(vlayer, nvec, step0, vbuf[warp][0], fill_slot, drop);
 #pragma unroll 1
             for (int vs = 0; vs < VSTEPS; ++vs) {
-                const uint64_t step = step0 + uint64_t(vs) * ENC_WARPS;
+                const uint32_t step = step0 + uint32_t(vs * ENC_WARPS);
                 if (vs + 1 < VSTEPS)
-                    v_prefetch(vlayer, a.chunks, step + ENC_WARPS, vbuf[warp][(vs + 1) & 1], fill_slot, drop);
+                    v_prefetch<D>(vlayer, nvec, step + ENC_WARPS, vbuf[warp][(vs + 1) & 1], fill_slot, drop);
                 else
                     cp_async_commit();  // keep one group per iteration
                 cp_async_wait<1>();     // this lane's copies of this step have landed
                 __syncwarp();           // ... and every other lane's
-                if (step < a.steps_per_layer)  // warp-uniform
-                    flags |= v_encode_step<D>(a, vlayer, lay, step, vbuf[warp][vs & 1], hb);
+                if (step < nsteps)  // warp-uniform
+                    flags |= v_encode_step<D>(vlayer, vsec, ssec, nvec, step, vbuf[warp][vs & 1], hb);
                 __syncwarp();           // the buffer is read before it is refilled
             }
             cp_async_wait<0>();
