@@ -676,7 +676,8 @@ template <int D>
 __global__ void __launch_bounds__(ENC_THREADS, 3) encode_pool(const __grid_constant__ EncodeArgs a) {
     __shared__ __align__(16) uint4 vbuf[ENC_WARPS][2][128];  // per warp: two steps of value data
     __shared__ uint32_t red[ENC_WARPS];
-    __shared__ uint32_t s_item[2], s_flag;
+    __shared__ uint4 s_item[2];  // (queue index, kind, layer, id), decoded once by thread 0
+    __shared__ uint32_t s_flag;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint64_t keep = l2_evict_last_policy(), drop = l2_evict_first_policy();
     uint32_t hb[2][2];
@@ -684,19 +685,23 @@ __global__ void __launch_bounds__(ENC_THREADS, 3) encode_pool(const __grid_const
     const int fill_slot = v_fill_slot<D>(lane);
     uint32_t flags = 0;
     // The next queue index is fetched while the current item runs (thread 0
-    // holds it in a register); the broadcast slot alternates between two
-    // words so one barrier per item suffices.
+    // holds it in a register) and decoded by thread 0 alone; the broadcast
+    // slot alternates between two entries so one barrier per item suffices.
     uint32_t next = 0;
     if (threadIdx.x == 0) next = atomicAdd(&a.ctl->next_item, 1u);
     for (uint32_t k = 0;; ++k) {
-        if (threadIdx.x == 0) s_item[k & 1u] = next;
+        if (threadIdx.x == 0) {
+            int kd = 0, ly = 0;
+            uint32_t ix = 0;
+            if (next < a.total_items) item_of(a, next, kd, ly, ix);
+            s_item[k & 1u] = make_uint4(next, uint32_t(kd), uint32_t(ly), ix);
+        }
         __syncthreads();
-        const uint32_t t = s_item[k & 1u];
-        if (t >= a.total_items) break;
+        const uint4 it = s_item[k & 1u];
+        if (it.x >= a.total_items) break;
         if (threadIdx.x == 0) next = atomicAdd(&a.ctl->next_item, 1u);
-        int kind, layer;
-        uint32_t id;
-        item_of(a, t, kind, layer, id);
+        const int kind = int(it.y), layer = int(it.z);
+        const uint32_t id = it.w;
         if (kind == ITEM_ABSMAX) {
             absmax_slice(a, layer, id, keep, red);
             if (threadIdx.x == 0) {
@@ -887,7 +892,8 @@ __device__ uint32_t q8_slice(const EncodeArgs &a, int l, uint32_t p, uint64_t po
 template <int D>
 __global__ void __launch_bounds__(ENC_THREADS, 3) encode_pool_q8q(const __grid_constant__ EncodeArgs a) {
     __shared__ __align__(16) uint4 vbuf[ENC_WARPS][2][128];  // per warp: two steps of value data
-    __shared__ uint32_t s_item[2], s_last;
+    __shared__ uint4 s_item[2];  // (queue index, kind, layer, id), decoded once by thread 0
+    __shared__ uint32_t s_last;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint64_t drop = l2_evict_first_policy();
     uint32_t hb[2][2];
@@ -898,15 +904,18 @@ __global__ void __launch_bounds__(ENC_THREADS, 3) encode_pool_q8q(const __grid_c
     uint32_t next = 0;
     if (threadIdx.x == 0) next = atomicAdd(&a.ctl->next_item, 1u);
     for (uint32_t k = 0;; ++k) {
-        if (threadIdx.x == 0) s_item[k & 1u] = next;
+        if (threadIdx.x == 0) {
+            int kd = 0;
+            uint32_t ix = 0;
+            if (next < a.total_items) mixed_item(a, next % M, kd, ix);
+            s_item[k & 1u] = make_uint4(next, uint32_t(kd), next / M, ix);
+        }
         __syncthreads();
-        const uint32_t t = s_item[k & 1u];
-        if (t >= a.total_items) break;
+        const uint4 it = s_item[k & 1u];
+        if (it.x >= a.total_items) break;
         if (threadIdx.x == 0) next = atomicAdd(&a.ctl->next_item, 1u);
-        const int layer = int(t / M);
-        int kind;
-        uint32_t id;
-        mixed_item(a, t % M, kind, id);
+        const int kind = int(it.y), layer = int(it.z);
+        const uint32_t id = it.w;
         if (kind == ITEM_KEYS) {
             flags |= q8_slice(a, layer, id, drop);
         } else {
