@@ -6,10 +6,10 @@
 //
 // One persistent kernel, encode_pool, works through an ordered queue of
 // items.  For every layer l (queue order in item_of):
-//   1. P key slices "absmax": max|k| over one slice of K_l -> a partial.  The
-//      block that finishes the layer's last slice folds the P partials into
-//      the layer's scale s = m/127, writes it to the pool and the key
-//      quantizer's parameters to the workspace, and releases ready[l].
+//   1. P key slices "absmax": max|k| over 64 KB of K_l, folded into the
+//      layer's maximum with atomicMax.  The block that finishes the layer's
+//      last slice computes the scale s = m/127, writes it to the pool and the
+//      key quantizer's parameters to the workspace, and releases ready[l].
 //   2. the layer's value batches (4 warp steps of VPW vectors per warp, each
 //      warp prefetching its next step into shared memory with cp.async),
 //      interleaved with P key slices "quantize": each waits (bounded) for
@@ -29,8 +29,7 @@ namespace kvp {
 
 constexpr int ENC_THREADS = 256;
 constexpr int ENC_WARPS = ENC_THREADS / 32;
-constexpr uint64_t SLICE_MIN_CHUNKS = 4096;  // 16-byte chunks (64 KB of keys) per slice, at least
-constexpr int MAX_SLICES = 256;              // per layer
+constexpr uint64_t SLICE_CHUNKS = 4096;      // 16-byte chunks (64 KB of keys) per slice, at most
 constexpr float RNE_MAGIC = 12582912.0f;     // 1.5 * 2^23
 constexpr uint32_t SPIN_LIMIT = 1u << 24;    // ~1.7 s of 100 ns sleeps
 constexpr int VSTEPS = 4;                    // value warp steps per warp per item
@@ -45,6 +44,7 @@ struct EncodeCtl {
     uint32_t pad;
     uint32_t slices_done[KVP_MAX_LAYERS];  // absmax slices finished, per layer
     uint32_t ready[KVP_MAX_LAYERS];        // 1 once the layer's key parameters are written
+    uint32_t kmax[KVP_MAX_LAYERS];         // max of the layer's sign-cleared bf16 key patterns
 };
 
 struct EncodeArgs {
@@ -52,7 +52,6 @@ struct EncodeArgs {
     const uint4 *v[KVP_MAX_LAYERS];
     uint8_t *pool;
     EncodeCtl *ctl;
-    uint32_t *partials;  // [L][P]
     float4 *kparams;     // [L]: s_eff, 1/s_eff, prescale1, prescale2
     PoolGeom geo;
     uint64_t chunks;            // 16-byte chunks per layer of K (H*T*d/8)
@@ -71,22 +70,18 @@ struct EncodeArgs {
 };
 
 struct WsLayout {
-    uint64_t ctl, partials, kparams, total;
+    uint64_t ctl, kparams, total;
 };
 
 static inline int slices_per_layer(uint64_t chunks) {
-    uint64_t p = (chunks + SLICE_MIN_CHUNKS - 1) / SLICE_MIN_CHUNKS;
-    if (p < 1) p = 1;
-    if (p > MAX_SLICES) p = MAX_SLICES;
-    return int(p);
+    const uint64_t p = (chunks + SLICE_CHUNKS - 1) / SLICE_CHUNKS;
+    return int(p < 1 ? 1 : p);
 }
 
-static inline WsLayout ws_layout(int L, uint64_t chunks) {
+static inline WsLayout ws_layout(int L) {
     WsLayout w;
-    const int P = slices_per_layer(chunks);
     w.ctl = 0;
-    w.partials = align256(sizeof(EncodeCtl));
-    w.kparams = align16(w.partials + 4ull * uint64_t(L) * uint64_t(P));
+    w.kparams = align256(sizeof(EncodeCtl));
     w.total = align16(w.kparams + 16ull * uint64_t(L));
     return w;
 }
@@ -143,9 +138,10 @@ __device__ __forceinline__ void item_of(const EncodeArgs &a, uint32_t t, int &ki
 }
 
 // ---------------------------------------------------------------------------
-// Keys, pass 1: partial max|k| of one slice, on the bf16 bit patterns with the
-// sign cleared (for finite values their order is the order of the magnitudes;
-// Inf/NaN patterns sort above every finite one, so they flag themselves).
+// Keys, pass 1: max|k| of one slice, folded into the layer's maximum, on the
+// bf16 bit patterns with the sign cleared (for finite values their order is
+// the order of the magnitudes; Inf/NaN patterns sort above every finite one,
+// so they flag themselves).
 // ---------------------------------------------------------------------------
 __device__ void absmax_slice(const EncodeArgs &a, int l, uint32_t p, uint64_t pol, uint32_t *red) {
     const uint64_t c0 = uint64_t(p) * a.chunks_per_slice;
@@ -178,7 +174,7 @@ __device__ void absmax_slice(const EncodeArgs &a, int l, uint32_t p, uint64_t po
         uint32_t r = red[0];
 #pragma unroll
         for (int i = 1; i < ENC_WARPS; ++i) r = max(r, red[i]);
-        a.partials[uint64_t(l) * a.P + p] = r;
+        atomicMax(&a.ctl->kmax[l], r);
     }
     __syncthreads();
 }
@@ -195,17 +191,10 @@ __device__ void zero_layer_gaps(const EncodeArgs &a, int l) {
         for (uint64_t i = gaps[gi][0] + threadIdx.x; i < gaps[gi][1]; i += ENC_THREADS) lay[i] = 0;
 }
 
-__device__ void finalize_layer(const EncodeArgs &a, int l, uint32_t *red) {
-    __threadfence();  // the other blocks' partials (written before their counter increments)
-    uint32_t m = 0;
-    const volatile uint32_t *part = a.partials + uint64_t(l) * a.P;
-    for (int i = threadIdx.x; i < a.P; i += ENC_THREADS) m = max(m, part[i]);
-    m = __reduce_max_sync(0xffffffffu, m);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
-    __syncthreads();
+__device__ void finalize_layer(const EncodeArgs &a, int l) {
     if (threadIdx.x == 0) {
-        uint32_t r = red[0];
-        for (int i = 1; i < ENC_WARPS; ++i) r = max(r, red[i]);
+        __threadfence();  // the other blocks' maxima (folded in before their counter increments)
+        const uint32_t r = *reinterpret_cast<volatile uint32_t *>(&a.ctl->kmax[l]);
         const bool finite = r < 0x7F80u;
         if (!finite) atomicOr(&a.ctl->flags, FLAG_NONFINITE);
         const float mk = __uint_as_float(r << 16);  // max|k|, exact
@@ -709,7 +698,7 @@ __global__ void __launch_bounds__(ENC_THREADS, 3) encode_pool(const __grid_const
                 s_flag = atomicAdd(&a.ctl->slices_done[layer], 1u) == uint32_t(a.P) - 1u;
             }
             __syncthreads();
-            if (s_flag) finalize_layer(a, layer, red);
+            if (s_flag) finalize_layer(a, layer);
         } else if (kind == ITEM_KEYS) {
             if (threadIdx.x == 0) {
                 // bounded wait for the layer's scale (released by another block)
@@ -991,8 +980,7 @@ extern "C" int kvp_test_fail_next_encode(int layer, uint32_t spin_iters) {
 
 extern "C" size_t kvpool_workspace_bytes(const kvp_shape *s) {
     if (shape_ok(s) != KVP_OK) return 0;
-    const uint64_t chunks = uint64_t(s->n_kv_heads) * uint64_t(s->n_tokens) * uint64_t(s->head_dim) / 8;
-    return size_t(ws_layout(s->n_layers, chunks).total);
+    return size_t(ws_layout(s->n_layers).total);
 }
 
 extern "C" size_t kvpool_pool_bytes_ex(const kvp_shape *s, int k_mode) {
@@ -1033,7 +1021,7 @@ extern "C" int kvpool_encode_ex(const kvp_shape *s, int k_mode, const void *cons
     const PoolGeom geo = pool_geom(L, s->n_kv_heads, s->head_dim, s->n_tokens);
     if (pool_bytes < (k_mode == KVP_K_Q8_0 ? geo.total_q8 : geo.total)) return KVP_ERR_SIZE;
     const uint64_t chunks = uint64_t(s->n_kv_heads) * uint64_t(s->n_tokens) * uint64_t(s->head_dim) / 8;
-    const WsLayout wl = ws_layout(L, chunks);
+    const WsLayout wl = ws_layout(L);
     if (ws_bytes < wl.total) return KVP_ERR_SIZE;
 
     EncodeArgs a;
@@ -1045,7 +1033,6 @@ extern "C" int kvpool_encode_ex(const kvp_shape *s, int k_mode, const void *cons
     a.pool = static_cast<uint8_t *>(pool);
     uint8_t *w = static_cast<uint8_t *>(ws);
     a.ctl = reinterpret_cast<EncodeCtl *>(w + wl.ctl);
-    a.partials = reinterpret_cast<uint32_t *>(w + wl.partials);
     a.kparams = reinterpret_cast<float4 *>(w + wl.kparams);
     a.geo = geo;
     a.chunks = chunks;

@@ -1,8 +1,8 @@
 // kvpool_noalloc.cu -- kvpool_encode for callers that cannot allocate device
 // memory.
 //
-// kvpool_encode takes a caller-provided workspace for its per-block partial
-// maxima, value-block error flags and per-layer key parameters.  Some callers
+// kvpool_encode takes a caller-provided workspace for its work-queue control
+// block and per-layer key parameters.  Some callers
 // have no way to provide one: a plug-in loaded into another program's process
 // that must not allocate behind its host's memory manager (for instance a
 // server whose caching allocator already holds the GPU memory), or a caller on

@@ -121,9 +121,10 @@ typedef struct kvp_card_header {
 size_t kvpool_pool_bytes(const kvp_shape *shape);
 
 /* Bytes of device workspace kvpool_encode needs for this shape (0 for an
- * invalid shape).  The workspace holds per-block partial maxima and
- * per-layer quantization parameters; its contents need no initialisation
- * and are dead after the encode's kernels finish. */
+ * invalid shape).  The workspace holds the encoder's work-queue control
+ * block (queue head, per-layer key maxima and ready flags) and per-layer
+ * quantization parameters; its contents need no initialisation and are
+ * dead after the encode's kernels finish. */
 size_t kvpool_workspace_bytes(const kvp_shape *shape);
 
 /* Encode a whole KV cache into a pool ("PolyKV" 2.B).
@@ -202,9 +203,10 @@ int kvpool_status(const void *pool, void *stream);
  * (no cudaMalloc, cudaFree or allocating library call): the workspace is a
  * fixed array of KVP_NOALLOC_SCRATCH_BYTES in the library's device memory.
  *  Arguments and results are those of kvpool_encode minus ws / ws_bytes.
- *  Shapes whose kvpool_workspace_bytes() exceeds KVP_NOALLOC_SCRATCH_BYTES
- *    (more than 247 layers at the largest per-layer partial count, 256) are
- *    rejected with KVP_ERR_SIZE before anything is enqueued.
+ *  The encoder's workspace is a control block of about 6 KB plus 16 bytes
+ *    per layer, so every shape kvpool_encode accepts fits in the array.  A
+ *    shape it refuses is refused here with the same code, before anything
+ *    is enqueued.
  *  The first call in each CUDA context looks up the array's device address
  *    (with that context current) and caches it under the driver's context
  *    id; make that first call before any stream capture.  A context created

@@ -60,10 +60,13 @@ def test_noalloc_encode_matches_workspace_encode_twice():
         assert torch.equal(got, ref), "pool bytes differ for %r" % (shape,)
 
 
-def test_noalloc_rejects_shapes_beyond_its_scratch():
-    too_many_layers = (250, 8, 128, 32768)   # workspace 264,352 B > 262,144 B
-    assert kv.kvpool_workspace_bytes(too_many_layers) > kv.KVP_NOALLOC_SCRATCH_BYTES
-    rc = kv.kvpool_encode_noalloc(too_many_layers, [0] * 250, [0] * 250, 0, 0)
-    assert rc == kv.KVP_ERR_SIZE
-    fits = (200, 8, 128, 32768)
-    assert kv.kvpool_workspace_bytes(fits) <= kv.KVP_NOALLOC_SCRATCH_BYTES
+def test_noalloc_scratch_covers_every_shape():
+    """The encoder's workspace is its control block plus 16 bytes per layer,
+    so the scratch array holds it for the largest shape the encoder accepts;
+    a shape past that limit is refused before anything is enqueued."""
+    largest = (kv.KVP_MAX_LAYERS, 8, 128, 32768)
+    assert 0 < kv.kvpool_workspace_bytes(largest) <= kv.KVP_NOALLOC_SCRATCH_BYTES
+    too_many_layers = (kv.KVP_MAX_LAYERS + 1, 8, 128, 16)
+    assert kv.kvpool_workspace_bytes(too_many_layers) == 0
+    n = kv.KVP_MAX_LAYERS + 1
+    assert kv.kvpool_encode_noalloc(too_many_layers, [0] * n, [0] * n, 0, 0) == kv.KVP_ERR_SIZE
