@@ -6,7 +6,7 @@
 //
 // One persistent kernel, encode_pool, works through an ordered queue of
 // items.  For every layer l (queue order in item_of):
-//   1. P key slices "absmax": max|k| over 64 KB of K_l, folded into the
+//   1. P key slices "absmax": max|k| over 128 KB of K_l, folded into the
 //      layer's maximum with atomicMax.  The block that finishes the layer's
 //      last slice computes the scale s = m/127, writes it to the pool and the
 //      key quantizer's parameters to the workspace, and releases ready[l].
@@ -29,7 +29,7 @@ namespace kvp {
 
 constexpr int ENC_THREADS = 256;
 constexpr int ENC_WARPS = ENC_THREADS / 32;
-constexpr uint64_t SLICE_CHUNKS = 4096;      // 16-byte chunks (64 KB of keys) per slice, at most
+constexpr uint64_t SLICE_CHUNKS = 8192;      // 16-byte chunks (128 KB of keys) per slice, at most
 constexpr float RNE_MAGIC = 12582912.0f;     // 1.5 * 2^23
 constexpr uint32_t SPIN_LIMIT = 1u << 24;    // ~1.7 s of 100 ns sleeps
 constexpr int VSTEPS = 4;                    // value warp steps per warp per item
