@@ -188,6 +188,46 @@ __device__ __forceinline__ void pack_load(const CardArgs &a, const PackPos &pos,
     }
 }
 
+// The group's 32 codes from its 16 words of bf16 pairs: the low mantissa
+// bits of (x - z_h) * r + 1.5*2^23, clamped to [0, qmax] only when the
+// group's extremes leave the code range (CLAMP), packed b bits each.
+template <bool CLAMP>
+__device__ __forceinline__ void pack_codes(const uint32_t (&ws)[16], int b, float2 negz, float2 inv2, float lo_c,
+                                           float hi_c, uint32_t (&out)[8]) {
+    const float2 mg = make_float2(RNE_MAGIC_C, RNE_MAGIC_C);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {  // 8 values (4 words) at a time
+        uint32_t q[8];  // the code in the low bits, higher bits not cleared
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t wv = ws[4 * e + i];
+            float2 tf = __ffma2_rn(__fadd2_rn(make_float2(bf16_lo(wv), bf16_hi(wv)), negz), inv2, mg);
+            if (CLAMP) {
+                tf.x = fminf(fmaxf(tf.x, lo_c), hi_c);
+                tf.y = fminf(fmaxf(tf.y, lo_c), hi_c);
+            }
+            q[2 * i] = __float_as_uint(tf.x);
+            q[2 * i + 1] = __float_as_uint(tf.y);
+        }
+        if (b == 8) {
+            out[2 * e] = pack_bytes4(q[0], q[1], q[2], q[3]);
+            out[2 * e + 1] = pack_bytes4(q[4], q[5], q[6], q[7]);
+        } else if (b == 4) {
+            uint32_t by[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) by[i] = (q[2 * i] & 0xFu) | ((q[2 * i + 1] & 0xFu) << 4);
+            out[e] = pack_bytes4(by[0], by[1], by[2], by[3]);
+        } else {
+            const uint32_t b0 = (q[0] & 3u) | ((q[1] & 3u) << 2) | ((q[2] & 3u) << 4) | ((q[3] & 3u) << 6);
+            const uint32_t b1 = (q[4] & 3u) | ((q[5] & 3u) << 2) | ((q[6] & 3u) << 4) | ((q[7] & 3u) << 6);
+            if (e & 1)
+                out[e >> 1] |= (b0 << 16) | (b1 << 24);
+            else
+                out[e >> 1] = b0 | (b1 << 8);
+        }
+    }
+}
+
 __global__ void __launch_bounds__(CARD_THREADS, 4) card_pack(const __grid_constant__ CardArgs a) {
     const kvp_card_header *hdr = reinterpret_cast<const kvp_card_header *>(a.card);
     if (hdr->error & (FLAG_BITS | FLAG_SIZE)) return;
@@ -286,39 +326,11 @@ __global__ void __launch_bounds__(CARD_THREADS, 4) card_pack(const __grid_consta
                 const float tmn = fmaf(mn - zf, inv, RNE_MAGIC_C), tmx = fmaf(mx - zf, inv, RNE_MAGIC_C);
                 const bool clamp = !(tmn >= lo_c && tmx <= hi_c);
                 const float2 negz = make_float2(-zf, -zf), inv2 = make_float2(inv, inv);
-                const float2 mg = make_float2(RNE_MAGIC_C, RNE_MAGIC_C);
                 uint32_t out[8];  // packed codes: 4b bytes
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {  // 8 values (4 words) at a time
-                    uint32_t q[8];  // the code in the low bits, higher bits not cleared
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const uint32_t wv = ws[4 * e + i];
-                        float2 tf = __ffma2_rn(__fadd2_rn(make_float2(bf16_lo(wv), bf16_hi(wv)), negz), inv2, mg);
-                        if (clamp) {
-                            tf.x = fminf(fmaxf(tf.x, lo_c), hi_c);
-                            tf.y = fminf(fmaxf(tf.y, lo_c), hi_c);
-                        }
-                        q[2 * i] = __float_as_uint(tf.x);
-                        q[2 * i + 1] = __float_as_uint(tf.y);
-                    }
-                    if (b == 8) {
-                        out[2 * e] = pack_bytes4(q[0], q[1], q[2], q[3]);
-                        out[2 * e + 1] = pack_bytes4(q[4], q[5], q[6], q[7]);
-                    } else if (b == 4) {
-                        uint32_t by[4];
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) by[i] = (q[2 * i] & 0xFu) | ((q[2 * i + 1] & 0xFu) << 4);
-                        out[e] = pack_bytes4(by[0], by[1], by[2], by[3]);
-                    } else {
-                        const uint32_t b0 = (q[0] & 3u) | ((q[1] & 3u) << 2) | ((q[2] & 3u) << 4) | ((q[3] & 3u) << 6);
-                        const uint32_t b1 = (q[4] & 3u) | ((q[5] & 3u) << 2) | ((q[6] & 3u) << 4) | ((q[7] & 3u) << 6);
-                        if (e & 1)
-                            out[e >> 1] |= (b0 << 16) | (b1 << 24);
-                        else
-                            out[e >> 1] = b0 | (b1 << 8);
-                    }
-                }
+                if (clamp)
+                    pack_codes<true>(ws, b, negz, inv2, lo_c, hi_c, out);
+                else
+                    pack_codes<false>(ws, b, negz, inv2, lo_c, hi_c, out);
                 uint8_t *codes = rec + uint64_t(kv) * code_bytes;
                 if (b == 8) {
                     uint4 *o = reinterpret_cast<uint4 *>(codes) + 2 * gi;
