@@ -133,11 +133,13 @@ __device__ uint16_t group_scale_f16(float mx, float mn, float qmax, float rcp_qm
     // estimate within one fp16 step of the answer; the checks below make it exact
     uint32_t h = __half_as_ushort(__float2half_rn(hi * rcp_qmax));
     if (h >= 0x0401u && h <= 0x7BFFu) {  // h and h - 1 normal: midpoints by bit arithmetic
-        int c = cmp_mid(hi, lo, f16_mid_above(h), qmax);
-        if (c > 0 || (c == 0 && (h & 1u))) return uint16_t(h + 1);
-        c = cmp_mid(hi, lo, f16_mid_above(h - 1), qmax);
-        if (c < 0 || (c == 0 && (h & 1u))) return uint16_t(h - 1);
-        return uint16_t(h);
+        // at most one of the two moves applies (the midpoints are ordered)
+        const float ru = fmaf(-f16_mid_above(h), qmax, hi) + lo;
+        const float rl = fmaf(-f16_mid_above(h - 1), qmax, hi) + lo;
+        const bool odd = (h & 1u) != 0;
+        const uint32_t up = (ru > 0.0f || (ru == 0.0f && odd)) ? 1u : 0u;
+        const uint32_t dn = (rl < 0.0f || (rl == 0.0f && odd)) ? 1u : 0u;
+        return uint16_t(h + up - dn);
     }
     if (h == 0x7C00u) return cmp_mid(hi, lo, 65520.0f, qmax) < 0 ? uint16_t(0x7BFFu) : uint16_t(h);
     const float vh = __half2float(__ushort_as_half(uint16_t(h)));
@@ -179,7 +181,8 @@ __device__ __forceinline__ void pack_load(const CardArgs &a, const PackPos &pos,
                                           int gshift, uint32_t T, uint4 (&w)[4]) {
     if (gi < ngroups) {
         const int h = gi >> gshift, gg = gi & ((1 << gshift) - 1);
-        const uint4 *p = a.src[pos.kv][pos.l] + (uint64_t(h) * T + pos.t) * cpr + gg * 4;
+        const uint32_t row = uint32_t(h) * T + pos.t;  // H T < 2^31
+        const uint4 *p = a.src[pos.kv][pos.l] + uint64_t(row) * uint32_t(cpr) + gg * 4;
 #pragma unroll
         for (int q = 0; q < 4; ++q) w[q] = __ldg(p + q);
     } else {
@@ -279,15 +282,16 @@ __global__ void __launch_bounds__(CARD_THREADS, 4) card_pack(const __grid_consta
         const uint32_t t = pos.t;
         const int l = pos.l;
         const int b = bits[t];
-        uint8_t *rec = a.card + a.off_layers + uint64_t(l) * stride + offs[t];
+        uint8_t *rec = a.card + a.off_layers + uint64_t(uint32_t(l)) * stride + offs[t];
+        const uint32_t hd = uint32_t(a.H) * uint32_t(a.d);  // H d < 2^31
         if (b == 16) {
             if (gi < ngroups) {
-                uint4 *out = reinterpret_cast<uint4 *>(rec + uint64_t(kv) * a.H * a.d * 2) + 4 * gi;
+                uint4 *out = reinterpret_cast<uint4 *>(rec + (kv ? 2u * hd : 0u)) + 4 * gi;
 #pragma unroll
                 for (int q = 0; q < 4; ++q) out[q] = w[q];
             }
         } else {
-            const uint64_t code_bytes = uint64_t(a.H) * a.d * b / 8;
+            const uint32_t code_bytes = hd * uint32_t(b) / 8u;
             if (gi < ngroups) {
                 const float qmax = float((1 << b) - 1);
                 const uint32_t ws[16] = {w[0].x, w[0].y, w[0].z, w[0].w, w[1].x, w[1].y, w[1].z, w[1].w,
@@ -331,7 +335,7 @@ __global__ void __launch_bounds__(CARD_THREADS, 4) card_pack(const __grid_consta
                     pack_codes<true>(ws, b, negz, inv2, lo_c, hi_c, out);
                 else
                     pack_codes<false>(ws, b, negz, inv2, lo_c, hi_c, out);
-                uint8_t *codes = rec + uint64_t(kv) * code_bytes;
+                uint8_t *codes = rec + (kv ? code_bytes : 0u);
                 if (b == 8) {
                     uint4 *o = reinterpret_cast<uint4 *>(codes) + 2 * gi;
                     o[0] = make_uint4(out[0], out[1], out[2], out[3]);
@@ -341,12 +345,12 @@ __global__ void __launch_bounds__(CARD_THREADS, 4) card_pack(const __grid_consta
                 } else {
                     reinterpret_cast<uint2 *>(codes)[gi] = make_uint2(out[0], out[1]);
                 }
-                uint32_t *par = reinterpret_cast<uint32_t *>(rec + 2 * code_bytes + uint64_t(kv) * a.H * (a.d / 32) * 4);
+                uint32_t *par = reinterpret_cast<uint32_t *>(rec + 2u * code_bytes + (kv ? hd / 8u : 0u));
                 par[gi] = sb | (zb << 16);
             }
             // zero the record's padding (sizes are multiples of 8, records of 16)
             if (kv == 1 && lane == 0 && round == rounds - 1) {
-                const uint64_t used = 2 * code_bytes + 2ull * a.H * (a.d / 32) * 4;
+                const uint64_t used = 2ull * code_bytes + hd / 4u;
                 const uint64_t padded = card_record_bytes(b, a.H, a.d);
                 if (padded > used) *reinterpret_cast<uint2 *>(rec + used) = make_uint2(0, 0);
             }
