@@ -177,9 +177,10 @@ struct PackPos {
     int l, kv;
 };
 
+template <bool FULL>
 __device__ __forceinline__ void pack_load(const CardArgs &a, const PackPos &pos, int gi, int ngroups, int cpr,
                                           int gshift, uint32_t T, uint4 (&w)[4]) {
-    if (gi < ngroups) {
+    if (FULL || gi < ngroups) {
         const int h = gi >> gshift, gg = gi & ((1 << gshift) - 1);
         const uint32_t row = uint32_t(h) * T + pos.t;  // H T < 2^31
         const uint4 *p = a.src[pos.kv][pos.l] + uint64_t(row) * uint32_t(cpr) + gg * 4;
@@ -231,6 +232,9 @@ __device__ __forceinline__ void pack_codes(const uint32_t (&ws)[16], int b, floa
     }
 }
 
+// FULL: every round holds 32 groups (H d / 32 is a multiple of 32), so no
+// lane is idle and the per-lane group checks drop out.
+template <bool FULL>
 __global__ void __launch_bounds__(CARD_THREADS, 4) card_pack(const __grid_constant__ CardArgs a) {
     const kvp_card_header *hdr = reinterpret_cast<const kvp_card_header *>(a.card);
     if (hdr->error & (FLAG_BITS | FLAG_SIZE)) return;
@@ -258,7 +262,7 @@ __global__ void __launch_bounds__(CARD_THREADS, 4) card_pack(const __grid_consta
     pos.l = int((task >> 1) / T);
     int round = 0;
     uint4 w[4];
-    if (task < tasks) pack_load(a, pos, lane, ngroups, cpr, gshift, T, w);
+    if (task < tasks) pack_load<FULL>(a, pos, lane, ngroups, cpr, gshift, T, w);
     while (task < tasks) {
         // the next round of this warp's sequence, loaded now
         uint32_t ntask = task;
@@ -275,7 +279,7 @@ __global__ void __launch_bounds__(CARD_THREADS, 4) card_pack(const __grid_consta
             }
         }
         uint4 wn[4];
-        if (ntask < tasks) pack_load(a, npos, nround * 32 + lane, ngroups, cpr, gshift, T, wn);
+        if (ntask < tasks) pack_load<FULL>(a, npos, nround * 32 + lane, ngroups, cpr, gshift, T, wn);
 
         const int gi = round * 32 + lane;
         const int kv = pos.kv;
@@ -285,14 +289,14 @@ __global__ void __launch_bounds__(CARD_THREADS, 4) card_pack(const __grid_consta
         uint8_t *rec = a.card + a.off_layers + uint64_t(uint32_t(l)) * stride + offs[t];
         const uint32_t hd = uint32_t(a.H) * uint32_t(a.d);  // H d < 2^31
         if (b == 16) {
-            if (gi < ngroups) {
+            if (FULL || gi < ngroups) {
                 uint4 *out = reinterpret_cast<uint4 *>(rec + (kv ? 2u * hd : 0u)) + 4 * gi;
 #pragma unroll
                 for (int q = 0; q < 4; ++q) out[q] = w[q];
             }
         } else {
             const uint32_t code_bytes = hd * uint32_t(b) / 8u;
-            if (gi < ngroups) {
+            if (FULL || gi < ngroups) {
                 const float qmax = float((1 << b) - 1);
                 const uint32_t ws[16] = {w[0].x, w[0].y, w[0].z, w[0].w, w[1].x, w[1].y, w[1].z, w[1].w,
                                          w[2].x, w[2].y, w[2].z, w[2].w, w[3].x, w[3].y, w[3].z, w[3].w};
@@ -661,7 +665,10 @@ extern "C" int cachecard_pack(const kvp_shape *s, uint64_t model_id, int64_t pos
     // 64 registers (4 blocks/SM) and two resident grids' worth of blocks: more
     // loads in flight for this latency-bound kernel (measured 0.185 -> 0.176 ms
     // on the 4K-token Llama-3-8B step; 5 blocks/SM is slower)
-    card_pack<<<card_grid(card_pack, tasks, 2), CARD_THREADS, 0, st>>>(a);
+    if ((s->n_kv_heads * (s->head_dim / 32)) % 32 == 0)
+        card_pack<true><<<card_grid(card_pack<true>, tasks, 2), CARD_THREADS, 0, st>>>(a);
+    else
+        card_pack<false><<<card_grid(card_pack<false>, tasks, 2), CARD_THREADS, 0, st>>>(a);
     card_zero_tails<<<L, CARD_THREADS, 0, st>>>(a);
     count_launch(3);
     return launch_status();
