@@ -306,16 +306,16 @@ __device__ void quant_slice(const EncodeArgs &a, int l, uint32_t p, uint64_t pol
     const uint4 *src = a.k[l];
     uint2 *dst = reinterpret_cast<uint2 *>(a.pool + a.geo.off_layers + uint64_t(l) * a.geo.layer_stride);
     uint64_t c = c0 + threadIdx.x;
-    for (; c + 3 * ENC_THREADS < c1; c += 4 * ENC_THREADS) {
-        uint4 w[4];
+    for (; c + 7 * ENC_THREADS < c1; c += 8 * ENC_THREADS) {
+        uint4 w[8];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) w[u] = ld_v4_policy(src + c + u * ENC_THREADS, pol);
+        for (int u = 0; u < 8; ++u) w[u] = ld_v4_policy(src + c + u * ENC_THREADS, pol);
         if (pre) {
 #pragma unroll
-            for (int u = 0; u < 4; ++u) __stcs(dst + c + u * ENC_THREADS, k_quant8<true>(w[u], kp));
+            for (int u = 0; u < 8; ++u) __stcs(dst + c + u * ENC_THREADS, k_quant8<true>(w[u], kp));
         } else {
 #pragma unroll
-            for (int u = 0; u < 4; ++u) __stcs(dst + c + u * ENC_THREADS, k_quant8<false>(w[u], kp));
+            for (int u = 0; u < 8; ++u) __stcs(dst + c + u * ENC_THREADS, k_quant8<false>(w[u], kp));
         }
     }
     for (; c < c1; c += ENC_THREADS) {
