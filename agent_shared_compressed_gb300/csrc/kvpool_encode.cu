@@ -10,8 +10,9 @@
 //      layer's maximum with atomicMax.  The block that finishes the layer's
 //      last slice computes the scale s = m/127, writes it to the pool and the
 //      key quantizer's parameters to the workspace, and releases ready[l].
-//   2. the layer's value batches (4 warp steps of VPW vectors per warp, each
-//      warp prefetching its next step into shared memory with cp.async),
+//   2. the layer's value batches (4 warp steps of 1024 value coordinates per
+//      warp, each step copied into shared memory with cp.async while the
+//      previous one is encoded; the rotation runs on the tensor cores),
 //      interleaved with P key slices "quantize": each waits (bounded) for
 //      ready[l], then writes the int8 codes = the integer nearest to the
 //      exact k/s.  The key slice is re-read soon after its first read, from
