@@ -168,11 +168,13 @@ def _bits(a):
     return (np.asarray(a, np.float32).view(np.uint32) >> 16).astype(np.uint16)
 
 
-def test_degenerate_layers_match_oracle():
+@pytest.mark.parametrize("d", [128, 64])
+def test_degenerate_layers_match_oracle(d):
     """Zero tensors (s = 0, codes 0 / 4, sigma 0), a tiny-magnitude layer (key
     scale below 2^-100, value norms below 2^-50), exact ties in k/s (s = 1,
-    half-integer keys), one-hot and constant value vectors."""
-    L, H, d, T = 4, 2, 128, 24
+    half-integer keys), one-hot and constant value vectors; both head_dims
+    (at 64 each lane of the value encoder holds two vectors)."""
+    L, H, T = 4, 2, 24
     rng = np.random.default_rng(0)
     ks, vs = [], []
     ks.append(np.zeros((H, T, d), np.uint16)); vs.append(np.zeros((H, T, d), np.uint16))
@@ -202,6 +204,28 @@ def test_degenerate_layers_match_oracle():
         assert_bf16_close(synth.bits16(ck[1][l].bf16((H, T, d))), ok_[0][l], "K layer %d" % l)
         assert_bf16_close(synth.bits16(cv[1][l].bf16((H, T, d))), ov[0][l], "V layer %d" % l)
     assert not ck[0][0].t.any() and not cv[0][0].t.any()
+
+
+@pytest.mark.parametrize("d", [128, 64])
+def test_mixed_magnitude_vectors_in_one_warp_step(d):
+    """Zero, tiny (norm below 2^-50), ordinary and large value vectors next to
+    one another, so one warp step of the value encoder holds all of them:
+    the zero vectors code as 4, the tiny ones are rescaled, the others not."""
+    L, H, T = 1, 2, 40
+    rng = np.random.default_rng(3)
+    scale = np.array([0.0, 1e-20, 1.0, 1e3, 1e-30, 7.0, 0.0, 1e-3])[np.arange(T) % 8]
+    v = rng.normal(size=(H, T, d)) * scale[None, :, None]
+    ks = [_bits(rng.normal(size=(H, T, d)))]
+    vs = [_bits(v)]
+    shape = (L, H, d, T)
+    pool, status, _ = gpu_encode(ks, vs, shape)
+    assert status == kv.KVP_OK
+    ora, flags, u = O.pool_encode(ks, vs, want_u=True)
+    assert flags == 0
+    assert_pool_parity(pool.host(), ora, u, L, H, d, T)
+    sec = pool_sections(pool.host(), L, H, d, T)
+    codes = unpack3_np(sec["vpacked"][0], d).reshape(H, T, d)
+    assert np.all(codes[:, scale == 0.0, :] == 4)
 
 
 @pytest.mark.parametrize("where,value,code", [("k", np.nan, kv.KVP_ERR_NONFINITE), ("k", np.inf, kv.KVP_ERR_NONFINITE),
