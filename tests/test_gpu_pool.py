@@ -228,11 +228,12 @@ def test_mixed_magnitude_vectors_in_one_warp_step(d):
     assert np.all(codes[:, scale == 0.0, :] == 4)
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("where,value,code", [("k", np.nan, kv.KVP_ERR_NONFINITE), ("k", np.inf, kv.KVP_ERR_NONFINITE),
                                               ("v", np.nan, kv.KVP_ERR_NONFINITE), ("v", -np.inf, kv.KVP_ERR_NONFINITE),
                                               ("v", 1e6, kv.KVP_ERR_RANGE)])
-def test_device_detected_errors(where, value, code):
-    L, H, d, T = 2, 2, 64, 16
+def test_device_detected_errors(where, value, code, d):
+    L, H, T = 2, 2, 16
     ks, vs = cpu_inputs(L, H, T, d, seed=1)
     arr = (ks if where == "k" else vs)[1].copy()
     if value == 1e6:
@@ -244,6 +245,27 @@ def test_device_detected_errors(where, value, code):
     assert status == code
     _, flags, _ = O.pool_encode(ks, vs)
     assert flags == {kv.KVP_ERR_NONFINITE: O.FLAG_NONFINITE, kv.KVP_ERR_RANGE: O.FLAG_RANGE}[code]
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_sigma_near_the_fp16_limit(d):
+    """A constant value vector has sigma = |x|: 59,904 is an fp16 value just
+    below the largest (no error, sigma stored exactly); 70,144 is above it (a
+    range error).  Both sides agree with the oracle."""
+    L, H, T = 1, 2, 16
+    for x, code in ((6.0e4, kv.KVP_OK), (7.0e4, kv.KVP_ERR_RANGE)):
+        ks, vs = cpu_inputs(L, H, T, d, seed=2)
+        arr = vs[0].copy()
+        arr[1, 5, :] = _bits(np.full(d, x))
+        vs[0] = arr
+        pool, status, _ = gpu_encode(ks, vs, (L, H, d, T))
+        assert status == code
+        ora, flags, _ = O.pool_encode(ks, vs)
+        assert flags == (0 if code == kv.KVP_OK else O.FLAG_RANGE)
+        if code == kv.KVP_OK:
+            xv = float((np.uint32(_bits(np.array([x]))[0]) << np.uint32(16)).view(np.float32))
+            sec = pool_sections(pool.host(), L, H, d, T)
+            assert int(sec["sigma"][0][1, 5]) == O.f64_to_f16(xv)
 
 
 # --- full-size workloads, sampled -------------------------------------------
