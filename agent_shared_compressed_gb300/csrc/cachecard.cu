@@ -232,6 +232,78 @@ __device__ __forceinline__ void pack_codes(const uint32_t (&ws)[16], int b, floa
     }
 }
 
+// The codes and group parameters of one group (one lane) of a b-bit pack
+// round, B < 16: min / max, the fp16 scale and zero point, the codes.  B is a
+// template argument so that each bitwidth's code path is straight-line (with
+// a run-time b the 4K-token step's pack took 0.149 against 0.135 ms).
+template <int B, bool FULL>
+__device__ __forceinline__ void pack_group(const CardArgs &a, uint8_t *rec, const uint4 (&w)[4], int gi, int ngroups,
+                                           int kv, uint32_t hd, int lane, int round, int rounds, uint32_t &flags) {
+    const uint32_t code_bytes = hd * uint32_t(B) / 8u;
+    if (FULL || gi < ngroups) {
+        const float qmax = float((1 << B) - 1);
+        const uint32_t ws[16] = {w[0].x, w[0].y, w[0].z, w[0].w, w[1].x, w[1].y, w[1].z, w[1].w,
+                                 w[2].x, w[2].y, w[2].z, w[2].w, w[3].x, w[3].y, w[3].z, w[3].w};
+        // min / max on the packed bf16 pairs (exact).  The maximum
+        // propagates NaN, so a group holding Inf or NaN has a non-finite
+        // min or max.
+        __nv_bfloat162 mnp = *reinterpret_cast<const __nv_bfloat162 *>(&ws[0]), mxp = mnp;
+#pragma unroll
+        for (int i = 1; i < 16; ++i) {
+            const __nv_bfloat162 pr = *reinterpret_cast<const __nv_bfloat162 *>(&ws[i]);
+            mnp = __hmin2(mnp, pr);
+            mxp = __hmax2_nan(mxp, pr);
+        }
+        const float mn = fminf(__low2float(mnp), __high2float(mnp));
+        const float mx0 = __low2float(mxp), mx1 = __high2float(mxp);
+        const float mx = fmaxf(mx0, mx1);
+        const bool nf = !(fabsf(mn) <= 3.0e38f) || !(fabsf(mx0) <= 3.0e38f) || !(fabsf(mx1) <= 3.0e38f);
+        const uint32_t sb = group_scale_f16(mx, mn, qmax, 1.0f / qmax);
+        const uint32_t zb = __half_as_ushort(__float2half_rn(mn));
+        if (nf)
+            flags |= FLAG_NONFINITE;
+        else if (((sb & 0x7C00u) == 0x7C00u) || ((zb & 0x7C00u) == 0x7C00u))
+            flags |= FLAG_RANGE;
+        const float sf = __half2float(__ushort_as_half(uint16_t(sb)));
+        const float zf = __half2float(__ushort_as_half(uint16_t(zb)));
+        const float inv = (sf > 0.0f && sf <= 65504.0f) ? __fdividef(1.0f, sf) : 0.0f;
+        // code = clamp(round((x - z_h) / s_h), 0, 2^b - 1): the low mantissa
+        // bits of (x - z_h) * r + 1.5*2^23, r the fast reciprocal of s_h
+        // (within 2 ulp): for codes up to 255 the estimate is within 8e-5
+        // of the exact quotient, so it rounds the same way unless that
+        // quotient lies within 8e-5 of a half-integer.  The map is
+        // monotone, so the clamp is needed only if the group's extremes
+        // fall outside the code range.
+        const float lo_c = RNE_MAGIC_C, hi_c = RNE_MAGIC_C + qmax;
+        const float tmn = fmaf(mn - zf, inv, RNE_MAGIC_C), tmx = fmaf(mx - zf, inv, RNE_MAGIC_C);
+        const bool clamp = !(tmn >= lo_c && tmx <= hi_c);
+        const float2 negz = make_float2(-zf, -zf), inv2 = make_float2(inv, inv);
+        uint32_t out[8];  // packed codes: 4b bytes
+        if (clamp)
+            pack_codes<true>(ws, B, negz, inv2, lo_c, hi_c, out);
+        else
+            pack_codes<false>(ws, B, negz, inv2, lo_c, hi_c, out);
+        uint8_t *codes = rec + (kv ? code_bytes : 0u);
+        if (B == 8) {
+            uint4 *o = reinterpret_cast<uint4 *>(codes) + 2 * gi;
+            o[0] = make_uint4(out[0], out[1], out[2], out[3]);
+            o[1] = make_uint4(out[4], out[5], out[6], out[7]);
+        } else if (B == 4) {
+            reinterpret_cast<uint4 *>(codes)[gi] = make_uint4(out[0], out[1], out[2], out[3]);
+        } else {
+            reinterpret_cast<uint2 *>(codes)[gi] = make_uint2(out[0], out[1]);
+        }
+        uint32_t *par = reinterpret_cast<uint32_t *>(rec + 2u * code_bytes + (kv ? hd / 8u : 0u));
+        par[gi] = sb | (zb << 16);
+    }
+    // zero the record's padding (sizes are multiples of 8, records of 16)
+    if (kv == 1 && lane == 0 && round == rounds - 1) {
+        const uint64_t used = 2ull * code_bytes + hd / 4u;
+        const uint64_t padded = card_record_bytes(B, a.H, a.d);
+        if (padded > used) *reinterpret_cast<uint2 *>(rec + used) = make_uint2(0, 0);
+    }
+}
+
 // FULL: every round holds 32 groups (H d / 32 is a multiple of 32), so no
 // lane is idle and the per-lane group checks drop out.
 template <bool FULL>
@@ -294,70 +366,12 @@ __global__ void __launch_bounds__(CARD_THREADS, 4) card_pack(const __grid_consta
 #pragma unroll
                 for (int q = 0; q < 4; ++q) out[q] = w[q];
             }
-        } else {
-            const uint32_t code_bytes = hd * uint32_t(b) / 8u;
-            if (FULL || gi < ngroups) {
-                const float qmax = float((1 << b) - 1);
-                const uint32_t ws[16] = {w[0].x, w[0].y, w[0].z, w[0].w, w[1].x, w[1].y, w[1].z, w[1].w,
-                                         w[2].x, w[2].y, w[2].z, w[2].w, w[3].x, w[3].y, w[3].z, w[3].w};
-                // min / max on the packed bf16 pairs (exact).  The maximum
-                // propagates NaN, so a group holding Inf or NaN has a non-finite
-                // min or max.
-                __nv_bfloat162 mnp = *reinterpret_cast<const __nv_bfloat162 *>(&ws[0]), mxp = mnp;
-#pragma unroll
-                for (int i = 1; i < 16; ++i) {
-                    const __nv_bfloat162 pr = *reinterpret_cast<const __nv_bfloat162 *>(&ws[i]);
-                    mnp = __hmin2(mnp, pr);
-                    mxp = __hmax2_nan(mxp, pr);
-                }
-                const float mn = fminf(__low2float(mnp), __high2float(mnp));
-                const float mx0 = __low2float(mxp), mx1 = __high2float(mxp);
-                const float mx = fmaxf(mx0, mx1);
-                const bool nf = !(fabsf(mn) <= 3.0e38f) || !(fabsf(mx0) <= 3.0e38f) || !(fabsf(mx1) <= 3.0e38f);
-                const uint32_t sb = group_scale_f16(mx, mn, qmax, 1.0f / qmax);
-                const uint32_t zb = __half_as_ushort(__float2half_rn(mn));
-                if (nf)
-                    flags |= FLAG_NONFINITE;
-                else if (((sb & 0x7C00u) == 0x7C00u) || ((zb & 0x7C00u) == 0x7C00u))
-                    flags |= FLAG_RANGE;
-                const float sf = __half2float(__ushort_as_half(uint16_t(sb)));
-                const float zf = __half2float(__ushort_as_half(uint16_t(zb)));
-                const float inv = (sf > 0.0f && sf <= 65504.0f) ? __fdividef(1.0f, sf) : 0.0f;
-                // code = clamp(round((x - z_h) / s_h), 0, 2^b - 1): the low mantissa
-                // bits of (x - z_h) * r + 1.5*2^23, r the fast reciprocal of s_h
-                // (within 2 ulp): for codes up to 255 the estimate is within 8e-5
-                // of the exact quotient, so it rounds the same way unless that
-                // quotient lies within 8e-5 of a half-integer.  The map is
-                // monotone, so the clamp is needed only if the group's extremes
-                // fall outside the code range.
-                const float lo_c = RNE_MAGIC_C, hi_c = RNE_MAGIC_C + qmax;
-                const float tmn = fmaf(mn - zf, inv, RNE_MAGIC_C), tmx = fmaf(mx - zf, inv, RNE_MAGIC_C);
-                const bool clamp = !(tmn >= lo_c && tmx <= hi_c);
-                const float2 negz = make_float2(-zf, -zf), inv2 = make_float2(inv, inv);
-                uint32_t out[8];  // packed codes: 4b bytes
-                if (clamp)
-                    pack_codes<true>(ws, b, negz, inv2, lo_c, hi_c, out);
-                else
-                    pack_codes<false>(ws, b, negz, inv2, lo_c, hi_c, out);
-                uint8_t *codes = rec + (kv ? code_bytes : 0u);
-                if (b == 8) {
-                    uint4 *o = reinterpret_cast<uint4 *>(codes) + 2 * gi;
-                    o[0] = make_uint4(out[0], out[1], out[2], out[3]);
-                    o[1] = make_uint4(out[4], out[5], out[6], out[7]);
-                } else if (b == 4) {
-                    reinterpret_cast<uint4 *>(codes)[gi] = make_uint4(out[0], out[1], out[2], out[3]);
-                } else {
-                    reinterpret_cast<uint2 *>(codes)[gi] = make_uint2(out[0], out[1]);
-                }
-                uint32_t *par = reinterpret_cast<uint32_t *>(rec + 2u * code_bytes + (kv ? hd / 8u : 0u));
-                par[gi] = sb | (zb << 16);
-            }
-            // zero the record's padding (sizes are multiples of 8, records of 16)
-            if (kv == 1 && lane == 0 && round == rounds - 1) {
-                const uint64_t used = 2ull * code_bytes + hd / 4u;
-                const uint64_t padded = card_record_bytes(b, a.H, a.d);
-                if (padded > used) *reinterpret_cast<uint2 *>(rec + used) = make_uint2(0, 0);
-            }
+        } else if (b == 2) {
+            pack_group<2, FULL>(a, rec, w, gi, ngroups, kv, hd, lane, round, rounds, flags);
+        } else if (b == 4) {
+            pack_group<4, FULL>(a, rec, w, gi, ngroups, kv, hd, lane, round, rounds, flags);
+        } else {  // 8: card_scan has flagged any other bitwidth, and this kernel then returns at once
+            pack_group<8, FULL>(a, rec, w, gi, ngroups, kv, hd, lane, round, rounds, flags);
         }
         task = ntask;
         pos = npos;
@@ -431,24 +445,28 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float (&y)[8]) {
 }
 
 // One (layer, token, K|V) task of a plain unpack, by one warp: lanes over
-// the H * d/8 chunks of the token.
-__device__ __forceinline__ void unpack_task_plain(const CardArgs &a, const uint8_t *rec, uint4 *dst, int b, int kv,
-                                                  uint32_t t, int lane) {
+// the H * d/8 chunks of the token.  B: the token's bitwidth, a template
+// argument so that each bitwidth's code path is straight-line (a run-time b
+// inside the chunk loop costs the 4K-token step's unpack 3 %).
+template <int B>
+__device__ __forceinline__ void unpack_task_b(const CardArgs &a, const uint8_t *rec, uint4 *dst, int kv, uint32_t t,
+                                              int lane) {
     const int cpr = a.d / 8;
     const int cshift = a.d == 128 ? 4 : 3;
     const int nchunks = a.H * cpr;
     const uint32_t T = uint32_t(a.T);
-    if (b == 16) {
-        const uint4 *in = reinterpret_cast<const uint4 *>(rec + uint64_t(kv) * a.H * a.d * 2);
+    const uint32_t hd = uint32_t(a.H) * uint32_t(a.d);
+    if (B == 16) {
+        const uint4 *in = reinterpret_cast<const uint4 *>(rec + (kv ? 2u * hd : 0u));
         for (int c = lane; c < nchunks; c += 32) {
             const int h = c >> cshift, ch = c & (cpr - 1);
             st_stream_v4(dst + (uint64_t(h) * T + t) * cpr + ch, ld_stream_v4(in + c));
         }
         return;
     }
-    const uint64_t code_bytes = uint64_t(a.H) * a.d * b / 8;
-    const uint8_t *codes = rec + uint64_t(kv) * code_bytes;
-    const uint32_t *par = reinterpret_cast<const uint32_t *>(rec + 2 * code_bytes + uint64_t(kv) * a.H * (a.d / 32) * 4);
+    const uint32_t code_bytes = hd * uint32_t(B) / 8u;
+    const uint8_t *codes = rec + (kv ? code_bytes : 0u);
+    const uint32_t *par = reinterpret_cast<const uint32_t *>(rec + 2u * code_bytes + (kv ? hd / 8u : 0u));
     for (int c0 = 0; c0 < nchunks; c0 += 4 * 32) {
         // up to 4 chunks' codes and group parameters per lane in flight
         uint2 cw[4];
@@ -459,7 +477,7 @@ __device__ __forceinline__ void unpack_task_plain(const CardArgs &a, const uint8
             cw[it] = make_uint2(0, 0);
             pw[it] = 0;
             if (c < nchunks) {
-                cw[it] = card_chunk_codes(b, codes, c);
+                cw[it] = card_chunk_codes(B, codes, c);
                 pw[it] = par[c >> 2];
             }
         }
@@ -468,10 +486,21 @@ __device__ __forceinline__ void unpack_task_plain(const CardArgs &a, const uint8
             const int c = c0 + it * 32 + lane;
             if (c >= nchunks) break;
             float y[8];
-            card_chunk_values(b, cw[it], pw[it], y);
+            card_chunk_values(B, cw[it], pw[it], y);
             const int h = c >> cshift, ch = c & (cpr - 1);
             st_stream_v4(dst + (uint64_t(h) * T + t) * cpr + ch, pack_bf16x8(y));
         }
+    }
+}
+
+// b: a checked bitwidth (2, 4, 8 or 16).
+__device__ __forceinline__ void unpack_task_plain(const CardArgs &a, const uint8_t *rec, uint4 *dst, int b, int kv,
+                                                  uint32_t t, int lane) {
+    switch (b) {
+    case 2: unpack_task_b<2>(a, rec, dst, kv, t, lane); break;
+    case 4: unpack_task_b<4>(a, rec, dst, kv, t, lane); break;
+    case 8: unpack_task_b<8>(a, rec, dst, kv, t, lane); break;
+    default: unpack_task_b<16>(a, rec, dst, kv, t, lane); break;
     }
 }
 
@@ -488,7 +517,9 @@ __device__ __forceinline__ const uint8_t *unpack_record(const CardArgs &a, int l
     return a.card + a.off_layers + uint64_t(l) * a.layer_stride + offs[t];
 }
 
-__global__ void __launch_bounds__(CARD_THREADS) card_unpack(const __grid_constant__ CardArgs a) {
+// 48 registers, 5 blocks/SM (at 52 the allocator drops to 4 and the 8K-token
+// card unpack takes 0.266 against 0.244 ms)
+__global__ void __launch_bounds__(CARD_THREADS, 5) card_unpack(const __grid_constant__ CardArgs a) {
     const int lane = threadIdx.x & 31;
     const uint32_t T = uint32_t(a.T);
     const uint32_t tasks = uint32_t(a.L) * T * 2u;  // fits: checked on the host
@@ -516,13 +547,87 @@ __global__ void __launch_bounds__(CARD_THREADS) card_unpack(const __grid_constan
 // coordinates per packed f32x2 instruction, and rounded to bf16 once.  Values
 // are unpacked as by card_unpack.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(CARD_THREADS, 4) card_unpack_rope(const __grid_constant__ CardArgs a) {
-    const int lane = threadIdx.x & 31;
+// The keys of one token, turned: lanes over the H d/16 pairs of chunks
+// (c, c + d/16) of a head row, which hold the coordinates (i, i + d/2) that
+// one rotary frequency couples; two pairs (four chunks) per lane in flight.
+// B: the token's bitwidth, a template argument so that each bitwidth's
+// code path is straight-line.  rc, rs: (cos, sin) of the lane's 8
+// frequencies, two per packed register.
+template <int B>
+__device__ __forceinline__ void rope_keys(const CardArgs &a, const uint8_t *rec, uint4 *dst, uint32_t t, int lane,
+                                          const float2 (&rc)[4], const float2 (&rs)[4]) {
+    constexpr int b = B;
     const int cpr = a.d / 8, half = cpr / 2;  // chunks per row, per half row
     const int hshift = a.d == 128 ? 3 : 2;     // log2(half)
     const int npairs = a.H * half;
+    const int chl = lane & (half - 1);  // the lane's chunk within the half row, the same for every pair
+    const uint32_t T = uint32_t(a.T);
+    const uint64_t code_bytes = uint64_t(a.H) * a.d * b / 8;
+    const uint32_t *par = reinterpret_cast<const uint32_t *>(rec + 2 * code_bytes);
+    for (int p0 = 0; p0 < npairs; p0 += 2 * 32) {
+        uint4 ra[2], rb[2];
+        uint32_t pa[2], pb[2];
+#pragma unroll
+        for (int it = 0; it < 2; ++it) {
+            const int p = p0 + it * 32 + lane;
+            ra[it] = rb[it] = make_uint4(0, 0, 0, 0);
+            pa[it] = pb[it] = 0;
+            if (p < npairs) {
+                const int ca = (p >> hshift) * cpr + (p & (half - 1)), cb = ca + half;
+                if (b == 16) {  // resolved at compile time
+                    ra[it] = ld_stream_v4(reinterpret_cast<const uint4 *>(rec) + ca);
+                    rb[it] = ld_stream_v4(reinterpret_cast<const uint4 *>(rec) + cb);
+                } else {
+                    const uint2 x = card_chunk_codes(b, rec, ca), y = card_chunk_codes(b, rec, cb);
+                    ra[it] = make_uint4(x.x, x.y, 0, 0);
+                    rb[it] = make_uint4(y.x, y.y, 0, 0);
+                    pa[it] = par[ca >> 2];
+                    pb[it] = par[cb >> 2];
+                }
+            }
+        }
+#pragma unroll
+        for (int it = 0; it < 2; ++it) {
+            const int p = p0 + it * 32 + lane;
+            if (p >= npairs) break;
+            const int h = p >> hshift;
+            const int ca = h * cpr + chl, cb = ca + half;
+            float ya[8], yb[8];
+            if (b == 16) {
+                const uint32_t wa[4] = {ra[it].x, ra[it].y, ra[it].z, ra[it].w};
+                const uint32_t wb[4] = {rb[it].x, rb[it].y, rb[it].z, rb[it].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    ya[2 * e] = bf16_lo(wa[e]);
+                    ya[2 * e + 1] = bf16_hi(wa[e]);
+                    yb[2 * e] = bf16_lo(wb[e]);
+                    yb[2 * e + 1] = bf16_hi(wb[e]);
+                }
+            } else {
+                card_chunk_values(b, make_uint2(ra[it].x, ra[it].y), pa[it], ya);
+                card_chunk_values(b, make_uint2(rb[it].x, rb[it].y), pb[it], yb);
+            }
+            // oa = ya cos - yb sin, ob = ya sin + yb cos: one product rounded, then one fma
+            float oa[8], ob[8];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 xa = make_float2(ya[2 * e], ya[2 * e + 1]), xb = make_float2(yb[2 * e], yb[2 * e + 1]);
+                const float2 ta = __fmul2_rn(xb, rs[e]), tb = __fmul2_rn(xb, rc[e]);
+                const float2 u = __ffma2_rn(xa, rc[e], make_float2(-ta.x, -ta.y));
+                const float2 w = __ffma2_rn(xa, rs[e], tb);
+                oa[2 * e] = u.x, oa[2 * e + 1] = u.y;
+                ob[2 * e] = w.x, ob[2 * e + 1] = w.y;
+            }
+            st_stream_v4(dst + (uint64_t(h) * T + t) * cpr + (ca - h * cpr), pack_bf16x8(oa));
+            st_stream_v4(dst + (uint64_t(h) * T + t) * cpr + (cb - h * cpr), pack_bf16x8(ob));
+        }
+    }
+}
+
+__global__ void __launch_bounds__(CARD_THREADS, 4) card_unpack_rope(const __grid_constant__ CardArgs a) {
+    const int lane = threadIdx.x & 31;
     // a lane's chunk within the half row is the same for every pair it takes
-    const int chl = lane & (half - 1);
+    const int chl = lane & (a.d / 16 - 1);
     float2 rc[4], rs[4];  // (cos, sin) of the lane's 8 frequencies, two per packed register
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -532,9 +637,15 @@ __global__ void __launch_bounds__(CARD_THREADS, 4) card_unpack_rope(const __grid
     }
     const uint32_t T = uint32_t(a.T);
     const uint32_t tasks = uint32_t(a.L) * T * 2u;
+    // The grid's warp count is even, so task = 2 (l T + t) + kv would give each
+    // warp one half (keys or values) for good, and the warps with the heavier
+    // key turns would run on alone at the end.  The half is flipped on each of
+    // the warp's turns instead: warps 2j and 2j + 1 still take complementary
+    // halves of the same token, so every (token, half) is taken once.
+    int flip = 0;
     for (uint32_t task = blockIdx.x * CARD_WARPS + (threadIdx.x >> 5); task < tasks;
-         task += gridDim.x * CARD_WARPS) {
-        const int kv = int(task & 1u);
+         task += gridDim.x * CARD_WARPS, flip ^= 1) {
+        const int kv = int(task & 1u) ^ flip;
         const uint32_t lt = task >> 1;
         const uint32_t t = lt % T;
         const int l = int(lt / T);
@@ -546,66 +657,11 @@ __global__ void __launch_bounds__(CARD_THREADS, 4) card_unpack_rope(const __grid
             unpack_task_plain(a, rec, dst, b, kv, t, lane);
             continue;
         }
-        const uint64_t code_bytes = uint64_t(a.H) * a.d * b / 8;
-        const uint32_t *par = reinterpret_cast<const uint32_t *>(rec + 2 * code_bytes);
-        for (int p0 = 0; p0 < npairs; p0 += 2 * 32) {
-            // two pairs (four chunks) per lane in flight
-            uint4 ra[2], rb[2];
-            uint32_t pa[2], pb[2];
-#pragma unroll
-            for (int it = 0; it < 2; ++it) {
-                const int p = p0 + it * 32 + lane;
-                ra[it] = rb[it] = make_uint4(0, 0, 0, 0);
-                pa[it] = pb[it] = 0;
-                if (p < npairs) {
-                    const int ca = (p >> hshift) * cpr + (p & (half - 1)), cb = ca + half;
-                    if (b == 16) {
-                        ra[it] = ld_stream_v4(reinterpret_cast<const uint4 *>(rec) + ca);
-                        rb[it] = ld_stream_v4(reinterpret_cast<const uint4 *>(rec) + cb);
-                    } else {
-                        const uint2 x = card_chunk_codes(b, rec, ca), y = card_chunk_codes(b, rec, cb);
-                        ra[it] = make_uint4(x.x, x.y, 0, 0);
-                        rb[it] = make_uint4(y.x, y.y, 0, 0);
-                        pa[it] = par[ca >> 2];
-                        pb[it] = par[cb >> 2];
-                    }
-                }
-            }
-#pragma unroll
-            for (int it = 0; it < 2; ++it) {
-                const int p = p0 + it * 32 + lane;
-                if (p >= npairs) break;
-                const int h = p >> hshift;
-                const int ca = h * cpr + chl, cb = ca + half;
-                float ya[8], yb[8];
-                if (b == 16) {
-                    const uint32_t wa[4] = {ra[it].x, ra[it].y, ra[it].z, ra[it].w};
-                    const uint32_t wb[4] = {rb[it].x, rb[it].y, rb[it].z, rb[it].w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        ya[2 * e] = bf16_lo(wa[e]);
-                        ya[2 * e + 1] = bf16_hi(wa[e]);
-                        yb[2 * e] = bf16_lo(wb[e]);
-                        yb[2 * e + 1] = bf16_hi(wb[e]);
-                    }
-                } else {
-                    card_chunk_values(b, make_uint2(ra[it].x, ra[it].y), pa[it], ya);
-                    card_chunk_values(b, make_uint2(rb[it].x, rb[it].y), pb[it], yb);
-                }
-                // oa = ya cos - yb sin, ob = ya sin + yb cos: one product rounded, then one fma
-                float oa[8], ob[8];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 xa = make_float2(ya[2 * e], ya[2 * e + 1]), xb = make_float2(yb[2 * e], yb[2 * e + 1]);
-                    const float2 ta = __fmul2_rn(xb, rs[e]), tb = __fmul2_rn(xb, rc[e]);
-                    const float2 u = __ffma2_rn(xa, rc[e], make_float2(-ta.x, -ta.y));
-                    const float2 w = __ffma2_rn(xa, rs[e], tb);
-                    oa[2 * e] = u.x, oa[2 * e + 1] = u.y;
-                    ob[2 * e] = w.x, ob[2 * e + 1] = w.y;
-                }
-                st_stream_v4(dst + (uint64_t(h) * T + t) * cpr + (ca - h * cpr), pack_bf16x8(oa));
-                st_stream_v4(dst + (uint64_t(h) * T + t) * cpr + (cb - h * cpr), pack_bf16x8(ob));
-            }
+        switch (b) {  // unpack_record has checked b
+        case 2: rope_keys<2>(a, rec, dst, t, lane, rc, rs); break;
+        case 4: rope_keys<4>(a, rec, dst, t, lane, rc, rs); break;
+        case 8: rope_keys<8>(a, rec, dst, t, lane, rc, rs); break;
+        default: rope_keys<16>(a, rec, dst, t, lane, rc, rs); break;
         }
     }
 }
