@@ -12,7 +12,7 @@ from .binding import (  # noqa: F401
     Shape, cachecard_bytes, cachecard_pack, cachecard_read_header, cachecard_status, cachecard_unpack,
     cachecard_unpack_at,
     check, declared_functions, kvp_bandwidth_probe, KVP_PROBE_STORE, KVP_PROBE_BULK_STORE, KVP_PROBE_COPY,
-    kvp_launch_count, kvp_test_fail_next_encode, kvp_test_limit_next_attend, kvp_strerror, kvpool_attend, kvpool_attend_workspace_bytes, kvpool_attend_lora,
+    kvp_launch_count, kvp_test_fail_next_encode, kvp_test_limit_next_attend, kvp_test_limit_next_unpack, kvp_strerror, kvpool_attend, kvpool_attend_workspace_bytes, kvpool_attend_lora,
     kvpool_attend_lora_workspace_bytes, kvpool_decode_into, kvpool_encode, kvpool_encode_ex, kvpool_encode_noalloc, KVP_NOALLOC_SCRATCH_BYTES,
     kvpool_pool_bytes, kvpool_pool_bytes_ex, kvpool_status, KVP_K_PER_TENSOR, KVP_K_Q8_0, kvpool_workspace_bytes, load,
 )

@@ -92,6 +92,7 @@ _SIGS = {
     "kvp_bandwidth_probe": (C.c_int, [C.c_int, _vp, _vp, C.c_size_t, _vp]),
     "kvp_test_fail_next_encode": (C.c_int, [C.c_int, C.c_uint32]),
     "kvp_test_limit_next_attend": (C.c_int, [C.c_uint32]),
+    "kvp_test_limit_next_unpack": (C.c_int, [C.c_uint32]),
 }
 
 _lib = None
@@ -276,6 +277,10 @@ def kvp_test_fail_next_encode(layer, spin_iters):
 
 def kvp_test_limit_next_attend(polls):
     return load().kvp_test_limit_next_attend(int(polls))
+
+
+def kvp_test_limit_next_unpack(polls):
+    return load().kvp_test_limit_next_unpack(int(polls))
 
 
 class KVPError(RuntimeError):

@@ -20,7 +20,7 @@ LIB = os.path.join(PKG, "libkvcodec.so")
 
 SOURCES = ["kvp_host.cu", "kvpool_encode.cu", "kvpool_decode.cu", "cachecard.cu", "kvpool_noalloc.cu", "kvpool_attend.cu",
            "kvp_probe.cu"]
-HEADERS = ["kvp_internal.cuh", "kvp_vec.cuh"]
+HEADERS = ["kvp_internal.cuh", "kvp_vec.cuh", "kvp_async.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

@@ -8,6 +8,7 @@
 // cachecard_unpack: card_unpack, the inverse, one warp per record half.
 #include <cmath>
 
+#include "kvp_async.cuh"
 #include "kvp_internal.cuh"
 
 namespace kvp {
@@ -27,6 +28,8 @@ struct CardArgs {
     int64_t pos_offset;
     uint64_t off_offsets, off_layers, layer_stride;
     int L, H, T, d;
+    uint32_t it_dt, it_dl;  // staged unpack: (token, layer) step of a warp's tasks
+    uint32_t wait_polls;    // staged unpack: polls of a buffer's copies before giving up
     int64_t shift;      // unpack_at: target offset - card offset
     float2 rot[64];     // unpack_at: (cos, sin) of shift * w_i for the d/2 rotary frequencies w_i
 };
@@ -510,7 +513,7 @@ __device__ __forceinline__ const uint8_t *unpack_record(const CardArgs &a, int l
     const uint8_t *bits = a.card + CARD_HEADER_BYTES;
     const uint32_t *offs = reinterpret_cast<const uint32_t *>(a.card + a.off_offsets);
     b = bits[t];
-    if (!valid_bits(b) || uint64_t(offs[t]) + card_record_bytes(b, a.H, a.d) > a.layer_stride) {
+    if (!valid_bits(b) || (offs[t] & 15u) != 0 || uint64_t(offs[t]) + card_record_bytes(b, a.H, a.d) > a.layer_stride) {
         if (lane == 0) atomicOr(&reinterpret_cast<kvp_card_header *>(a.card)->error, FLAG_HEADER);
         return nullptr;
     }
@@ -666,10 +669,255 @@ __global__ void __launch_bounds__(CARD_THREADS, 4) card_unpack_rope(const __grid
     }
 }
 
+// ---------------------------------------------------------------------------
+// Staged unpack.  Each warp has two shared-memory buffers, each with its
+// mbarrier.  While it dequantizes task k from one buffer, the half-record
+// (codes and group parameters, or the bf16 half of a 16-bit token) of task
+// k + 1 lands in the other by bulk copies that its lane 0 issued, and the
+// bitwidth and offset of task k + 2 are loaded: a task's record reads are in
+// flight through the previous task's arithmetic and stores, with no
+// registers held for them.  A warp's tasks advance by a fixed (token, layer)
+// step, and the halves are taken as in card_unpack (ROPE = false) and
+// card_unpack_rope (ROPE = true).  Used where two buffers of 2 H d bytes per
+// warp fit 48 KB per block and every part of a record starts on a 16-byte
+// boundary (d = 128, or H even).
+// ---------------------------------------------------------------------------
+constexpr uint32_t CARD_WAIT_LIMIT = 1u << 22;  // polls, about half a second
+
+// A task's position, bitwidth and record offset; ok: its record may be read.
+struct StagedTask {
+    uint32_t t, l, off;
+    int b;
+    bool ok;
+};
+
+__device__ __forceinline__ void staged_load_hdr(const CardArgs &a, StagedTask &x) {
+    x.b = 0;
+    x.off = 0;
+    x.ok = false;
+    if (x.l < uint32_t(a.L)) {
+        x.b = (a.card + CARD_HEADER_BYTES)[x.t];
+        x.off = reinterpret_cast<const uint32_t *>(a.card + a.off_offsets)[x.t];
+    }
+}
+
+__device__ __forceinline__ void staged_check(const CardArgs &a, StagedTask &x) {
+    x.ok = x.l < uint32_t(a.L) && valid_bits(x.b) && (x.off & 15u) == 0 &&
+           uint64_t(x.off) + card_record_bytes(x.b, a.H, a.d) <= a.layer_stride;
+}
+
+__device__ __forceinline__ StagedTask staged_next(const CardArgs &a, const StagedTask &x) {
+    StagedTask n;
+    n.t = x.t + a.it_dt;
+    n.l = x.l + a.it_dl;
+    if (n.t >= uint32_t(a.T)) {
+        n.t -= uint32_t(a.T);
+        n.l += 1;
+    }
+    staged_load_hdr(a, n);
+    return n;
+}
+
+// Lane 0: the bulk copies of half kv of task x's record into `stage`
+// (codes, then group parameters), completing on `bar`.
+__device__ __forceinline__ void staged_issue(const CardArgs &a, const StagedTask &x, int kv, uint32_t stage,
+                                             uint32_t bar, uint64_t pol) {
+    const uint8_t *rec = a.card + a.off_layers + uint64_t(x.l) * a.layer_stride + x.off;
+    const uint32_t hd = uint32_t(a.H) * uint32_t(a.d);
+    fence_proxy_async();  // the warp's reads of this buffer (last task) come first
+    if (x.b == 16) {
+        mbar_expect_tx(bar, 2u * hd);
+        bulk_g2s(stage, rec + (kv ? 2u * hd : 0u), 2u * hd, bar, pol);
+    } else {
+        const uint32_t cb = hd * uint32_t(x.b) / 8u, pb = hd / 8u;
+        mbar_expect_tx(bar, cb + pb);
+        bulk_g2s(stage, rec + (kv ? cb : 0u), cb, bar, pol);
+        bulk_g2s(stage + cb, rec + 2u * cb + (kv ? pb : 0u), pb, bar, pol);
+    }
+}
+
+// One plain half-task from its staged half-record.
+template <int B>
+__device__ __forceinline__ void unpack_staged_b(const CardArgs &a, const uint8_t *stage, uint4 *dst, uint32_t t,
+                                                int lane) {
+    const int cpr = a.d / 8;
+    const int cshift = a.d == 128 ? 4 : 3;
+    const int nchunks = a.H * cpr;
+    const uint32_t T = uint32_t(a.T);
+    const uint32_t code_bytes = uint32_t(a.H) * uint32_t(a.d) * uint32_t(B) / 8u;
+    for (int c0 = 0; c0 < nchunks; c0 += 4 * 32) {
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+            const int c = c0 + it * 32 + lane;
+            if (c >= nchunks) break;
+            const int h = c >> cshift, ch = c & (cpr - 1);
+            uint4 v;
+            if (B == 16) {
+                v = reinterpret_cast<const uint4 *>(stage)[c];
+            } else {
+                float y[8];
+                card_chunk_values(B, card_chunk_codes(B, stage, c),
+                                  reinterpret_cast<const uint32_t *>(stage + code_bytes)[c >> 2], y);
+                v = pack_bf16x8(y);
+            }
+            st_stream_v4(dst + (uint64_t(h) * T + t) * cpr + ch, v);
+        }
+    }
+}
+
+// The keys of one token, turned, from the staged half-record (pairs of chunks
+// as in rope_keys).
+template <int B>
+__device__ __forceinline__ void rope_staged_b(const CardArgs &a, const uint8_t *stage, uint4 *dst, uint32_t t,
+                                              int lane, const float2 (&rc)[4], const float2 (&rs)[4]) {
+    const int cpr = a.d / 8, half = cpr / 2;
+    const int hshift = a.d == 128 ? 3 : 2;
+    const int npairs = a.H * half;
+    const int chl = lane & (half - 1);
+    const uint32_t T = uint32_t(a.T);
+    const uint32_t code_bytes = uint32_t(a.H) * uint32_t(a.d) * uint32_t(B) / 8u;
+    const uint32_t *par = reinterpret_cast<const uint32_t *>(stage + code_bytes);
+    for (int p0 = 0; p0 < npairs; p0 += 2 * 32) {
+#pragma unroll
+      for (int it = 0; it < 2; ++it) {
+        const int p = p0 + it * 32 + lane;
+        if (p >= npairs) break;
+        const int h = p >> hshift;
+        const int ca = h * cpr + chl, cb = ca + half;
+        float ya[8], yb[8];
+        if (B == 16) {
+            const uint4 ra = reinterpret_cast<const uint4 *>(stage)[ca], rb = reinterpret_cast<const uint4 *>(stage)[cb];
+            const uint32_t wa[4] = {ra.x, ra.y, ra.z, ra.w}, wb[4] = {rb.x, rb.y, rb.z, rb.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                ya[2 * e] = bf16_lo(wa[e]);
+                ya[2 * e + 1] = bf16_hi(wa[e]);
+                yb[2 * e] = bf16_lo(wb[e]);
+                yb[2 * e + 1] = bf16_hi(wb[e]);
+            }
+        } else {
+            card_chunk_values(B, card_chunk_codes(B, stage, ca), par[ca >> 2], ya);
+            card_chunk_values(B, card_chunk_codes(B, stage, cb), par[cb >> 2], yb);
+        }
+        // oa = ya cos - yb sin, ob = ya sin + yb cos: one product rounded, then one fma
+        float oa[8], ob[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 xa = make_float2(ya[2 * e], ya[2 * e + 1]), xb = make_float2(yb[2 * e], yb[2 * e + 1]);
+            const float2 ta = __fmul2_rn(xb, rs[e]), tb = __fmul2_rn(xb, rc[e]);
+            const float2 u = __ffma2_rn(xa, rc[e], make_float2(-ta.x, -ta.y));
+            const float2 w = __ffma2_rn(xa, rs[e], tb);
+            oa[2 * e] = u.x, oa[2 * e + 1] = u.y;
+            ob[2 * e] = w.x, ob[2 * e + 1] = w.y;
+        }
+        uint4 *row = dst + (uint64_t(h) * T + t) * cpr;
+        st_stream_v4(row + chl, pack_bf16x8(oa));
+        st_stream_v4(row + chl + half, pack_bf16x8(ob));
+      }
+    }
+}
+
+template <bool ROPE>
+__global__ void __launch_bounds__(CARD_THREADS, ROPE ? 4 : 5) card_unpack_staged(const __grid_constant__ CardArgs a,
+                                                                        uint32_t stage_bytes) {
+    extern __shared__ uint4 s_stage[];  // [warp][2] mbarriers (128 bytes), then [warp][2] buffers
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint8_t *base = reinterpret_cast<uint8_t *>(s_stage);
+    const uint32_t bar0 = smem_addr(base) + 16u * uint32_t(warp);
+    uint8_t *stages = base + 16u * CARD_WARPS + uint32_t(warp) * 2u * stage_bytes;
+    const uint32_t st0 = smem_addr(stages);
+    if (lane == 0) {
+        mbar_init1(bar0);
+        mbar_init1(bar0 + 8);
+        mbar_init_fence();
+    }
+    __syncwarp();
+    float2 rc[4], rs[4];  // ROPE: (cos, sin) of the lane's 8 frequencies, two per packed register
+    if (ROPE) {
+        const int chl = lane & (a.d / 16 - 1);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 r0 = a.rot[chl * 8 + 2 * e], r1 = a.rot[chl * 8 + 2 * e + 1];
+            rc[e] = make_float2(r0.x, r1.x);
+            rs[e] = make_float2(r0.y, r1.y);
+        }
+    }
+    const uint64_t pol = l2_evict_first_policy();  // the card is read once
+    const uint32_t w = blockIdx.x * CARD_WARPS + uint32_t(warp);
+    const int kv0 = int(w & 1u);
+    StagedTask c;  // task k
+    c.t = (w >> 1) % uint32_t(a.T);
+    c.l = (w >> 1) / uint32_t(a.T);
+    staged_load_hdr(a, c);
+    staged_check(a, c);
+    if (lane == 0 && c.ok) staged_issue(a, c, kv0, st0, bar0, pol);
+    StagedTask n = staged_next(a, c);  // task k + 1
+    uint32_t phase = 0;                // bit s: parity of buffer s's next phase
+    for (uint32_t k = 0; c.l < uint32_t(a.L); ++k) {
+        const uint32_t s = k & 1u;
+        const int kv = kv0 ^ (ROPE ? int(s) : 0);
+        staged_check(a, n);
+        if (lane == 0 && n.ok) staged_issue(a, n, kv ^ (ROPE ? 1 : 0), st0 + (s ^ 1u) * stage_bytes, bar0 + 8u * (s ^ 1u), pol);
+        const StagedTask nn = staged_next(a, n);  // task k + 2: its header lands during this task
+        if (c.ok) {
+            const bool ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8u * s, (phase >> s) & 1u, a.wait_polls));
+            if (!ok) {
+                // give up: record it, let the copies in flight (this buffer's
+                // and the other's) land, with the normal limit, and leave
+                if (lane == 0) atomicOr(&reinterpret_cast<kvp_card_header *>(a.card)->error, FLAG_TIMEOUT);
+                mbar_wait(bar0 + 8u * s, (phase >> s) & 1u, CARD_WAIT_LIMIT);
+                if (n.ok) mbar_wait(bar0 + 8u * (s ^ 1u), (phase >> (s ^ 1u)) & 1u, CARD_WAIT_LIMIT);
+                return;
+            }
+            phase ^= 1u << s;
+            const uint8_t *stage = stages + s * stage_bytes;
+            uint4 *dst = a.dst[kv][c.l];
+            if (ROPE && kv == 0) {
+                switch (c.b) {
+                case 2: rope_staged_b<2>(a, stage, dst, c.t, lane, rc, rs); break;
+                case 4: rope_staged_b<4>(a, stage, dst, c.t, lane, rc, rs); break;
+                case 8: rope_staged_b<8>(a, stage, dst, c.t, lane, rc, rs); break;
+                default: rope_staged_b<16>(a, stage, dst, c.t, lane, rc, rs); break;
+                }
+            } else {
+                switch (c.b) {
+                case 2: unpack_staged_b<2>(a, stage, dst, c.t, lane); break;
+                case 4: unpack_staged_b<4>(a, stage, dst, c.t, lane); break;
+                case 8: unpack_staged_b<8>(a, stage, dst, c.t, lane); break;
+                default: unpack_staged_b<16>(a, stage, dst, c.t, lane); break;
+                }
+            }
+        } else if (lane == 0) {
+            atomicOr(&reinterpret_cast<kvp_card_header *>(a.card)->error, FLAG_HEADER);
+        }
+        __syncwarp();  // every lane is done with this buffer before it is refilled
+        c = n;
+        n = nn;
+    }
+}
+
+// The (token, layer) step of a warp's staged-unpack tasks for a grid of
+// `grid` blocks: half the grid's warp count, in tokens.
+static void set_unpack_steps(CardArgs &a, int grid) {
+    const uint32_t dlt = uint32_t(grid) * uint32_t(CARD_WARPS / 2);
+    a.it_dt = dlt % uint32_t(a.T);
+    a.it_dl = dlt / uint32_t(a.T);
+}
+
+// Bytes of one staging buffer (the largest half-record, 2 H d bytes) when the
+// staged unpack applies to the shape, else 0.
+static uint32_t unpack_stage_bytes(const CardArgs &a) {
+    const uint64_t hd = uint64_t(a.H) * uint64_t(a.d);
+    if (a.d != 128 && (a.H & 1)) return 0;  // V group parameters would start 8 bytes off a 16-byte boundary
+    if (16u * CARD_WARPS + uint64_t(CARD_WARPS) * 2u * 2u * hd > 48u * 1024u) return 0;
+    return uint32_t(2u * hd);
+}
+
 template <typename K>
-static int card_grid(K kernel, uint64_t tasks, int waves) {
+static int card_grid(K kernel, uint64_t tasks, int waves, size_t smem = 0) {
     int occ = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, CARD_THREADS, 0) != cudaSuccess || occ < 1) occ = 1;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, CARD_THREADS, smem) != cudaSuccess || occ < 1)
+        occ = 1;
     const uint64_t want = (tasks + CARD_WARPS - 1) / CARD_WARPS;
     const uint64_t cap = uint64_t(sm_count()) * uint64_t(occ) * uint64_t(waves);
     return int(want < cap ? (want < 1 ? 1 : want) : cap);
@@ -730,6 +978,10 @@ extern "C" int cachecard_pack(const kvp_shape *s, uint64_t model_id, int64_t pos
     return launch_status();
 }
 
+// Failure-path testing (kvp_test_limit_next_unpack): consumed by the next
+// unpack call on the calling thread.
+static thread_local uint32_t t_unpack_polls = CARD_WAIT_LIMIT;
+
 // Host checks and launch arguments shared by both unpack entry points.
 static int unpack_setup(const void *card, const kvp_card_header *hdr, void *const *k_dst, void *const *v_dst,
                         CardArgs &a) {
@@ -766,6 +1018,8 @@ static int unpack_setup(const void *card, const kvp_card_header *hdr, void *cons
     a.T = s.n_tokens;
     a.d = s.head_dim;
     a.shift = 0;
+    a.wait_polls = t_unpack_polls;
+    t_unpack_polls = CARD_WAIT_LIMIT;
     return KVP_OK;
 }
 
@@ -778,7 +1032,15 @@ extern "C" int cachecard_unpack(const void *card, const kvp_card_header *hdr, vo
     const uint64_t tasks = uint64_t(a.L) * uint64_t(a.T) * 2u;
     // store-heavy: several resident grids' worth of blocks spread the
     // concurrent stores (as in the pool decoder)
-    card_unpack<<<card_grid(card_unpack, tasks, 3), CARD_THREADS, 0, st>>>(a);
+    const uint32_t sb = unpack_stage_bytes(a);
+    if (sb) {
+        const size_t smem = 16u * CARD_WARPS + size_t(CARD_WARPS) * 2u * sb;
+        const int grid = card_grid(card_unpack_staged<false>, tasks, 3, smem);
+        set_unpack_steps(a, grid);
+        card_unpack_staged<false><<<grid, CARD_THREADS, smem, st>>>(a, sb);
+    } else {
+        card_unpack<<<card_grid(card_unpack, tasks, 3), CARD_THREADS, 0, st>>>(a);
+    }
     count_launch(1);
     return launch_status();
 }
@@ -797,7 +1059,20 @@ extern "C" int cachecard_unpack_at(const void *card, const kvp_card_header *hdr,
     }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const uint64_t tasks = uint64_t(a.L) * uint64_t(a.T) * 2u;
-    card_unpack_rope<<<card_grid(card_unpack_rope, tasks, 3), CARD_THREADS, 0, st>>>(a);
+    const uint32_t sb = unpack_stage_bytes(a);
+    if (sb) {
+        const size_t smem = 16u * CARD_WARPS + size_t(CARD_WARPS) * 2u * sb;
+        const int grid = card_grid(card_unpack_staged<true>, tasks, 3, smem);
+        set_unpack_steps(a, grid);
+        card_unpack_staged<true><<<grid, CARD_THREADS, smem, st>>>(a, sb);
+    } else {
+        card_unpack_rope<<<card_grid(card_unpack_rope, tasks, 3), CARD_THREADS, 0, st>>>(a);
+    }
     count_launch(1);
     return launch_status();
+}
+
+extern "C" int kvp_test_limit_next_unpack(uint32_t polls) {
+    t_unpack_polls = polls;
+    return KVP_OK;
 }

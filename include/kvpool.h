@@ -397,6 +397,18 @@ int kvp_test_fail_next_encode(int layer, uint32_t spin_iters);
  * every block gives up on its first sub-chunk).  Returns KVP_OK. */
 int kvp_test_limit_next_attend(uint32_t polls);
 
+/* Failure-path testing of CacheCard unpack.  Where the shape lets it stage
+ * records in shared memory (d = 128 or an even n_kv_heads, and 64 n_kv_heads
+ * head_dim bytes of buffers per block within 48 KB), unpack waits, with a
+ * bounded number of polls, for the bulk copies of each record; a wait that
+ * runs out is reported by cachecard_status as KVP_ERR_TIMEOUT (the warp
+ * first lets its copies in flight land, with the normal limit, and leaves
+ * that layer's outputs incomplete) and leaves the CUDA context usable.
+ * Makes the NEXT cachecard_unpack / cachecard_unpack_at on this thread poll
+ * each record's copies at most `polls` times (0: not at all, so every warp
+ * gives up on its first record); other shapes ignore it.  Returns KVP_OK. */
+int kvp_test_limit_next_unpack(uint32_t polls);
+
 #ifdef __cplusplus
 }
 #endif

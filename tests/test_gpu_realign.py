@@ -75,6 +75,7 @@ CASES = [  # (L, H, d, T, pos_src, pos_dst, frequencies)
     (1, 8, 128, 300, 0, 4096, "llama3"),
     (3, 2, 128, 9, 5000, 12, "unit"),
     (2, 4, 64, 65, 17, -40000, "ramp"),
+    (1, 16, 128, 40, 3, 700, "llama3"),  # records too large to stage: the direct kernel
 ]
 
 
@@ -127,3 +128,39 @@ def test_unpack_at_full_size():
     _, vp = unpack(card, L, H, T, d)
     for l in range(L):
         np.testing.assert_array_equal(vu[l], vp[l])
+
+
+@pytest.mark.parametrize("realign", [False, True])
+def test_unpack_wait_timeout_is_reported(realign):
+    """The staged unpack's bounded wait for a record's bulk copies, made to run
+    out on every warp's first record, is reported by cachecard_status as
+    KVP_ERR_TIMEOUT with the context still usable; the hook applies to one
+    call only, and the next unpack of a fresh card is whole and correct."""
+    L, H, d, T = 2, 8, 128, 300
+    ks, vs = synth.kv_layers(L, H, T, d, seed=11, device="cuda")
+    bits = synth.card_bits(T, seed=11).numpy()
+    w = inv_freq(d, "llama3")
+    card = pack(ks, vs, bits, (L, H, d, T), 0)
+    hdr = kv.CardHeader()
+    assert kv.cachecard_read_header(card.t, hdr) == kv.KVP_OK
+    ko = [torch.empty(H * T * d, dtype=torch.bfloat16, device="cuda") for _ in range(L)]
+    vo = [torch.empty(H * T * d, dtype=torch.bfloat16, device="cuda") for _ in range(L)]
+    assert kv.kvp_test_limit_next_unpack(0) == kv.KVP_OK
+    if realign:
+        rc = kv.cachecard_unpack_at(card.t, hdr, 4096, w, ko, vo)
+    else:
+        rc = kv.cachecard_unpack(card.t, hdr, ko, vo)
+    assert rc == kv.KVP_OK
+    torch.cuda.synchronize()
+    assert kv.cachecard_status(card.t) == kv.KVP_ERR_TIMEOUT
+    card2 = pack(ks, vs, bits, (L, H, d, T), 0)          # the first card keeps its error word
+    ku, vu = unpack(card2, L, H, T, d, 4096 if realign else None, w if realign else None)
+    if realign:
+        ok_, _ = O.card_unpack_at(card2.host(), 4096, w)
+        for l in range(L):
+            assert_keys_close(ku[l], ok_[l], "K layer %d" % l)
+    kp, vp = unpack(card2, L, H, T, d)
+    for l in range(L):
+        np.testing.assert_array_equal(vu[l], vp[l])
+        if not realign:
+            np.testing.assert_array_equal(ku[l], kp[l])
