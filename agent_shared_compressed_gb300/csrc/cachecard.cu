@@ -5,7 +5,10 @@
 //
 // cachecard_pack: card_scan (one block: bitwidths -> record offsets, header)
 // then card_pack (one warp per (layer, token, K|V) record half).
-// cachecard_unpack: card_unpack, the inverse, one warp per record half.
+// cachecard_unpack: the inverse, one warp per record half: card_unpack_staged
+// (the next record brought into shared memory by bulk copies while the
+// current one is unpacked) where its buffers fit, else card_unpack.
+// cachecard_unpack_at: the same with the keys turned to new positions.
 #include <cmath>
 
 #include "kvp_async.cuh"

@@ -23,6 +23,7 @@
 // A operand).  The warps' states are merged in shared memory at the end.
 // attend_combine merges the splits (log-sum-exp), applies the inverse
 // transform and writes out / lse.  Exponentials are base 2 throughout.
+#include "kvp_async.cuh"
 #include "kvp_vec.cuh"
 
 namespace kvp {
@@ -78,41 +79,9 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
-// Bulk copies (the TMA engine's 1-D form) from global into shared memory,
-// each completing on an mbarrier that counts the bytes still to land.
-__device__ __forceinline__ uint32_t att_smem(const void *p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void att_mbar_init(uint32_t bar) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void att_mbar_expect(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ bool att_mbar_try(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n}"
-        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
-    return ok != 0u;
-}
-// Waits for the completion of the barrier's phase of the given parity; gives
-// up (false) after `limit` polls (ATT_WAIT_LIMIT: about half a second).
+// Waits on the bulk-copy ring give up after ATT_WAIT_LIMIT polls (about half
+// a second) and report KVP_ERR_TIMEOUT.
 constexpr uint32_t ATT_WAIT_LIMIT = 1u << 22;
-__device__ __forceinline__ bool att_mbar_wait(uint32_t bar, uint32_t parity, uint32_t limit) {
-    for (uint32_t i = 0; i < limit; ++i) {
-        if (att_mbar_try(bar, parity)) return true;
-        if (i >= 16) __nanosleep(128);
-    }
-    return false;
-}
-__device__ __forceinline__ void att_bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                 ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
-}
-// Orders this thread's earlier generic-proxy accesses of shared memory before
-// its later bulk copies into it.
-__device__ __forceinline__ void att_fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // Shared memory of the split kernel (bytes).  A ring of NST raw sub-chunks
 // (the pool's bytes as they are, filled by bulk copies), then the staged
@@ -176,13 +145,13 @@ __device__ __forceinline__ void issue_chunk(uint8_t *raw, uint32_t bar, const ui
         qb = uint32_t(align16(qs + nt * (D / 32) * 2) - (qs & ~uintptr_t(15)));
     }
     if constexpr (R > 0) lb = nt * R * 2;
-    att_mbar_expect(bar, kb + vb + sb + qb + lb);
-    att_bulk_load(att_smem(raw + SM::RAW_K), ksrc, kb, bar);
-    att_bulk_load(att_smem(raw + SM::RAW_V), reinterpret_cast<const void *>(v & ~uintptr_t(15)), vb, bar);
-    att_bulk_load(att_smem(raw + SM::RAW_SG), reinterpret_cast<const void *>(sg & ~uintptr_t(15)), sb, bar);
+    mbar_expect_tx(bar, kb + vb + sb + qb + lb);
+    bulk_g2s(smem_addr(raw + SM::RAW_K), ksrc, kb, bar);
+    bulk_g2s(smem_addr(raw + SM::RAW_V), reinterpret_cast<const void *>(v & ~uintptr_t(15)), vb, bar);
+    bulk_g2s(smem_addr(raw + SM::RAW_SG), reinterpret_cast<const void *>(sg & ~uintptr_t(15)), sb, bar);
     if constexpr (Q8)
-        att_bulk_load(att_smem(raw + SM::RAW_KS), reinterpret_cast<const void *>(qs & ~uintptr_t(15)), qb, bar);
-    if constexpr (R > 0) att_bulk_load(att_smem(raw + SM::RAW_LR), vlr + uint64_t(t0) * R, lb, bar);
+        bulk_g2s(smem_addr(raw + SM::RAW_KS), reinterpret_cast<const void *>(qs & ~uintptr_t(15)), qb, bar);
+    if constexpr (R > 0) bulk_g2s(smem_addr(raw + SM::RAW_LR), vlr + uint64_t(t0) * R, lb, bar);
 }
 
 // Raw slot -> staged tiles (whole block): keys int8 -> exact bf16 (|q| <= 127
@@ -284,7 +253,7 @@ __device__ __forceinline__ void attend_passes(const AttendArgs &a, uint32_t *sme
     constexpr int PW = D + R;         // floats per partial row
     constexpr int NST = SM::NST;
     uint8_t *sm8 = reinterpret_cast<uint8_t *>(smem);
-    const uint32_t bar0 = att_smem(sm8);                                   // [NST] mbarriers, 8 bytes each
+    const uint32_t bar0 = smem_addr(sm8);                                   // [NST] mbarriers, 8 bytes each
     uint8_t *ring = sm8 + SM::OFF_RING;                                    // [NST] raw sub-chunks
     uint32_t *Qs = reinterpret_cast<uint32_t *>(sm8 + SM::OFF_Q);          // [ATT_MT][RW] bf16 pairs
     uint32_t *Kt = reinterpret_cast<uint32_t *>(sm8 + SM::OFF_K);          // [ATT_TC][RW] bf16 pairs
@@ -307,15 +276,15 @@ __device__ __forceinline__ void attend_passes(const AttendArgs &a, uint32_t *sme
     const int sub0 = split * a.per_split, sub1 = min(a.nsub, sub0 + a.per_split);
     const int nsubs = sub1 - sub0;
     if (tid == 0) {
-        for (int sl = 0; sl < NST; ++sl) att_mbar_init(bar0 + 8 * sl);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        for (int sl = 0; sl < NST; ++sl) mbar_init1(bar0 + 8 * sl);
+        mbar_init_fence();
     }
     uint32_t phases = 0;  // bit sl: parity of slot sl's next completion (the same in every thread)
 
     for (int m0 = 0; m0 < a.QH; m0 += RP) {
         __syncthreads();  // the barriers are set up; the previous pass's merge slots are read
         if (tid == 0) {   // the ring's first sub-chunks are requested before the query tile
-            att_fence_proxy_async();
+            fence_proxy_async();
             for (int sl = 0; sl < NST && sl < nsubs; ++sl)
                 issue_chunk<D, Q8, R>(ring + sl * SM::SLOT, bar0 + 8 * sl, lay, a.geo, vbase, (sub0 + sl) * ATT_TC,
                                       a.T, kscales, a.vlr);
@@ -358,7 +327,7 @@ __device__ __forceinline__ void attend_passes(const AttendArgs &a, uint32_t *sme
             const int t0 = sub * ATT_TC;
             uint8_t *raw = ring + sl * SM::SLOT;
             if (i > 0) __syncthreads();  // every warp is done with the staged tiles
-            const bool ok = att_mbar_wait(bar0 + 8 * sl, (phases >> sl) & 1u, a.wait_polls);
+            const bool ok = mbar_wait(bar0 + 8 * sl, (phases >> sl) & 1u, a.wait_polls);
             phases ^= 1u << sl;
             {
                 const uint64_t n0 = vbase + uint64_t(t0);
@@ -372,7 +341,7 @@ __device__ __forceinline__ void attend_passes(const AttendArgs &a, uint32_t *sme
                 break;
             }
             if (tid == 0 && i + NST < nsubs) {  // refill the slot with the sub-chunk NST ahead
-                att_fence_proxy_async();
+                fence_proxy_async();
                 issue_chunk<D, Q8, R>(raw, bar0 + 8 * sl, lay, a.geo, vbase, t0 + NST * ATT_TC, a.T, kscales, a.vlr);
             }
             if (!active) continue;
@@ -526,7 +495,7 @@ __device__ __forceinline__ void attend_passes(const AttendArgs &a, uint32_t *sme
                          FLAG_TIMEOUT);
                 for (int k = failed_at; k < nsubs && k < failed_at + NST; ++k) {
                     const int sl = k % NST;
-                    att_mbar_wait(bar0 + 8 * sl, ((phases >> sl) & 1u) ^ (k == failed_at ? 1u : 0u), ATT_WAIT_LIMIT);
+                    mbar_wait(bar0 + 8 * sl, ((phases >> sl) & 1u) ^ (k == failed_at ? 1u : 0u), ATT_WAIT_LIMIT);
                 }
             }
             return;
