@@ -42,10 +42,10 @@
  *    by the *_status calls.  No kernel traps or asserts.  Two kinds of
  *    device-side wait exist, both bounded: the pool encoder's key-quantize
  *    work waits for its layer's scale, released by another block of the same
- *    kernel, and pool attention waits on mbarriers for its own bulk copies
- *    into shared memory.  A wait that runs out is recorded in the error word
- *    and reported as KVP_ERR_TIMEOUT by kvpool_status; the CUDA context stays
- *    usable.
+ *    kernel; pool attention and CacheCard unpack wait on mbarriers for their
+ *    own bulk copies into shared memory.  A wait that runs out is recorded in
+ *    the pool's or the card's error word and reported as KVP_ERR_TIMEOUT by
+ *    kvpool_status / cachecard_status; the CUDA context stays usable.
  */
 #ifndef KVPOOL_H
 #define KVPOOL_H
