@@ -1038,7 +1038,9 @@ extern "C" int cachecard_unpack(const void *card, const kvp_card_header *hdr, vo
     const uint32_t sb = unpack_stage_bytes(a);
     if (sb) {
         const size_t smem = 16u * CARD_WARPS + size_t(CARD_WARPS) * 2u * sb;
-        const int grid = card_grid(card_unpack_staged<false>, tasks, 3, smem);
+        // eight resident grids' worth of blocks: 4K-token step unpack 0.117 ms
+        // against 0.121 (three) and 0.119 (six); 8K-token card 0.231 against 0.242
+        const int grid = card_grid(card_unpack_staged<false>, tasks, 8, smem);
         set_unpack_steps(a, grid);
         card_unpack_staged<false><<<grid, CARD_THREADS, smem, st>>>(a, sb);
     } else {
@@ -1065,7 +1067,9 @@ extern "C" int cachecard_unpack_at(const void *card, const kvp_card_header *hdr,
     const uint32_t sb = unpack_stage_bytes(a);
     if (sb) {
         const size_t smem = 16u * CARD_WARPS + size_t(CARD_WARPS) * 2u * sb;
-        const int grid = card_grid(card_unpack_staged<true>, tasks, 3, smem);
+        // four resident grids' worth of blocks (8K-token card: 0.250 ms; one, two,
+        // three, six, eight and twelve: 0.267, 0.257, 0.251, 0.251, 0.253, 0.258)
+        const int grid = card_grid(card_unpack_staged<true>, tasks, 4, smem);
         set_unpack_steps(a, grid);
         card_unpack_staged<true><<<grid, CARD_THREADS, smem, st>>>(a, sb);
     } else {
