@@ -340,12 +340,21 @@ __global__ void __launch_bounds__(CARD_THREADS, 4) card_pack(const __grid_consta
     pos.l = int((task >> 1) / T);
     int round = 0;
     uint4 w[4];
-    if (task < tasks) pack_load<FULL>(a, pos, lane, ngroups, cpr, gshift, T, w);
+    int b = 0;         // the task's bitwidth and record offset, loaded with its first round
+    uint32_t off = 0;
+    if (task < tasks) {
+        pack_load<FULL>(a, pos, lane, ngroups, cpr, gshift, T, w);
+        b = bits[pos.t];
+        off = offs[pos.t];
+    }
     while (task < tasks) {
-        // the next round of this warp's sequence, loaded now
+        // the next round of this warp's sequence, loaded now (with the next
+        // task's bitwidth and offset, so that no header load is waited for)
         uint32_t ntask = task;
         PackPos npos = pos;
         int nround = round + 1;
+        int nb = b;
+        uint32_t noff = off;
         if (nround == rounds) {
             nround = 0;
             ntask += tstep;
@@ -357,14 +366,18 @@ __global__ void __launch_bounds__(CARD_THREADS, 4) card_pack(const __grid_consta
             }
         }
         uint4 wn[4];
-        if (ntask < tasks) pack_load<FULL>(a, npos, nround * 32 + lane, ngroups, cpr, gshift, T, wn);
+        if (ntask < tasks) {
+            pack_load<FULL>(a, npos, nround * 32 + lane, ngroups, cpr, gshift, T, wn);
+            if (nround == 0) {
+                nb = bits[npos.t];
+                noff = offs[npos.t];
+            }
+        }
 
         const int gi = round * 32 + lane;
         const int kv = pos.kv;
-        const uint32_t t = pos.t;
         const int l = pos.l;
-        const int b = bits[t];
-        uint8_t *rec = a.card + a.off_layers + uint64_t(uint32_t(l)) * stride + offs[t];
+        uint8_t *rec = a.card + a.off_layers + uint64_t(uint32_t(l)) * stride + off;
         const uint32_t hd = uint32_t(a.H) * uint32_t(a.d);  // H d < 2^31
         if (b == 16) {
             if (FULL || gi < ngroups) {
@@ -382,6 +395,8 @@ __global__ void __launch_bounds__(CARD_THREADS, 4) card_pack(const __grid_consta
         task = ntask;
         pos = npos;
         round = nround;
+        b = nb;
+        off = noff;
 #pragma unroll
         for (int q = 0; q < 4; ++q) w[q] = wn[q];
     }
