@@ -105,6 +105,31 @@ def test_card_pack_unpack_match_oracle(shape):
         np.testing.assert_array_equal(vu[l][:, full], vs[l][:, full])
 
 
+@pytest.mark.parametrize("shape", [(2, 8, 128, 64), (2, 3, 64, 37)])
+def test_card_pack_from_16_byte_aligned_layers(shape):
+    """Layers with only the 16-byte alignment the ABI asks for (not 32-byte)
+    pack to a card byte-identical to the one packed from 512-byte aligned
+    copies, and it matches the oracle's."""
+    L, H, d, T = shape
+    ks, vs, bits = inputs(L, H, T, d, seed=T + 7)
+    kd, vd = bf16_dev_layers(ks), bf16_dev_layers(vs)
+
+    def shifted(t):
+        buf = torch.empty(t.numel() + 8, dtype=torch.bfloat16, device="cuda")
+        view = buf[8:8 + t.numel()]                      # 16 bytes past a 512-byte aligned start
+        view.copy_(t.reshape(-1))
+        assert view.data_ptr() % 32 == 16
+        return view
+
+    card_a, st_a = gpu_pack(kd, vd, bits, shape)
+    card_u, st_u = gpu_pack([shifted(k) for k in kd], [shifted(v) for v in vd], bits, shape)
+    assert st_a == kv.KVP_OK and st_u == kv.KVP_OK
+    np.testing.assert_array_equal(card_u.host(), card_a.host())
+    oimg, flags, r = O.card_pack(ks, vs, bits, want_r=True)
+    assert flags == 0
+    assert_card_parity(card_u.host(), oimg, r, L, H, d, T, bits)
+
+
 def test_card_on_grid_values_roundtrip_exactly():
     """Groups whose values sit on their own quantization grid (s, z exact in
     fp16, every value z + q*s exact in bf16) come back bit-exact."""
