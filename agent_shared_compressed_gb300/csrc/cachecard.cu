@@ -697,7 +697,7 @@ __global__ void __launch_bounds__(CARD_THREADS, 4) card_unpack_rope(const __grid
 // registers held for them.  A warp's tasks advance by a fixed (token, layer)
 // step, and the halves are taken as in card_unpack (ROPE = false) and
 // card_unpack_rope (ROPE = true).  Used where two buffers of 2 H d bytes per
-// warp fit 48 KB per block and every part of a record starts on a 16-byte
+// warp fit 96 KB per block and every part of a record starts on a 16-byte
 // boundary (d = 128, or H even).
 // ---------------------------------------------------------------------------
 constexpr uint32_t CARD_WAIT_LIMIT = 1u << 22;  // polls, about half a second
@@ -923,11 +923,13 @@ static void set_unpack_steps(CardArgs &a, int grid) {
 }
 
 // Bytes of one staging buffer (the largest half-record, 2 H d bytes) when the
-// staged unpack applies to the shape, else 0.
+// staged unpack applies to the shape, else 0: the block's buffers fit 96 KB
+// (above 48 KB by opt-in; SmolLM2-1.7B's H d = 2048 takes 64 KB and unpacks
+// in 0.080 against 0.085 ms direct).
 static uint32_t unpack_stage_bytes(const CardArgs &a) {
     const uint64_t hd = uint64_t(a.H) * uint64_t(a.d);
     if (a.d != 128 && (a.H & 1)) return 0;  // V group parameters would start 8 bytes off a 16-byte boundary
-    if (16u * CARD_WARPS + uint64_t(CARD_WARPS) * 2u * 2u * hd > 48u * 1024u) return 0;
+    if (16u * CARD_WARPS + uint64_t(CARD_WARPS) * 2u * 2u * hd > 96u * 1024u) return 0;
     return uint32_t(2u * hd);
 }
 
@@ -1055,6 +1057,12 @@ extern "C" int cachecard_unpack(const void *card, const kvp_card_header *hdr, vo
         const size_t smem = 16u * CARD_WARPS + size_t(CARD_WARPS) * 2u * sb;
         // eight resident grids' worth of blocks: 4K-token step unpack 0.117 ms
         // against 0.121 (three) and 0.119 (six); 8K-token card 0.231 against 0.242
+        if (smem > 48u * 1024u &&
+            cudaFuncSetAttribute(card_unpack_staged<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
+                cudaSuccess) {
+            (void)cudaGetLastError();  // leave no sticky error for the next call to report
+            return KVP_ERR_CUDA;
+        }
         const int grid = card_grid(card_unpack_staged<false>, tasks, 8, smem);
         set_unpack_steps(a, grid);
         card_unpack_staged<false><<<grid, CARD_THREADS, smem, st>>>(a, sb);
@@ -1084,6 +1092,12 @@ extern "C" int cachecard_unpack_at(const void *card, const kvp_card_header *hdr,
         const size_t smem = 16u * CARD_WARPS + size_t(CARD_WARPS) * 2u * sb;
         // four resident grids' worth of blocks (8K-token card: 0.250 ms; one, two,
         // three, six, eight and twelve: 0.267, 0.257, 0.251, 0.251, 0.253, 0.258)
+        if (smem > 48u * 1024u &&
+            cudaFuncSetAttribute(card_unpack_staged<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
+                cudaSuccess) {
+            (void)cudaGetLastError();  // leave no sticky error for the next call to report
+            return KVP_ERR_CUDA;
+        }
         const int grid = card_grid(card_unpack_staged<true>, tasks, 4, smem);
         set_unpack_steps(a, grid);
         card_unpack_staged<true><<<grid, CARD_THREADS, smem, st>>>(a, sb);

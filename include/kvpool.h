@@ -398,8 +398,8 @@ int kvp_test_fail_next_encode(int layer, uint32_t spin_iters);
 int kvp_test_limit_next_attend(uint32_t polls);
 
 /* Failure-path testing of CacheCard unpack.  Where the shape lets it stage
- * records in shared memory (d = 128 or an even n_kv_heads, and 64 n_kv_heads
- * head_dim bytes of buffers per block within 48 KB), unpack waits, with a
+ * records in shared memory (d = 128 or an even n_kv_heads, and 32 n_kv_heads
+ * head_dim bytes of buffers per block within 96 KB), unpack waits, with a
  * bounded number of polls, for the bulk copies of each record; a wait that
  * runs out is reported by cachecard_status as KVP_ERR_TIMEOUT (the warp
  * first lets its copies in flight land, with the normal limit, and leaves

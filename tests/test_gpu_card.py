@@ -79,7 +79,7 @@ def assert_card_parity(gimg, oimg, r, L, H, d, T, bits):
 
 
 @pytest.mark.parametrize("shape", [(3, 5, 64, 37), (2, 8, 128, 64), (1, 1, 64, 1), (2, 3, 128, 50),
-                                   (1, 8, 128, 1500), (2, 32, 64, 129)])
+                                   (1, 8, 128, 1500), (2, 32, 64, 129), (1, 32, 128, 33)])
 def test_card_pack_unpack_match_oracle(shape):
     L, H, d, T = shape
     ks, vs, bits = inputs(L, H, T, d, seed=T + L)

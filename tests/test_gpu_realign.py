@@ -75,7 +75,8 @@ CASES = [  # (L, H, d, T, pos_src, pos_dst, frequencies)
     (1, 8, 128, 300, 0, 4096, "llama3"),
     (3, 2, 128, 9, 5000, 12, "unit"),
     (2, 4, 64, 65, 17, -40000, "ramp"),
-    (1, 16, 128, 40, 3, 700, "llama3"),  # records too large to stage: the direct kernel
+    (1, 16, 128, 40, 3, 700, "llama3"),  # staged in more than 48 KB of shared memory per block
+    (1, 32, 128, 20, 9, 2000, "ramp"),   # records too large to stage: the direct kernel
 ]
 
 
