@@ -89,9 +89,13 @@ constexpr uint32_t ATT_WAIT_LIMIT = 1u << 22;
 // centroids (rows of RW words: 16-byte multiples, conflict-free ldmatrix),
 // sigma, the centroid pair table, q8_0 block scales and the low-rank tile.
 // After the loop the warps' states are merged from offset BAR_BYTES on.
-template <int D, int R = 0>
+// PIPE (passes of at most 32 query rows, no low-rank tile): two sets of
+// staged tiles, so that a sub-chunk is staged while the one before it is
+// multiplied; the ring is two slots deep and the Q tile 32 rows.
+template <int D, int R = 0, bool PIPE = false>
 struct AttendSmem {
-    static constexpr int NST = R > 0 ? 3 : 4;  // ring depth
+    static constexpr int NST = PIPE ? 2 : (R > 0 ? 3 : 4);  // ring depth
+    static constexpr int QROWS = PIPE ? 32 : ATT_MT;        // rows of the Q tile
     static constexpr int RW = D / 2 + 4;       // 32-bit words per Q / K / C row
     static constexpr int LW = R / 2 + 4;       // words per low-rank row (LoRA attention)
     static constexpr int MS = D + R + 8;       // floats per row of a warp's merge slot (conflict-free float2 stores)
@@ -106,19 +110,32 @@ struct AttendSmem {
     static constexpr uint32_t BAR_BYTES = 64;
     static constexpr uint32_t OFF_RING = BAR_BYTES;
     static constexpr uint32_t OFF_Q = OFF_RING + NST * SLOT;
-    static constexpr uint32_t OFF_K = OFF_Q + ATT_MT * RW * 4;
+    static constexpr uint32_t OFF_K = OFF_Q + QROWS * RW * 4;
     static constexpr uint32_t OFF_C = OFF_K + ATT_TC * RW * 4;
     static constexpr uint32_t OFF_SIG = OFF_C + ATT_TC * RW * 4;
     static constexpr uint32_t OFF_LUT = OFF_SIG + ATT_TC * 4;
     static constexpr uint32_t OFF_KSB = OFF_LUT + 64 * 4;
     static constexpr uint32_t OFF_LS = OFF_KSB + ATT_TC * (D / 32) * 4;
-    static constexpr uint32_t STAGE_END = OFF_LS + (R > 0 ? ATT_TC * LW * 4 : 0);
+    static constexpr uint32_t END0 = OFF_LS + (R > 0 ? ATT_TC * LW * 4 : 0);
+    // PIPE: the second set of staged tiles (the pair table is shared)
+    static constexpr uint32_t OFF_K1 = END0;
+    static constexpr uint32_t OFF_C1 = OFF_K1 + ATT_TC * RW * 4;
+    static constexpr uint32_t OFF_SIG1 = OFF_C1 + ATT_TC * RW * 4;
+    static constexpr uint32_t OFF_KSB1 = OFF_SIG1 + ATT_TC * 4;
+    static constexpr uint32_t OFF_LS1 = OFF_KSB1 + ATT_TC * (D / 32) * 4;
+    static constexpr uint32_t STAGE_END = PIPE ? OFF_LS1 + (R > 0 ? ATT_TC * LW * 4 : 0) : END0;
     static constexpr uint32_t MERGE_END = BAR_BYTES + ATT_WARPS * (16 * MS + 32) * 4;
     static constexpr size_t bytes = STAGE_END > MERGE_END ? STAGE_END : MERGE_END;
     static_assert(SLOT % 16 == 0 && RAW_V % 16 == 0 && RAW_SG % 16 == 0 && RAW_KS % 16 == 0 && RAW_LR % 16 == 0,
                   "bulk-copy destinations are 16-byte aligned");
     static_assert(NST * 8 <= BAR_BYTES, "one mbarrier per slot");
+    static_assert(END0 % 16 == 0 && OFF_C1 % 16 == 0, "staged tiles are 16-byte aligned");
 };
+
+// The split kernel's shared memory: pipelined for passes of at most 32 query
+// rows (TPW = 16) without a low-rank tile.
+template <int D, int TPW, int R>
+using SplitSmem = AttendSmem<D, R, TPW == 16 && R == 0>;
 
 // Thread 0: the bulk copies of sub-chunk tokens t0 .. t0 + nt - 1 of KV head
 // (vbase / T) into one raw slot, completing on its barrier.  Every source is
@@ -242,7 +259,8 @@ __device__ __forceinline__ void stage_raw(const uint8_t *raw, int t0, int T, int
 // two 16-row tiles per pass, for blocks with at most 32 query rows).
 template <int D, int TPW, bool Q8, int R>
 __device__ __forceinline__ void attend_passes(const AttendArgs &a, uint32_t *smem, const uint16_t *kscales) {
-    using SM = AttendSmem<D, R>;
+    using SM = SplitSmem<D, TPW, R>;
+    constexpr bool PIPE = TPW == 16 && R == 0;  // sub-chunk i + 1 staged while sub-chunk i is multiplied
     constexpr int RW = SM::RW, MSW = SM::MS;
     constexpr int MS = TPW / 8;       // 16-row tiles per pass
     constexpr int RP = 16 * MS;       // query rows per pass
@@ -252,6 +270,7 @@ __device__ __forceinline__ void attend_passes(const AttendArgs &a, uint32_t *sme
     constexpr int LW = SM::LW;
     constexpr int PW = D + R;         // floats per partial row
     constexpr int NST = SM::NST;
+    static_assert(RP <= SM::QROWS, "the Q tile holds a pass's rows");
     uint8_t *sm8 = reinterpret_cast<uint8_t *>(smem);
     const uint32_t bar0 = smem_addr(sm8);                                   // [NST] mbarriers, 8 bytes each
     uint8_t *ring = sm8 + SM::OFF_RING;                                    // [NST] raw sub-chunks
@@ -262,6 +281,12 @@ __device__ __forceinline__ void attend_passes(const AttendArgs &a, uint32_t *sme
     uint32_t *lut = reinterpret_cast<uint32_t *>(sm8 + SM::OFF_LUT);       // [64] (c[lo], c[hi]) fp16 pairs
     float *kst = reinterpret_cast<float *>(sm8 + SM::OFF_KSB);             // [ATT_TC][D/32] q8_0 key block scales
     uint32_t *Lt = reinterpret_cast<uint32_t *>(sm8 + SM::OFF_LS);         // [ATT_TC][LW] low-rank fp16 pairs
+    // PIPE: the second tile set (never touched otherwise)
+    uint32_t *Kt1 = reinterpret_cast<uint32_t *>(sm8 + SM::OFF_K1);
+    uint32_t *Ct1 = reinterpret_cast<uint32_t *>(sm8 + SM::OFF_C1);
+    float *st1 = reinterpret_cast<float *>(sm8 + SM::OFF_SIG1);
+    float *kst1 = reinterpret_cast<float *>(sm8 + SM::OFF_KSB1);
+    uint32_t *Lt1 = reinterpret_cast<uint32_t *>(sm8 + SM::OFF_LS1);
     float *mrg = reinterpret_cast<float *>(sm8 + SM::BAR_BYTES);  // after the loop: [warps][16][MSW] acc, [warps][32] m, l
 
     const int h = blockIdx.x, split = blockIdx.y;
@@ -322,168 +347,211 @@ __device__ __forceinline__ void attend_passes(const AttendArgs &a, uint32_t *sme
 
         __syncthreads();  // the pair table and the query tile are in
         int failed_at = -1;
-        for (int i = 0; i < nsubs; ++i) {
-            const int sub = sub0 + i, sl = i % NST;
-            const int t0 = sub * ATT_TC;
-            uint8_t *raw = ring + sl * SM::SLOT;
-            if (i > 0) __syncthreads();  // every warp is done with the staged tiles
-            const bool ok = mbar_wait(bar0 + 8 * sl, (phases >> sl) & 1u, a.wait_polls);
-            phases ^= 1u << sl;
-            {
-                const uint64_t n0 = vbase + uint64_t(t0);
-                const uint32_t voff = uint32_t(reinterpret_cast<uintptr_t>(lay + a.geo.sec_v + n0 * (3 * D / 8)) & 15u);
-                const uint32_t soff = uint32_t(reinterpret_cast<uintptr_t>(lay + a.geo.sec_sigma + n0 * 2) & 15u);
-                const uint32_t qoff = Q8 ? uint32_t(reinterpret_cast<uintptr_t>(kscales + n0 * (D / 32)) & 15u) : 0u;
-                stage_raw<D, Q8, R>(raw, t0, a.T, tid, voff, soff, qoff, Kt, Ct, st, lut, kst, Lt);
-            }
-            if (__syncthreads_or(!ok)) {  // the tiles are staged and the slot is free, unless a wait ran out
-                failed_at = i;
-                break;
-            }
-            if (tid == 0 && i + NST < nsubs) {  // refill the slot with the sub-chunk NST ahead
+        // sub-chunk j (raw slot j % NST) staged into tile set `set`
+        auto stage_sub = [&](int j, int set) {
+            const int t0 = (sub0 + j) * ATT_TC;
+            const uint64_t n0 = vbase + uint64_t(t0);
+            const uint32_t voff = uint32_t(reinterpret_cast<uintptr_t>(lay + a.geo.sec_v + n0 * (3 * D / 8)) & 15u);
+            const uint32_t soff = uint32_t(reinterpret_cast<uintptr_t>(lay + a.geo.sec_sigma + n0 * 2) & 15u);
+            const uint32_t qoff = Q8 ? uint32_t(reinterpret_cast<uintptr_t>(kscales + n0 * (D / 32)) & 15u) : 0u;
+            stage_raw<D, Q8, R>(ring + (j % NST) * SM::SLOT, t0, a.T, tid, voff, soff, qoff, set ? Kt1 : Kt,
+                                set ? Ct1 : Ct, set ? st1 : st, lut, set ? kst1 : kst, set ? Lt1 : Lt);
+        };
+        // thread 0: sub-chunk j's slot refilled with the sub-chunk NST ahead
+        auto refill = [&](int j) {
+            if (tid == 0 && j + NST < nsubs) {
+                const int sl = j % NST;
                 fence_proxy_async();
-                issue_chunk<D, Q8, R>(raw, bar0 + 8 * sl, lay, a.geo, vbase, t0 + NST * ATT_TC, a.T, kscales, a.vlr);
+                issue_chunk<D, Q8, R>(ring + sl * SM::SLOT, bar0 + 8 * sl, lay, a.geo, vbase,
+                                      (sub0 + j + NST) * ATT_TC, a.T, kscales, a.vlr);
             }
-            if (!active) continue;
+        };
+        if constexpr (PIPE) {
+            if (nsubs > 0) {  // sub-chunk 0 into the first tile set
+                const bool ok = mbar_wait(bar0, phases & 1u, a.wait_polls);
+                phases ^= 1u;
+                stage_sub(0, 0);
+                if (__syncthreads_or(!ok))
+                    failed_at = 0;
+                else
+                    refill(0);
+            }
+        }
+        for (int i = 0; i < nsubs && failed_at < 0; ++i) {
+            const int sub = sub0 + i;
+            int cur = 0;           // the tile set sub-chunk i is in
+            bool ok_next = true;   // PIPE: sub-chunk i + 1's copies landed in time
+            if constexpr (PIPE) {
+                cur = i & 1;
+                if (i + 1 < nsubs) {  // the next sub-chunk into the other tile set
+                    const int sl = (i + 1) % NST;
+                    ok_next = mbar_wait(bar0 + 8 * sl, (phases >> sl) & 1u, a.wait_polls);
+                    phases ^= 1u << sl;
+                    stage_sub(i + 1, cur ^ 1);
+                }
+            } else {
+                const int sl = i % NST;
+                if (i > 0) __syncthreads();  // every warp is done with the staged tiles
+                const bool ok = mbar_wait(bar0 + 8 * sl, (phases >> sl) & 1u, a.wait_polls);
+                phases ^= 1u << sl;
+                stage_sub(i, 0);
+                if (__syncthreads_or(!ok)) {  // the tiles are staged and the slot is free, unless a wait ran out
+                    failed_at = i;
+                    break;
+                }
+                refill(i);
+            }
+            const uint32_t *Kc = cur ? Kt1 : Kt, *Cc = cur ? Ct1 : Ct, *Lc = cur ? Lt1 : Lt;
+            const float *sc = cur ? st1 : st, *kc = cur ? kst1 : kst;
+            if (active) {
 
-            // S = Q K^T for rows mi*16.., tokens th*TPW..
-            float s[NS][4];
-#pragma unroll
-            for (int nt = 0; nt < NS; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.0f;
-            if constexpr (!Q8) {
-#pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    uint32_t qa[4];
-                    ldsm_x4(qa, Qs + (mi * 16 + (lane & 15)) * RW + ks * 8 + (lane >> 4) * 4);
-#pragma unroll
-                    for (int np = 0; np < NS; np += 2) {
-                        uint32_t kb[4];
-                        const int tok = th * TPW + np * 8 + (lane & 7) + ((lane >> 4) << 3);
-                        ldsm_x4(kb, Kt + tok * RW + ks * 8 + ((lane >> 3) & 1) * 4);
-                        mma_bf16(s[np], qa, kb[0], kb[1]);
-                        mma_bf16(s[np + 1], qa, kb[2], kb[3]);
-                    }
-                }
-            } else {
-                // q8_0: each 32-key block's exact partial products, one n-tile
-                // at a time, added in scaled by that token's block scale
-#pragma unroll
-                for (int nt = 0; nt < NS; ++nt) {
-                    const int tok = th * TPW + nt * 8 + (lane & 7);
-                    const int tl = th * TPW + nt * 8 + 2 * tig;
-#pragma unroll 1
-                    for (int blk = 0; blk < D / 32; ++blk) {
-                        float t1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                        uint32_t kb[4];  // k-steps 2 blk and 2 blk + 1 of this n-tile
-                        ldsm_x4(kb, Kt + tok * RW + blk * 16 + (lane >> 3) * 4);
-#pragma unroll
-                        for (int kk = 0; kk < 2; ++kk) {
-                            uint32_t qa[4];
-                            ldsm_x4(qa, Qs + (mi * 16 + (lane & 15)) * RW + (2 * blk + kk) * 8 + (lane >> 4) * 4);
-                            mma_bf16(t1, qa, kb[2 * kk], kb[2 * kk + 1]);
+                // S = Q K^T for rows mi*16.., tokens th*TPW..
+                float s[NS][4];
+    #pragma unroll
+                for (int nt = 0; nt < NS; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.0f;
+                if constexpr (!Q8) {
+    #pragma unroll
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        uint32_t qa[4];
+                        ldsm_x4(qa, Qs + (mi * 16 + (lane & 15)) * RW + ks * 8 + (lane >> 4) * 4);
+    #pragma unroll
+                        for (int np = 0; np < NS; np += 2) {
+                            uint32_t kb[4];
+                            const int tok = th * TPW + np * 8 + (lane & 7) + ((lane >> 4) << 3);
+                            ldsm_x4(kb, Kc + tok * RW + ks * 8 + ((lane >> 3) & 1) * 4);
+                            mma_bf16(s[np], qa, kb[0], kb[1]);
+                            mma_bf16(s[np + 1], qa, kb[2], kb[3]);
                         }
-                        const float c0 = kst[tl * (D / 32) + blk], c1 = kst[(tl + 1) * (D / 32) + blk];
-                        s[nt][0] = fmaf(t1[0], c0, s[nt][0]);
-                        s[nt][1] = fmaf(t1[1], c1, s[nt][1]);
-                        s[nt][2] = fmaf(t1[2], c0, s[nt][2]);
-                        s[nt][3] = fmaf(t1[3], c1, s[nt][3]);
+                    }
+                } else {
+                    // q8_0: each 32-key block's exact partial products, one n-tile
+                    // at a time, added in scaled by that token's block scale
+    #pragma unroll
+                    for (int nt = 0; nt < NS; ++nt) {
+                        const int tok = th * TPW + nt * 8 + (lane & 7);
+                        const int tl = th * TPW + nt * 8 + 2 * tig;
+    #pragma unroll 1
+                        for (int blk = 0; blk < D / 32; ++blk) {
+                            float t1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                            uint32_t kb[4];  // k-steps 2 blk and 2 blk + 1 of this n-tile
+                            ldsm_x4(kb, Kc + tok * RW + blk * 16 + (lane >> 3) * 4);
+    #pragma unroll
+                            for (int kk = 0; kk < 2; ++kk) {
+                                uint32_t qa[4];
+                                ldsm_x4(qa, Qs + (mi * 16 + (lane & 15)) * RW + (2 * blk + kk) * 8 + (lane >> 4) * 4);
+                                mma_bf16(t1, qa, kb[2 * kk], kb[2 * kk + 1]);
+                            }
+                            const float c0 = kc[tl * (D / 32) + blk], c1 = kc[(tl + 1) * (D / 32) + blk];
+                            s[nt][0] = fmaf(t1[0], c0, s[nt][0]);
+                            s[nt][1] = fmaf(t1[1], c1, s[nt][1]);
+                            s[nt][2] = fmaf(t1[2], c0, s[nt][2]);
+                            s[nt][3] = fmaf(t1[3], c1, s[nt][3]);
+                        }
                     }
                 }
-            }
-            // online softmax over this warp's slice (rows g and g+8 of the tile)
-            const int tbase = sub * ATT_TC + th * TPW;
-            float cm[2] = {-INFINITY, -INFINITY};
-            if (tbase + TPW <= a.T) {  // warp-uniform: every token of the slice is real
-#pragma unroll
-                for (int nt = 0; nt < NS; ++nt) {
-                    const float2 lo = __fmul2_rn(make_float2(s[nt][0], s[nt][1]), make_float2(qk2, qk2));
-                    const float2 hi = __fmul2_rn(make_float2(s[nt][2], s[nt][3]), make_float2(qk2, qk2));
-                    s[nt][0] = lo.x, s[nt][1] = lo.y, s[nt][2] = hi.x, s[nt][3] = hi.y;
-                    cm[0] = fmaxf(cm[0], fmaxf(s[nt][0], s[nt][1]));
-                    cm[1] = fmaxf(cm[1], fmaxf(s[nt][2], s[nt][3]));
-                }
-            } else {
-#pragma unroll
-                for (int nt = 0; nt < NS; ++nt) {
-                    const int tk = tbase + nt * 8 + 2 * tig;
-                    s[nt][0] = tk < a.T ? s[nt][0] * qk2 : -INFINITY;
-                    s[nt][1] = tk + 1 < a.T ? s[nt][1] * qk2 : -INFINITY;
-                    s[nt][2] = tk < a.T ? s[nt][2] * qk2 : -INFINITY;
-                    s[nt][3] = tk + 1 < a.T ? s[nt][3] * qk2 : -INFINITY;
-                    cm[0] = fmaxf(cm[0], fmaxf(s[nt][0], s[nt][1]));
-                    cm[1] = fmaxf(cm[1], fmaxf(s[nt][2], s[nt][3]));
-                }
-            }
-            float ref[2], al[2];
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                cm[i] = fmaxf(cm[i], __shfl_xor_sync(0xffffffffu, cm[i], 1));
-                cm[i] = fmaxf(cm[i], __shfl_xor_sync(0xffffffffu, cm[i], 2));
-                const float nm = fmaxf(mx[i], cm[i]);
-                ref[i] = nm == -INFINITY ? 0.0f : nm;  // a slice with no token yet: p = 0, nothing to rescale
-                al[i] = exp2f(mx[i] - ref[i]);
-                mx[i] = nm;
-                ls[i] *= al[i];
-            }
-            {
-                const float2 a0 = make_float2(al[0], al[0]), a1 = make_float2(al[1], al[1]);
-#pragma unroll
-                for (int nt = 0; nt < NV; ++nt) {
-                    const float2 lo = __fmul2_rn(make_float2(acc[nt][0], acc[nt][1]), a0);
-                    const float2 hi = __fmul2_rn(make_float2(acc[nt][2], acc[nt][3]), a1);
-                    acc[nt][0] = lo.x, acc[nt][1] = lo.y, acc[nt][2] = hi.x, acc[nt][3] = hi.y;
-                }
-            }
-            if constexpr (R > 0) {
-#pragma unroll
-                for (int nt = 0; nt < NL; ++nt) {
-                    lracc[nt][0] *= al[0];
-                    lracc[nt][1] *= al[0];
-                    lracc[nt][2] *= al[1];
-                    lracc[nt][3] *= al[1];
-                }
-            }
-            // P' = p * sigma as fp16 A fragments: the S accumulator of n-tiles
-            // 2kk, 2kk+1 is the A operand of k-step kk
-#pragma unroll
-            for (int kk = 0; kk < NS / 2; ++kk) {
-                uint32_t pa[4], pl[4];  // p * sigma for the pool's values; p for the low-rank cache
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    const int nt = 2 * kk + hf;
-                    const int tl = th * TPW + nt * 8 + 2 * tig;
-                    const float s0 = st[tl], s1 = st[tl + 1];
-                    const float p0 = exp2f(s[nt][0] - ref[0]), p1 = exp2f(s[nt][1] - ref[0]);
-                    const float p2 = exp2f(s[nt][2] - ref[1]), p3 = exp2f(s[nt][3] - ref[1]);
-                    ls[0] += p0 + p1;
-                    ls[1] += p2 + p3;
-                    pa[2 * hf] = pack_half2(p0 * s0, p1 * s1);
-                    pa[2 * hf + 1] = pack_half2(p2 * s0, p3 * s1);
-                    if constexpr (R > 0) {
-                        pl[2 * hf] = pack_half2(p0, p1);
-                        pl[2 * hf + 1] = pack_half2(p2, p3);
+                // online softmax over this warp's slice (rows g and g+8 of the tile)
+                const int tbase = sub * ATT_TC + th * TPW;
+                float cm[2] = {-INFINITY, -INFINITY};
+                if (tbase + TPW <= a.T) {  // warp-uniform: every token of the slice is real
+    #pragma unroll
+                    for (int nt = 0; nt < NS; ++nt) {
+                        const float2 lo = __fmul2_rn(make_float2(s[nt][0], s[nt][1]), make_float2(qk2, qk2));
+                        const float2 hi = __fmul2_rn(make_float2(s[nt][2], s[nt][3]), make_float2(qk2, qk2));
+                        s[nt][0] = lo.x, s[nt][1] = lo.y, s[nt][2] = hi.x, s[nt][3] = hi.y;
+                        cm[0] = fmaxf(cm[0], fmaxf(s[nt][0], s[nt][1]));
+                        cm[1] = fmaxf(cm[1], fmaxf(s[nt][2], s[nt][3]));
+                    }
+                } else {
+    #pragma unroll
+                    for (int nt = 0; nt < NS; ++nt) {
+                        const int tk = tbase + nt * 8 + 2 * tig;
+                        s[nt][0] = tk < a.T ? s[nt][0] * qk2 : -INFINITY;
+                        s[nt][1] = tk + 1 < a.T ? s[nt][1] * qk2 : -INFINITY;
+                        s[nt][2] = tk < a.T ? s[nt][2] * qk2 : -INFINITY;
+                        s[nt][3] = tk + 1 < a.T ? s[nt][3] * qk2 : -INFINITY;
+                        cm[0] = fmaxf(cm[0], fmaxf(s[nt][0], s[nt][1]));
+                        cm[1] = fmaxf(cm[1], fmaxf(s[nt][2], s[nt][3]));
                     }
                 }
-                // A += P' C over tokens th*TPW + kk*16 .. +15, every dim
-#pragma unroll
-                for (int np = 0; np < NV; np += 2) {
-                    uint32_t cb[4];
-                    const int tok = th * TPW + kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
-                    ldsm_x4_t(cb, Ct + tok * RW + np * 4 + (lane >> 4) * 4);
-                    mma_f16(acc[np], pa, cb[0], cb[1]);
-                    mma_f16(acc[np + 1], pa, cb[2], cb[3]);
+                float ref[2], al[2];
+    #pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    cm[i] = fmaxf(cm[i], __shfl_xor_sync(0xffffffffu, cm[i], 1));
+                    cm[i] = fmaxf(cm[i], __shfl_xor_sync(0xffffffffu, cm[i], 2));
+                    const float nm = fmaxf(mx[i], cm[i]);
+                    ref[i] = nm == -INFINITY ? 0.0f : nm;  // a slice with no token yet: p = 0, nothing to rescale
+                    al[i] = exp2f(mx[i] - ref[i]);
+                    mx[i] = nm;
+                    ls[i] *= al[i];
+                }
+                {
+                    const float2 a0 = make_float2(al[0], al[0]), a1 = make_float2(al[1], al[1]);
+    #pragma unroll
+                    for (int nt = 0; nt < NV; ++nt) {
+                        const float2 lo = __fmul2_rn(make_float2(acc[nt][0], acc[nt][1]), a0);
+                        const float2 hi = __fmul2_rn(make_float2(acc[nt][2], acc[nt][3]), a1);
+                        acc[nt][0] = lo.x, acc[nt][1] = lo.y, acc[nt][2] = hi.x, acc[nt][3] = hi.y;
+                    }
                 }
                 if constexpr (R > 0) {
-                    // Flash-LoRA reorder: P V_lr over the same tokens, r columns
-#pragma unroll
-                    for (int np = 0; np < NL; np += 2) {
-                        uint32_t lb[4];
-                        const int tok = th * TPW + kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
-                        ldsm_x4_t(lb, Lt + tok * LW + np * 4 + (lane >> 4) * 4);
-                        mma_f16(lracc[np], pl, lb[0], lb[1]);
-                        mma_f16(lracc[np + 1], pl, lb[2], lb[3]);
+    #pragma unroll
+                    for (int nt = 0; nt < NL; ++nt) {
+                        lracc[nt][0] *= al[0];
+                        lracc[nt][1] *= al[0];
+                        lracc[nt][2] *= al[1];
+                        lracc[nt][3] *= al[1];
                     }
                 }
+                // P' = p * sigma as fp16 A fragments: the S accumulator of n-tiles
+                // 2kk, 2kk+1 is the A operand of k-step kk
+    #pragma unroll
+                for (int kk = 0; kk < NS / 2; ++kk) {
+                    uint32_t pa[4], pl[4];  // p * sigma for the pool's values; p for the low-rank cache
+    #pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        const int nt = 2 * kk + hf;
+                        const int tl = th * TPW + nt * 8 + 2 * tig;
+                        const float s0 = sc[tl], s1 = sc[tl + 1];
+                        const float p0 = exp2f(s[nt][0] - ref[0]), p1 = exp2f(s[nt][1] - ref[0]);
+                        const float p2 = exp2f(s[nt][2] - ref[1]), p3 = exp2f(s[nt][3] - ref[1]);
+                        ls[0] += p0 + p1;
+                        ls[1] += p2 + p3;
+                        pa[2 * hf] = pack_half2(p0 * s0, p1 * s1);
+                        pa[2 * hf + 1] = pack_half2(p2 * s0, p3 * s1);
+                        if constexpr (R > 0) {
+                            pl[2 * hf] = pack_half2(p0, p1);
+                            pl[2 * hf + 1] = pack_half2(p2, p3);
+                        }
+                    }
+                    // A += P' C over tokens th*TPW + kk*16 .. +15, every dim
+    #pragma unroll
+                    for (int np = 0; np < NV; np += 2) {
+                        uint32_t cb[4];
+                        const int tok = th * TPW + kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+                        ldsm_x4_t(cb, Cc + tok * RW + np * 4 + (lane >> 4) * 4);
+                        mma_f16(acc[np], pa, cb[0], cb[1]);
+                        mma_f16(acc[np + 1], pa, cb[2], cb[3]);
+                    }
+                    if constexpr (R > 0) {
+                        // Flash-LoRA reorder: P V_lr over the same tokens, r columns
+    #pragma unroll
+                        for (int np = 0; np < NL; np += 2) {
+                            uint32_t lb[4];
+                            const int tok = th * TPW + kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+                            ldsm_x4_t(lb, Lc + tok * LW + np * 4 + (lane >> 4) * 4);
+                            mma_f16(lracc[np], pl, lb[0], lb[1]);
+                            mma_f16(lracc[np + 1], pl, lb[2], lb[3]);
+                        }
+                    }
+                }
+            }
+            if constexpr (PIPE) {
+                // the next tile set is staged and this one is free, unless a wait ran out
+                if (__syncthreads_or(!ok_next)) {
+                    failed_at = i + 1;
+                    break;
+                }
+                refill(i + 1);
             }
         }
         if (failed_at >= 0) {
@@ -728,7 +796,7 @@ static bool attend_smem_ready() {
         // two blocks per SM need the largest shared-memory carveout; without
         // the preference the driver may configure the SM for one block
         if (cudaFuncSetAttribute(attend_split<D, TPW, R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 int(AttendSmem<D, R>::bytes)) != cudaSuccess ||
+                                 int(SplitSmem<D, TPW, R>::bytes)) != cudaSuccess ||
             cudaFuncSetAttribute(attend_split<D, TPW, R>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  int(cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
             return false;
@@ -740,7 +808,7 @@ static bool attend_smem_ready() {
 template <int D, int TPW, int R>
 static int attend_launch(const AttendArgs &a, dim3 grid, unsigned cgrid, cudaStream_t st) {
     if (!attend_smem_ready<D, TPW, R>()) return KVP_ERR_CUDA;
-    attend_split<D, TPW, R><<<grid, ATT_THREADS, AttendSmem<D, R>::bytes, st>>>(a);
+    attend_split<D, TPW, R><<<grid, ATT_THREADS, SplitSmem<D, TPW, R>::bytes, st>>>(a);
     // programmatic dependent launch: the combine's blocks are placed while the
     // split runs and wait (griddepcontrol.wait) for its results
     cudaLaunchConfig_t cfg = {};
@@ -781,7 +849,7 @@ static int attend_target_blocks() {
     int occ = 0;
     if (!attend_smem_ready<128, 32, 0>() ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, attend_split<128, 32, 0>, ATT_THREADS,
-                                                      AttendSmem<128, 0>::bytes) != cudaSuccess ||
+                                                      SplitSmem<128, 32, 0>::bytes) != cudaSuccess ||
         occ < 1) {
         (void)cudaGetLastError();
         occ = 1;
