@@ -668,12 +668,24 @@ __global__ void __launch_bounds__(CMB_THREADS) attend_combine(const __grid_const
     constexpr int PW = D + R;   // floats per partial row
     __shared__ float wacc[CMB_WARPS][D + (R > 0 ? 32 : 0)];
     __shared__ float wml[CMB_WARPS][2];
-    // launched as a programmatic dependent of the split kernel: its partial
-    // rows and statistics are complete and visible after this wait
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    __shared__ __align__(16) uint16_t sb[R > 0 ? R : 1][R > 0 ? D : 8];  // LoRA: B_a's rows, this head's columns
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ag = blockIdx.x / a.NQ, j = blockIdx.x % a.NQ;
     const int h = j / a.G, r = ag * a.G + j % a.G;
+    if constexpr (R > 0) {
+        // the agent's up-projection is an input, not a result of the split
+        // kernel (which runs after every earlier kernel of the stream is
+        // done), so it is read before the wait, while the split finishes
+        const uint16_t *bh = a.lora_b + uint64_t(ag) * R * uint64_t(a.H) * D + uint64_t(h) * D;
+        for (int i = threadIdx.x; i < R * (D / 8); i += CMB_THREADS) {
+            const int k = i / (D / 8), c = i % (D / 8);
+            *reinterpret_cast<uint4 *>(&sb[k][c * 8]) =
+                *reinterpret_cast<const uint4 *>(bh + uint64_t(k) * a.H * D + c * 8);
+        }
+    }
+    // launched as a programmatic dependent of the split kernel: its partial
+    // rows and statistics are complete and visible after this wait
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const uint64_t row0 = uint64_t(h) * a.nsplit * uint64_t(a.QHP) + r;  // split sp: row0 + sp * QHP
     float m = -INFINITY, l = 0.0f, acc[PL], lrv = 0.0f;
 #pragma unroll
@@ -762,11 +774,10 @@ __global__ void __launch_bounds__(CMB_THREADS) attend_combine(const __grid_const
     if constexpr (R > 0) {
         // (P V_lr / l) B_a, restricted to this KV head's d columns
         const float il = 1.0f / l;
-        const uint16_t *bh = a.lora_b + uint64_t(ag) * R * uint64_t(a.H) * D + uint64_t(h) * D + lane * PL;
 #pragma unroll 4
         for (int k = 0; k < R; ++k) {
             const float c = __shfl_sync(0xffffffffu, lrv, k) * il;
-            const uint16_t *bk = bh + uint64_t(k) * a.H * D;
+            const uint16_t *bk = &sb[k][lane * PL];
             if constexpr (PL == 4) {
                 const uint2 w = *reinterpret_cast<const uint2 *>(bk);
                 acc[0] = fmaf(c, bf16_lo(w.x), acc[0]);
