@@ -635,6 +635,10 @@ __device__ __forceinline__ void attend_passes(const AttendArgs &a, uint32_t *sme
 template <int D, int TPW, int R>
 __global__ void __launch_bounds__(ATT_THREADS, 2) attend_split(const __grid_constant__ AttendArgs a) {
     extern __shared__ __align__(16) uint32_t smem[];
+    // launched as a programmatic dependent of whatever precedes it on the
+    // stream: the pool and the queries are read only after this wait (it
+    // returns at once unless that kernel let this grid start early)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const uint32_t *hdr = reinterpret_cast<const uint32_t *>(a.pool);
     const uint32_t kmode = hdr[POOL_KMODE_WORD];
     if (hdr[0] != POOL_MAGIC || hdr[1] != POOL_VERSION || hdr[2] != uint32_t(a.L) || hdr[3] != uint32_t(a.H) ||
@@ -672,6 +676,9 @@ __global__ void __launch_bounds__(CMB_THREADS) attend_combine(const __grid_const
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ag = blockIdx.x / a.NQ, j = blockIdx.x % a.NQ;
     const int h = j / a.G, r = ag * a.G + j % a.G;
+    // a following split kernel (the next layer's attention) may be placed
+    // now: it waits for this grid's completion before it reads anything
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if constexpr (R > 0) {
         // the agent's up-projection is an input, not a result of the split
         // kernel (which runs after every earlier kernel of the stream is
@@ -819,7 +826,20 @@ static bool attend_smem_ready() {
 template <int D, int TPW, int R>
 static int attend_launch(const AttendArgs &a, dim3 grid, unsigned cgrid, cudaStream_t st) {
     if (!attend_smem_ready<D, TPW, R>()) return KVP_ERR_CUDA;
-    attend_split<D, TPW, R><<<grid, ATT_THREADS, SplitSmem<D, TPW, R>::bytes, st>>>(a);
+    // programmatic dependent launch on both kernels: the split's blocks may be
+    // placed while the kernel before it (a previous layer's combine) finishes,
+    // and wait (griddepcontrol.wait) for it before reading
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t scfg = {};
+    scfg.gridDim = grid;
+    scfg.blockDim = dim3(ATT_THREADS);
+    scfg.dynamicSmemBytes = SplitSmem<D, TPW, R>::bytes;
+    scfg.stream = st;
+    scfg.attrs = attr;
+    scfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&scfg, attend_split<D, TPW, R>, a) != cudaSuccess) return KVP_ERR_CUDA;
     // programmatic dependent launch: the combine's blocks are placed while the
     // split runs and wait (griddepcontrol.wait) for its results
     cudaLaunchConfig_t cfg = {};
@@ -827,9 +847,6 @@ static int attend_launch(const AttendArgs &a, dim3 grid, unsigned cgrid, cudaStr
     cfg.blockDim = dim3(CMB_THREADS);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (cudaLaunchKernelEx(&cfg, attend_combine<D, R>, a) != cudaSuccess) return KVP_ERR_CUDA;
