@@ -166,3 +166,46 @@ def test_attend_wait_timeout_is_reported_and_context_survives():
     res, res_lse = _attend(pool2, shape, 0, q.cuda(), 0.1)
     assert kv.kvpool_status(pool2) == kv.KVP_OK
     _check(pool2.cpu().numpy(), shape, 0, synth.bits16(q), 0.1, res, res_lse)
+
+
+def test_attend_calls_chained_without_synchronization():
+    """Attention calls back to back on one stream, with no host
+    synchronization in between: every layer of a pool, then the pool
+    re-encoded from other caches in place and attended again.  The split
+    kernel may be placed while the previous call's combine still runs (a
+    programmatic dependent launch), so each call must still see the
+    queries, the pool and the previous kernels' writes in stream order."""
+    shape = (3, 8, 128, 700)
+    L, H, d, T = shape
+    ks_a, vs_a = synth.kv_layers(L, H, T, d, seed=51, device="cuda")
+    ks_b, vs_b = synth.kv_layers(L, H, T, d, seed=52, device="cuda")
+    pool = torch.empty(kv.kvpool_pool_bytes(shape), dtype=torch.uint8, device="cuda")
+    pws = torch.empty(kv.kvpool_workspace_bytes(shape), dtype=torch.uint8, device="cuda")
+    g = torch.Generator(device="cpu").manual_seed(9)
+    q = torch.randn(3, 32, d, generator=g).to(torch.bfloat16)
+    qd = q.cuda()
+    na, nq = q.shape[0], q.shape[1]
+    wsb = kv.kvpool_attend_workspace_bytes(shape, na, nq)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    outs, lses = [], []
+
+    def attend_all():
+        for layer in range(L):
+            o = torch.empty(na, nq, d, dtype=torch.float32, device="cuda")
+            s = torch.empty(na, nq, dtype=torch.float32, device="cuda")
+            assert kv.kvpool_attend(pool, shape, layer, na, nq, qd, 0.09, o, s, ws, wsb) == kv.KVP_OK
+            outs.append(o)
+            lses.append(s)
+
+    assert kv.kvpool_encode(shape, ks_a, vs_a, pool, pool.numel(), pws, pws.numel()) == kv.KVP_OK
+    attend_all()
+    img_a = pool.clone()
+    assert kv.kvpool_encode(shape, ks_b, vs_b, pool, pool.numel(), pws, pws.numel()) == kv.KVP_OK
+    attend_all()
+    torch.cuda.synchronize()
+    assert kv.kvpool_status(pool) == kv.KVP_OK
+    qb = synth.bits16(q)
+    for i, img in enumerate([img_a.cpu().numpy(), pool.cpu().numpy()]):
+        for layer in range(L):
+            k = i * L + layer
+            _check(img, shape, layer, qb, 0.09, outs[k].cpu().numpy(), lses[k].cpu().numpy())
