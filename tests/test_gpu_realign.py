@@ -15,7 +15,7 @@ import agent_shared_compressed_gb300 as kv
 from agent_shared_compressed_gb300 import build as kvbuild
 from agent_shared_compressed_gb300 import synth
 import oracle as O
-from kvhelp import Guarded, bf16_dev_layers, f32_of_bf16
+from kvhelp import Guarded, assert_bf16_close, bf16_dev_layers, f32_of_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -165,3 +165,31 @@ def test_unpack_wait_timeout_is_reported(realign):
         np.testing.assert_array_equal(vu[l], vp[l])
         if not realign:
             np.testing.assert_array_equal(ku[l], kp[l])
+
+
+@pytest.mark.parametrize("shape,fill", [((1, 8, 128, 1), 16), ((1, 8, 128, 1), 2), ((2, 8, 128, 5), 16),
+                                        ((2, 8, 128, 5), 2), ((1, 4, 64, 3), 8), ((3, 2, 128, 2), 4)])
+def test_staged_unpack_edge_cases(shape, fill):
+    """The staged unpack (every shape here stages) at its edges: a single
+    token, fewer tokens than a block has warps, and every record at the
+    largest (16-bit) or smallest (2-bit) size; plain and realigning unpack
+    against the oracle, values of the two bit-identical."""
+    L, H, d, T = shape
+    ks, vs = synth.kv_layers(L, H, T, d, seed=T + fill, device="cpu")
+    ks, vs = [synth.bits16(k) for k in ks], [synth.bits16(v) for v in vs]
+    bits = np.full(T, fill, np.uint8)
+    card = pack(bf16_dev_layers(ks), bf16_dev_layers(vs), bits, shape, 11)
+    kp, vp = unpack(card, L, H, T, d)
+    ok_, ov = O.card_unpack(card.host())
+    for l in range(L):
+        assert_bf16_close(kp[l], ok_[l], "K layer %d" % l)
+        assert_bf16_close(vp[l], ov[l], "V layer %d" % l)
+        if fill == 16:
+            np.testing.assert_array_equal(kp[l], ks[l])
+            np.testing.assert_array_equal(vp[l], vs[l])
+    w = inv_freq(d, "llama3")
+    ku, vu = unpack(card, L, H, T, d, 11 + 3000, w)
+    oka, _ = O.card_unpack_at(card.host(), 11 + 3000, w)
+    for l in range(L):
+        assert_keys_close(ku[l], oka[l], "K layer %d" % l)
+        np.testing.assert_array_equal(vu[l], vp[l])
