@@ -318,6 +318,10 @@ __device__ __forceinline__ void attend_passes(const AttendArgs &a, uint32_t *sme
             const float c0 = centroid_e4(uint32_t(tid & 7)) * 1e-4f, c1 = centroid_e4(uint32_t(tid >> 3)) * 1e-4f;
             lut[tid] = pack_half2(c0, c1);
         }
+        // the kernel before this one (see attend_split) has completed and its
+        // writes are visible past this point; the queries are read, and the
+        // workspace written, only after it
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         {   // the query tile: every load of a thread issued before its stores
             constexpr int QPT = (RP * (D / 8) + ATT_THREADS - 1) / ATT_THREADS;
             uint4 v[QPT];
@@ -635,10 +639,13 @@ __device__ __forceinline__ void attend_passes(const AttendArgs &a, uint32_t *sme
 template <int D, int TPW, int R>
 __global__ void __launch_bounds__(ATT_THREADS, 2) attend_split(const __grid_constant__ AttendArgs a) {
     extern __shared__ __align__(16) uint32_t smem[];
-    // launched as a programmatic dependent of whatever precedes it on the
-    // stream: the pool and the queries are read only after this wait (it
-    // returns at once unless that kernel let this grid start early)
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // Launched as a programmatic dependent of whatever precedes it on the
+    // stream, and waits for it (griddepcontrol.wait) before it reads the
+    // queries or writes its workspace.  The pool (and a LoRA cache) is read
+    // before that wait: the only kernel that lets this grid start early is the
+    // combine of a previous attention call, which writes neither, and any
+    // other kernel before it (an encode, a caller's kernel) has completed
+    // before this grid starts.
     const uint32_t *hdr = reinterpret_cast<const uint32_t *>(a.pool);
     const uint32_t kmode = hdr[POOL_KMODE_WORD];
     if (hdr[0] != POOL_MAGIC || hdr[1] != POOL_VERSION || hdr[2] != uint32_t(a.L) || hdr[3] != uint32_t(a.H) ||
