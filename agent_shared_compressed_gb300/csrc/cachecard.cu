@@ -914,6 +914,27 @@ __global__ void __launch_bounds__(CARD_THREADS, ROPE ? 4 : 5) card_unpack_staged
     }
 }
 
+// Dynamic shared memory above the default 48 KB is opted into once per device
+// and kernel, for the largest size asked so far.
+template <bool ROPE>
+static bool unpack_smem_ready(size_t smem) {
+    if (smem <= 48u * 1024u) return true;
+    static size_t done[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    if (done[dev] >= smem) return true;
+    if (cudaFuncSetAttribute(card_unpack_staged<ROPE>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
+        cudaSuccess) {
+        (void)cudaGetLastError();  // leave no sticky error for the next call to report
+        return false;
+    }
+    done[dev] = smem;
+    return true;
+}
+
 // The (token, layer) step of a warp's staged-unpack tasks for a grid of
 // `grid` blocks: half the grid's warp count, in tokens.
 static void set_unpack_steps(CardArgs &a, int grid) {
@@ -1057,12 +1078,7 @@ extern "C" int cachecard_unpack(const void *card, const kvp_card_header *hdr, vo
         const size_t smem = 16u * CARD_WARPS + size_t(CARD_WARPS) * 2u * sb;
         // eight resident grids' worth of blocks: 4K-token step unpack 0.117 ms
         // against 0.121 (three) and 0.119 (six); 8K-token card 0.231 against 0.242
-        if (smem > 48u * 1024u &&
-            cudaFuncSetAttribute(card_unpack_staged<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
-                cudaSuccess) {
-            (void)cudaGetLastError();  // leave no sticky error for the next call to report
-            return KVP_ERR_CUDA;
-        }
+        if (!unpack_smem_ready<false>(smem)) return KVP_ERR_CUDA;
         const int grid = card_grid(card_unpack_staged<false>, tasks, 8, smem);
         set_unpack_steps(a, grid);
         card_unpack_staged<false><<<grid, CARD_THREADS, smem, st>>>(a, sb);
@@ -1092,12 +1108,7 @@ extern "C" int cachecard_unpack_at(const void *card, const kvp_card_header *hdr,
         const size_t smem = 16u * CARD_WARPS + size_t(CARD_WARPS) * 2u * sb;
         // four resident grids' worth of blocks (8K-token card: 0.250 ms; one, two,
         // three, six, eight and twelve: 0.267, 0.257, 0.251, 0.251, 0.253, 0.258)
-        if (smem > 48u * 1024u &&
-            cudaFuncSetAttribute(card_unpack_staged<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
-                cudaSuccess) {
-            (void)cudaGetLastError();  // leave no sticky error for the next call to report
-            return KVP_ERR_CUDA;
-        }
+        if (!unpack_smem_ready<true>(smem)) return KVP_ERR_CUDA;
         const int grid = card_grid(card_unpack_staged<true>, tasks, 4, smem);
         set_unpack_steps(a, grid);
         card_unpack_staged<true><<<grid, CARD_THREADS, smem, st>>>(a, sb);
