@@ -319,7 +319,12 @@ int cachecard_read_header(const void *card, kvp_card_header *out, void *stream);
 /* Receiver injection ("QKVShare" Methodology 3): rebuild every layer's bf16
  * K and V ([H][T][d]) from the card: x = bf16(q * s_h + z_h), 16-bit tokens
  * verbatim.  hdr is the header read by cachecard_read_header.  k_dst, v_dst:
- * host arrays of n_layers device pointers (16-byte aligned). */
+ * host arrays of n_layers device pointers (16-byte aligned).  The header's
+ * fields are checked on the host (KVP_ERR_HEADER); a token whose bitwidth is
+ * invalid or whose record offset is not 16-byte aligned or does not fit the
+ * layer stride is left unwritten, and cachecard_status then reports
+ * KVP_ERR_HEADER.  Where the shape allows it (see kvp_test_limit_next_unpack)
+ * records are staged through shared memory by bulk copies. */
 int cachecard_unpack(const void *card, const kvp_card_header *hdr,
                      void *const *k_dst, void *const *v_dst, void *stream);
 
