@@ -176,6 +176,42 @@ def test_card_invalid_bits_and_small_buffer():
     assert np.all(card2.host()[geo["off_layers"]:] == 0x5A)
 
 
+@pytest.mark.parametrize("shape", [(2, 8, 128, 20), (1, 32, 128, 9)])
+def test_card_unpack_rejects_corrupt_records(shape):
+    """A card corrupted after packing: one token's record offset moved off its
+    16-byte boundary, another's bitwidth byte set to 3.  Both records are
+    rejected before anything is read from them (the staged kernel, first
+    shape, and the direct one, second); cachecard_status reports
+    KVP_ERR_HEADER, and every other token unpacks as from the intact card."""
+    L, H, d, T = shape
+    ks, vs, bits = inputs(L, H, T, d, seed=T + 3)
+    kd, vd = bf16_dev_layers(ks), bf16_dev_layers(vs)
+    card, status = gpu_pack(kd, vd, bits, shape)
+    assert status == kv.KVP_OK
+    hdr0, k0, v0 = gpu_unpack(card, L, H, T, d)
+    img = card.host().copy()
+    offs = img[hdr0.off_offsets:hdr0.off_offsets + 4 * T].view(np.uint32)
+    offs[3] += 8                                        # misaligned, still inside the layer
+    img[hdr0.off_bits + 6] = 3                          # not a bitwidth
+    bad = Guarded(img.size)
+    bad.t[: img.size].copy_(torch.from_numpy(img))
+    hdr = kv.CardHeader()
+    assert kv.cachecard_read_header(bad.t, hdr) == kv.KVP_OK
+    ko = [Guarded(H * T * d * 2, fill=0xFF) for _ in range(L)]
+    vo = [Guarded(H * T * d * 2, fill=0xFF) for _ in range(L)]
+    assert kv.cachecard_unpack(bad.t, hdr, [g.t for g in ko], [g.t for g in vo]) == kv.KVP_OK
+    torch.cuda.synchronize()
+    assert kv.cachecard_status(bad.t) == kv.KVP_ERR_HEADER
+    assert all(g.canary_ok() for g in ko + vo)
+    keep = np.ones(T, bool)
+    keep[[3, 6]] = False
+    for l in range(L):
+        ku, vu = synth.bits16(ko[l].bf16((H, T, d))), synth.bits16(vo[l].bf16((H, T, d)))
+        np.testing.assert_array_equal(ku[:, keep], k0[l][:, keep])
+        np.testing.assert_array_equal(vu[:, keep], v0[l][:, keep])
+        assert np.all(ku[:, ~keep] == 0xFFFF) and np.all(vu[:, ~keep] == 0xFFFF)   # left unwritten
+
+
 def test_card_nonfinite_and_range_flags():
     L, H, d, T = 1, 1, 64, 4
     ks, vs, _ = inputs(L, H, T, d, seed=3)
