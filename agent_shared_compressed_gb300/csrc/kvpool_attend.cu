@@ -689,13 +689,15 @@ __global__ void __launch_bounds__(CMB_THREADS) attend_combine(const __grid_const
     if constexpr (R > 0) {
         // the agent's up-projection is an input, not a result of the split
         // kernel (which runs after every earlier kernel of the stream is
-        // done), so it is read before the wait, while the split finishes
+        // done), so it is requested before the wait, by asynchronous copies
+        // that stay in flight beside the partial-row loads below
         const uint16_t *bh = a.lora_b + uint64_t(ag) * R * uint64_t(a.H) * D + uint64_t(h) * D;
+        const uint64_t keep = l2_evict_last_policy();  // read by the agent's other query heads too
         for (int i = threadIdx.x; i < R * (D / 8); i += CMB_THREADS) {
             const int k = i / (D / 8), c = i % (D / 8);
-            *reinterpret_cast<uint4 *>(&sb[k][c * 8]) =
-                *reinterpret_cast<const uint4 *>(bh + uint64_t(k) * a.H * D + c * 8);
+            cp_async16(&sb[k][c * 8], bh + uint64_t(k) * a.H * D + c * 8, 16, keep);
         }
+        cp_async_commit();
     }
     // launched as a programmatic dependent of the split kernel: its partial
     // rows and statistics are complete and visible after this wait
@@ -743,7 +745,10 @@ __global__ void __launch_bounds__(CMB_THREADS) attend_combine(const __grid_const
     }
 #pragma unroll
     for (int e = 0; e < PL; ++e) wacc[warp][lane * PL + e] = acc[e];
-    if constexpr (R > 0) wacc[warp][D + lane] = lrv;
+    if constexpr (R > 0) {
+        wacc[warp][D + lane] = lrv;
+        cp_async_wait<0>();  // this thread's share of B_a is in (the barrier below publishes it)
+    }
     if (lane == 0) {
         wml[warp][0] = m;
         wml[warp][1] = l;
